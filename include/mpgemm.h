@@ -1,0 +1,227 @@
+/*
+ * mpgemm — mixed-precision tensor-core matrix product for sm_103a (GB300).
+ *
+ * C ABI.  Plain pointers and integer sizes only; no C++ or framework types.
+ *
+ * Computes, for every batch index b,
+ *     C_b = alpha * A_b * B_b + beta * C_b
+ * with A_b (m x k), B_b (k x n), C_b (m x n, row-major fp32), under an explicit
+ * precision policy.  The operation and its parameters follow:
+ *   - "tile_matmul(): use the cuBLASDx register-accumulator API with suggested
+ *     shared layouts for Tensor Core precisions", section "Description": every
+ *     call computes C = alpha*A*B + beta*C in place;
+ *   - "Tensor Core operands: a matrix instruction still needs a layout
+ *     contract", first paragraph: row-major / column-major operands and the
+ *     leading dimension (element distance between successive rows, resp.
+ *     columns; padding may make it larger than the visible extent);
+ *   - same page, third paragraph: FP16 or BF16 multiplicands with FP32
+ *     accumulation, TF32, and the rounding each conversion adds;
+ *   - "qsa_prompt_attn: Volta (sm_70) m8n8k4 kernel - keep the hi and lo halves
+ *     in separate accumulator chains", sections "What's going on" and "The fix":
+ *     FP32 operands split into FP16 hi and lo halves, with the hi and lo
+ *     products accumulated in separate chains and summed in plain FP32.
+ *
+ * Conventions common to every entry point:
+ *   - Device pointers are raw CUDA device addresses owned by the caller; the
+ *     library never frees or retains them after the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Compute calls are asynchronous on that stream.
+ *   - Every call returns an mpg_status; on failure the reason is available
+ *     from mpg_last_error_string() (thread-local, valid until the next call
+ *     on the same thread).  Argument errors are detected on the host before
+ *     anything is launched.
+ *   - No entry point allocates device memory on the compute path.  Scratch
+ *     (split-K partial sums) lives in a caller-provided workspace sized by
+ *     mpg_gemm_workspace_size().
+ */
+#ifndef MPGEMM_H_
+#define MPGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage order of an operand (layout contract, "Tensor Core operands: a
+ * matrix instruction still needs a layout contract", first paragraph).
+ *   ROW_MAJOR: element (r, c) at r*ld + c, ld >= number of columns.
+ *   COL_MAJOR: element (r, c) at c*ld + r, ld >= number of rows. */
+typedef enum { MPG_ROW_MAJOR = 0, MPG_COL_MAJOR = 1 } mpg_layout;
+
+/* Storage type of A and B.  C is always fp32, row-major. */
+typedef enum { MPG_F32 = 0, MPG_F16 = 1, MPG_BF16 = 2 } mpg_dtype;
+
+/* Precision policy ("Tensor Core operands ...", third paragraph; "qsa_prompt_attn
+ * ...", "The fix").
+ *   FP16_F32ACC  multiplicands rounded to fp16 (RNE) — fp32 inputs are
+ *                converted on load, fp16 inputs are used as stored; products
+ *                accumulated in fp32 on the tensor cores.
+ *   BF16_F32ACC  same with bf16 (fp32 or bf16 inputs).
+ *   TF32         fp32 inputs fed to the tf32 tensor-core path, fp32 accumulate.
+ *   SPLIT_FP16_3CHAIN  fp32 inputs split on load into fp16 hi/lo halves
+ *                (see mpg_options for the exact split); hi*hi, hi*lo and lo*hi
+ *                accumulate in three separate fp32 accumulators that are summed
+ *                in plain fp32 in the epilogue: acc = hh + 2^-11 * (hl + lh).
+ *   SPLIT_FP16_1CHAIN  the same three products accumulated in ONE accumulator
+ *                (the shared-chain variant, kept for comparison; its lo is the
+ *                plain fp16(x*2^s - hi), without the 2^11 scale).
+ *   FP32_FFMA    plain fp32 CUDA-core product: each output is one sequential
+ *                fmaf chain over k in ascending order (the comparator). */
+typedef enum {
+  MPG_FP16_F32ACC = 0,
+  MPG_BF16_F32ACC = 1,
+  MPG_TF32 = 2,
+  MPG_SPLIT_FP16_3CHAIN = 3,
+  MPG_SPLIT_FP16_1CHAIN = 4,
+  MPG_FP32_FFMA = 5
+} mpg_precision;
+
+typedef enum {
+  MPG_OK = 0,
+  MPG_ERR_INVALID_ARG = 1,  /* bad size, leading dimension, stride or pointer */
+  MPG_ERR_UNSUPPORTED = 2,  /* dtype / mode combination the library does not offer */
+  MPG_ERR_NO_DEVICE = 3,    /* no CUDA device, or not an sm_103 device */
+  MPG_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+  MPG_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed */
+  MPG_ERR_TIMEOUT = 6       /* a kernel's bounded wait expired (see mpg_device_status) */
+} mpg_status;
+
+/* Optional knobs.  Initialise with mpg_options_init(); a NULL options pointer
+ * means the defaults. */
+typedef struct {
+  /* Split modes: A is split as x*2^split_exp_a and B as x*2^split_exp_b before
+   * hi = fp16(x*2^s), lo = fp16((x*2^s - hi) * 2^L) (L = 11 for 3CHAIN, 0 for
+   * 1CHAIN); the scale is undone exactly in the epilogue.  Use it to lift
+   * operands whose magnitudes sit below fp16's normal range (2^-14), e.g.
+   * softmax probabilities.  Default 0.  Range [-100, 100]. */
+  int32_t split_exp_a;
+  int32_t split_exp_b;
+  /* Number of K partitions (split-K).  0 = chosen by the library. */
+  int32_t splitk;
+  /* 1 = load operands with plain global loads even where TMA applies
+   * (exercises the path used for unaligned leading dimensions).  Default 0. */
+  int32_t force_generic_load;
+  /* Tile width along N: 0 = chosen by the library, else 64, 128 or 256
+   * (256 only for the direct fp16/bf16/tf32 paths). */
+  int32_t tile_n;
+  /* Upper bound for any single wait inside a kernel, in nanoseconds.
+   * 0 = default (2 s).  On expiry the kernel stops, records MPG_ERR_TIMEOUT in
+   * the device status word and returns without hanging the GPU. */
+  int64_t wait_timeout_ns;
+  int32_t reserved[8];
+} mpg_options;
+
+void mpg_options_init(mpg_options* opt);
+
+/* The product.
+ *   m, n, k      >= 0; batch >= 0.  m == 0, n == 0 or batch == 0: no-op.
+ *                k == 0: C = beta*C.  beta == 0: C is not read.
+ *                alpha == 0: A and B are not read.
+ *   A            device pointer; a_layout ROW_MAJOR requires lda >= k,
+ *                COL_MAJOR requires lda >= m (lda >= 1 always).
+ *   strideA      elements between consecutive batch matrices of A; 0 means
+ *                packed (m*lda for row-major, k*lda for column-major).
+ *   B            likewise with (k x n): ROW_MAJOR ldb >= n, COL_MAJOR ldb >= k.
+ *   C            device pointer, row-major fp32, ldc >= n; strideC 0 = m*ldc.
+ *   mode         precision policy; allowed input dtypes per mode:
+ *                  FP16_F32ACC: A, B both F32 or both F16
+ *                  BF16_F32ACC: A, B both F32 or both BF16
+ *                  TF32, SPLIT_*, FP32_FFMA: A, B both F32
+ *                anything else returns MPG_ERR_UNSUPPORTED.
+ *   workspace    device scratch of at least mpg_gemm_workspace_size(...)
+ *                bytes (may be NULL when that size is 0).  Its contents on
+ *                entry are ignored.  Calls that share a workspace must be
+ *                ordered on one stream.
+ * Pointers need only element alignment; 16-byte aligned pointers and leading
+ * dimensions whose byte size is a multiple of 16 take the TMA load path, any
+ * other alignment takes the generic-load path (same results, lower speed).
+ * The memory C_b occupies must not overlap A or B. */
+mpg_status mpg_gemm(int64_t m, int64_t n, int64_t k, int64_t batch,
+                    const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
+                    const void* B, int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                    float* C, int64_t ldc, int64_t strideC,
+                    float alpha, float beta, mpg_precision mode,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* mpg_gemm with options (NULL = defaults). */
+mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch,
+                       const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
+                       const void* B, int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                       float* C, int64_t ldc, int64_t strideC,
+                       float alpha, float beta, mpg_precision mode,
+                       void* workspace, size_t workspace_bytes, void* stream,
+                       const mpg_options* opt);
+
+/* Bytes of workspace mpg_gemm / mpg_gemm_ex need for this problem (0 if none).
+ * Depends only on the sizes, the mode, the options and the current device. */
+size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
+                               mpg_precision mode, const mpg_options* opt);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns MPG_ERR_TIMEOUT if any kernel since the
+ * last call gave up a bounded wait, MPG_ERR_CUDA if the stream reports an
+ * error, else MPG_OK. */
+mpg_status mpg_device_status(void* stream);
+
+/* Thread-local description of the last failure on this thread. */
+const char* mpg_last_error_string(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int mpg_version(void);
+
+/* ---- accumulator fragment map of mma.sync m16n8k16 (f32 accumulator) ------
+ * "feat(cuda-device): derive the m16n8k16 accumulator fragment layout",
+ * sections "The layout is a mixed-radix numeral" and "API".  Pure host
+ * functions, no CUDA.  lane in [0, 32), j in [0, 4). */
+
+/* Position (row in [0,16), col in [0,8)) of value j of lane `lane`.
+ * Returns 0, or -1 for an out-of-range argument (outputs untouched). */
+int mpg_acc_coords(int lane, int j, int* row, int* col);
+
+/* Row-major offset in the 16x8 tile, in numeral form
+ * (j&1)*1 + (lane%4)*2 + (lane/4)*8 + (j>>1)*64; -1 if out of range. */
+int mpg_acc_offset(int lane, int j);
+
+/* Offset of value j of lane `lane` in a strided destination whose tile starts
+ * at (tile_row, tile_col) with row stride row_stride:
+ *     (tile_row + row) * row_stride + tile_col + col.
+ * Returns -1 (the "None" of the page) when an argument is out of range, a
+ * coordinate is negative, col would not fit in the row (tile_col + col >=
+ * row_stride), or the offset would reach `limit` or overflow int64. */
+int64_t mpg_acc_matrix_offset(int lane, int j, int64_t tile_row, int64_t tile_col,
+                              int64_t row_stride, int64_t limit);
+
+/* Inverse of mpg_acc_offset: offset in [0,128) -> (lane, j).  Returns 0 or -1. */
+int mpg_acc_decode(int offset, int* lane, int* j);
+
+/* Accumulator map of the tcgen05 path used by this library (M = 128,
+ * cta_group::1): value `reg` returned by tcgen05.ld.32x32b to lane `lane` of
+ * warp `warp`, reading columns starting at `col_base`, holds D(row, col) with
+ * row = 32*(warp % 4) + lane and col = col_base + reg.  Returns 0 or -1. */
+int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int* col);
+
+/* ---- hardware checks ------------------------------------------------------ */
+
+/* One mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 by one warp.
+ *   A: device, 16x16 fp16 (raw 16-bit codes), row-major, ld 16.
+ *   B: device, 16x8 fp16, column-major (element (k, n) at n*16 + k).
+ *   D: device, 128 floats; D[lane*4 + j] receives the raw accumulator value j
+ *      of lane `lane` (C = 0), unscattered, so the caller can place it with
+ *      mpg_acc_coords and compare with a host product.
+ * Fragments are gathered with the A/B operand layouts of the PTX ISA. */
+mpg_status mpg_probe_mma_m16n8k16(const void* A, const void* B, float* D, void* stream);
+
+/* Failure-detection self test: launches one kernel whose single wait is on an
+ * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then
+ * synchronises.  Returns MPG_ERR_TIMEOUT when the kernel gave up the wait and
+ * returned cleanly (the expected outcome); the device status word is cleared
+ * afterwards.  Touches no caller memory. */
+mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPGEMM_H_ */

@@ -1,0 +1,558 @@
+// Host side of the C ABI: argument validation, plan selection (which kernel,
+// tile width, split-K), TMA tensor-map encoding and launch.  Nothing here
+// allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "mpgemm.h"
+
+namespace mpg {
+bool tc_lookup_direct(Op op, int bn, TcKernel* out);
+bool tc_lookup_staged(Conv conv, int bn, TcKernel* out);
+bool tc_lookup_generic(Conv conv, Op op, SrcT st, int bn, TcKernel* out);
+
+bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out) {
+  switch (src) {
+    case Src::kTmaDirect: return tc_lookup_direct(op, bn, out);
+    case Src::kTmaStaged: return tc_lookup_staged(conv, bn, out);
+    default: return tc_lookup_generic(conv, op, st, bn, out);
+  }
+}
+}  // namespace mpg
+
+using namespace mpg;
+
+namespace {
+
+thread_local std::string t_err;
+
+mpg_status fail(mpg_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  uint32_t* status = nullptr;
+  std::atomic<uint64_t> smem_set_mask[4];  // kernels whose smem attribute was set (by slot)
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+mpg_status get_device(DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return fail(MPG_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+  }
+  if (dev >= kMaxDevices) return fail(MPG_ERR_NO_DEVICE, "device index %d beyond %d", dev, kMaxDevices);
+  DeviceInfo& d = g_devices[dev];
+  if (d.ready) {
+    *out = &d;
+    return MPG_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      return fail(MPG_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    }
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.status = status_word_ptr();
+    if (!d.status) return fail(MPG_ERR_CUDA, "cannot resolve the device status word");
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return fail(MPG_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    for (auto& m : d.smem_set_mask) m.store(0);
+    d.ready = true;
+  }
+  *out = &d;
+  return MPG_OK;
+}
+
+int elem_bytes(mpg_dtype t) { return t == MPG_F32 ? 4 : 2; }
+
+// --------------------------------------------------------------------------
+// planning
+// --------------------------------------------------------------------------
+enum class Kind { kNoop, kScale, kFfma, kTc };
+
+struct Plan {
+  Kind kind = Kind::kNoop;
+  Src src = Src::kTmaDirect;
+  Conv conv = Conv::kNone;
+  Op op = Op::kF16;
+  SrcT st = SrcT::kF32;
+  int bn = 128;
+  int splits = 1;
+};
+
+struct Operand {
+  const void* ptr;
+  int64_t ld, stride;
+  mpg_dtype dt;
+  mpg_layout layout;
+};
+
+bool tma_ok(const Operand& x, int64_t batch) {
+  const int64_t es = elem_bytes(x.dt);
+  if (reinterpret_cast<uintptr_t>(x.ptr) % 16 != 0) return false;
+  if ((x.ld * es) % 16 != 0 || x.ld * es >= (int64_t(1) << 40)) return false;
+  if (batch > 1 && ((x.stride * es) % 16 != 0 || x.stride * es >= (int64_t(1) << 40))) return false;
+  return true;
+}
+
+// Number of K partitions from the sizes alone, so that the workspace query
+// and the call agree whatever path the pointers select.  Counted with
+// 128 x 128 tiles and 32-wide k-blocks.
+int choose_splits(int64_t m, int64_t n, int64_t k, int64_t batch, int sm_count, const mpg_options& o) {
+  const int64_t kb = (k + 31) / 32;
+  if (o.splitk > 0) return (int)std::min<int64_t>(o.splitk, std::max<int64_t>(kb, 1));
+  const int64_t tiles = batch * ((m + 127) / 128) * ((n + 127) / 128);
+  if (tiles * 2 > sm_count || kb < 16) return 1;
+  int64_t s = sm_count / tiles;
+  s = std::min<int64_t>(s, kb / 8);
+  return (int)std::max<int64_t>(s, 1);
+}
+
+size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch) {
+  return splits > 1 ? (size_t)splits * (size_t)batch * (size_t)m * (size_t)n * sizeof(float) : 0;
+}
+
+mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
+                     float alpha, mpg_precision mode, const mpg_options& o, int sm_count, size_t ws_bytes,
+                     Plan* plan) {
+  Plan p;
+  if (m == 0 || n == 0 || batch == 0) {
+    p.kind = Kind::kNoop;
+    *plan = p;
+    return MPG_OK;
+  }
+  if (k == 0 || alpha == 0.0f) {
+    p.kind = Kind::kScale;
+    *plan = p;
+    return MPG_OK;
+  }
+  if (mode == MPG_FP32_FFMA) {
+    p.kind = Kind::kFfma;
+    *plan = p;
+    return MPG_OK;
+  }
+  p.kind = Kind::kTc;
+  const bool f32 = (A.dt == MPG_F32);
+  bool direct_layout_ok = true;
+  switch (mode) {
+    case MPG_FP16_F32ACC:
+      p.op = Op::kF16;
+      p.conv = f32 ? Conv::kRoundF16 : Conv::kNone;
+      p.st = f32 ? SrcT::kF32 : SrcT::kF16;
+      break;
+    case MPG_BF16_F32ACC:
+      p.op = Op::kBF16;
+      p.conv = f32 ? Conv::kRoundBF16 : Conv::kNone;
+      p.st = f32 ? SrcT::kF32 : SrcT::kBF16;
+      break;
+    case MPG_TF32:
+      p.op = Op::kTF32;
+      p.conv = Conv::kNone;
+      p.st = SrcT::kF32;
+      // tf32 shared-memory tiles are kept K-major: the direct TMA path needs
+      // a row-major A and a column-major B
+      direct_layout_ok = (A.layout == MPG_ROW_MAJOR && B.layout == MPG_COL_MAJOR);
+      break;
+    case MPG_SPLIT_FP16_3CHAIN:
+      p.op = Op::kF16;
+      p.conv = Conv::kSplit3;
+      p.st = SrcT::kF32;
+      break;
+    case MPG_SPLIT_FP16_1CHAIN:
+      p.op = Op::kF16;
+      p.conv = Conv::kSplit1;
+      p.st = SrcT::kF32;
+      break;
+    default:
+      return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
+  }
+  const bool tma = !o.force_generic_load && tma_ok(A, batch) && tma_ok(B, batch);
+  if (tma && p.conv == Conv::kNone && direct_layout_ok) p.src = Src::kTmaDirect;
+  else if (tma && p.conv != Conv::kNone) p.src = Src::kTmaStaged;
+  else p.src = Src::kGeneric;
+
+  // tile width along N
+  int bn;
+  if (p.src == Src::kGeneric) {
+    bn = 128;
+  } else if (p.src == Src::kTmaDirect) {
+    bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
+  } else if (p.conv == Conv::kSplit3) {
+    bn = (n <= 64 || k <= 512) ? 64 : 128;
+  } else {
+    bn = n <= 64 ? 64 : 128;
+  }
+  if (o.tile_n != 0) {
+    TcKernel probe;
+    if (!tc_kernel_lookup(p.src, p.conv, p.op, p.st, o.tile_n, &probe))
+      return fail(MPG_ERR_UNSUPPORTED, "tile_n %d is not available on this path", o.tile_n);
+    bn = o.tile_n;
+  }
+  p.bn = bn;
+
+  int splits = choose_splits(m, n, k, batch, sm_count, o);
+  if (splits > 1 && splitk_bytes(splits, m, n, batch) > ws_bytes) {
+    if (o.splitk > 0)
+      return fail(MPG_ERR_WORKSPACE, "split-K with %d partitions needs %zu workspace bytes, got %zu", splits,
+                  splitk_bytes(splits, m, n, batch), ws_bytes);
+    splits = 1;  // automatic choice: no workspace, no split
+  }
+  p.splits = splits;
+  *plan = p;
+  return MPG_OK;
+}
+
+// --------------------------------------------------------------------------
+// validation
+// --------------------------------------------------------------------------
+mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
+                    const float* C, int64_t ldc, int64_t strideC, float alpha, mpg_precision mode,
+                    const mpg_options& o) {
+  const int64_t kMax = 0x7FFFFFFF;
+  if (m < 0 || n < 0 || k < 0 || batch < 0)
+    return fail(MPG_ERR_INVALID_ARG, "negative size (m=%lld n=%lld k=%lld batch=%lld)", (long long)m,
+                (long long)n, (long long)k, (long long)batch);
+  if (m > kMax || n > kMax || k > kMax || batch > kMax)
+    return fail(MPG_ERR_INVALID_ARG, "size beyond 2^31-1");
+  if ((int)mode < 0 || (int)mode > (int)MPG_FP32_FFMA) return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
+  for (const Operand* x : {&A, &B}) {
+    if ((int)x->dt < 0 || (int)x->dt > 2) return fail(MPG_ERR_INVALID_ARG, "unknown dtype %d", (int)x->dt);
+    if ((int)x->layout < 0 || (int)x->layout > 1) return fail(MPG_ERR_INVALID_ARG, "unknown layout %d", (int)x->layout);
+  }
+  if (A.dt != B.dt) return fail(MPG_ERR_UNSUPPORTED, "A and B must have the same dtype");
+  switch (mode) {
+    case MPG_FP16_F32ACC:
+      if (A.dt != MPG_F32 && A.dt != MPG_F16) return fail(MPG_ERR_UNSUPPORTED, "FP16_F32ACC takes F32 or F16 inputs");
+      break;
+    case MPG_BF16_F32ACC:
+      if (A.dt != MPG_F32 && A.dt != MPG_BF16) return fail(MPG_ERR_UNSUPPORTED, "BF16_F32ACC takes F32 or BF16 inputs");
+      break;
+    default:
+      if (A.dt != MPG_F32) return fail(MPG_ERR_UNSUPPORTED, "this precision mode takes F32 inputs");
+  }
+  // leading dimensions (layout contract)
+  const int64_t a_min = (A.layout == MPG_ROW_MAJOR) ? std::max<int64_t>(k, 1) : std::max<int64_t>(m, 1);
+  const int64_t b_min = (B.layout == MPG_ROW_MAJOR) ? std::max<int64_t>(n, 1) : std::max<int64_t>(k, 1);
+  if (A.ld < a_min) return fail(MPG_ERR_INVALID_ARG, "lda=%lld smaller than %lld", (long long)A.ld, (long long)a_min);
+  if (B.ld < b_min) return fail(MPG_ERR_INVALID_ARG, "ldb=%lld smaller than %lld", (long long)B.ld, (long long)b_min);
+  if (ldc < std::max<int64_t>(n, 1)) return fail(MPG_ERR_INVALID_ARG, "ldc=%lld smaller than n", (long long)ldc);
+  if (A.stride < 0 || B.stride < 0 || strideC < 0) return fail(MPG_ERR_INVALID_ARG, "negative batch stride");
+  if (o.split_exp_a < -100 || o.split_exp_a > 100 || o.split_exp_b < -100 || o.split_exp_b > 100)
+    return fail(MPG_ERR_INVALID_ARG, "split exponent outside [-100, 100]");
+  if (o.splitk < 0) return fail(MPG_ERR_INVALID_ARG, "negative splitk");
+  if (o.wait_timeout_ns < 0) return fail(MPG_ERR_INVALID_ARG, "negative wait timeout");
+  if (m == 0 || n == 0 || batch == 0) return MPG_OK;
+  if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
+  if (reinterpret_cast<uintptr_t>(C) % 4 != 0) return fail(MPG_ERR_INVALID_ARG, "C not 4-byte aligned");
+  if (k > 0 && alpha != 0.0f) {
+    if (!A.ptr || !B.ptr) return fail(MPG_ERR_INVALID_ARG, "A or B is NULL");
+    if (reinterpret_cast<uintptr_t>(A.ptr) % elem_bytes(A.dt) != 0 ||
+        reinterpret_cast<uintptr_t>(B.ptr) % elem_bytes(B.dt) != 0)
+      return fail(MPG_ERR_INVALID_ARG, "A or B not aligned to its element size");
+  }
+  return MPG_OK;
+}
+
+void resolve_options(const mpg_options* opt, mpg_options* o) {
+  mpg_options_init(o);
+  if (opt) *o = *opt;
+}
+
+CUtensorMapDataType tma_dtype(mpg_dtype t) {
+  return t == MPG_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                      : (t == MPG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+// 3-D map {inner, outer, batch}, box {box_inner, box_outer, 1}, 128B swizzle.
+mpg_status encode_map(CUtensorMap* map, const Operand& x, int64_t inner, int64_t outer, int64_t batch,
+                      int box_inner, int box_outer) {
+  const int64_t es = elem_bytes(x.dt);
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)std::max<int64_t>(batch, 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)(x.ld * es),
+                           (cuuint64_t)(batch > 1 ? x.stride * es : x.ld * es * std::max<int64_t>(outer, 1))};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, tma_dtype(x.dt), 3, const_cast<void*>(x.ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MPG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MPG_OK;
+}
+
+mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, int64_t k, int64_t batch,
+                     const Operand& A, const Operand& B, float* C, int64_t ldc, int64_t strideC, float alpha,
+                     float beta, const mpg_options& o, void* workspace, cudaStream_t stream) {
+  TcKernel kern;
+  if (!mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern))
+    return fail(MPG_ERR_UNSUPPORTED, "no kernel for this configuration");
+  if (kern.smem_bytes > dev->max_smem_optin)
+    return fail(MPG_ERR_UNSUPPORTED, "kernel needs %d bytes of shared memory, device offers %d", kern.smem_bytes,
+                dev->max_smem_optin);
+  // the dynamic shared-memory attribute is set once per kernel per device
+  {
+    const uintptr_t key = reinterpret_cast<uintptr_t>(kern.fn);
+    static std::mutex attr_mu;
+    static const void* done[kMaxDevices][64];
+    static int ndone[kMaxDevices];
+    int devid = (int)(dev - g_devices);
+    std::lock_guard<std::mutex> lock(attr_mu);
+    bool found = false;
+    for (int i = 0; i < ndone[devid]; ++i)
+      if (reinterpret_cast<uintptr_t>(done[devid][i]) == key) found = true;
+    if (!found) {
+      cudaError_t e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kern.smem_bytes);
+      if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      if (ndone[devid] < 64) done[devid][ndone[devid]++] = kern.fn;
+    }
+  }
+
+  TcParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int BK = (plan.src == Src::kTmaDirect) ? (plan.op == Op::kTF32 ? 32 : 64) : 32;
+  const int BM = 128;
+  const int bn = plan.bn;
+  const bool a_mn = (A.layout == MPG_COL_MAJOR);
+  const bool b_mn = (B.layout == MPG_ROW_MAJOR);
+  const int64_t a_stride = A.stride ? A.stride : (a_mn ? k * A.ld : m * A.ld);
+  const int64_t b_stride = B.stride ? B.stride : (b_mn ? k * B.ld : n * B.ld);
+  Operand Ax = A, Bx = B;
+  Ax.stride = a_stride;
+  Bx.stride = b_stride;
+  if (plan.src != Src::kGeneric) {
+    mpg_status s;
+    // staged path: fp32 boxes of 32 elements (128 bytes) per line
+    if (!a_mn) s = encode_map(&p.map_a, Ax, k, m, batch, BK, BM);
+    else s = encode_map(&p.map_a, Ax, m, k, batch, BK, BK);
+    if (s != MPG_OK) return s;
+    if (!b_mn) s = encode_map(&p.map_b, Bx, k, n, batch, BK, bn);
+    else s = encode_map(&p.map_b, Bx, n, k, batch, BK, BK);
+    if (s != MPG_OK) return s;
+  }
+  p.a = A.ptr;
+  p.b = B.ptr;
+  p.lda = A.ld;
+  p.ldb = B.ld;
+  p.stride_a = a_stride;
+  p.stride_b = b_stride;
+  p.c = C;
+  p.ldc = ldc;
+  p.stride_c = strideC ? strideC : m * ldc;
+  p.m = (int32_t)m;
+  p.n = (int32_t)n;
+  p.k = (int32_t)k;
+  p.batch = (int32_t)batch;
+  p.a_mn_major = a_mn;
+  p.b_mn_major = b_mn;
+  p.num_m_blk = (int32_t)((m + BM - 1) / BM);
+  p.num_n_blk = (int32_t)((n + bn - 1) / bn);
+  p.num_k_blk = (int32_t)((k + BK - 1) / BK);
+  int kb_per = (p.num_k_blk + plan.splits - 1) / plan.splits;
+  int splits_eff = (p.num_k_blk + kb_per - 1) / kb_per;
+  p.splits = splits_eff;
+  p.kb_per_split = kb_per;
+  const int64_t tiles = (int64_t)splits_eff * batch * p.num_m_blk * p.num_n_blk;
+  if (tiles > 0x7FFFFFFF) return fail(MPG_ERR_INVALID_ARG, "too many tiles");
+  p.num_tiles = (int32_t)tiles;
+  p.group_m = 16;
+  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (batch == 1 || p.stride_c % 4 == 0);
+  p.partial = splits_eff > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.p_vec_ok = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(workspace) % 16 == 0);
+  const bool split = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit1);
+  const int sa = split ? o.split_exp_a : 0, sb = split ? o.split_exp_b : 0;
+  p.alpha = (float)std::ldexp((double)alpha, -(sa + sb));
+  p.beta = beta;
+  p.scale_a = std::ldexp(1.0f, sa);
+  p.scale_b = std::ldexp(1.0f, sb);
+  p.status = dev->status;
+  p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
+
+  const int grid = (int)std::min<int64_t>(tiles, dev->sm_count);
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(kern.fn, dim3(grid), dim3(kern.block), args, kern.smem_bytes, stream);
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  if (splits_eff > 1) {
+    // the reduction applies alpha (incl. the split scale) and beta
+    e = launch_splitk_reduce(p.partial, splits_eff, C, ldc, p.stride_c, p.m, p.n, p.batch, p.alpha, beta, stream);
+    if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
+  }
+  return MPG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mpg_options_init(mpg_options* opt) {
+  if (!opt) return;
+  std::memset(opt, 0, sizeof(*opt));
+}
+
+int mpg_version(void) { return 100; }
+
+const char* mpg_last_error_string(void) { return t_err.c_str(); }
+
+size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode,
+                               const mpg_options* opt) {
+  mpg_options o;
+  resolve_options(opt, &o);
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || mode == MPG_FP32_FFMA) return 0;
+  DeviceInfo* dev = nullptr;
+  int sm = 152;
+  if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
+  t_err.clear();
+  return splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
+}
+
+mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
+                       int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B, int64_t ldb,
+                       int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout, float* C, int64_t ldc,
+                       int64_t strideC, float alpha, float beta, mpg_precision mode, void* workspace,
+                       size_t workspace_bytes, void* stream, const mpg_options* opt) {
+  t_err.clear();
+  mpg_options o;
+  resolve_options(opt, &o);
+  Operand Aop{A, lda, strideA, a_dtype, a_layout};
+  Operand Bop{B, ldb, strideB, b_dtype, b_layout};
+  mpg_status s = validate(m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, mode, o);
+  if (s != MPG_OK) return s;
+  if (m == 0 || n == 0 || batch == 0) return MPG_OK;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return fail(MPG_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  if (!workspace) workspace_bytes = 0;
+  DeviceInfo* dev = nullptr;
+  s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  Plan plan;
+  s = make_plan(m, n, k, batch, Aop, Bop, alpha, mode, o, dev->sm_count, workspace_bytes, &plan);
+  if (s != MPG_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t sc = strideC ? strideC : m * ldc;
+  cudaError_t e = cudaSuccess;
+  switch (plan.kind) {
+    case Kind::kNoop:
+      return MPG_OK;
+    case Kind::kScale:
+      e = launch_scale_c(C, ldc, sc, (int32_t)m, (int32_t)n, (int32_t)batch, beta, st);
+      break;
+    case Kind::kFfma: {
+      FfmaParams fp;
+      fp.a = static_cast<const float*>(A);
+      fp.b = static_cast<const float*>(B);
+      fp.c = C;
+      fp.lda = lda;
+      fp.ldb = ldb;
+      fp.ldc = ldc;
+      fp.a_col_major = (a_layout == MPG_COL_MAJOR);
+      fp.b_col_major = (b_layout == MPG_COL_MAJOR);
+      fp.stride_a = strideA ? strideA : (fp.a_col_major ? k * lda : m * lda);
+      fp.stride_b = strideB ? strideB : (fp.b_col_major ? n * ldb : k * ldb);
+      fp.stride_c = sc;
+      fp.m = (int32_t)m;
+      fp.n = (int32_t)n;
+      fp.k = (int32_t)k;
+      fp.batch = (int32_t)batch;
+      fp.alpha = alpha;
+      fp.beta = beta;
+      e = launch_ffma(fp, st);
+      break;
+    }
+    case Kind::kTc:
+      return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
+  }
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
+mpg_status mpg_gemm(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda, int64_t strideA,
+                    mpg_dtype a_dtype, mpg_layout a_layout, const void* B, int64_t ldb, int64_t strideB,
+                    mpg_dtype b_dtype, mpg_layout b_layout, float* C, int64_t ldc, int64_t strideC, float alpha,
+                    float beta, mpg_precision mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout, C,
+                     ldc, strideC, alpha, beta, mode, workspace, workspace_bytes, stream, nullptr);
+}
+
+mpg_status mpg_device_status(void* stream) {
+  t_err.clear();
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const uint32_t zero = 0;
+    cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (word & kStatusTimeout) return fail(MPG_ERR_TIMEOUT, "a kernel gave up a bounded wait (status 0x%x)", word);
+    return fail(MPG_ERR_CUDA, "device status 0x%x", word);
+  }
+  return MPG_OK;
+}
+
+mpg_status mpg_probe_mma_m16n8k16(const void* A, const void* B, float* D, void* stream) {
+  t_err.clear();
+  if (!A || !B || !D) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = launch_probe_mma(A, B, D, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
+mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
+  t_err.clear();
+  if (timeout_ns < 1000000 || timeout_ns > 10000000000ll)
+    return fail(MPG_ERR_INVALID_ARG, "timeout_ns outside [1 ms, 10 s]");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_selftest_wait(dev->status, (uint64_t)timeout_ns, st);
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+  return mpg_device_status(stream);
+}
+
+}  // extern "C"

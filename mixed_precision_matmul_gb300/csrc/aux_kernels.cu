@@ -1,0 +1,136 @@
+// Small kernels around the main product: the device status word, C = beta*C
+// (k == 0 or alpha == 0), the split-K reduction, the mma.sync m16n8k16
+// accumulator-layout probe and the bounded-wait self test.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mpg {
+
+// One status word per device (a module global: every device that loads the
+// library holds its own copy).
+__device__ uint32_t g_status_word;
+
+uint32_t* status_word_ptr() {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<uint32_t*>(ptr);
+}
+
+namespace {
+
+__global__ void scale_c_kernel(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
+                               float beta) {
+  const int64_t per = (int64_t)m * n;
+  const int64_t total = per * batch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / per;
+    const int64_t r = (i - b * per) / n;
+    const int64_t col = i - b * per - r * n;
+    float* dst = c + b * stride_c + r * ldc + col;
+    *dst = (beta != 0.0f) ? beta * *dst : 0.0f;
+  }
+}
+
+// out = alpha * (partial[0] + partial[1] + ... ) + beta * C, partial sums
+// added in split order.
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int32_t splits, float* c, int64_t ldc,
+                                     int64_t stride_c, int32_t m, int32_t n, int32_t batch, float alpha,
+                                     float beta) {
+  const int64_t per = (int64_t)m * n;
+  const int64_t total = per * batch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    float s = partial[i];
+    for (int sp = 1; sp < splits; ++sp) s += partial[(int64_t)sp * total + i];
+    const int64_t b = i / per;
+    const int64_t r = (i - b * per) / n;
+    const int64_t col = i - b * per - r * n;
+    float* dst = c + b * stride_c + r * ldc + col;
+    *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * s) : alpha * s;
+  }
+}
+
+// One warp, one mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32.
+// Operand fragments gathered per the PTX ISA layouts (groupID = lane/4,
+// threadID_in_group = lane%4):
+//   A (16x16 row): a0 = A[g][2t..2t+1], a1 = A[g+8][2t..], a2 = A[g][2t+8..], a3 = A[g+8][2t+8..]
+//   B (16x8 col):  b0 = B[2t..2t+1][g], b1 = B[2t+8..2t+9][g]
+// The accumulator fragment is written out unscattered: D[lane*4 + j].
+__global__ void probe_mma_kernel(const unsigned short* __restrict__ A, const unsigned short* __restrict__ B,
+                                 float* __restrict__ D) {
+  const int lane = threadIdx.x;
+  const int g = lane >> 2, t = lane & 3;
+  auto pack = [](unsigned short lo, unsigned short hi) { return (uint32_t)lo | ((uint32_t)hi << 16); };
+  const uint32_t a0 = pack(A[g * 16 + 2 * t], A[g * 16 + 2 * t + 1]);
+  const uint32_t a1 = pack(A[(g + 8) * 16 + 2 * t], A[(g + 8) * 16 + 2 * t + 1]);
+  const uint32_t a2 = pack(A[g * 16 + 2 * t + 8], A[g * 16 + 2 * t + 9]);
+  const uint32_t a3 = pack(A[(g + 8) * 16 + 2 * t + 8], A[(g + 8) * 16 + 2 * t + 9]);
+  // B column-major: element (k, n) at n*16 + k
+  const uint32_t b0 = pack(B[g * 16 + 2 * t], B[g * 16 + 2 * t + 1]);
+  const uint32_t b1 = pack(B[g * 16 + 2 * t + 8], B[g * 16 + 2 * t + 9]);
+  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  D[lane * 4 + 0] = d0;
+  D[lane * 4 + 1] = d1;
+  D[lane * 4 + 2] = d2;
+  D[lane * 4 + 3] = d3;
+}
+
+// A single bounded wait on an mbarrier that nothing arrives at: the wait must
+// expire, record the timeout in the status word and let the kernel return.
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl c;
+    c.abort = &abort_flag;
+    c.status = status;
+    c.limit_ns = limit_ns;
+    (void)mbar_wait(&bar, 0, c);
+  }
+  __syncthreads();
+}
+
+int grid_for(int64_t total) {
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return blocks < 1 ? 1 : (int)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_scale_c(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
+                           float beta, cudaStream_t stream) {
+  scale_c_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(c, ldc, stride_c, m, n, batch, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c, int64_t ldc, int64_t stride_c,
+                                 int32_t m, int32_t n, int32_t batch, float alpha, float beta,
+                                 cudaStream_t stream) {
+  splitk_reduce_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(partial, splits, c, ldc, stride_c, m,
+                                                                                  n, batch, alpha, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_t stream) {
+  probe_mma_kernel<<<1, 32, 0, stream>>>(static_cast<const unsigned short*>(a),
+                                         static_cast<const unsigned short*>(b), d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mpg

@@ -1,0 +1,109 @@
+// Internal structures shared between the host planner (api.cu) and the kernel
+// translation units.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mpg {
+
+// Where the operands of the tensor-core kernel come from.
+enum class Src : int {
+  kTmaDirect = 0,  // TMA straight into the MMA operand stages (16-bit or tf32 data)
+  kTmaStaged = 1,  // TMA of fp32 into staging buffers, converter warps -> fp16/bf16 stages
+  kGeneric = 2,    // converter warps load from global memory (any alignment)
+};
+
+// What the converter does to each fp32 (or 16-bit) element.
+enum class Conv : int {
+  kNone = 0,      // operand used as stored (direct path, or a plain copy)
+  kRoundF16 = 1,  // fp32 -> fp16 round-to-nearest-even
+  kRoundBF16 = 2, // fp32 -> bf16 round-to-nearest-even
+  kSplit3 = 3,    // fp32 -> hi, lo*2^11; three accumulator chains
+  kSplit1 = 4,    // fp32 -> hi, lo; one shared accumulator chain
+};
+
+// Bits of the device status word.
+enum : uint32_t {
+  kStatusTimeout = 1u << 0,  // some bounded wait expired
+  kStatusBadArg = 1u << 1,   // a kernel saw arguments it cannot honour
+};
+
+// Element type the tensor core consumes.
+enum class Op : int { kF16 = 0, kBF16 = 1, kTF32 = 2 };
+
+// Storage type of the source operand.
+enum class SrcT : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+struct TcParams {
+  CUtensorMap map_a;  // used by the TMA paths only
+  CUtensorMap map_b;
+  const void* a;      // generic path addressing (element units of the source type)
+  const void* b;
+  int64_t lda, ldb, stride_a, stride_b;
+  float* c;
+  int64_t ldc, stride_c;
+  float* partial;     // split-K partial sums [split][batch][m][n] (ld = n), or null
+  int32_t m, n, k, batch;
+  int32_t a_mn_major, b_mn_major;  // 1: operand stored with M (resp. N) contiguous
+  int32_t num_m_blk, num_n_blk, num_k_blk;
+  int32_t splits, kb_per_split;
+  int32_t num_tiles;
+  int32_t group_m;
+  int32_t c_vec_ok;   // C base 16-byte aligned and ldc % 4 == 0
+  int32_t p_vec_ok;   // partial buffer: n % 4 == 0
+  float alpha;        // already multiplied by 2^-(split_exp_a + split_exp_b)
+  float beta;
+  float scale_a, scale_b;  // 2^split_exp_a, 2^split_exp_b (split converter)
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+struct LaunchInfo {
+  int grid;
+  int block;
+  int smem_bytes;
+};
+
+// One instantiated tensor-core kernel: its launch shape and entry.
+struct TcKernel {
+  const void* fn;
+  int block;
+  int smem_bytes;
+  int bn;
+};
+
+// Look up the tensor-core kernel for a configuration; returns false if this
+// combination is not instantiated.
+bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out);
+
+// Plain fp32 FFMA comparator.
+struct FfmaParams {
+  const float* a;
+  const float* b;
+  float* c;
+  int64_t lda, ldb, ldc, stride_a, stride_b, stride_c;
+  int32_t m, n, k, batch;
+  int32_t a_col_major, b_col_major;
+  float alpha, beta;
+};
+cudaError_t launch_ffma(const FfmaParams& p, cudaStream_t stream);
+
+// C = beta * C (beta == 0: C = 0 without reading it).
+cudaError_t launch_scale_c(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
+                           float beta, cudaStream_t stream);
+
+// C = alpha * sum_s partial[s] + beta * C, partial laid out [split][batch][m][n].
+cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c, int64_t ldc, int64_t stride_c,
+                                 int32_t m, int32_t n, int32_t batch, float alpha, float beta,
+                                 cudaStream_t stream);
+
+cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_t stream);
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Device status word of the current device (allocated by the runtime as a
+// module global; one per device).
+uint32_t* status_word_ptr();
+
+}  // namespace mpg

@@ -1,0 +1,624 @@
+// The tensor-core product C = alpha*A*B + beta*C for sm_103a.
+//
+// One persistent, warp-specialised kernel template:
+//   warp 0       TMA producer (direct and staged paths)
+//   warp 1       TMEM allocator and the single thread that issues tcgen05.mma
+//   warps 2..5   epilogue: tcgen05.ld -> chain sum -> alpha/beta -> stores
+//   warps 6..13  converters (staged and generic paths): fp32 -> fp16/bf16 or
+//                the hi/lo split, written into the swizzled operand stages
+//
+// The accumulator lives in TMEM for the whole K loop (the register/accumulator
+// residency of "tile_matmul(): use the cuBLASDx register-accumulator API ...",
+// "Proposed change"); operand stages use the 128-byte (64-byte for 64-byte
+// lines) swizzled layouts so the tensor core reads them without bank
+// conflicts ("... suggested (swizzled) shared layouts").  The hi/lo chains of
+// the split modes follow "qsa_prompt_attn: ... keep the hi and lo halves in
+// separate accumulator chains", section "The fix".
+//
+// Accumulator layout (M = 128, cta_group::1): row i of the tile is TMEM lane i,
+// column j is TMEM column (buffer base + j).  Warp w reads lanes 32*(w%4) ..
+// 32*(w%4)+31 with tcgen05.ld.32x32b.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mpg {
+
+template <Src S, Conv CV, Op O, SrcT ST, int BN_>
+struct TcTraits {
+  static constexpr Src kSrc = S;
+  static constexpr Conv kConv = CV;
+  static constexpr Op kOp = O;
+  static constexpr SrcT kSrcT = ST;
+  static constexpr int BM = 128;
+  static constexpr int BN = BN_;
+  static constexpr int kOpBytes = (O == Op::kTF32) ? 4 : 2;
+  // k elements per stage: 128-byte lines for the direct path, 32 elements
+  // (one 128-byte line of fp32 source) for the converter paths.
+  static constexpr int BK = (S == Src::kTmaDirect) ? (128 / kOpBytes) : 32;
+  static constexpr int kRowBytes = BK * kOpBytes;  // 128 or 64
+  static constexpr uint32_t kSwizzle = (kRowBytes == 128) ? kSwizzle128B : kSwizzle64B;
+  static constexpr int kKSteps = kRowBytes / 32;   // MMAs of 32 bytes of K each
+  static constexpr int kInstrK = 32 / kOpBytes;    // 16 (f16/bf16) or 8 (tf32)
+  static constexpr bool kSplit = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
+  static constexpr int kCopies = kSplit ? 2 : 1;
+  static constexpr int kATile = BM * kRowBytes;
+  static constexpr int kBTile = BN * kRowBytes;
+  static constexpr int kOpStage = kCopies * (kATile + kBTile);
+  static constexpr bool kStaged = (S == Src::kTmaStaged);
+  static constexpr bool kHasConv = (S != Src::kTmaDirect);
+  static constexpr int kStgATile = kStaged ? BM * 128 : 0;
+  static constexpr int kStgBTile = kStaged ? BN * 128 : 0;
+  static constexpr int kStgStage = kStgATile + kStgBTile;
+  static constexpr int kBudget = 196 * 1024;
+  static constexpr int kStagesRaw = kBudget / (kOpStage + kStgStage);
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static_assert(kStages >= 2, "pipeline needs two stages");
+  static constexpr int kConvWarps = kHasConv ? 8 : 0;
+  static constexpr int kConvThreads = kConvWarps * 32;
+  static constexpr int kThreads = (6 + kConvWarps) * 32;
+  // TMEM: columns of one accumulator (all chains), buffers, allocation
+  static constexpr int kChainCols = (CV == Conv::kSplit3) ? 3 * BN : BN;
+  static constexpr int kAccStride = kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
+                                    : kChainCols <= 256 ? 256 : 512;
+  static constexpr int kAccBufs = (2 * kAccStride <= 512) ? 2 : 1;
+  static constexpr int kTmemCols = kAccBufs * kAccStride;
+  static constexpr int kEpiBytes = 4 * 32 * 32 * 4;
+  static constexpr int kNumBars = 4 * kStages + 2 * kAccBufs + 1;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kOpStage + kStgStage) + kEpiBytes +
+                                    kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(BN % BK == 0 && BM % BK == 0, "regions of MN-major tiles");
+  static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : (O == Op::kBF16) ? 1u : 2u;
+};
+
+struct TileCoord {
+  int s, b, mb, nb, kb0, kb1;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const TcParams& p, int t) {
+  TileCoord c;
+  const int per_batch = p.num_m_blk * p.num_n_blk;
+  const int per_split = per_batch * p.batch;
+  c.s = t / per_split;
+  int r = t - c.s * per_split;
+  c.b = r / per_batch;
+  r -= c.b * per_batch;
+  const int G = p.group_m;
+  const int group_size = G * p.num_n_blk;
+  const int g = r / group_size;
+  const int first_m = g * G;
+  const int gm = min(G, p.num_m_blk - first_m);
+  const int within = r - g * group_size;
+  c.mb = first_m + within % gm;
+  c.nb = within / gm;
+  c.kb0 = c.s * p.kb_per_split;
+  c.kb1 = min(p.num_k_blk, c.kb0 + p.kb_per_split);
+  return c;
+}
+
+// All lanes of the warp wait; the warp continues only if every lane succeeded.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Waits used at teardown: bounded, but independent of the abort flag, so that
+// copies and MMAs already in flight finish before the CTA releases its
+// shared memory and TMEM.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_test(bar, parity)) return;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// Byte offset of 16-byte chunk `ch` of line `line` in a swizzled tile whose
+// lines are `RB` bytes: 128B pattern XORs chunk bits [4,7) with address bits
+// [7,10); the 64B pattern XORs bits [4,6) with bits [7,9).
+template <int RB>
+__device__ __forceinline__ uint32_t swz_chunk_offset(uint32_t line, uint32_t ch) {
+  if constexpr (RB == 128) {
+    return line * 128u + ((ch ^ (line & 7u)) << 4);
+  } else {
+    return line * 64u + ((ch ^ ((line >> 1) & 3u)) << 4);
+  }
+}
+
+template <class T>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, bool mn_major, int ks) {
+  constexpr uint32_t RB = T::kRowBytes;
+  if (!mn_major) {
+    // K-major: 8-line swizzle atoms stacked along M/N at SBO = 8 lines; the
+    // K step moves the start address by 32 bytes inside the 128/64-byte line.
+    return make_smem_desc(tile_addr + ks * 32u, 16u, 8u * RB, T::kSwizzle);
+  } else {
+    // MN-major: atoms of (RB bytes of M/N) x (8 k-lines); regions of BK lines
+    // repeat along M/N at LBO, 8-line groups along K at SBO.
+    return make_smem_desc(tile_addr + ks * (uint32_t)T::kInstrK * RB, (uint32_t)T::BK * RB, 8u * RB, T::kSwizzle);
+  }
+}
+
+// -------------------------------------------------------------------------
+// converter helpers
+// -------------------------------------------------------------------------
+template <SrcT ST>
+struct SrcElem;
+template <>
+struct SrcElem<SrcT::kF32> {
+  using type = float;
+  __device__ static float load(const float* p) { return __ldg(p); }
+};
+template <>
+struct SrcElem<SrcT::kF16> {
+  using type = unsigned short;
+  __device__ static unsigned short load(const unsigned short* p) { return __ldg(p); }
+};
+template <>
+struct SrcElem<SrcT::kBF16> {
+  using type = unsigned short;
+  __device__ static unsigned short load(const unsigned short* p) { return __ldg(p); }
+};
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo_elem, float hi_elem) {
+  __half2 h = __floats2half2_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Split of two fp32 values: hi = fp16(x*s), lo = fp16((x*s - hi) * 2^L).
+// x*s and the residual are exact in fp32 (power-of-two scale; the residual of
+// an 11-bit rounding of a 24-bit significand has at most 13 bits).
+template <int L>
+__device__ __forceinline__ void split_pair(float x0, float x1, float s, uint32_t& hi, uint32_t& lo) {
+  const float y0 = x0 * s, y1 = x1 * s;
+  __half2 h = __floats2half2_rn(y0, y1);
+  const float2 hb = __half22float2(h);
+  const float r0 = y0 - hb.x, r1 = y1 - hb.y;
+  constexpr float kL = (L == 11) ? 2048.0f : 1.0f;
+  __half2 l = __floats2half2_rn(r0 * kL, r1 * kL);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+// Convert 4 consecutive source values (as fp32 or raw 16-bit codes) of line
+// `lg`, chunk `ch`, and store them into the operand tile(s) at `hi_tile`
+// (and `lo_tile` for the split).
+template <class T>
+__device__ __forceinline__ void emit_chunk(const float (&x)[4], const unsigned short (&h)[4], uint32_t hi_tile,
+                                           uint32_t lo_tile, uint32_t lg, uint32_t ch, float scale,
+                                           bool transpose) {
+  if constexpr (T::kOpBytes == 4) {
+    if (transpose) {
+      // tf32 operands are kept K-major in shared memory: an MN-major source
+      // chunk (k line `lg % BK`, 4 consecutive M/N values) scatters into 4
+      // lines of the K-major tile
+      const uint32_t kline = lg % T::BK;
+      const uint32_t mn0 = (lg / T::BK) * T::BK + ch * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t addr = hi_tile + swz_chunk_offset<128>(mn0 + e, kline >> 2) + ((kline & 3u) << 2);
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(__float_as_uint(x[e])) : "memory");
+      }
+      return;
+    }
+    // tf32 operand: fp32 copied into 128-byte swizzled lines
+    st_shared_v4(hi_tile + swz_chunk_offset<128>(lg, ch), __float_as_uint(x[0]), __float_as_uint(x[1]),
+                 __float_as_uint(x[2]), __float_as_uint(x[3]));
+  } else {
+    // 16-bit operand, 64-byte lines: 4 values = half of a 16-byte chunk
+    const uint32_t off = swz_chunk_offset<64>(lg, ch >> 1) + ((ch & 1u) << 3);
+    if constexpr (T::kConv == Conv::kNone) {
+      st_shared_v2(hi_tile + off, (uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+    } else if constexpr (T::kConv == Conv::kRoundF16) {
+      st_shared_v2(hi_tile + off, pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]));
+    } else if constexpr (T::kConv == Conv::kRoundBF16) {
+      st_shared_v2(hi_tile + off, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    } else {
+      constexpr int L = (T::kConv == Conv::kSplit3) ? 11 : 0;
+      uint32_t h01, l01, h23, l23;
+      split_pair<L>(x[0], x[1], scale, h01, l01);
+      split_pair<L>(x[2], x[3], scale, h23, l23);
+      st_shared_v2(hi_tile + off, h01, h23);
+      st_shared_v2(lo_tile + off, l01, l23);
+    }
+  }
+}
+
+// -------------------------------------------------------------------------
+// the kernel
+// -------------------------------------------------------------------------
+template <class T>
+__global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base (swizzle atoms repeat every 1024 bytes)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* op_base = smem;
+  uint8_t* stg_base = op_base + T::kStages * T::kOpStage;
+  float* epi_base = reinterpret_cast<float*>(stg_base + T::kStages * T::kStgStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_base) + T::kEpiBytes);
+  uint64_t* op_full = bars;                       // operand stage ready for the MMA
+  uint64_t* op_empty = bars + T::kStages;         // operand stage consumed by the MMA
+  uint64_t* stg_full = bars + 2 * T::kStages;     // staging filled by TMA
+  uint64_t* stg_empty = bars + 3 * T::kStages;    // staging read by the converters
+  uint64_t* acc_full = bars + 4 * T::kStages;     // accumulator complete
+  uint64_t* acc_empty = acc_full + T::kAccBufs;   // accumulator drained by the epilogue
+  uint64_t* done_bar = acc_empty + T::kAccBufs;   // all MMAs of this CTA finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < T::kStages; ++i) {
+      if constexpr (T::kHasConv) {
+        mbar_init(&op_full[i], T::kConvThreads);
+      } else {
+        mbar_init(&op_full[i], 1);
+      }
+      mbar_init(&op_empty[i], 1);
+      mbar_init(&stg_full[i], 1);
+      mbar_init(&stg_empty[i], T::kConvThreads > 0 ? T::kConvThreads : 1);
+    }
+    for (int i = 0; i < T::kAccBufs; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, T::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  WaitCtl ctl;
+  ctl.abort = abort_flag;
+  ctl.status = p.status;
+  ctl.limit_ns = p.wait_limit_ns;
+
+  const uint32_t op_smem = smem_addr(op_base);
+  const uint32_t stg_smem = smem_addr(stg_base);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if constexpr (T::kSrc != Src::kGeneric) {
+      if (lane == 0) {
+        tma_prefetch_map(&p.map_a);
+        tma_prefetch_map(&p.map_b);
+        // direct path: TMA into the operand stage (op_full/op_empty);
+        // staged path: TMA into the staging buffer (stg_full/stg_empty)
+        uint64_t* fullb = T::kStaged ? stg_full : op_full;
+        uint64_t* emptyb = T::kStaged ? stg_empty : op_empty;
+        constexpr int kLineBytes = T::kStaged ? 128 : T::kRowBytes;
+        constexpr int kABytes = T::BM * kLineBytes;
+        constexpr int kStageBytes = T::kStaged ? T::kStgStage : T::kOpStage;
+        constexpr int kRegion = T::BK * kLineBytes;  // bytes of one MN-major region
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+          const TileCoord tc = decode_tile(p, t);
+          for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
+            const uint32_t st = it % T::kStages;
+            const uint32_t ph = (it / T::kStages) & 1u;
+            if (!mbar_wait(&emptyb[st], ph ^ 1u, ctl)) { ok = false; break; }
+            uint8_t* dst = (T::kStaged ? stg_base + st * T::kStgStage : op_base + st * T::kOpStage);
+            mbar_arrive_expect_tx(&fullb[st], kStageBytes);
+            const int k0 = kb * T::BK;
+            if (!p.a_mn_major) {
+              tma_load_3d(dst, &p.map_a, &fullb[st], k0, tc.mb * T::BM, tc.b);
+            } else {
+#pragma unroll
+              for (int g = 0; g < T::BM / T::BK; ++g)
+                tma_load_3d(dst + g * kRegion, &p.map_a, &fullb[st], tc.mb * T::BM + g * T::BK, k0, tc.b);
+            }
+            uint8_t* dstb = dst + kABytes;
+            if (!p.b_mn_major) {
+              tma_load_3d(dstb, &p.map_b, &fullb[st], k0, tc.nb * T::BN, tc.b);
+            } else {
+#pragma unroll
+              for (int g = 0; g < T::BN / T::BK; ++g)
+                tma_load_3d(dstb + g * kRegion, &p.map_b, &fullb[st], tc.nb * T::BN + g * T::BK, k0, tc.b);
+            }
+          }
+        }
+        // let copies already issued land before the CTA may exit
+        const uint32_t n_drain = it < (uint32_t)T::kStages ? it : (uint32_t)T::kStages;
+        for (uint32_t i = it - n_drain; i < it; ++i)
+          drain_wait(&fullb[i % T::kStages], (i / T::kStages) & 1u, p.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // shared-memory majorness of the operands: 16-bit tiles keep the
+      // source's majorness; tf32 tiles are always K-major
+      const bool a_mn = (T::kOp == Op::kTF32) ? false : (p.a_mn_major != 0);
+      const bool b_mn = (T::kOp == Op::kTF32) ? false : (p.b_mn_major != 0);
+      uint32_t it = 0, titer = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++titer) {
+        const TileCoord tc = decode_tile(p, t);
+        const uint32_t ab = titer % T::kAccBufs;
+        const uint32_t aph = (titer / T::kAccBufs) & 1u;
+        if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctl)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + ab * T::kAccStride;
+        const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::BN);
+        const uint32_t idesc_2n =
+            make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::kConv == Conv::kSplit3 ? 2 * T::BN : T::BN);
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
+          const uint32_t st = it % T::kStages;
+          const uint32_t ph = (it / T::kStages) & 1u;
+          if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_hi = op_smem + st * T::kOpStage;
+          const uint32_t a_lo = a_hi + T::kATile;                       // split only
+          const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
+          const uint32_t b_lo = b_hi + T::kBTile;                       // split only
+#pragma unroll
+          for (int ks = 0; ks < T::kKSteps; ++ks) {
+            const uint32_t acc = (kb > tc.kb0 || ks > 0) ? 1u : 0u;
+            const uint64_t da_hi = operand_desc<T>(a_hi, a_mn, ks);
+            const uint64_t db_hi = operand_desc<T>(b_hi, b_mn, ks);
+            if constexpr (T::kOp == Op::kTF32) {
+              mma_tf32(d0, da_hi, db_hi, idesc_n, acc);
+            } else if constexpr (T::kConv == Conv::kSplit3) {
+              // [hh | hl] = A_hi * [B_hi | B_lo]  (B_hi and B_lo are adjacent)
+              mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
+              // lh = A_lo * B_hi
+              mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
+            } else if constexpr (T::kConv == Conv::kSplit1) {
+              // one chain: hh, hl and lh all accumulate into the same columns
+              mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+              mma_f16(d0, da_hi, operand_desc<T>(b_lo, b_mn, ks), idesc_n, 1u);
+              mma_f16(d0, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, 1u);
+            } else {
+              mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+            }
+          }
+          mma_commit(&op_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[ab]);
+      }
+      // wait for every MMA this thread issued before TMEM is released
+      mma_commit(done_bar);
+      drain_wait(done_bar, 0, p.wait_limit_ns);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    float* stg = epi_base + (warp - 2) * 1024;
+    const uint32_t stg_addr = smem_addr(stg);
+    uint32_t titer = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++titer) {
+      const TileCoord tc = decode_tile(p, t);
+      const uint32_t ab = titer % T::kAccBufs;
+      const uint32_t aph = (titer / T::kAccBufs) & 1u;
+      if (!warp_wait(&acc_full[ab], aph, ctl)) break;
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + lane_off + ab * T::kAccStride;
+      float* out;
+      int64_t ldo;
+      float alpha, beta;
+      bool vec_ok;
+      if (p.splits > 1) {
+        out = p.partial + ((int64_t)tc.s * p.batch + tc.b) * (int64_t)p.m * p.n;
+        ldo = p.n;
+        alpha = 1.0f;
+        beta = 0.0f;
+        vec_ok = p.p_vec_ok != 0;
+      } else {
+        out = p.c + (int64_t)tc.b * p.stride_c;
+        ldo = p.ldc;
+        alpha = p.alpha;
+        beta = p.beta;
+        vec_ok = p.c_vec_ok != 0;
+      }
+      const int row_base = tc.mb * T::BM + 32 * q;
+#pragma unroll 1
+      for (int cc = 0; cc < T::BN / 32; ++cc) {
+        float v[32];
+        tmem_ld_32cols(tacc + cc * 32, v);
+        if constexpr (T::kConv == Conv::kSplit3) {
+          float u[32], w[32];
+          tmem_ld_32cols(tacc + T::BN + cc * 32, u);
+          tmem_ld_32cols(tacc + 2 * T::BN + cc * 32, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = v[j] + 0x1p-11f * (u[j] + w[j]);
+        } else {
+          tmem_ld_wait();
+        }
+        if (cc == T::BN / 32 - 1) {
+          // this warp's share of the accumulator is now in registers
+          tc_fence_before_sync();
+          mbar_arrive(&acc_empty[ab]);
+        }
+        const int col_base = tc.nb * T::BN + cc * 32;
+        if (row_base >= p.m || col_base >= p.n) continue;
+        // transpose through a per-warp swizzled 32x32 staging tile so that
+        // global stores are row-contiguous
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
+                       __float_as_uint(v[4 * ch + 1]), __float_as_uint(v[4 * ch + 2]),
+                       __float_as_uint(v[4 * ch + 3]));
+        }
+        __syncwarp();
+        if (vec_ok && col_base + 32 <= p.n) {
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + (lane >> 3);
+            const int ch = lane & 7;
+            const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
+            const int grow = row_base + r;
+            if (grow < p.m) {
+              float4* dst = reinterpret_cast<float4*>(out + (int64_t)grow * ldo + col_base + ch * 4);
+              float4 o;
+              if (beta != 0.0f) {
+                const float4 c0 = *dst;
+                o.x = fmaf(beta, c0.x, alpha * x.x);
+                o.y = fmaf(beta, c0.y, alpha * x.y);
+                o.z = fmaf(beta, c0.z, alpha * x.z);
+                o.w = fmaf(beta, c0.w, alpha * x.w);
+              } else {
+                o.x = alpha * x.x;
+                o.y = alpha * x.y;
+                o.z = alpha * x.z;
+                o.w = alpha * x.w;
+              }
+              *dst = o;
+            }
+          }
+        } else {
+          const int gcol = col_base + lane;
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
+            const int grow = row_base + r;
+            if (grow < p.m && gcol < p.n) {
+              float* dst = out + (int64_t)grow * ldo + gcol;
+              *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * x) : alpha * x;
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    if constexpr (T::kHasConv) {
+      const int ct = threadIdx.x - 6 * 32;
+      constexpr int kChunks = (T::BM + T::BN) * 8;  // 4-element chunks per stage
+      constexpr int kPerThread = kChunks / T::kConvThreads;
+      static_assert(kChunks % T::kConvThreads == 0, "chunk split");
+      using SE = SrcElem<T::kSrcT>;
+      using E = typename SE::type;
+      const E* __restrict__ ga = reinterpret_cast<const E*>(p.a);
+      const E* __restrict__ gb = reinterpret_cast<const E*>(p.b);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = decode_tile(p, t);
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
+          const uint32_t st = it % T::kStages;
+          const uint32_t ph = (it / T::kStages) & 1u;
+          if constexpr (T::kStaged) {
+            if (!warp_wait(&stg_full[st], ph, ctl)) { ok = false; break; }
+          }
+          float x[kPerThread][4];
+          unsigned short h[kPerThread][4];
+          const int k0 = kb * T::BK;
+          // ---- gather: staging (TMA-written, 128B-swizzled fp32) or global
+#pragma unroll
+          for (int i = 0; i < kPerThread; ++i) {
+            const int w = ct + i * T::kConvThreads;
+            const bool isA = w < T::BM * 8;
+            const int wl = isA ? w : w - T::BM * 8;
+            const uint32_t lg = wl >> 3, ch = wl & 7;
+            if constexpr (T::kStaged) {
+              const uint32_t base = stg_smem + st * T::kStgStage + (isA ? 0u : (uint32_t)T::kStgATile);
+              const float4 v = ld_shared_f4(base + swz_chunk_offset<128>(lg, ch));
+              x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
+            } else {
+              const bool mn = isA ? p.a_mn_major : p.b_mn_major;
+              const int rows_lim = isA ? p.m : p.n;
+              const int row0 = isA ? tc.mb * T::BM : tc.nb * T::BN;
+              const int64_t ld = isA ? p.lda : p.ldb;
+              const E* g = (isA ? ga : gb) + (int64_t)tc.b * (isA ? p.stride_a : p.stride_b);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                int r, kk;
+                if (!mn) {
+                  r = row0 + (int)lg;
+                  kk = k0 + (int)ch * 4 + e;
+                } else {
+                  r = row0 + (int)(lg / T::BK) * T::BK + (int)ch * 4 + e;
+                  kk = k0 + (int)(lg % T::BK);
+                }
+                const bool in = (r < rows_lim) && (kk < p.k);
+                const int64_t idx = mn ? (int64_t)kk * ld + r : (int64_t)r * ld + kk;
+                if constexpr (T::kSrcT == SrcT::kF32) {
+                  x[i][e] = in ? SE::load(g + idx) : 0.0f;
+                  h[i][e] = 0;
+                } else {
+                  h[i][e] = in ? SE::load(g + idx) : (unsigned short)0;
+                  x[i][e] = 0.0f;
+                }
+              }
+            }
+          }
+          if constexpr (T::kStaged) {
+            // staging data is in registers: hand the buffer back to TMA
+            mbar_arrive(&stg_empty[st]);
+          }
+          if (!warp_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          // ---- convert and scatter into the swizzled operand tiles
+          const uint32_t a_hi = op_smem + st * T::kOpStage;
+          const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
+#pragma unroll
+          for (int i = 0; i < kPerThread; ++i) {
+            const int w = ct + i * T::kConvThreads;
+            const bool isA = w < T::BM * 8;
+            const int wl = isA ? w : w - T::BM * 8;
+            const uint32_t lg = wl >> 3, ch = wl & 7;
+            const uint32_t hi_tile = isA ? a_hi : b_hi;
+            const uint32_t lo_tile = hi_tile + (isA ? (uint32_t)T::kATile : (uint32_t)T::kBTile);
+            emit_chunk<T>(x[i], h[i], hi_tile, lo_tile, lg, ch, isA ? p.scale_a : p.scale_b,
+                          isA ? (p.a_mn_major != 0) : (p.b_mn_major != 0));
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&op_full[st]);
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, T::kTmemCols);
+  }
+}
+
+template <class T>
+bool tc_fill(TcKernel* out) {
+  out->fn = reinterpret_cast<const void*>(&tc_gemm_kernel<T>);
+  out->block = T::kThreads;
+  out->smem_bytes = T::kSmemBytes;
+  out->bn = T::BN;
+  return true;
+}
+
+}  // namespace mpg

@@ -1,0 +1,179 @@
+"""CPU tests of the C ABI: the library loads and exports every declared
+symbol, arguments are validated on the host before anything launches, and the
+host decode of accumulator fragments satisfies the properties its page lists
+(checked against the oracle's independent transcription of the PTX formulas).
+"""
+import ctypes
+
+import pytest
+
+import mixed_precision_matmul_gb300 as mpg
+
+
+@pytest.fixture(scope="module")
+def L():
+    mpg.build()
+    return mpg.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = mpg.header_functions()
+    assert len(names) >= 14
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in mpgemm.h but not exported"
+
+
+def test_version_and_options_init(L):
+    assert L.mpg_version() >= 100
+    o = mpg.options()
+    assert (o.split_exp_a, o.split_exp_b, o.splitk, o.force_generic_load, o.tile_n, o.wait_timeout_ns) == (0,) * 6
+
+
+# ---------------------------------------------------------------- validation
+def _call(m=64, n=64, k=64, batch=1, A=16, lda=64, sA=0, adt=mpg.F32, alay=mpg.ROW_MAJOR,
+          B=16, ldb=64, sB=0, bdt=mpg.F32, blay=mpg.ROW_MAJOR, C=16, ldc=64, sC=0,
+          alpha=1.0, beta=0.0, mode=mpg.TF32, opts=None):
+    return mpg.gemm_raw(m, n, k, batch, A, lda, sA, adt, alay, B, ldb, sB, bdt, blay, C, ldc, sC,
+                        alpha, beta, mode, opts=opts, check=False)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=-1), mpg.ERR_INVALID_ARG),
+    (dict(k=-5), mpg.ERR_INVALID_ARG),
+    (dict(batch=-1), mpg.ERR_INVALID_ARG),
+    (dict(m=2 ** 31), mpg.ERR_INVALID_ARG),
+    (dict(lda=63), mpg.ERR_INVALID_ARG),                           # row-major A needs lda >= k
+    (dict(alay=mpg.COL_MAJOR, m=100, lda=99), mpg.ERR_INVALID_ARG),  # col-major A needs lda >= m
+    (dict(ldb=10), mpg.ERR_INVALID_ARG),
+    (dict(blay=mpg.COL_MAJOR, k=70, lda=70, ldb=69), mpg.ERR_INVALID_ARG),
+    (dict(ldc=63), mpg.ERR_INVALID_ARG),
+    (dict(sA=-1), mpg.ERR_INVALID_ARG),
+    (dict(adt=mpg.F16, bdt=mpg.F16, mode=mpg.TF32), mpg.ERR_UNSUPPORTED),
+    (dict(adt=mpg.BF16, bdt=mpg.BF16, mode=mpg.FP16_F32ACC), mpg.ERR_UNSUPPORTED),
+    (dict(adt=mpg.F16, bdt=mpg.F16, mode=mpg.SPLIT_FP16_3CHAIN), mpg.ERR_UNSUPPORTED),
+    (dict(adt=mpg.F16, bdt=mpg.F32, mode=mpg.FP16_F32ACC), mpg.ERR_UNSUPPORTED),
+    (dict(mode=17), mpg.ERR_UNSUPPORTED),
+    (dict(adt=7), mpg.ERR_INVALID_ARG),
+    (dict(alay=3), mpg.ERR_INVALID_ARG),
+    (dict(C=0), mpg.ERR_INVALID_ARG),
+    (dict(A=0), mpg.ERR_INVALID_ARG),
+    (dict(C=18), mpg.ERR_INVALID_ARG),                             # C not 4-byte aligned
+    (dict(A=18), mpg.ERR_INVALID_ARG),                             # fp32 A not 4-byte aligned
+])
+def test_invalid_arguments_rejected_before_launch(L, kw, expect):
+    assert _call(**kw) == expect
+    assert mpg.last_error() != ""
+
+
+def test_option_ranges_rejected(L):
+    assert _call(opts=mpg.options(split_exp_a=101)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(splitk=-2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(wait_timeout_ns=-1)) == mpg.ERR_INVALID_ARG
+
+
+def test_empty_problems_are_noops_without_a_device(L):
+    # m, n or batch zero: nothing to do, no device needed, NULL pointers fine
+    assert _call(m=0, A=0, B=0, C=0) == mpg.OK
+    assert _call(n=0, A=0, B=0, C=0) == mpg.OK
+    assert _call(batch=0, A=0, B=0, C=0) == mpg.OK
+
+
+def test_alpha_zero_does_not_need_operands(L):
+    # alpha == 0: A and B are not read, so NULL operands pass validation
+    # (the call then needs a device, which this host does not have)
+    st = _call(alpha=0.0, A=0, B=0)
+    assert st in (mpg.OK, mpg.ERR_NO_DEVICE)
+
+
+def test_workspace_size_is_zero_for_large_problems(L):
+    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC) == 0
+    assert mpg.workspace_size(0, 8, 8, 1, mpg.TF32) == 0
+    assert mpg.workspace_size(64, 64, 64, 1, mpg.FP32_FFMA) == 0
+
+
+def test_workspace_size_for_skinny_long_k(L):
+    # 2048 x 128 output over k = 32768 has 16 tiles: split-K wants partials
+    ws = mpg.workspace_size(2048, 128, 32768, 1, mpg.SPLIT_FP16_3CHAIN)
+    assert ws > 0 and ws % (2048 * 128 * 4) == 0
+    ws2 = mpg.workspace_size(2048, 128, 32768, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(splitk=4))
+    assert ws2 == 4 * 2048 * 128 * 4
+
+
+# ---------------------------------------------------------------- acc decode
+def test_acc_coords_matches_oracle_row_col_formula(L, orc):
+    for lane in range(32):
+        for j in range(4):
+            assert mpg.acc_coords(lane, j) == orc.acc_coords(lane, j)
+
+
+def test_acc_bijection_ownership_map(L):
+    seen = {}
+    for lane in range(32):
+        for j in range(4):
+            rc = mpg.acc_coords(lane, j)
+            assert rc not in seen, "overlap"
+            seen[rc] = (lane, j)
+    assert len(seen) == 128 and set(seen) == {(r, c) for r in range(16) for c in range(8)}
+
+
+def test_acc_numeral_equals_row_col(L):
+    for lane in range(32):
+        for j in range(4):
+            r, c = mpg.acc_coords(lane, j)
+            assert mpg.acc_offset(lane, j) == r * 8 + c
+
+
+def test_acc_decode_is_inverse_over_all_points(L):
+    for off in range(128):
+        lane, j = mpg.acc_decode(off)
+        assert mpg.acc_offset(lane, j) == off
+    for lane in range(32):
+        for j in range(4):
+            assert mpg.acc_decode(mpg.acc_offset(lane, j)) == (lane, j)
+    assert mpg.acc_decode(-1) is None and mpg.acc_decode(128) is None
+
+
+def test_fragment_index_split_over_two_digits(L):
+    for lane in range(32):
+        r0, c0 = mpg.acc_coords(lane, 0)
+        assert mpg.acc_coords(lane, 1) == (r0, c0 + 1)
+        assert mpg.acc_coords(lane, 2) == (r0 + 8, c0)
+        assert mpg.acc_coords(lane, 3) == (r0 + 8, c0 + 1)
+
+
+def test_strided_placement_stays_disjoint(L):
+    # four tiles of a 32 x 24 destination with row stride 40: every offset is
+    # hit by at most one (tile, lane, j) and equals (row)*stride + col
+    stride, seen = 40, set()
+    for tr, tc in ((0, 0), (0, 8), (16, 0), (16, 16)):
+        for lane in range(32):
+            for j in range(4):
+                off = mpg.acc_matrix_offset(lane, j, tr, tc, stride, 32 * stride)
+                r, c = mpg.acc_coords(lane, j)
+                assert off == (tr + r) * stride + tc + c
+                assert off not in seen
+                seen.add(off)
+    assert len(seen) == 4 * 128
+
+
+def test_matrix_offset_overflow_and_bounds_rejected(L):
+    assert mpg.acc_matrix_offset(0, 0, 0, 0, 8, 128) == 0
+    assert mpg.acc_matrix_offset(31, 3, 0, 0, 8, 128) == 127
+    assert mpg.acc_matrix_offset(31, 3, 0, 0, 8, 127) is None       # reaches the limit
+    assert mpg.acc_matrix_offset(0, 1, 0, 7, 8, 10 ** 6) is None     # column spills past the row
+    assert mpg.acc_matrix_offset(0, 0, 2 ** 62, 0, 4, 2 ** 63 - 1) is None  # int64 overflow
+    assert mpg.acc_matrix_offset(0, 0, -1, 0, 8, 128) is None
+    assert mpg.acc_matrix_offset(32, 0, 0, 0, 8, 128) is None
+    assert mpg.acc_matrix_offset(0, 4, 0, 0, 8, 128) is None
+
+
+def test_tmem_accumulator_map(L):
+    rows = set()
+    for warp in range(2, 6):
+        for lane in range(32):
+            r, c = mpg.tmem_acc_coords(warp, lane, 5, 64)
+            assert c == 69
+            rows.add(r)
+    assert rows == set(range(128))
+    assert mpg.tmem_acc_coords(0, 32, 0) is None
+    assert mpg.tmem_acc_coords(0, 0, 0, 512) is None

@@ -1,0 +1,66 @@
+"""GPU: fp32 operands converted on load (TMA staging + converter warps):
+fp16 / bf16 rounding and the hi/lo split in its three-chain and one-chain
+forms, against both oracle modes."""
+import pytest
+
+import mixed_precision_matmul_gb300 as mpg
+from helpers import TOL, Case
+
+pytestmark = pytest.mark.gpu
+
+R, Cm = mpg.ROW_MAJOR, mpg.COL_MAJOR
+SHAPES = [
+    (128, 128, 32, R, R, (0, 0, 0), 0),
+    (128, 128, 32, R, Cm, (0, 0, 0), 0),
+    (128, 128, 32, Cm, R, (0, 0, 0), 0),
+    (128, 128, 32, Cm, Cm, (0, 0, 0), 0),
+    (333, 270, 150, R, R, (4, 4, 4), 0),       # ragged tails, padded
+    (140, 300, 72, Cm, R, (8, 0, 4), 64),      # 64-wide tiles
+    (100, 100, 600, R, Cm, (0, 4, 0), 128),    # long K
+]
+
+
+@pytest.mark.parametrize("mode", [mpg.FP16_F32ACC, mpg.BF16_F32ACC])
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES)
+def test_round_on_load_parity(mode, m, n, k, al, bl, pad, tile_n):
+    mpg.build()
+    opts = mpg.options(tile_n=tile_n) if tile_n else None
+    c = Case(m, n, k, mode, a_layout=al, b_layout=bl, pad=pad, alpha=0.5, beta=1.5, opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES)
+def test_split3_parity(m, n, k, al, bl, pad, tile_n):
+    mpg.build()
+    opts = mpg.options(tile_n=tile_n) if tile_n else None
+    c = Case(m, n, k, mpg.SPLIT_FP16_3CHAIN, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=-1.0,
+             opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)
+    assert eR <= TOL["split"], (eR, eQ)
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES[:5])
+def test_split1_parity(m, n, k, al, bl, pad, tile_n):
+    mpg.build()
+    c = Case(m, n, k, mpg.SPLIT_FP16_1CHAIN, a_layout=al, b_layout=bl, pad=pad)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)
+
+
+def test_split_operand_scale():
+    """Operands far below fp16's normal range need the power-of-two operand
+    scale; with it the split stays within the fp32-input error bar."""
+    mpg.build()
+    import synthetic
+    a = synthetic.uniform((1, 200, 300), 71, 0.0, 1e-5)   # ~softmax-sized values
+    b = synthetic.normal((1, 300, 130), 72)
+    opts = mpg.options(split_exp_a=14)
+    c = Case(200, 130, 300, mpg.SPLIT_FP16_3CHAIN, a=a, b=b, opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)

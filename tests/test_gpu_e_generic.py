@@ -1,0 +1,37 @@
+"""GPU: the generic-load path (converter warps read global memory directly),
+used where TMA cannot describe the operands: leading dimensions whose byte
+size is not a multiple of 16, unaligned base pointers, or on request."""
+import pytest
+
+import mixed_precision_matmul_gb300 as mpg
+from helpers import TOL, Case
+
+pytestmark = pytest.mark.gpu
+
+R, Cm = mpg.ROW_MAJOR, mpg.COL_MAJOR
+
+
+@pytest.mark.parametrize("mode,dt", [
+    (mpg.BF16_F32ACC, "bf16"), (mpg.FP16_F32ACC, "f16"), (mpg.TF32, "f32"),
+    (mpg.FP16_F32ACC, "f32"), (mpg.BF16_F32ACC, "f32"),
+    (mpg.SPLIT_FP16_3CHAIN, "f32"), (mpg.SPLIT_FP16_1CHAIN, "f32"),
+])
+@pytest.mark.parametrize("m,n,k,al,bl,pad,force", [
+    (129, 131, 67, R, R, (2, 3, 1), 0),      # odd leading dims: TMA impossible
+    (150, 100, 90, Cm, Cm, (3, 1, 0), 0),
+    (128, 128, 64, R, Cm, (0, 0, 0), 1),     # aligned, generic on request
+    (64, 200, 96, Cm, R, (0, 0, 0), 1),
+])
+def test_generic_parity(mode, dt, m, n, k, al, bl, pad, force):
+    mpg.build()
+    opts = mpg.options(force_generic_load=force)
+    c = Case(m, n, k, mode, in_dtype=dt, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=0.5,
+             dist="normal", opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    if mode == mpg.TF32:
+        assert eR <= TOL["tf32"], eR
+    else:
+        assert eQ <= TOL["q16"], (eR, eQ)
+    if mode == mpg.SPLIT_FP16_3CHAIN:
+        assert eR <= TOL["split"], eR
