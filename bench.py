@@ -1,0 +1,574 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-core product C = alpha*A*B + beta*C on GB300.
+
+Headline workload (the 8192^3 square product the targets are quoted on):
+    M = N = K = 8192, A and B bf16 N(0,1) row-major, C fp32 N(0,1),
+    alpha = 1, beta = 0.5, precision bf16 in / fp32 accumulate.
+One step = one call of the library's product on resident device buffers.
+Per precision mode the line also carries TFLOP/s, the fraction of the tensor
+roofline and the normalised error against the FP64 oracle for the other
+workload shapes (square uniform 256^3, batched 2048 x 64x64x4096, log-uniform
+4096^3, the attention pair, tf32 / fp16 / split / FFMA at 8192^3 or 4096^3).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+        [--no-modes] [--no-cpu]
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU; the value is the sum over ranks of the work divided
+by the slowest rank's time (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s per precision mode, % of GB300 tensor peak; max rel err vs FP64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor-core rates relative to bf16 (nominal ratios: tf32 = 1/2 of bf16)
+RATIO = {"bf16": 1.0, "fp16": 1.0, "tf32": 0.5}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def bf16_tensor_from_codes(torch, codes, device):
+    return torch.from_numpy(codes.view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class Workload:
+    """Inputs on the device plus the host copies the oracle needs."""
+
+    def __init__(self, name, m, n, k, batch, mode_name, A, B, C0, lda, ldb, ldc, sa, sb, sc,
+                 a_layout, b_layout, dt_code, alpha, beta, host, opts=None, algo_bytes=None):
+        self.__dict__.update(locals())
+        del self.__dict__["self"]
+
+    @property
+    def flops(self):
+        return 2.0 * self.m * self.n * self.k * self.batch
+
+
+def make_headline(torch, mpg, synthetic, device):
+    m = n = k = 8192
+    a = synthetic.normal((m, k), synthetic.SEED_A)
+    b = synthetic.normal((k, n), synthetic.SEED_B)
+    c0 = synthetic.normal((m, n), synthetic.SEED_C0)
+    a16 = synthetic.bf16_codes_from_f32(a)
+    b16 = synthetic.bf16_codes_from_f32(b)
+    A = bf16_tensor_from_codes(torch, a16, device)
+    B = bf16_tensor_from_codes(torch, b16, device)
+    C0 = torch.from_numpy(c0).to(device)
+    host = {"a16": a16, "b16": b16, "c0": c0}
+    algo = 2 * m * k + 2 * k * n + 4 * m * n * 2   # A, B read; C read (beta != 0) and written
+    return Workload("gemm_bf16_8192", m, n, k, 1, "bf16", A, B, C0, k, n, n, 0, 0, 0,
+                    mpg.ROW_MAJOR, mpg.ROW_MAJOR, mpg.BF16, 1.0, 0.5, host, algo_bytes=algo)
+
+
+def run_step(mpg, w, C, ws=0, ws_bytes=0, stream=0):
+    mpg.gemm_raw(w.m, w.n, w.k, w.batch, w.A.data_ptr(), w.lda, w.sa, w.dt_code, w.a_layout,
+                 w.B.data_ptr(), w.ldb, w.sb, w.dt_code, w.b_layout, C.data_ptr(), w.ldc, w.sc,
+                 w.alpha, w.beta, mpg.MODE_NAMES[w.mode_name], ws, ws_bytes, stream, w.opts)
+
+
+def time_steps(torch, fn, steps, warmup, stream):
+    """Device time of `steps` back-to-back calls (CUDA events on `stream`)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)  # ms
+
+
+# ---------------------------------------------------------------------------
+# per precision mode (other workload shapes)
+# ---------------------------------------------------------------------------
+def mode_cases(torch, mpg, synthetic, device):
+    """Yield (label, Workload) for the per-mode table; built lazily."""
+    def f32_square(n_, seed_dist, mode_name, b_layout="row"):
+        if seed_dist == "uniform":
+            a = synthetic.uniform((n_, n_), synthetic.SEED_A)
+            b = synthetic.uniform((n_, n_), synthetic.SEED_B)
+        elif seed_dist == "normal":
+            a = synthetic.normal((n_, n_), synthetic.SEED_A)
+            b = synthetic.normal((n_, n_), synthetic.SEED_B)
+        else:
+            a = synthetic.loguniform_signed((n_, n_), synthetic.SEED_A)
+            b = synthetic.loguniform_signed((n_, n_), synthetic.SEED_B)
+        A = torch.from_numpy(a).to(device)
+        if b_layout == "col":
+            B = torch.from_numpy(np.ascontiguousarray(b.T)).to(device)
+            bl, ldb = mpg.COL_MAJOR, n_
+        else:
+            B = torch.from_numpy(b).to(device)
+            bl, ldb = mpg.ROW_MAJOR, n_
+        algo = 4 * n_ * n_ * 2 + 4 * n_ * n_
+        return Workload(f"{seed_dist}_{n_}", n_, n_, n_, 1, mode_name, A, B, None, n_, ldb, n_, 0, 0, 0,
+                        mpg.ROW_MAJOR, bl, mpg.F32, 1.0, 0.0,
+                        {"a": a, "b": b, "b_col": b_layout == "col"}, algo_bytes=algo)
+
+    # C1: 256^3 uniform, four modes
+    for mn in ("fp16", "bf16", "tf32", "split3"):
+        yield f"square256_{mn}", lambda mn=mn: f32_square(256, "uniform", mn)
+    # C3-shaped 8192^3 in the other precisions
+    yield "square8192_tf32", lambda: f32_square(8192, "normal", "tf32", "col")
+    yield "square8192_fp16_onload", lambda: f32_square(8192, "normal", "fp16")
+    # C4: 4096^3 log-uniform: split3 vs split1 vs tf32 vs FFMA (B column-major
+    # so that tf32 takes its direct path; every mode sees the same layout)
+    for mn in ("split3", "split1", "tf32", "ffma"):
+        yield f"loguniform4096_{mn}", lambda mn=mn: f32_square(4096, "loguniform", mn, "col")
+    # C2: batched 2048 x (64x4096 * 4096x64), padded leading dims
+    for mn in ("tf32", "fp16"):
+        yield f"batched2048_{mn}", lambda mn=mn: make_batched(torch, mpg, synthetic, device, mn)
+    # C5: attention pair in split3
+    yield "attention_qkt_split3", lambda: make_attention(torch, mpg, synthetic, device, "qkt")
+    yield "attention_pv_split3", lambda: make_attention(torch, mpg, synthetic, device, "pv")
+
+
+def make_batched(torch, mpg, synthetic, device, mode_name):
+    batch, m, n, k, pad = 2048, 64, 64, 4096, 8
+    lda = ldb = k + pad
+    ldc = n + pad
+    a = np.zeros((batch, m, lda), np.float32)
+    a[:, :, :k] = synthetic.uniform((batch, m, k), synthetic.SEED_A)
+    bt = np.zeros((batch, n, ldb), np.float32)     # B column-major: stored as B^T rows
+    bt[:, :, :k] = synthetic.uniform((batch, n, k), synthetic.SEED_B)
+    A = torch.from_numpy(a).to(device)
+    B = torch.from_numpy(bt).to(device)
+    algo = 4 * batch * (m * k + k * n) + 4 * batch * m * n
+    return Workload(f"batched2048_{mode_name}", m, n, k, batch, mode_name, A, B, None, lda, ldb, ldc,
+                    m * lda, n * ldb, m * ldc, mpg.ROW_MAJOR, mpg.COL_MAJOR, mpg.F32, 1.0, 0.0,
+                    {"a": a, "bt": bt}, algo_bytes=algo)
+
+
+def make_attention(torch, mpg, synthetic, device, which):
+    q, kk, p, v = synthetic.attention_inputs()
+    if which == "qkt":
+        # S = Q K^T: A = Q (2048x128 row-major), B = K^T, i.e. K stored row-major = B column-major
+        A = torch.from_numpy(q).to(device)
+        B = torch.from_numpy(kk).to(device)
+        algo = 4 * (2048 * 128 + 32768 * 128 + 2048 * 32768)
+        return Workload("attention_qkt", 2048, 32768, 128, 1, "split3", A, B, None, 128, 128, 32768,
+                        0, 0, 0, mpg.ROW_MAJOR, mpg.COL_MAJOR, mpg.F32, 1.0, 0.0,
+                        {"a": q, "b": kk.T}, algo_bytes=algo)
+    A = torch.from_numpy(p).to(device)
+    B = torch.from_numpy(v).to(device)
+    algo = 4 * (2048 * 32768 + 32768 * 128 + 2048 * 128)
+    # P holds probabilities (<= 1): lift it into fp16's normal range by 2^14
+    opts = mpg.options(split_exp_a=14)
+    return Workload("attention_pv", 2048, 128, 32768, 1, "split3", A, B, None, 32768, 128, 128,
+                    0, 0, 0, mpg.ROW_MAJOR, mpg.ROW_MAJOR, mpg.F32, 1.0, 0.0,
+                    {"a": p, "b": v, "exp_a": 14}, opts=opts, algo_bytes=algo)
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU baseline leg only)
+# ---------------------------------------------------------------------------
+def cpu_baseline_leg(orc, w, C_gpu_rows, rows, nthreads, quant):
+    """Time the FP64 oracle on the listed rows of a workload (all columns) and
+    return (seconds, max normalised error of the GPU rows against it)."""
+    host = w.host
+    if "a16" in host:
+        a = orc.Bf16(host["a16"][rows])
+        b = orc.Bf16(host["b16"])
+        c0 = host["c0"][rows]
+    else:
+        a = host["a"][rows]
+        b = host["b"]
+        c0 = None
+    t0 = time.perf_counter()
+    ref, den = orc.gemm(a, b, c0, w.alpha, w.beta, quant, quant, nthreads=nthreads)
+    secs = time.perf_counter() - t0
+    return secs, orc.max_rel_err(C_gpu_rows, ref, den)
+
+
+def points_error(orc, w, C_gpu, quant, count=512, seed=5):
+    """Normalised error of sampled output elements against the oracle."""
+    host = w.host
+    g = np.random.Generator(np.random.PCG64(seed))
+    if w.batch > 1:
+        bsel = g.integers(0, w.batch, size=8)
+        worst = 0.0
+        for bi in bsel:
+            rows = g.integers(0, w.m, size=count // 8)
+            cols = g.integers(0, w.n, size=count // 8)
+            ref, den = orc.gemm_points(host["a"][bi], host["bt"][bi], w.k, rows, cols, None, w.alpha,
+                                       w.beta, quant, quant, a_col_major=False, b_col_major=True)
+            got = C_gpu[bi][rows, cols]
+            worst = max(worst, orc.max_rel_err(got, ref, den))
+        return worst
+    rows = g.integers(0, w.m, size=count)
+    cols = g.integers(0, w.n, size=count)
+    s = host.get("exp_a", 0)
+    b = host["b"]
+    ref, den = orc.gemm_points(host["a"], np.ascontiguousarray(b), w.k, rows, cols, None, w.alpha, w.beta,
+                               quant, quant, a_s=s)
+    return orc.max_rel_err(C_gpu[rows, cols], ref, den)
+
+
+# ---------------------------------------------------------------------------
+def ours(args):
+    import torch
+
+    import mixed_precision_matmul_gb300 as mpg
+    import synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    mpg.build()
+    mpg.lib()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    w = make_headline(torch, mpg, synthetic, device)
+    C = w.C0.clone()
+
+    def step():
+        run_step(mpg, w, C, stream=sh)
+
+    # warm-up, then the timed region bracketed by barrier + synchronize
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = mpg.device_status()
+    if status != mpg.OK:
+        raise RuntimeError(f"device status {mpg.STATUS.get(status)} after the timed region")
+
+    ms_per_step = elapsed_ms / args.steps
+    per_rank_tflops = w.flops / (ms_per_step * 1e-3) / 1e12
+    value = per_rank_tflops * world
+    peak_bf16 = peaks["bf16_tflops"]
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64 draws, shapes and distributions of the pages' workloads)",
+        "config": {
+            "workload": "gemm_bf16_8192: C = alpha*A*B + beta*C, M=N=K=8192, A,B bf16 N(0,1) row-major, "
+                        "C fp32 N(0,1), alpha=1, beta=0.5, bf16 in / fp32 accumulate (tcgen05)",
+            "l2": "inputs larger than L2 (A+B+C = 768 MB per step), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "gpu_launches": args.steps,   # one tcgen05 kernel per step at this shape (no split-K)
+        "clocks": clocks,
+        "peaks": {**peaks, "source": peak_src},
+    }
+    # roofline of the dominant kernel (the only kernel of the step)
+    tflops = w.flops / (ms_per_step * 1e-3) / 1e12
+    result["roofline"] = {
+        "bound": "tensor", "achieved": round(tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
+        "frac": round(tflops / peak_bf16, 4), "traffic": NCU_TRAFFIC.get("gemm_bf16_8192"),
+        "algorithmic_bytes": w.algo_bytes,
+        "peak_note": f"bf16 dense, {peak_src} burst (cuBLAS)",
+    }
+
+    # end to end through the public API with host buffers: H2D of A, B, C0
+    # from pinned memory, the product, D2H of C
+    if args.e2e_steps > 0:
+        hA = w.A.cpu().pin_memory()
+        hB = w.B.cpu().pin_memory()
+        hC0 = w.C0.cpu().pin_memory()
+        hC = torch.empty_like(hC0).pin_memory()
+        dA = torch.empty_like(w.A)
+        dB = torch.empty_like(w.B)
+        dC = torch.empty_like(w.C0)
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dC.copy_(hC0, non_blocking=True)
+            mpg.gemm_raw(w.m, w.n, w.k, 1, dA.data_ptr(), w.lda, 0, w.dt_code, w.a_layout,
+                         dB.data_ptr(), w.ldb, 0, w.dt_code, w.b_layout, dC.data_ptr(), w.ldc, 0,
+                         w.alpha, w.beta, mpg.BF16_F32ACC, 0, 0, sh)
+            hC.copy_(dC, non_blocking=True)
+
+        e2e_ms = time_steps(torch, e2e_step, args.e2e_steps, 2, stream) / args.e2e_steps
+        if dist:
+            t = torch.tensor([e2e_ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = (hA.numel() + hB.numel()) * 2 + hC0.numel() * 4
+        result["e2e"] = {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 4,
+                         "ms_per_step": round(e2e_ms, 4)}
+        del hA, hB, hC0, hC, dA, dB, dC
+
+    # per precision mode, other workload shapes (each timed on its own)
+    modes = {}
+    mode_outputs = {}
+    if args.modes and rank == 0:
+        for label, make in mode_cases(torch, mpg, synthetic, device):
+            mw = make()
+            Cm = torch.zeros((mw.batch, mw.m, mw.ldc) if mw.batch > 1 else (mw.m, mw.ldc),
+                             dtype=torch.float32, device=device)
+            ws_bytes = mpg.workspace_size(mw.m, mw.n, mw.k, mw.batch, mpg.MODE_NAMES[mw.mode_name], mw.opts)
+            ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+            iters = max(3, min(50, int(2e12 / max(mw.flops, 1))))
+            ms = time_steps(torch, lambda: run_step(mpg, mw, Cm, ws.data_ptr(), ws_bytes, sh), iters, 3,
+                            stream) / iters
+            tf = mw.flops / (ms * 1e-3) / 1e12
+            entry = {"ms": round(ms, 5), "tflops": round(tf, 2), "shape": [mw.batch, mw.m, mw.n, mw.k]}
+            rate = RATIO.get(mw.mode_name)
+            if rate:
+                entry["frac_of_tensor_peak"] = round(tf / (peak_bf16 * rate), 4)
+            elif mw.mode_name in ("split3", "split1"):
+                issued = 3.0 * tf
+                entry["tensor_issued_tflops"] = round(issued, 2)
+                entry["frac_of_tensor_peak"] = round(issued / peak_bf16, 4)
+            if mw.algo_bytes:
+                entry["gbs"] = round(mw.algo_bytes / (ms * 1e-3) / 1e9, 1)
+                entry["frac_of_hbm_peak"] = round(entry["gbs"] / peaks["hbm_gbs"], 4)
+            modes[label] = entry
+            Ch = Cm.cpu().numpy()
+            mode_outputs[label] = (mw, Ch[..., :mw.n] if mw.batch > 1 else Ch[:, :mw.n])
+            del Cm, ws
+            mw.A = mw.B = None
+            torch.cuda.empty_cache()
+        ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
+        for lbl in ("loguniform4096_split3", "loguniform4096_split1"):
+            if ffma and lbl in modes:
+                modes[lbl]["x_ffma"] = round(modes[lbl]["tflops"] / ffma, 2)
+        result["modes"] = modes
+
+    # CPU baseline: the oracle on a bounded sample of the headline workload
+    if args.cpu and rank == 0:
+        import oracle as orc
+        orc.build()
+        Chost = C.cpu().numpy()   # only its shape matters for the calibration run
+        nthreads = os.cpu_count() or 1
+        # calibrate on one row per thread, then size the sample to ~cpu_seconds
+        cal = np.arange(nthreads)
+        secs_cal, _ = cpu_baseline_leg(orc, w, Chost[cal], cal, nthreads, orc.Q_NONE)
+        nrows = int(max(nthreads, min(2048, nthreads * args.cpu_seconds / max(secs_cal, 1e-3))))
+        rows = np.arange(nrows)
+        # the timed steps fed C back into itself (beta != 0); the oracle's
+        # reference is one product from the original C0
+        C1 = w.C0.clone()
+        run_step(mpg, w, C1, stream=sh)
+        torch.cuda.synchronize()
+        Chost = C1.cpu().numpy()
+        secs, err = cpu_baseline_leg(orc, w, Chost[rows], rows, nthreads, orc.Q_NONE)
+        result["cpu_baseline"] = {
+            "value": round(2.0 * nrows * w.n * w.k / secs / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{nrows} rows x 8192 cols x 8192 k of the headline product (FP64 triple loop), "
+                      f"{secs:.1f} s",
+        }
+        result["max_rel_err"] = {"gemm_bf16_8192": err}
+        # per-mode error against the oracle on sampled outputs (mode R; the
+        # bf16/fp16 modes also against their quantised-input problem)
+        qmap = {"fp16": orc.Q_FP16, "bf16": orc.Q_BF16}
+        for label, (mw, Cg) in mode_outputs.items():
+            eR = points_error(orc, mw, Cg, orc.Q_NONE)
+            modes[label]["max_rel_err_vs_fp64"] = eR
+            if mw.mode_name in qmap:
+                modes[label]["max_rel_err_vs_quantised"] = points_error(orc, mw, Cg, qmap[mw.mode_name])
+        for lbl in ("loguniform4096_split3", "loguniform4096_split1"):
+            if lbl in modes and "loguniform4096_ffma" in modes:
+                f = modes["loguniform4096_ffma"]["max_rel_err_vs_fp64"]
+                modes[lbl]["err_x_ffma"] = round(modes[lbl]["max_rel_err_vs_fp64"] / f, 3) if f else None
+
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def reference(args):
+    """The oracle (FP64 CPU triple loop) timed on this host's cores on the
+    headline workload's configuration, a bounded sample of rows per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as orc
+    import synthetic
+    orc.build()
+    m = n = k = 8192
+    b16 = synthetic.bf16_codes_from_f32(synthetic.normal((k, n), synthetic.SEED_B))
+    a = synthetic.normal((m, k), synthetic.SEED_A)
+    c0 = synthetic.normal((m, n), synthetic.SEED_C0)
+    B = orc.Bf16(b16)
+    nthreads = os.cpu_count() or 1
+
+    def step(i, rows_per_step):
+        r = (np.arange(rows_per_step) + i * rows_per_step) % m
+        A = orc.Bf16(synthetic.bf16_codes_from_f32(a[r]))
+        orc.gemm(A, B, c0[r], 1.0, 0.5, nthreads=nthreads)
+
+    # size each step's sample so the whole run stays within ~ref_seconds
+    t0 = time.perf_counter()
+    step(0, nthreads)
+    per_row = (time.perf_counter() - t0) / nthreads
+    rows_per_step = int(max(1, min(4 * nthreads, args.ref_seconds / (args.steps + args.warmup) / per_row)))
+    for i in range(args.warmup):
+        step(i, rows_per_step)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i, rows_per_step)
+    secs = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * n * k * args.steps
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {
+            "workload": "gemm_bf16_8192: C = alpha*A*B + beta*C, M=N=K=8192, A,B bf16 N(0,1) row-major, "
+                        "C fp32 N(0,1), alpha=1, beta=0.5"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows x 8192 x 8192 per step (FP64 triple loop)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from the ncu capture summarised under profiles/ (None until taken
+# for the current kernel).
+NCU_TRAFFIC = {"gemm_bf16_8192": None}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-modes", dest="modes", action="store_false")
+    ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()
