@@ -203,13 +203,40 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   return v;
 }
 
-// Convert 4 consecutive source values (as fp32 or raw 16-bit codes) of line
-// `lg`, chunk `ch`, and store them into the operand tile(s) at `hi_tile`
-// (and `lo_tile` for the split).
+// Convert 4 consecutive source values (fp32, or raw 16-bit codes) into the
+// 32-bit words the operand tiles hold: for 16-bit operands w[0..1] are the
+// four converted values (hi for the split) and w[2..3] the split's lo; for
+// tf32 operands w[0..3] are the fp32 bits.
 template <class T>
-__device__ __forceinline__ void emit_chunk(const float (&x)[4], const unsigned short (&h)[4], uint32_t hi_tile,
-                                           uint32_t lo_tile, uint32_t lg, uint32_t ch, float scale,
-                                           bool transpose) {
+__device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned short (&h)[4], float scale,
+                                           uint32_t (&w)[4]) {
+  if constexpr (T::kOpBytes == 4) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(x[e]);
+  } else if constexpr (T::kConv == Conv::kNone) {
+    w[0] = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+    w[1] = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
+    w[2] = w[3] = 0;
+  } else if constexpr (T::kConv == Conv::kRoundF16) {
+    w[0] = pack_f16x2(x[0], x[1]);
+    w[1] = pack_f16x2(x[2], x[3]);
+    w[2] = w[3] = 0;
+  } else if constexpr (T::kConv == Conv::kRoundBF16) {
+    w[0] = pack_bf16x2(x[0], x[1]);
+    w[1] = pack_bf16x2(x[2], x[3]);
+    w[2] = w[3] = 0;
+  } else {
+    constexpr int L = (T::kConv == Conv::kSplit3) ? 11 : 0;
+    split_pair<L>(x[0], x[1], scale, w[0], w[2]);
+    split_pair<L>(x[2], x[3], scale, w[1], w[3]);
+  }
+}
+
+// Store one packed chunk (line `lg`, 16-byte source chunk `ch`) into the
+// operand tile(s) at `hi_tile` (and `lo_tile` for the split).
+template <class T>
+__device__ __forceinline__ void store_chunk(const uint32_t (&w)[4], uint32_t hi_tile, uint32_t lo_tile, uint32_t lg,
+                                            uint32_t ch, bool transpose) {
   if constexpr (T::kOpBytes == 4) {
     if (transpose) {
       // tf32 operands are kept K-major in shared memory: an MN-major source
@@ -220,30 +247,17 @@ __device__ __forceinline__ void emit_chunk(const float (&x)[4], const unsigned s
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t addr = hi_tile + swz_chunk_offset<128>(mn0 + e, kline >> 2) + ((kline & 3u) << 2);
-        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(__float_as_uint(x[e])) : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(w[e]) : "memory");
       }
-      return;
+    } else {
+      // tf32 operand: fp32 copied into 128-byte swizzled lines
+      st_shared_v4(hi_tile + swz_chunk_offset<128>(lg, ch), w[0], w[1], w[2], w[3]);
     }
-    // tf32 operand: fp32 copied into 128-byte swizzled lines
-    st_shared_v4(hi_tile + swz_chunk_offset<128>(lg, ch), __float_as_uint(x[0]), __float_as_uint(x[1]),
-                 __float_as_uint(x[2]), __float_as_uint(x[3]));
   } else {
     // 16-bit operand, 64-byte lines: 4 values = half of a 16-byte chunk
     const uint32_t off = swz_chunk_offset<64>(lg, ch >> 1) + ((ch & 1u) << 3);
-    if constexpr (T::kConv == Conv::kNone) {
-      st_shared_v2(hi_tile + off, (uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
-    } else if constexpr (T::kConv == Conv::kRoundF16) {
-      st_shared_v2(hi_tile + off, pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]));
-    } else if constexpr (T::kConv == Conv::kRoundBF16) {
-      st_shared_v2(hi_tile + off, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-    } else {
-      constexpr int L = (T::kConv == Conv::kSplit3) ? 11 : 0;
-      uint32_t h01, l01, h23, l23;
-      split_pair<L>(x[0], x[1], scale, h01, l01);
-      split_pair<L>(x[2], x[3], scale, h23, l23);
-      st_shared_v2(hi_tile + off, h01, h23);
-      st_shared_v2(lo_tile + off, l01, l23);
-    }
+    st_shared_v2(hi_tile + off, w[0], w[1]);
+    if constexpr (T::kSplit) st_shared_v2(lo_tile + off, w[2], w[3]);
   }
 }
 
@@ -537,20 +551,23 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           if constexpr (T::kStaged) {
             if (!warp_wait(&stg_full[st], ph, ctl)) { ok = false; break; }
           }
-          float x[kPerThread][4];
-          unsigned short h[kPerThread][4];
+          uint32_t w[kPerThread][4];
           const int k0 = kb * T::BK;
-          // ---- gather: staging (TMA-written, 128B-swizzled fp32) or global
+          // ---- gather (staging written by TMA, 128B-swizzled fp32; or
+          //      global memory) and convert into packed operand words
 #pragma unroll
           for (int i = 0; i < kPerThread; ++i) {
-            const int w = ct + i * T::kConvThreads;
-            const bool isA = w < T::BM * 8;
-            const int wl = isA ? w : w - T::BM * 8;
+            const int wi = ct + i * T::kConvThreads;
+            const bool isA = wi < T::BM * 8;
+            const int wl = isA ? wi : wi - T::BM * 8;
             const uint32_t lg = wl >> 3, ch = wl & 7;
+            float x[4];
+            unsigned short h[4];
             if constexpr (T::kStaged) {
               const uint32_t base = stg_smem + st * T::kStgStage + (isA ? 0u : (uint32_t)T::kStgATile);
               const float4 v = ld_shared_f4(base + swz_chunk_offset<128>(lg, ch));
-              x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
+              x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+              h[0] = h[1] = h[2] = h[3] = 0;
             } else {
               const bool mn = isA ? p.a_mn_major : p.b_mn_major;
               const int rows_lim = isA ? p.m : p.n;
@@ -570,33 +587,36 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 const bool in = (r < rows_lim) && (kk < p.k);
                 const int64_t idx = mn ? (int64_t)kk * ld + r : (int64_t)r * ld + kk;
                 if constexpr (T::kSrcT == SrcT::kF32) {
-                  x[i][e] = in ? SE::load(g + idx) : 0.0f;
-                  h[i][e] = 0;
+                  x[e] = in ? SE::load(g + idx) : 0.0f;
+                  h[e] = 0;
                 } else {
-                  h[i][e] = in ? SE::load(g + idx) : (unsigned short)0;
-                  x[i][e] = 0.0f;
+                  h[e] = in ? SE::load(g + idx) : (unsigned short)0;
+                  x[e] = 0.0f;
                 }
               }
             }
+            pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, w[i]);
           }
           if constexpr (T::kStaged) {
-            // staging data is in registers: hand the buffer back to TMA
+            // Every staging value has been consumed by the conversion above,
+            // so the reads are complete; order them before the TMA's
+            // (async-proxy) refill of this buffer, then hand it back.
+            fence_proxy_async_smem();
             mbar_arrive(&stg_empty[st]);
           }
           if (!warp_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
-          // ---- convert and scatter into the swizzled operand tiles
+          // ---- scatter into the swizzled operand tiles
           const uint32_t a_hi = op_smem + st * T::kOpStage;
           const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
 #pragma unroll
           for (int i = 0; i < kPerThread; ++i) {
-            const int w = ct + i * T::kConvThreads;
-            const bool isA = w < T::BM * 8;
-            const int wl = isA ? w : w - T::BM * 8;
+            const int wi = ct + i * T::kConvThreads;
+            const bool isA = wi < T::BM * 8;
+            const int wl = isA ? wi : wi - T::BM * 8;
             const uint32_t lg = wl >> 3, ch = wl & 7;
             const uint32_t hi_tile = isA ? a_hi : b_hi;
             const uint32_t lo_tile = hi_tile + (isA ? (uint32_t)T::kATile : (uint32_t)T::kBTile);
-            emit_chunk<T>(x[i], h[i], hi_tile, lo_tile, lg, ch, isA ? p.scale_a : p.scale_b,
-                          isA ? (p.a_mn_major != 0) : (p.b_mn_major != 0));
+            store_chunk<T>(w[i], hi_tile, lo_tile, lg, ch, isA ? (p.a_mn_major != 0) : (p.b_mn_major != 0));
           }
           fence_proxy_async_smem();
           mbar_arrive(&op_full[st]);

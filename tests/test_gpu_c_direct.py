@@ -87,3 +87,48 @@ def test_tf32_operand_rounding_model(orc, capsys):
     with capsys.disabled():
         print(f"\n[tf32 operand model] matches: {match}")
     assert match, "the tf32 result matches none of the rounding models"
+
+
+def _round_rz(x64):
+    """binary64 -> fp32 rounded toward zero."""
+    f = x64.astype(np.float32)
+    up = np.abs(f.astype(np.float64)) > np.abs(x64)
+    f[up] = np.nextafter(f[up], np.float32(0))
+    return f
+
+
+def test_accumulator_rounding_model(capsys):
+    """How the tensor core rounds its fp32 accumulator between MMA
+    instructions.  The first instruction loads 2^20-sized values, every later
+    one adds 16*c_j with c_j = 1 + j/1024, whose fraction is below the
+    accumulator's ulp (1/8): round-to-nearest and truncation then part ways.
+    The result is compared with both models, each applied once per
+    instruction (16 products summed exactly, then rounded into fp32)."""
+    mpg.build()
+    m, n, steps = 128, 64, 64
+    k = 16 * steps
+    a = np.ones((m, k), np.float32)
+    cj = (1.0 + np.arange(n) / 1024.0).astype(np.float32)
+    b = np.tile(cj, (k, 1)).astype(np.float32)
+    b[:16, :] = 65504.0
+    c = Case(m, n, k, mpg.FP16_F32ACC, in_dtype="f16", a_layout=R, b_layout=Cm, a=a, b=b,
+             c0=np.zeros((m, n), np.float32))
+    c.run()
+    got = c.result()[0][0].astype(np.float64)
+    assert np.all(c.result()[0] == got.astype(np.float32))   # every row the same
+    first = 16.0 * 65504.0
+    s = 16.0 * cj.astype(np.float64)
+    d_rn = np.full(n, first, np.float32)
+    d_rz = np.full(n, first, np.float32)
+    for _ in range(steps - 1):
+        d_rn = (d_rn.astype(np.float64) + s).astype(np.float32)
+        d_rz = _round_rz(d_rz.astype(np.float64) + s)
+    exact = first + (steps - 1) * s
+    match = [name for name, d in (("round-to-nearest", d_rn), ("truncation", d_rz))
+             if np.array_equal(d.astype(np.float64), got)]
+    with capsys.disabled():
+        print(f"\n[fp32 accumulator model] matches: {match}; max |got-exact| = "
+              f"{np.max(np.abs(got - exact)):.4g}, rn {np.max(np.abs(d_rn - exact)):.4g}, "
+              f"rz {np.max(np.abs(d_rz - exact)):.4g}")
+    # both models bound the error by one ulp per instruction
+    assert np.max(np.abs(got - exact)) <= (steps - 1) * 0.125

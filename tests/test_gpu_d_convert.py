@@ -64,3 +64,22 @@ def test_split_operand_scale():
     c.run()
     eR, eQ = c.errors()
     assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
+
+
+@pytest.mark.parametrize("mode", [mpg.FP16_F32ACC, mpg.BF16_F32ACC, mpg.SPLIT_FP16_3CHAIN,
+                                  mpg.SPLIT_FP16_1CHAIN])
+@pytest.mark.parametrize("tile_n", [64, 128])
+def test_many_tiles_per_persistent_cta(mode, tile_n):
+    """2048 x 2048 tiles over 152 persistent CTAs: every CTA walks many tiles
+    through the staging / operand rings and both accumulator buffers (the
+    regime where a staging buffer handed back to TMA too early showed up)."""
+    import numpy as np
+    import oracle
+    from helpers import MODE_Q
+    mpg.build()
+    c = Case(2048, 2048, 512, mode, b_layout=Cm, opts=mpg.options(tile_n=tile_n))
+    c.run()
+    C = c.result()
+    rows = np.array([0, 1, 127, 128, 1000, 1500, 2047])
+    ref, den = oracle.gemm(c.a[0][rows], c.b[0], c.c0[0][rows], 1.0, 0.0, MODE_Q[mode], MODE_Q[mode])
+    assert oracle.max_rel_err(C[0][rows], ref, den) <= TOL["q16"]
