@@ -154,6 +154,36 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch,
                        void* workspace, size_t workspace_bytes, void* stream,
                        const mpg_options* opt);
 
+/* The product for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is a convenience of this library.  Some
+ * callers cannot call cudaMalloc and so cannot hand mpg_gemm a workspace:
+ * plugins inside a host framework that owns all device memory and forbids
+ * raw allocations, and real-time or long-running services that allow no
+ * allocation (and no allocation failure) after start-up.  This entry point
+ * takes the same arguments as
+ * mpg_gemm_ex minus the workspace; when the problem is split along K, the
+ * partial sums go to a scratch array compiled into the library
+ * (MPG_NOALLOC_SCRATCH_BYTES = 16 MiB of device memory, present on every GPU
+ * that loads the library until the process exits).  It allocates nothing.
+ *   - Problems whose split-K partial sums would exceed that size (splits x
+ *     batch x m x n x 4 bytes) are rejected with MPG_ERR_WORKSPACE before
+ *     anything is launched; use mpg_gemm with a workspace for those.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one scratch array, and each call
+ *     overwrites the part it uses: calls that can overlap on the GPU
+ *     (different streams without ordering) race.  Order them on one stream.
+ * Results equal mpg_gemm_ex's for the same arguments and options. */
+#define MPG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
+                            const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
+                            const void* B, int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                            float* C, int64_t ldc, int64_t strideC,
+                            float alpha, float beta, mpg_precision mode, void* stream,
+                            const mpg_options* opt);
+
 /* Bytes of workspace mpg_gemm / mpg_gemm_ex need for this problem (0 if none).
  * Depends only on the sizes, the mode, the options and the current device. */
 size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,

@@ -95,6 +95,8 @@ def lib():
         L.mpg_gemm.restype = i32
         L.mpg_gemm_ex.argtypes = gemm_args + [ctypes.POINTER(Options)]
         L.mpg_gemm_ex.restype = i32
+        L.mpg_gemm_noalloc.argtypes = gemm_args[:20] + [vp, ctypes.POINTER(Options)]
+        L.mpg_gemm_noalloc.restype = i32
         L.mpg_gemm_workspace_size.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options)]
         L.mpg_gemm_workspace_size.restype = sz
         L.mpg_options_init.argtypes = [ctypes.POINTER(Options)]
@@ -162,6 +164,20 @@ def gemm_raw(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB
     st = lib().mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype,
                            b_layout, C, ldc, strideC, float(alpha), float(beta), mode, workspace or None,
                            workspace_bytes, stream or None, ctypes.byref(opts) if opts is not None else None)
+    if check:
+        _check(st)
+    return st
+
+
+def gemm_noalloc_raw(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype,
+                     b_layout, C, ldc, strideC, alpha, beta, mode, stream=0,
+                     opts: Options | None = None, check: bool = True) -> int:
+    """mpg_gemm_noalloc: the product without a workspace argument, for callers
+    that cannot allocate device memory (split-K partial sums go to the
+    library's fixed 16 MiB static scratch; larger needs are rejected)."""
+    st = lib().mpg_gemm_noalloc(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype,
+                                b_layout, C, ldc, strideC, float(alpha), float(beta), mode, stream or None,
+                                ctypes.byref(opts) if opts is not None else None)
     if check:
         _check(st)
     return st

@@ -419,6 +419,43 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   return MPG_OK;
 }
 
+// Scratch of mpg_gemm_noalloc: split-K partial sums for callers that cannot
+// allocate.  A module global, so every device that loads the library holds
+// one copy.  In host code this name is only a stand-in for the symbol, never
+// a device address: the address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_scratch[MPG_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+struct NoallocSlot {
+  bool ready = false;
+  void* ptr = nullptr;
+};
+NoallocSlot g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached.
+mpg_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(MPG_ERR_NO_DEVICE, "no current CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocSlot& slot = g_noalloc[dev];
+  if (!slot.ready) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return fail(MPG_ERR_CUDA, "cannot resolve the static scratch on device %d: %s", dev, cudaGetErrorString(e));
+    }
+    slot.ptr = ptr;
+    slot.ready = true;
+  }
+  *out = slot.ptr;
+  return MPG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -553,6 +590,41 @@ mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
   cudaError_t e = launch_selftest_wait(dev->status, (uint64_t)timeout_ns, st);
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
   return mpg_device_status(stream);
+}
+
+mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
+                            int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B, int64_t ldb,
+                            int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout, float* C, int64_t ldc,
+                            int64_t strideC, float alpha, float beta, mpg_precision mode, void* stream,
+                            const mpg_options* opt) {
+  t_err.clear();
+  mpg_options o;
+  resolve_options(opt, &o);
+  Operand Aop{A, lda, strideA, a_dtype, a_layout};
+  Operand Bop{B, ldb, strideB, b_dtype, b_layout};
+  mpg_status s = validate(m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, mode, o);
+  if (s != MPG_OK) return s;
+  if (m == 0 || n == 0 || batch == 0) return MPG_OK;
+  DeviceInfo* dev = nullptr;
+  s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  // the split-K scratch this problem needs (the same choice mpg_gemm makes)
+  size_t need = 0;
+  if (k > 0 && alpha != 0.0f && mode != MPG_FP32_FFMA)
+    need = splitk_bytes(choose_splits(m, n, k, batch, dev->sm_count, o), m, n, batch);
+  if (need > MPG_NOALLOC_SCRATCH_BYTES)
+    return fail(MPG_ERR_WORKSPACE,
+                "split-K partial sums need %zu bytes, more than the %u-byte static scratch of "
+                "mpg_gemm_noalloc; call mpg_gemm with a workspace instead",
+                need, (unsigned)MPG_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (need > 0) {
+    s = noalloc_scratch(&scratch);
+    if (s != MPG_OK) return s;
+  }
+  return mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout, C,
+                     ldc, strideC, alpha, beta, mode, scratch, need > 0 ? (size_t)MPG_NOALLOC_SCRATCH_BYTES : 0,
+                     stream, opt);
 }
 
 }  // extern "C"
