@@ -63,7 +63,8 @@ typedef enum { MPG_F32 = 0, MPG_F16 = 1, MPG_BF16 = 2 } mpg_dtype;
  *   SPLIT_FP16_3CHAIN  fp32 inputs split on load into fp16 hi/lo halves
  *                (see mpg_options for the exact split); hi*hi, hi*lo and lo*hi
  *                accumulate in three separate fp32 accumulators that are summed
- *                in plain fp32 in the epilogue: acc = hh + 2^-11 * (hl + lh).
+ *                in plain fp32 in the epilogue: acc = hh + 2^-11 * (hl + lh),
+ *                per K chunk, the chunk totals added in fp32 (split_chunk_k).
  *   SPLIT_FP16_1CHAIN  the same three products accumulated in ONE accumulator
  *                (the shared-chain variant, kept for comparison; its lo is the
  *                plain fp16(x*2^s - hi), without the 2^11 scale).
@@ -110,7 +111,15 @@ typedef struct {
    * 0 = default (2 s).  On expiry the kernel stops, records MPG_ERR_TIMEOUT in
    * the device status word and returns without hanging the GPU. */
   int64_t wait_timeout_ns;
-  int32_t reserved[8];
+  /* SPLIT_FP16_3CHAIN only: the K loop accumulates in chunks of this many k
+   * elements.  Each chunk starts fresh hh / hl / lh accumulators on the tensor
+   * cores; the epilogue adds the chunk's hh + 2^-11*(hl + lh) to an fp32
+   * running sum with round-to-nearest.  This bounds how long the tensor
+   * cores' own fp32 accumulation runs (its rounding is not round-to-nearest,
+   * see the design notes).  0 = default (256); negative = one chunk covering
+   * the whole K range.  Rounded up to a multiple of 32. */
+  int32_t split_chunk_k;
+  int32_t reserved[7];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);

@@ -57,7 +57,8 @@ class Options(ctypes.Structure):
         ("force_generic_load", ctypes.c_int32),
         ("tile_n", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
-        ("reserved", ctypes.c_int32 * 8),
+        ("split_chunk_k", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
     ]
 
 

@@ -46,6 +46,7 @@ mpg_status fail(mpg_status s, const char* fmt, ...) {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+constexpr int64_t kDefaultSplitChunkK = 256;
 
 struct DeviceInfo {
   bool ready = false;
@@ -406,6 +407,11 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.scale_b = std::ldexp(1.0f, sb);
   p.status = dev->status;
   p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
+  p.chunk_kb = 0;
+  if (plan.conv == Conv::kSplit3 && o.split_chunk_k >= 0) {
+    const int64_t chunk_k = o.split_chunk_k > 0 ? o.split_chunk_k : kDefaultSplitChunkK;
+    p.chunk_kb = (int32_t)std::min<int64_t>((chunk_k + BK - 1) / BK, p.num_k_blk);
+  }
 
   const int grid = (int)std::min<int64_t>(tiles, dev->sm_count);
   void* args[] = {&p};

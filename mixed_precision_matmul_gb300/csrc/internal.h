@@ -58,6 +58,7 @@ struct TcParams {
   float scale_a, scale_b;  // 2^split_exp_a, 2^split_exp_b (split converter)
   uint32_t* status;
   uint64_t wait_limit_ns;
+  int32_t chunk_kb;   // k-blocks per accumulation chunk (0: the whole k range of a tile)
 };
 
 struct LaunchInfo {

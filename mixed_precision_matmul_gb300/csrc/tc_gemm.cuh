@@ -61,12 +61,22 @@ struct TcTraits {
   static constexpr int kConvWarps = kHasConv ? 8 : 0;
   static constexpr int kConvThreads = kConvWarps * 32;
   static constexpr int kThreads = (6 + kConvWarps) * 32;
-  // TMEM: columns of one accumulator (all chains), buffers, allocation
+  // TMEM: columns of one accumulator (all chains), buffers, allocation.
+  // The three-chain split accumulates K in chunks: each chunk starts fresh
+  // chains, and the epilogue folds hh + 2^-11 (hl + lh) of every chunk into
+  // an fp32 running sum (round to nearest) kept in kRunCols extra columns.
+  static constexpr bool kPromote = (CV == Conv::kSplit3);
   static constexpr int kChainCols = (CV == Conv::kSplit3) ? 3 * BN : BN;
-  static constexpr int kAccStride = kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
+  static constexpr int kRunCols = kPromote ? BN : 0;
+  static constexpr int kAccStride = kPromote ? kChainCols
+                                    : kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
                                     : kChainCols <= 256 ? 256 : 512;
-  static constexpr int kAccBufs = (2 * kAccStride <= 512) ? 2 : 1;
-  static constexpr int kTmemCols = kAccBufs * kAccStride;
+  static constexpr int kAccBufs = (2 * kAccStride + kRunCols <= 512) ? 2 : 1;
+  static constexpr int kRunBase = kAccBufs * kAccStride;
+  static constexpr int kTmemUsed = kRunBase + kRunCols;
+  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                   : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
   static constexpr int kEpiBytes = 4 * 32 * 32 * 4;
   static constexpr int kNumBars = 4 * kStages + 2 * kAccBufs + 1;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kOpStage + kStgStage) + kEpiBytes +
@@ -377,52 +387,56 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       // source's majorness; tf32 tiles are always K-major
       const bool a_mn = (T::kOp == Op::kTF32) ? false : (p.a_mn_major != 0);
       const bool b_mn = (T::kOp == Op::kTF32) ? false : (p.b_mn_major != 0);
-      uint32_t it = 0, titer = 0;
+      uint32_t it = 0, g = 0;   // k-block iteration; accumulation chunk
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++titer) {
+      const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::BN);
+      const uint32_t idesc_2n =
+          make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::kConv == Conv::kSplit3 ? 2 * T::BN : T::BN);
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(p, t);
-        const uint32_t ab = titer % T::kAccBufs;
-        const uint32_t aph = (titer / T::kAccBufs) & 1u;
-        if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctl)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint32_t d0 = tmem_base + ab * T::kAccStride;
-        const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::BN);
-        const uint32_t idesc_2n =
-            make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::kConv == Conv::kSplit3 ? 2 * T::BN : T::BN);
-        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
-          const uint32_t st = it % T::kStages;
-          const uint32_t ph = (it / T::kStages) & 1u;
-          if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
+        const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
+        for (int c0 = tc.kb0; c0 < tc.kb1 && ok; c0 += ck, ++g) {
+          const int c1 = min(tc.kb1, c0 + ck);
+          const uint32_t ab = g % T::kAccBufs;
+          const uint32_t aph = (g / T::kAccBufs) & 1u;
+          if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctl)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint32_t a_hi = op_smem + st * T::kOpStage;
-          const uint32_t a_lo = a_hi + T::kATile;                       // split only
-          const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
-          const uint32_t b_lo = b_hi + T::kBTile;                       // split only
+          const uint32_t d0 = tmem_base + ab * T::kAccStride;
+          for (int kb = c0; kb < c1; ++kb, ++it) {
+            const uint32_t st = it % T::kStages;
+            const uint32_t ph = (it / T::kStages) & 1u;
+            if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t a_hi = op_smem + st * T::kOpStage;
+            const uint32_t a_lo = a_hi + T::kATile;                       // split only
+            const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
+            const uint32_t b_lo = b_hi + T::kBTile;                       // split only
 #pragma unroll
-          for (int ks = 0; ks < T::kKSteps; ++ks) {
-            const uint32_t acc = (kb > tc.kb0 || ks > 0) ? 1u : 0u;
-            const uint64_t da_hi = operand_desc<T>(a_hi, a_mn, ks);
-            const uint64_t db_hi = operand_desc<T>(b_hi, b_mn, ks);
-            if constexpr (T::kOp == Op::kTF32) {
-              mma_tf32(d0, da_hi, db_hi, idesc_n, acc);
-            } else if constexpr (T::kConv == Conv::kSplit3) {
-              // [hh | hl] = A_hi * [B_hi | B_lo]  (B_hi and B_lo are adjacent)
-              mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
-              // lh = A_lo * B_hi
-              mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
-            } else if constexpr (T::kConv == Conv::kSplit1) {
-              // one chain: hh, hl and lh all accumulate into the same columns
-              mma_f16(d0, da_hi, db_hi, idesc_n, acc);
-              mma_f16(d0, da_hi, operand_desc<T>(b_lo, b_mn, ks), idesc_n, 1u);
-              mma_f16(d0, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, 1u);
-            } else {
-              mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+            for (int ks = 0; ks < T::kKSteps; ++ks) {
+              const uint32_t acc = (kb > c0 || ks > 0) ? 1u : 0u;
+              const uint64_t da_hi = operand_desc<T>(a_hi, a_mn, ks);
+              const uint64_t db_hi = operand_desc<T>(b_hi, b_mn, ks);
+              if constexpr (T::kOp == Op::kTF32) {
+                mma_tf32(d0, da_hi, db_hi, idesc_n, acc);
+              } else if constexpr (T::kConv == Conv::kSplit3) {
+                // [hh | hl] = A_hi * [B_hi | B_lo]  (B_hi and B_lo are adjacent)
+                mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
+                // lh = A_lo * B_hi
+                mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
+              } else if constexpr (T::kConv == Conv::kSplit1) {
+                // one chain: hh, hl and lh all accumulate into the same columns
+                mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+                mma_f16(d0, da_hi, operand_desc<T>(b_lo, b_mn, ks), idesc_n, 1u);
+                mma_f16(d0, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, 1u);
+              } else {
+                mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+              }
             }
+            mma_commit(&op_empty[st]);
           }
-          mma_commit(&op_empty[st]);
+          if (!ok) break;
+          mma_commit(&acc_full[ab]);
         }
-        if (!ok) break;
-        mma_commit(&acc_full[ab]);
       }
       // wait for every MMA this thread issued before TMEM is released
       mma_commit(done_bar);
@@ -434,14 +448,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     float* stg = epi_base + (warp - 2) * 1024;
     const uint32_t stg_addr = smem_addr(stg);
-    uint32_t titer = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++titer) {
+    uint32_t g = 0;   // accumulation chunk, in the MMA warp's order
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const TileCoord tc = decode_tile(p, t);
-      const uint32_t ab = titer % T::kAccBufs;
-      const uint32_t aph = (titer / T::kAccBufs) & 1u;
-      if (!warp_wait(&acc_full[ab], aph, ctl)) break;
-      tc_fence_after_sync();
-      const uint32_t tacc = tmem_base + lane_off + ab * T::kAccStride;
+      const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
+      const int nchunks = (tc.kb1 - tc.kb0 + ck - 1) / ck;
       float* out;
       int64_t ldo;
       float alpha, beta;
@@ -461,73 +473,103 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       }
       const int row_base = tc.mb * T::BM + 32 * q;
 #pragma unroll 1
-      for (int cc = 0; cc < T::BN / 32; ++cc) {
-        float v[32];
-        tmem_ld_32cols(tacc + cc * 32, v);
-        if constexpr (T::kConv == Conv::kSplit3) {
-          float u[32], w[32];
-          tmem_ld_32cols(tacc + T::BN + cc * 32, u);
-          tmem_ld_32cols(tacc + 2 * T::BN + cc * 32, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = v[j] + 0x1p-11f * (u[j] + w[j]);
-        } else {
-          tmem_ld_wait();
-        }
-        if (cc == T::BN / 32 - 1) {
-          // this warp's share of the accumulator is now in registers
-          tc_fence_before_sync();
-          mbar_arrive(&acc_empty[ab]);
-        }
-        const int col_base = tc.nb * T::BN + cc * 32;
-        if (row_base >= p.m || col_base >= p.n) continue;
-        // transpose through a per-warp swizzled 32x32 staging tile so that
-        // global stores are row-contiguous
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
-                       __float_as_uint(v[4 * ch + 1]), __float_as_uint(v[4 * ch + 2]),
-                       __float_as_uint(v[4 * ch + 3]));
-        }
-        __syncwarp();
-        if (vec_ok && col_base + 32 <= p.n) {
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int r = it * 4 + (lane >> 3);
-            const int ch = lane & 7;
-            const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
-            const int grow = row_base + r;
-            if (grow < p.m) {
-              float4* dst = reinterpret_cast<float4*>(out + (int64_t)grow * ldo + col_base + ch * 4);
-              float4 o;
-              if (beta != 0.0f) {
-                const float4 c0 = *dst;
-                o.x = fmaf(beta, c0.x, alpha * x.x);
-                o.y = fmaf(beta, c0.y, alpha * x.y);
-                o.z = fmaf(beta, c0.z, alpha * x.z);
-                o.w = fmaf(beta, c0.w, alpha * x.w);
-              } else {
-                o.x = alpha * x.x;
-                o.y = alpha * x.y;
-                o.z = alpha * x.z;
-                o.w = alpha * x.w;
+      for (int ci = 0; ci < nchunks; ++ci, ++g) {
+        const uint32_t ab = g % T::kAccBufs;
+        const uint32_t aph = (g / T::kAccBufs) & 1u;
+        if (!warp_wait(&acc_full[ab], aph, ctl)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t tacc = tmem_base + lane_off + ab * T::kAccStride;
+        const uint32_t trun = tmem_base + lane_off + T::kRunBase;
+        const bool last = (ci == nchunks - 1);
+        const bool have_run = (ci > 0);
+  #pragma unroll 1
+        for (int cc = 0; cc < T::BN / 32; ++cc) {
+          float v[32];
+          if constexpr (T::kPromote) {
+            // chunk total hh + 2^-11 (hl + lh), plus the running sum of the
+            // earlier chunks of this tile
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float x0[16], x1[16], x2[16], r[16];
+              const uint32_t col = cc * 32 + h * 16;
+              tmem_ld_16cols(tacc + col, x0);
+              tmem_ld_16cols(tacc + T::BN + col, x1);
+              tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
+              if (have_run) tmem_ld_16cols(trun + col, r);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float x = x0[j] + 0x1p-11f * (x1[j] + x2[j]);
+                v[h * 16 + j] = have_run ? r[j] + x : x;
               }
-              *dst = o;
+            }
+            if (!last) {
+              tmem_st_16cols(trun + cc * 32, v);
+              tmem_st_16cols(trun + cc * 32 + 16, v + 16);
+            }
+          } else {
+            tmem_ld_32cols(tacc + cc * 32, v);
+            tmem_ld_wait();
+          }
+          if (cc == T::BN / 32 - 1) {
+            // this warp's share of the chunk is now in registers / the running sum
+            if constexpr (T::kPromote) {
+              if (!last) tmem_st_wait();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&acc_empty[ab]);
+          }
+          if (!last) continue;   // chunk folded into the running sum; nothing to store yet
+          const int col_base = tc.nb * T::BN + cc * 32;
+          if (row_base >= p.m || col_base >= p.n) continue;
+          // transpose through a per-warp swizzled 32x32 staging tile so that
+          // global stores are row-contiguous
+  #pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
+                         __float_as_uint(v[4 * ch + 1]), __float_as_uint(v[4 * ch + 2]),
+                         __float_as_uint(v[4 * ch + 3]));
+          }
+          __syncwarp();
+          if (vec_ok && col_base + 32 <= p.n) {
+  #pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = it * 4 + (lane >> 3);
+              const int ch = lane & 7;
+              const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
+              const int grow = row_base + r;
+              if (grow < p.m) {
+                float4* dst = reinterpret_cast<float4*>(out + (int64_t)grow * ldo + col_base + ch * 4);
+                float4 o;
+                if (beta != 0.0f) {
+                  const float4 c0 = *dst;
+                  o.x = fmaf(beta, c0.x, alpha * x.x);
+                  o.y = fmaf(beta, c0.y, alpha * x.y);
+                  o.z = fmaf(beta, c0.z, alpha * x.z);
+                  o.w = fmaf(beta, c0.w, alpha * x.w);
+                } else {
+                  o.x = alpha * x.x;
+                  o.y = alpha * x.y;
+                  o.z = alpha * x.z;
+                  o.w = alpha * x.w;
+                }
+                *dst = o;
+              }
+            }
+          } else {
+            const int gcol = col_base + lane;
+  #pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+              const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
+              const int grow = row_base + r;
+              if (grow < p.m && gcol < p.n) {
+                float* dst = out + (int64_t)grow * ldo + gcol;
+                *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * x) : alpha * x;
+              }
             }
           }
-        } else {
-          const int gcol = col_base + lane;
-#pragma unroll 4
-          for (int r = 0; r < 32; ++r) {
-            const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
-            const int grow = row_base + r;
-            if (grow < p.m && gcol < p.n) {
-              float* dst = out + (int64_t)grow * ldo + gcol;
-              *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * x) : alpha * x;
-            }
-          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
   } else {

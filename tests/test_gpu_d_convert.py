@@ -83,3 +83,17 @@ def test_many_tiles_per_persistent_cta(mode, tile_n):
     rows = np.array([0, 1, 127, 128, 1000, 1500, 2047])
     ref, den = oracle.gemm(c.a[0][rows], c.b[0], c.c0[0][rows], 1.0, 0.0, MODE_Q[mode], MODE_Q[mode])
     assert oracle.max_rel_err(C[0][rows], ref, den) <= TOL["q16"]
+
+
+@pytest.mark.parametrize("chunk_k", [-1, 32, 96, 256])
+@pytest.mark.parametrize("tile_n", [64, 128])
+def test_split3_chunked_accumulation(chunk_k, tile_n):
+    """The three-chain split folds each K chunk into an fp32 running sum kept
+    in TMEM: many small chunks, chunks not dividing K, and a single chunk
+    (no folding) must all meet both bars."""
+    mpg.build()
+    opts = mpg.options(tile_n=tile_n, split_chunk_k=chunk_k)
+    c = Case(300, 260, 700, mpg.SPLIT_FP16_3CHAIN, b_layout=Cm, alpha=1.5, beta=0.5, opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)

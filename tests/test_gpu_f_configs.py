@@ -114,6 +114,10 @@ def test_loguniform_4096_split_vs_one_chain_vs_tf32_vs_ffma(capsys):
         errs[mode] = row_errors(c, C, rows, oracle.Q_NONE)
         if mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_1CHAIN):
             errs[(mode, "Q")] = row_errors(c, C, rows, MODE_Q[mode])
+    # the three-chain split without chunked accumulation, for the record
+    c = Case(n, n, n, mpg.SPLIT_FP16_3CHAIN, a=a, b=b, b_layout=Cm, opts=mpg.options(split_chunk_k=-1))
+    c.run()
+    errs["split3 one chunk"] = row_errors(c, c.result(), rows, oracle.Q_NONE)
     show(capsys, "loguniform4096 errors vs FP64: " + ", ".join(
         f"{k}: {v:.3e}" for k, v in errs.items()))
     assert errs[mpg.SPLIT_FP16_3CHAIN] <= TOL["split"]
