@@ -292,6 +292,38 @@ def points_error(orc, w, C_gpu, quant, count=512, seed=5):
 
 
 # ---------------------------------------------------------------------------
+def one_mode(args):
+    """Time one row of the per-precision-mode table on its own (steps and
+    warm-up as given) and print its figures as one JSON line.  Used to time or
+    profile a single workload; not the benchmark's headline line."""
+    import torch
+
+    import mixed_precision_matmul_gb300 as mpg
+    import synthetic
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    mpg.build()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    cases = dict(mode_cases(torch, mpg, synthetic, device))
+    if args.mode not in cases:
+        raise SystemExit(f"unknown mode {args.mode}; one of {sorted(cases)}")
+    mw = cases[args.mode]()
+    Cm = torch.zeros((mw.batch, mw.m, mw.ldc) if mw.batch > 1 else (mw.m, mw.ldc), dtype=torch.float32,
+                     device=device)
+    ws_bytes = mpg.workspace_size(mw.m, mw.n, mw.k, mw.batch, mpg.MODE_NAMES[mw.mode_name], mw.opts)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    ms = time_steps(torch, lambda: run_step(mpg, mw, Cm, ws.data_ptr(), ws_bytes, sh), args.steps, args.warmup,
+                    stream) / args.steps
+    line = {"mode": args.mode, "shape": [mw.batch, mw.m, mw.n, mw.k], "ms": round(ms, 5),
+            "tflops": round(mw.flops / (ms * 1e-3) / 1e12, 2),
+            "gbs": round(mw.algo_bytes / (ms * 1e-3) / 1e9, 1) if mw.algo_bytes else None,
+            "peaks": {**peaks, "source": peak_src}}
+    print(json.dumps(line), flush=True)
+
+
 def ours(args):
     import torch
 
@@ -561,11 +593,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--mode", default=None,
+                    help="time only this row of the per-mode table (e.g. attention_qkt_split3)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         reference(args)
+    elif args.mode:
+        one_mode(args)
     else:
         ours(args)
 

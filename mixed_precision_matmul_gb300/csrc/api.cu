@@ -397,6 +397,15 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.num_tiles = (int32_t)tiles;
   p.group_m = 16;
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (batch == 1 || p.stride_c % 4 == 0);
+  // generic loads read 4 consecutive elements as one vector when the base,
+  // the leading dimension and the batch stride keep every chunk aligned
+  auto vec_ok = [&](const Operand& x, int64_t stride) {
+    const int64_t es = elem_bytes(x.dt);
+    return reinterpret_cast<uintptr_t>(x.ptr) % (4 * es) == 0 && x.ld % 4 == 0 &&
+           (batch == 1 || stride % 4 == 0);
+  };
+  p.a_vec_ok = vec_ok(A, a_stride);
+  p.b_vec_ok = vec_ok(B, b_stride);
   p.partial = splits_eff > 1 ? static_cast<float*>(workspace) : nullptr;
   p.p_vec_ok = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(workspace) % 16 == 0);
   const bool split = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit1);

@@ -5,71 +5,119 @@
 // so it stays FFMA-bound" path of "tile_matmul(): use the cuBLASDx
 // register-accumulator API ...", spike results, second bullet.
 //
-// Tiling: 128 x 128 output tile per 256-thread block, k-tiles of 8 staged in
-// shared memory (double buffered, prefetched through registers), 8 x 8
-// outputs per thread in registers.  Any layout, leading dimension and tail.
+// Tiling: 128 x 128 output tile per 256-thread block, k-tiles of 16 staged in
+// shared memory (double buffered, prefetched through registers; A stored
+// k-major so both operands are read as float4 broadcasts), 8 x 8 outputs per
+// thread in registers.  Interior tiles of aligned operands load float4
+// vectors; edge tiles and unaligned operands load element by element with
+// bounds checks.  Any layout, leading dimension and tail.
 #include "internal.h"
 
 namespace mpg {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 8, kThreads = 256;
+constexpr int kBM = 128, kBN = 128, kBK = 16, kThreads = 256;
 constexpr int kPad = 4;
 
-struct FfmaTileLoader {
-  // each thread loads 4 elements of the A tile and 4 of the B tile
-  __device__ static void load(const FfmaParams& p, const float* a, const float* b, int m0, int n0, int k0,
-                              float (&ra)[4], float (&rb)[4]) {
+template <bool A_COL, bool B_COL>
+struct Loader {
+  // Each thread fetches 8 elements of the A tile and 8 of the B tile per k-tile.
+  float ra[8], rb[8];
+
+  __device__ void load(const FfmaParams& p, const float* a, const float* b, int m0, int n0, int k0, bool vec) {
     const int t = threadIdx.x;
+    // ---- A (m x k)
+    if (vec && m0 + kBM <= p.m && k0 + kBK <= p.k) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int mm, kk;
-      if (p.a_col_major) {  // (m, k) at k*lda + m: 128 consecutive m per k
-        mm = t & 127;
-        kk = (t >> 7) + 2 * e;
-      } else {              // (m, k) at m*lda + k: 8 consecutive k per m
-        kk = t & 7;
-        mm = (t >> 3) + 32 * e;
+      for (int i = 0; i < 2; ++i) {
+        float4 v;
+        if constexpr (A_COL) {  // m contiguous: 32 float4 per k line
+          const int kk = (t >> 5) + 8 * i, mm = (t & 31) * 4;
+          v = __ldg(reinterpret_cast<const float4*>(a + (int64_t)(k0 + kk) * p.lda + m0 + mm));
+        } else {                // k contiguous: 4 float4 per row
+          const int mm = (t >> 2) + 64 * i, kk = (t & 3) * 4;
+          v = __ldg(reinterpret_cast<const float4*>(a + (int64_t)(m0 + mm) * p.lda + k0 + kk));
+        }
+        ra[4 * i] = v.x; ra[4 * i + 1] = v.y; ra[4 * i + 2] = v.z; ra[4 * i + 3] = v.w;
       }
-      const int gm = m0 + mm, gk = k0 + kk;
-      float v = 0.0f;
-      if (gm < p.m && gk < p.k) v = p.a_col_major ? __ldg(a + (int64_t)gk * p.lda + gm) : __ldg(a + (int64_t)gm * p.lda + gk);
-      ra[e] = v;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          int mm, kk;
+          if constexpr (A_COL) { kk = (t >> 5) + 8 * i; mm = (t & 31) * 4 + e; }
+          else { mm = (t >> 2) + 64 * i; kk = (t & 3) * 4 + e; }
+          const int gm = m0 + mm, gk = k0 + kk;
+          float v = 0.0f;
+          if (gm < p.m && gk < p.k)
+            v = A_COL ? __ldg(a + (int64_t)gk * p.lda + gm) : __ldg(a + (int64_t)gm * p.lda + gk);
+          ra[4 * i + e] = v;
+        }
     }
+    // ---- B (k x n)
+    if (vec && n0 + kBN <= p.n && k0 + kBK <= p.k) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int nn, kk;
-      if (p.b_col_major) {  // (k, n) at n*ldb + k
-        kk = t & 7;
-        nn = (t >> 3) + 32 * e;
-      } else {              // (k, n) at k*ldb + n
-        nn = t & 127;
-        kk = (t >> 7) + 2 * e;
+      for (int i = 0; i < 2; ++i) {
+        float4 v;
+        if constexpr (B_COL) {  // k contiguous: 4 float4 per column
+          const int nn = (t >> 2) + 64 * i, kk = (t & 3) * 4;
+          v = __ldg(reinterpret_cast<const float4*>(b + (int64_t)(n0 + nn) * p.ldb + k0 + kk));
+        } else {                // n contiguous: 32 float4 per k line
+          const int kk = (t >> 5) + 8 * i, nn = (t & 31) * 4;
+          v = __ldg(reinterpret_cast<const float4*>(b + (int64_t)(k0 + kk) * p.ldb + n0 + nn));
+        }
+        rb[4 * i] = v.x; rb[4 * i + 1] = v.y; rb[4 * i + 2] = v.z; rb[4 * i + 3] = v.w;
       }
-      const int gn = n0 + nn, gk = k0 + kk;
-      float v = 0.0f;
-      if (gn < p.n && gk < p.k) v = p.b_col_major ? __ldg(b + (int64_t)gn * p.ldb + gk) : __ldg(b + (int64_t)gk * p.ldb + gn);
-      rb[e] = v;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          int nn, kk;
+          if constexpr (B_COL) { nn = (t >> 2) + 64 * i; kk = (t & 3) * 4 + e; }
+          else { kk = (t >> 5) + 8 * i; nn = (t & 31) * 4 + e; }
+          const int gn = n0 + nn, gk = k0 + kk;
+          float v = 0.0f;
+          if (gn < p.n && gk < p.k)
+            v = B_COL ? __ldg(b + (int64_t)gn * p.ldb + gk) : __ldg(b + (int64_t)gk * p.ldb + gn);
+          rb[4 * i + e] = v;
+        }
     }
   }
-  __device__ static void store(const FfmaParams& p, float (*As)[kBM + kPad], float (*Bs)[kBN + kPad],
-                               const float (&ra)[4], const float (&rb)[4]) {
+
+  // shared tiles are k-major: As[k][m], Bs[k][n]
+  __device__ void store(float (*As)[kBM + kPad], float (*Bs)[kBN + kPad]) const {
     const int t = threadIdx.x;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (p.a_col_major) As[(t >> 7) + 2 * e][t & 127] = ra[e];
-      else As[t & 7][(t >> 3) + 32 * e] = ra[e];
-      if (p.b_col_major) Bs[t & 7][(t >> 3) + 32 * e] = rb[e];
-      else Bs[(t >> 7) + 2 * e][t & 127] = rb[e];
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (A_COL) {
+        const int kk = (t >> 5) + 8 * i, mm = (t & 31) * 4;
+        *reinterpret_cast<float4*>(&As[kk][mm]) = make_float4(ra[4 * i], ra[4 * i + 1], ra[4 * i + 2], ra[4 * i + 3]);
+      } else {
+        const int mm = (t >> 2) + 64 * i, kk = (t & 3) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) As[kk + e][mm] = ra[4 * i + e];
+      }
+      if constexpr (B_COL) {
+        const int nn = (t >> 2) + 64 * i, kk = (t & 3) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Bs[kk + e][nn] = rb[4 * i + e];
+      } else {
+        const int kk = (t >> 5) + 8 * i, nn = (t & 31) * 4;
+        *reinterpret_cast<float4*>(&Bs[kk][nn]) = make_float4(rb[4 * i], rb[4 * i + 1], rb[4 * i + 2], rb[4 * i + 3]);
+      }
     }
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams p) {
+template <bool A_COL, bool B_COL>
+__global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams p, int a_vec, int b_vec) {
   __shared__ __align__(16) float As[2][kBK][kBM + kPad];
   __shared__ __align__(16) float Bs[2][kBK][kBN + kPad];
   const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const bool vec = a_vec && b_vec;
   for (int bz = blockIdx.z; bz < p.batch; bz += gridDim.z) {
     const float* a = p.a + (int64_t)bz * p.stride_a;
     const float* b = p.b + (int64_t)bz * p.stride_b;
@@ -80,14 +128,14 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-    float ra[4], rb[4];
+    Loader<A_COL, B_COL> ld;
     const int num_kt = (p.k + kBK - 1) / kBK;
-    FfmaTileLoader::load(p, a, b, m0, n0, 0, ra, rb);
-    FfmaTileLoader::store(p, As[0], Bs[0], ra, rb);
+    ld.load(p, a, b, m0, n0, 0, vec);
+    ld.store(As[0], Bs[0]);
     __syncthreads();
     for (int kt = 0; kt < num_kt; ++kt) {
       const int cur = kt & 1;
-      if (kt + 1 < num_kt) FfmaTileLoader::load(p, a, b, m0, n0, (kt + 1) * kBK, ra, rb);
+      if (kt + 1 < num_kt) ld.load(p, a, b, m0, n0, (kt + 1) * kBK, vec);
 #pragma unroll
       for (int kk = 0; kk < kBK; ++kk) {
         const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4]);
@@ -101,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
-      if (kt + 1 < num_kt) FfmaTileLoader::store(p, As[cur ^ 1], Bs[cur ^ 1], ra, rb);
+      if (kt + 1 < num_kt) ld.store(As[cur ^ 1], Bs[cur ^ 1]);
       __syncthreads();
     }
 #pragma unroll
@@ -124,7 +172,15 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
 
 cudaError_t launch_ffma(const FfmaParams& p, cudaStream_t stream) {
   dim3 grid((p.n + kBN - 1) / kBN, (p.m + kBM - 1) / kBM, p.batch < 65535 ? p.batch : 65535);
-  ffma_gemm_kernel<<<grid, kThreads, 0, stream>>>(p);
+  // float4 loads need 16-byte aligned bases, leading dimensions and batch strides
+  auto aligned = [&](const float* x, int64_t ld, int64_t stride) {
+    return reinterpret_cast<uintptr_t>(x) % 16 == 0 && ld % 4 == 0 && (p.batch == 1 || stride % 4 == 0);
+  };
+  const int av = aligned(p.a, p.lda, p.stride_a), bv = aligned(p.b, p.ldb, p.stride_b);
+  if (p.a_col_major && p.b_col_major) ffma_gemm_kernel<true, true><<<grid, kThreads, 0, stream>>>(p, av, bv);
+  else if (p.a_col_major) ffma_gemm_kernel<true, false><<<grid, kThreads, 0, stream>>>(p, av, bv);
+  else if (p.b_col_major) ffma_gemm_kernel<false, true><<<grid, kThreads, 0, stream>>>(p, av, bv);
+  else ffma_gemm_kernel<false, false><<<grid, kThreads, 0, stream>>>(p, av, bv);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,7 @@ struct TcParams {
   int32_t num_tiles;
   int32_t group_m;
   int32_t c_vec_ok;   // C base 16-byte aligned and ldc % 4 == 0
+  int32_t a_vec_ok, b_vec_ok;  // 4-element chunks of A / B are vector-aligned (generic loads)
   int32_t p_vec_ok;   // partial buffer: n % 4 == 0
   float alpha;        // already multiplied by 2^-(split_exp_a + split_exp_b)
   float beta;

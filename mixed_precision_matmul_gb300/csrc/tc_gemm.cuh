@@ -616,24 +616,44 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               const int row0 = isA ? tc.mb * T::BM : tc.nb * T::BN;
               const int64_t ld = isA ? p.lda : p.ldb;
               const E* g = (isA ? ga : gb) + (int64_t)tc.b * (isA ? p.stride_a : p.stride_b);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                int r, kk;
-                if (!mn) {
-                  r = row0 + (int)lg;
-                  kk = k0 + (int)ch * 4 + e;
-                } else {
-                  r = row0 + (int)(lg / T::BK) * T::BK + (int)ch * 4 + e;
-                  kk = k0 + (int)(lg % T::BK);
-                }
-                const bool in = (r < rows_lim) && (kk < p.k);
-                const int64_t idx = mn ? (int64_t)kk * ld + r : (int64_t)r * ld + kk;
+              // the chunk's 4 elements are consecutive in memory: (row r0,
+              // k kk0..kk0+3) for K-major, (rows r0..r0+3, k kk0) for MN-major
+              int r0, kk0;
+              if (!mn) {
+                r0 = row0 + (int)lg;
+                kk0 = k0 + (int)ch * 4;
+              } else {
+                r0 = row0 + (int)(lg / T::BK) * T::BK + (int)ch * 4;
+                kk0 = k0 + (int)(lg % T::BK);
+              }
+              const int64_t idx0 = mn ? (int64_t)kk0 * ld + r0 : (int64_t)r0 * ld + kk0;
+              const bool whole = mn ? (r0 + 3 < rows_lim && kk0 < p.k) : (r0 < rows_lim && kk0 + 3 < p.k);
+              if (whole && (isA ? p.a_vec_ok : p.b_vec_ok)) {
+                // one aligned vector load (16 bytes of fp32, 8 of 16-bit codes)
                 if constexpr (T::kSrcT == SrcT::kF32) {
-                  x[e] = in ? SE::load(g + idx) : 0.0f;
-                  h[e] = 0;
+                  const float4 v = __ldg(reinterpret_cast<const float4*>(g + idx0));
+                  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+                  h[0] = h[1] = h[2] = h[3] = 0;
                 } else {
-                  h[e] = in ? SE::load(g + idx) : (unsigned short)0;
-                  x[e] = 0.0f;
+                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(g + idx0));
+                  h[0] = (unsigned short)(v.x & 0xFFFFu); h[1] = (unsigned short)(v.x >> 16);
+                  h[2] = (unsigned short)(v.y & 0xFFFFu); h[3] = (unsigned short)(v.y >> 16);
+                  x[0] = x[1] = x[2] = x[3] = 0.0f;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int r = mn ? r0 + e : r0;
+                  const int kk = mn ? kk0 : kk0 + e;
+                  const bool in = (r < rows_lim) && (kk < p.k);
+                  const int64_t idx = idx0 + e;
+                  if constexpr (T::kSrcT == SrcT::kF32) {
+                    x[e] = in ? SE::load(g + idx) : 0.0f;
+                    h[e] = 0;
+                  } else {
+                    h[e] = in ? SE::load(g + idx) : (unsigned short)0;
+                    x[e] = 0.0f;
+                  }
                 }
               }
             }
