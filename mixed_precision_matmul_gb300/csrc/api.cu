@@ -221,8 +221,12 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
   } else if (p.conv == Conv::kSplit3) {
     bn = (n <= 64 || k <= 512) ? 64 : 128;
-  } else {
+  } else if (p.conv == Conv::kSplit1) {
     bn = n <= 64 ? 64 : 128;
+  } else {
+    // fp32 -> fp16 / bf16 on load: the widest tile converts the fewest
+    // source bytes per flop
+    bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
   }
   if (o.tile_n != 0) {
     TcKernel probe;

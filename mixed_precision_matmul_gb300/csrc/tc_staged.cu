@@ -7,8 +7,10 @@ namespace mpg {
 bool tc_lookup_staged(Conv conv, int bn, TcKernel* out) {
 #define MPG_STAGED(CV, OPV, BNV)                                                   \
   if (conv == CV && bn == BNV) return tc_fill<TcTraits<Src::kTmaStaged, CV, OPV, SrcT::kF32, BNV>>(out);
+  MPG_STAGED(Conv::kRoundF16, Op::kF16, 256)
   MPG_STAGED(Conv::kRoundF16, Op::kF16, 128)
   MPG_STAGED(Conv::kRoundF16, Op::kF16, 64)
+  MPG_STAGED(Conv::kRoundBF16, Op::kBF16, 256)
   MPG_STAGED(Conv::kRoundBF16, Op::kBF16, 128)
   MPG_STAGED(Conv::kRoundBF16, Op::kBF16, 64)
   MPG_STAGED(Conv::kSplit3, Op::kF16, 128)

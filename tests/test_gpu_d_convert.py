@@ -97,3 +97,18 @@ def test_split3_chunked_accumulation(chunk_k, tile_n):
     c.run()
     eR, eQ = c.errors()
     assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
+
+
+@pytest.mark.parametrize("mode", [mpg.FP16_F32ACC, mpg.BF16_F32ACC])
+@pytest.mark.parametrize("m,n,k,al,bl,pad", [
+    (128, 256, 64, R, Cm, (0, 0, 0)),
+    (300, 520, 100, R, R, (4, 4, 4)),
+    (257, 700, 96, Cm, Cm, (7, 8, 0)),      # lda 264, ldb 104: TMA-aligned pitches
+])
+def test_round_on_load_256_wide_tiles(mode, m, n, k, al, bl, pad):
+    mpg.build()
+    c = Case(m, n, k, mode, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=0.5,
+             opts=mpg.options(tile_n=256))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)
