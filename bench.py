@@ -170,7 +170,7 @@ def time_steps(torch, fn, steps, warmup, stream):
 # ---------------------------------------------------------------------------
 def mode_cases(torch, mpg, synthetic, device):
     """Yield (label, Workload) for the per-mode table; built lazily."""
-    def f32_square(n_, seed_dist, mode_name, b_layout="row"):
+    def f32_square(n_, seed_dist, mode_name, b_layout="row", opts=None):
         if seed_dist == "uniform":
             a = synthetic.uniform((n_, n_), synthetic.SEED_A)
             b = synthetic.uniform((n_, n_), synthetic.SEED_B)
@@ -190,7 +190,7 @@ def mode_cases(torch, mpg, synthetic, device):
         algo = 4 * n_ * n_ * 2 + 4 * n_ * n_
         return Workload(f"{seed_dist}_{n_}", n_, n_, n_, 1, mode_name, A, B, None, n_, ldb, n_, 0, 0, 0,
                         mpg.ROW_MAJOR, bl, mpg.F32, 1.0, 0.0,
-                        {"a": a, "b": b, "b_col": b_layout == "col"}, algo_bytes=algo)
+                        {"a": a, "b": b, "b_col": b_layout == "col"}, opts=opts, algo_bytes=algo)
 
     # C1: 256^3 uniform, four modes
     for mn in ("fp16", "bf16", "tf32", "split3"):
@@ -198,10 +198,14 @@ def mode_cases(torch, mpg, synthetic, device):
     # C3-shaped 8192^3 in the other precisions
     yield "square8192_tf32", lambda: f32_square(8192, "normal", "tf32", "col")
     yield "square8192_fp16_onload", lambda: f32_square(8192, "normal", "fp16")
+    yield "square8192_fp16_prepass", lambda: f32_square(8192, "normal", "fp16", opts=mpg.options(prepass=1))
     # C4: 4096^3 log-uniform: split3 vs split1 vs tf32 vs FFMA (B column-major
     # so that tf32 takes its direct path; every mode sees the same layout)
     for mn in ("split3", "split1", "tf32", "ffma"):
         yield f"loguniform4096_{mn}", lambda mn=mn: f32_square(4096, "loguniform", mn, "col")
+    for mn in ("split3", "split1"):
+        yield f"loguniform4096_{mn}_prepass", lambda mn=mn: f32_square(4096, "loguniform", mn, "col",
+                                                                       opts=mpg.options(prepass=1))
     # C2: batched 2048 x (64x4096 * 4096x64), padded leading dims
     for mn in ("tf32", "fp16"):
         yield f"batched2048_{mn}", lambda mn=mn: make_batched(torch, mpg, synthetic, device, mn)
@@ -523,7 +527,8 @@ def ours(args):
             mw.A = mw.B = None
             torch.cuda.empty_cache()
         ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
-        for lbl in ("loguniform4096_split3", "loguniform4096_split1"):
+        for lbl in ("loguniform4096_split3", "loguniform4096_split1", "loguniform4096_split3_prepass",
+                    "loguniform4096_split1_prepass"):
             if ffma and lbl in modes:
                 modes[lbl]["x_ffma"] = round(modes[lbl]["tflops"] / ffma, 2)
         result["modes"] = modes

@@ -119,7 +119,16 @@ typedef struct {
    * see the design notes).  0 = default (256); negative = one chunk covering
    * the whole K range.  Rounded up to a multiple of 32. */
   int32_t split_chunk_k;
-  int32_t reserved[7];
+  /* 1 = convert fp32 operands in a separate pass (FP16_F32ACC, BF16_F32ACC
+   * and the split modes): one extra kernel reads A and B once and writes
+   * packed 16-bit copies (hi and lo halves for the split) into the caller's
+   * workspace, then the product runs on those copies on its direct TMA path.
+   * Same conversions and same results as the default; it needs a workspace
+   * of mpg_gemm_workspace_size() bytes queried with the same options
+   * (4 bytes per operand element for the split, 2 otherwise, plus split-K
+   * partials).  0 (default) = convert on the fly in the load stage. */
+  int32_t prepass;
+  int32_t reserved[6];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);

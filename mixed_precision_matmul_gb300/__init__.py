@@ -58,7 +58,8 @@ class Options(ctypes.Structure):
         ("tile_n", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
         ("split_chunk_k", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("prepass", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 

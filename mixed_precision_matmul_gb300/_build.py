@@ -29,6 +29,7 @@ SOURCES = [
     "tc_direct.cu",
     "tc_staged.cu",
     "tc_generic.cu",
+    "prepass.cu",
 ]
 HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh"]
 

@@ -15,13 +15,13 @@
 #include "mpgemm.h"
 
 namespace mpg {
-bool tc_lookup_direct(Op op, int bn, TcKernel* out);
+bool tc_lookup_direct(Conv conv, Op op, int bn, TcKernel* out);
 bool tc_lookup_staged(Conv conv, int bn, TcKernel* out);
 bool tc_lookup_generic(Conv conv, Op op, SrcT st, int bn, TcKernel* out);
 
 bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out) {
   switch (src) {
-    case Src::kTmaDirect: return tc_lookup_direct(op, bn, out);
+    case Src::kTmaDirect: return tc_lookup_direct(conv, op, bn, out);
     case Src::kTmaStaged: return tc_lookup_staged(conv, bn, out);
     default: return tc_lookup_generic(conv, op, st, bn, out);
   }
@@ -120,6 +120,8 @@ struct Plan {
   SrcT st = SrcT::kF32;
   int bn = 128;
   int splits = 1;
+  bool prepass = false;       // operands converted by a separate pass into the workspace
+  Conv pre_conv = Conv::kNone;
 };
 
 struct Operand {
@@ -152,6 +154,42 @@ int choose_splits(int64_t m, int64_t n, int64_t k, int64_t batch, int sm_count, 
 
 size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch) {
   return splits > 1 ? (size_t)splits * (size_t)batch * (size_t)m * (size_t)n * sizeof(float) : 0;
+}
+
+// Workspace of the separate conversion pass: packed 16-bit copies of A and B
+// (hi and lo for the split) after the split-K partials, each 256-byte aligned.
+// A copy keeps its operand's majorness; its lines are padded to a multiple of
+// 8 elements so that every line starts on a 16-byte boundary (TMA).
+struct PrepassLayout {
+  int64_t a_outer, a_inner, a_ld, b_outer, b_inner, b_ld;
+  size_t off_a_hi, off_a_lo, off_b_hi, off_b_lo, end;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+PrepassLayout prepass_layout(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_layout al, mpg_layout bl,
+                             bool split, size_t base) {
+  PrepassLayout L;
+  L.a_outer = (al == MPG_ROW_MAJOR) ? m : k;
+  L.a_inner = (al == MPG_ROW_MAJOR) ? k : m;
+  L.b_outer = (bl == MPG_ROW_MAJOR) ? k : n;
+  L.b_inner = (bl == MPG_ROW_MAJOR) ? n : k;
+  L.a_ld = (L.a_inner + 7) / 8 * 8;
+  L.b_ld = (L.b_inner + 7) / 8 * 8;
+  const size_t a_bytes = align256((size_t)batch * L.a_outer * L.a_ld * 2);
+  const size_t b_bytes = align256((size_t)batch * L.b_outer * L.b_ld * 2);
+  size_t off = align256(base);
+  L.off_a_hi = off; off += a_bytes;
+  L.off_a_lo = off; off += split ? a_bytes : 0;
+  L.off_b_hi = off; off += b_bytes;
+  L.off_b_lo = off; off += split ? b_bytes : 0;
+  L.end = off;
+  return L;
+}
+
+bool prepass_mode(mpg_precision mode) {
+  return mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC || mode == MPG_SPLIT_FP16_3CHAIN ||
+         mode == MPG_SPLIT_FP16_1CHAIN;
 }
 
 mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
@@ -209,7 +247,19 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   }
   const bool tma = !o.force_generic_load && tma_ok(A, batch) && tma_ok(B, batch);
-  if (tma && p.conv == Conv::kNone && direct_layout_ok) p.src = Src::kTmaDirect;
+  if (o.prepass == 1 && p.conv != Conv::kNone) {
+    // convert in a separate pass; the product reads packed 16-bit copies
+    // (always TMA-aligned) on its direct path
+    p.prepass = true;
+    p.pre_conv = p.conv;
+    p.src = Src::kTmaDirect;
+    if (p.conv == Conv::kRoundF16 || p.conv == Conv::kRoundBF16) {
+      p.conv = Conv::kNone;
+      p.st = (p.op == Op::kBF16) ? SrcT::kBF16 : SrcT::kF16;
+    } else {
+      p.st = SrcT::kF16;
+    }
+  } else if (tma && p.conv == Conv::kNone && direct_layout_ok) p.src = Src::kTmaDirect;
   else if (tma && p.conv != Conv::kNone) p.src = Src::kTmaStaged;
   else p.src = Src::kGeneric;
 
@@ -217,7 +267,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   int bn;
   if (p.src == Src::kGeneric) {
     bn = 128;
-  } else if (p.src == Src::kTmaDirect) {
+  } else if (p.src == Src::kTmaDirect && p.conv == Conv::kNone) {
     bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
   } else if (p.conv == Conv::kSplit3) {
     bn = (n <= 64 || k <= 512) ? 64 : 128;
@@ -237,6 +287,14 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   p.bn = bn;
 
   int splits = choose_splits(m, n, k, batch, sm_count, o);
+  if (p.prepass) {
+    const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout,
+                                           p.conv == Conv::kSplit3 || p.conv == Conv::kSplit1,
+                                           splitk_bytes(splits, m, n, batch));
+    if (L.end > ws_bytes)
+      return fail(MPG_ERR_WORKSPACE, "the separate conversion pass needs %zu workspace bytes, got %zu", L.end,
+                  ws_bytes);
+  }
   if (splits > 1 && splitk_bytes(splits, m, n, batch) > ws_bytes) {
     if (o.splitk > 0)
       return fail(MPG_ERR_WORKSPACE, "split-K with %d partitions needs %zu workspace bytes, got %zu", splits,
@@ -327,7 +385,8 @@ mpg_status encode_map(CUtensorMap* map, const Operand& x, int64_t inner, int64_t
 
 mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, int64_t k, int64_t batch,
                      const Operand& A, const Operand& B, float* C, int64_t ldc, int64_t strideC, float alpha,
-                     float beta, const mpg_options& o, void* workspace, cudaStream_t stream) {
+                     float beta, const mpg_options& o, void* workspace, cudaStream_t stream,
+                     const Operand* A_lo = nullptr, const Operand* B_lo = nullptr) {
   TcKernel kern;
   if (!mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern))
     return fail(MPG_ERR_UNSUPPORTED, "no kernel for this configuration");
@@ -373,6 +432,18 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
     if (!b_mn) s = encode_map(&p.map_b, Bx, k, n, batch, BK, bn);
     else s = encode_map(&p.map_b, Bx, n, k, batch, BK, BK);
     if (s != MPG_OK) return s;
+    if (A_lo && B_lo) {
+      // lo halves of pre-split operands: same geometry as the hi halves
+      Operand Al = *A_lo, Bl = *B_lo;
+      Al.stride = a_stride;
+      Bl.stride = b_stride;
+      if (!a_mn) s = encode_map(&p.map_a_lo, Al, k, m, batch, BK, BM);
+      else s = encode_map(&p.map_a_lo, Al, m, k, batch, BK, BK);
+      if (s != MPG_OK) return s;
+      if (!b_mn) s = encode_map(&p.map_b_lo, Bl, k, n, batch, BK, bn);
+      else s = encode_map(&p.map_b_lo, Bl, n, k, batch, BK, BK);
+      if (s != MPG_OK) return s;
+    }
   }
   p.a = A.ptr;
   p.b = B.ptr;
@@ -497,7 +568,17 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   int sm = 152;
   if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
   t_err.clear();
-  return splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
+  const size_t partials = splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
+  if (o.prepass == 1 && prepass_mode(mode)) {
+    // layouts are not known here: take the larger of the two line paddings
+    const bool split = (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN);
+    size_t worst = 0;
+    for (mpg_layout al : {MPG_ROW_MAJOR, MPG_COL_MAJOR})
+      for (mpg_layout bl : {MPG_ROW_MAJOR, MPG_COL_MAJOR})
+        worst = std::max(worst, prepass_layout(m, n, k, batch, al, bl, split, partials).end);
+    return worst;
+  }
+  return partials;
 }
 
 mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
@@ -553,8 +634,35 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       e = launch_ffma(fp, st);
       break;
     }
-    case Kind::kTc:
-      return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
+    case Kind::kTc: {
+      if (!plan.prepass)
+        return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
+      // separate conversion pass into the workspace, then the direct path
+      const bool split = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit1);
+      const PrepassLayout L = prepass_layout(m, n, k, batch, a_layout, b_layout, split,
+                                             splitk_bytes(plan.splits, m, n, batch));
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      uint16_t* a_hi = reinterpret_cast<uint16_t*>(ws + L.off_a_hi);
+      uint16_t* a_lo = split ? reinterpret_cast<uint16_t*>(ws + L.off_a_lo) : nullptr;
+      uint16_t* b_hi = reinterpret_cast<uint16_t*>(ws + L.off_b_hi);
+      uint16_t* b_lo = split ? reinterpret_cast<uint16_t*>(ws + L.off_b_lo) : nullptr;
+      const int sa = split ? o.split_exp_a : 0, sb = split ? o.split_exp_b : 0;
+      const int64_t sA = strideA ? strideA : L.a_outer * lda;
+      const int64_t sB = strideB ? strideB : L.b_outer * ldb;
+      e = launch_prepass(plan.pre_conv, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi,
+                         a_lo, L.a_ld, std::ldexp(1.0f, sa), dev->sm_count, st);
+      if (e == cudaSuccess)
+        e = launch_prepass(plan.pre_conv, static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi,
+                           b_lo, L.b_ld, std::ldexp(1.0f, sb), dev->sm_count, st);
+      if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "conversion pass launch: %s", cudaGetErrorString(e));
+      const mpg_dtype cdt = (plan.op == Op::kBF16) ? MPG_BF16 : MPG_F16;
+      Operand Ah{a_hi, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
+      Operand Bh{b_hi, L.b_ld, L.b_outer * L.b_ld, cdt, b_layout};
+      Operand Al{a_lo, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
+      Operand Bl{b_lo, L.b_ld, L.b_outer * L.b_ld, cdt, b_layout};
+      return launch_tc(plan, dev, m, n, k, batch, Ah, Bh, C, ldc, strideC, alpha, beta, o, workspace, st,
+                       split ? &Al : nullptr, split ? &Bl : nullptr);
+    }
   }
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return MPG_OK;

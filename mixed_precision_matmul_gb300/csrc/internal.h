@@ -39,6 +39,8 @@ enum class SrcT : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 struct TcParams {
   CUtensorMap map_a;  // used by the TMA paths only
   CUtensorMap map_b;
+  CUtensorMap map_a_lo;  // direct split path: the lo halves of pre-split operands
+  CUtensorMap map_b_lo;
   const void* a;      // generic path addressing (element units of the source type)
   const void* b;
   int64_t lda, ldb, stride_a, stride_b;
@@ -102,6 +104,16 @@ cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c,
                                  cudaStream_t stream);
 
 cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_t stream);
+
+// Separate conversion pass: a stored fp32 matrix (per batch `outer` lines of
+// `inner` elements, leading dimension ld_in, batch stride stride_in) into
+// packed 16-bit copies with leading dimension ld_out (batch stride
+// outer * ld_out).  conv: kRoundF16, kRoundBF16, kSplit3 (hi, lo*2^11) or
+// kSplit1 (hi, lo); `lo` is written for the split only.  x is scaled by
+// `scale` (a power of two) before the split.
+cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
+                           int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
+                           int sm_count, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Device status word of the current device (allocated by the runtime as a

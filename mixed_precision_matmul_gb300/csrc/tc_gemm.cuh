@@ -357,20 +357,23 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             uint8_t* dst = (T::kStaged ? stg_base + st * T::kStgStage : op_base + st * T::kOpStage);
             mbar_arrive_expect_tx(&fullb[st], kStageBytes);
             const int k0 = kb * T::BK;
-            if (!p.a_mn_major) {
-              tma_load_3d(dst, &p.map_a, &fullb[st], k0, tc.mb * T::BM, tc.b);
+            // one operand tile: a single K-major box, or MN-major regions of BK
+            auto load_tile = [&](const CUtensorMap* map, uint8_t* d, bool mn, int row0, int rows) {
+              if (!mn) {
+                tma_load_3d(d, map, &fullb[st], k0, row0, tc.b);
+              } else {
+                for (int g = 0; g < rows / T::BK; ++g)
+                  tma_load_3d(d + g * kRegion, map, &fullb[st], row0 + g * T::BK, k0, tc.b);
+              }
+            };
+            load_tile(&p.map_a, dst, p.a_mn_major, tc.mb * T::BM, T::BM);
+            if constexpr (T::kSplit && !T::kHasConv) {
+              // pre-split operands: hi and lo halves of A, then of B
+              load_tile(&p.map_a_lo, dst + T::kATile, p.a_mn_major, tc.mb * T::BM, T::BM);
+              load_tile(&p.map_b, dst + 2 * T::kATile, p.b_mn_major, tc.nb * T::BN, T::BN);
+              load_tile(&p.map_b_lo, dst + 2 * T::kATile + T::kBTile, p.b_mn_major, tc.nb * T::BN, T::BN);
             } else {
-#pragma unroll
-              for (int g = 0; g < T::BM / T::BK; ++g)
-                tma_load_3d(dst + g * kRegion, &p.map_a, &fullb[st], tc.mb * T::BM + g * T::BK, k0, tc.b);
-            }
-            uint8_t* dstb = dst + kABytes;
-            if (!p.b_mn_major) {
-              tma_load_3d(dstb, &p.map_b, &fullb[st], k0, tc.nb * T::BN, tc.b);
-            } else {
-#pragma unroll
-              for (int g = 0; g < T::BN / T::BK; ++g)
-                tma_load_3d(dstb + g * kRegion, &p.map_b, &fullb[st], tc.nb * T::BN + g * T::BK, k0, tc.b);
+              load_tile(&p.map_b, dst + kABytes, p.b_mn_major, tc.nb * T::BN, T::BN);
             }
           }
         }

@@ -112,3 +112,48 @@ def test_round_on_load_256_wide_tiles(mode, m, n, k, al, bl, pad):
     c.run()
     eR, eQ = c.errors()
     assert eQ <= TOL["q16"], (eR, eQ)
+
+
+@pytest.mark.parametrize("mode", [mpg.FP16_F32ACC, mpg.BF16_F32ACC, mpg.SPLIT_FP16_3CHAIN,
+                                  mpg.SPLIT_FP16_1CHAIN])
+@pytest.mark.parametrize("m,n,k,al,bl,pad,batch", [
+    (128, 128, 64, R, Cm, (0, 0, 0), 1),
+    (333, 270, 150, R, R, (4, 4, 4), 1),
+    (140, 300, 72, Cm, R, (3, 1, 4), 2),       # odd pitches: the copies are re-pitched for TMA
+    (100, 100, 700, R, Cm, (0, 4, 0), 1),      # split-K as well
+])
+def test_separate_conversion_pass(mode, m, n, k, al, bl, pad, batch):
+    """Operands converted by the separate pass into the workspace, then the
+    direct TMA path: same bars as the on-the-fly conversion."""
+    mpg.build()
+    c = Case(m, n, k, mode, batch=batch, a_layout=al, b_layout=bl, pad=pad, alpha=1.25, beta=-0.5,
+             opts=mpg.options(prepass=1))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)
+    if mode == mpg.SPLIT_FP16_3CHAIN:
+        assert eR <= TOL["split"], eR
+
+
+def test_separate_conversion_pass_operand_scale():
+    import synthetic
+    mpg.build()
+    a = synthetic.uniform((1, 200, 300), 71, 0.0, 1e-5)
+    b = synthetic.normal((1, 300, 130), 72)
+    c = Case(200, 130, 300, mpg.SPLIT_FP16_3CHAIN, a=a, b=b, opts=mpg.options(split_exp_a=14, prepass=1))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
+
+
+def test_separate_conversion_pass_needs_workspace():
+    import torch
+    mpg.build()
+    m = n = k = 256
+    A = torch.zeros((m, k), device="cuda")
+    B = torch.zeros((k, n), device="cuda")
+    C = torch.zeros((m, n), device="cuda")
+    st = mpg.gemm_raw(m, n, k, 1, A.data_ptr(), k, 0, mpg.F32, R, B.data_ptr(), n, 0, mpg.F32, R, C.data_ptr(), n,
+                      0, 1.0, 0.0, mpg.SPLIT_FP16_3CHAIN, opts=mpg.options(prepass=1), check=False)
+    assert st == mpg.ERR_WORKSPACE
+    assert mpg.workspace_size(m, n, k, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(prepass=1)) >= 4 * (m * k + k * n)

@@ -1,0 +1,55 @@
+"""GPU: a seeded random sweep over the product's parameter space — precision
+mode, storage type, both layouts, ragged sizes, leading-dimension padding,
+batches, alpha/beta, tile width, forced generic loads, split-K — each case
+checked against the oracle with the bar of its mode."""
+import numpy as np
+import pytest
+
+import mixed_precision_matmul_gb300 as mpg
+from helpers import TOL, Case
+
+pytestmark = pytest.mark.gpu
+
+MODES = [(mpg.FP16_F32ACC, "f32"), (mpg.FP16_F32ACC, "f16"), (mpg.BF16_F32ACC, "f32"),
+         (mpg.BF16_F32ACC, "bf16"), (mpg.TF32, "f32"), (mpg.SPLIT_FP16_3CHAIN, "f32"),
+         (mpg.SPLIT_FP16_1CHAIN, "f32"), (mpg.FP32_FFMA, "f32")]
+
+
+def _cases(n=64, seed=20251):
+    g = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for i in range(n):
+        mode, dt = MODES[i % len(MODES)]
+        m = int(g.integers(1, 300))
+        nn = int(g.integers(1, 300))
+        k = int(g.integers(1, 400))
+        batch = int(g.choice([1, 1, 1, 2, 3]))
+        al = int(g.integers(0, 2))
+        bl = int(g.integers(0, 2))
+        pad = tuple(int(x) for x in g.choice([0, 0, 1, 3, 8], size=3))
+        alpha = float(g.choice([1.0, -0.5, 2.0]))
+        beta = float(g.choice([0.0, 0.0, 1.0, -0.75]))
+        force = int(g.random() < 0.2)
+        splitk = int(g.choice([0, 0, 0, 2, 3])) if mode != mpg.FP32_FFMA else 0
+        prepass = int(g.random() < 0.3 and dt == "f32" and mode not in (mpg.TF32, mpg.FP32_FFMA))
+        out.append((i, mode, dt, m, nn, k, batch, al, bl, pad, alpha, beta, force, splitk, prepass))
+    return out
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: f"c{c[0]}")
+def test_random_case(case):
+    i, mode, dt, m, n, k, batch, al, bl, pad, alpha, beta, force, splitk, prepass = case
+    mpg.build()
+    opts = mpg.options(force_generic_load=force, splitk=splitk, prepass=prepass)
+    c = Case(m, n, k, mode, batch=batch, in_dtype=dt, a_layout=al, b_layout=bl, pad=pad,
+             alpha=alpha, beta=beta, seed=i, dist="normal", opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    if mode == mpg.TF32:
+        assert eR <= TOL["tf32"], eR
+    elif mode == mpg.FP32_FFMA:
+        assert eR <= TOL["q16"], eR
+    else:
+        assert eQ <= TOL["q16"], (eR, eQ)
+    if mode == mpg.SPLIT_FP16_3CHAIN:
+        assert eR <= TOL["split"], eR
