@@ -209,9 +209,11 @@ def mode_cases(torch, mpg, synthetic, device):
     # C2: batched 2048 x (64x4096 * 4096x64), padded leading dims
     for mn in ("tf32", "fp16"):
         yield f"batched2048_{mn}", lambda mn=mn: make_batched(torch, mpg, synthetic, device, mn)
-    # C5: attention pair in split3
+    # C5: attention pair in split3 (conversion in the load stage, and by the separate pass)
     yield "attention_qkt_split3", lambda: make_attention(torch, mpg, synthetic, device, "qkt")
     yield "attention_pv_split3", lambda: make_attention(torch, mpg, synthetic, device, "pv")
+    yield "attention_qkt_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "qkt", 1)
+    yield "attention_pv_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "pv", 1)
 
 
 def make_batched(torch, mpg, synthetic, device, mode_name):
@@ -230,7 +232,7 @@ def make_batched(torch, mpg, synthetic, device, mode_name):
                     {"a": a, "bt": bt}, algo_bytes=algo)
 
 
-def make_attention(torch, mpg, synthetic, device, which):
+def make_attention(torch, mpg, synthetic, device, which, prepass=0):
     q, kk, p, v = synthetic.attention_inputs()
     if which == "qkt":
         # S = Q K^T: A = Q (2048x128 row-major), B = K^T, i.e. K stored row-major = B column-major
@@ -239,12 +241,12 @@ def make_attention(torch, mpg, synthetic, device, which):
         algo = 4 * (2048 * 128 + 32768 * 128 + 2048 * 32768)
         return Workload("attention_qkt", 2048, 32768, 128, 1, "split3", A, B, None, 128, 128, 32768,
                         0, 0, 0, mpg.ROW_MAJOR, mpg.COL_MAJOR, mpg.F32, 1.0, 0.0,
-                        {"a": q, "b": kk.T}, algo_bytes=algo)
+                        {"a": q, "b": kk.T}, opts=mpg.options(prepass=prepass), algo_bytes=algo)
     A = torch.from_numpy(p).to(device)
     B = torch.from_numpy(v).to(device)
     algo = 4 * (2048 * 32768 + 32768 * 128 + 2048 * 128)
     # P holds probabilities (<= 1): lift it into fp16's normal range by 2^14
-    opts = mpg.options(split_exp_a=14)
+    opts = mpg.options(split_exp_a=14, prepass=prepass)
     return Workload("attention_pv", 2048, 128, 32768, 1, "split3", A, B, None, 32768, 128, 128,
                     0, 0, 0, mpg.ROW_MAJOR, mpg.ROW_MAJOR, mpg.F32, 1.0, 0.0,
                     {"a": p, "b": v, "exp_a": 14}, opts=opts, algo_bytes=algo)

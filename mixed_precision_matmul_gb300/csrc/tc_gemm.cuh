@@ -3,9 +3,12 @@
 // One persistent, warp-specialised kernel template:
 //   warp 0       TMA producer (direct and staged paths)
 //   warp 1       TMEM allocator and the single thread that issues tcgen05.mma
-//   warps 2..5   epilogue: tcgen05.ld -> chain sum -> alpha/beta -> stores
-//   warps 6..13  converters (staged and generic paths): fp32 -> fp16/bf16 or
-//                the hi/lo split, written into the swizzled operand stages
+//   warps 2..    epilogue: tcgen05.ld -> chain sum -> alpha/beta -> stores
+//                (4 warps, one per TMEM lane quarter; 8 on the direct path,
+//                two per quarter, each taking half of the tile's columns)
+//   then         converters (staged and generic paths, 8 warps): fp32 ->
+//                fp16/bf16 or the hi/lo split, written into the swizzled
+//                operand stages
 //
 // The accumulator lives in TMEM for the whole K loop (the register/accumulator
 // residency of "tile_matmul(): use the cuBLASDx register-accumulator API ...",
@@ -60,7 +63,10 @@ struct TcTraits {
   static_assert(kStages >= 2, "pipeline needs two stages");
   static constexpr int kConvWarps = kHasConv ? 8 : 0;
   static constexpr int kConvThreads = kConvWarps * 32;
-  static constexpr int kThreads = (6 + kConvWarps) * 32;
+  static constexpr int kEpiWarps = kHasConv ? 4 : 8;
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kConvWarp0 = 2 + kEpiWarps;    // first converter warp
+  static constexpr int kThreads = (2 + kEpiWarps + kConvWarps) * 32;
   // TMEM: columns of one accumulator (all chains), buffers, allocation.
   // The three-chain split accumulates K in chunks: each chunk starts fresh
   // chains, and the epilogue folds hh + 2^-11 (hl + lh) of every chunk into
@@ -77,7 +83,7 @@ struct TcTraits {
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  static constexpr int kEpiBytes = 4 * 32 * 32 * 4;
+  static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
   static constexpr int kNumBars = 4 * kStages + 2 * kAccBufs + 1;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kOpStage + kStgStage) + kEpiBytes +
                                     kNumBars * 8 + 16;
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
     }
     for (int i = 0; i < T::kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], T::kEpiThreads);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -445,11 +451,16 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       mma_commit(done_bar);
       drain_wait(done_bar, 0, p.wait_limit_ns);
     }
-  } else if (warp < 6) {
+  } else if (warp < T::kConvWarp0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     float* stg = epi_base + (warp - 2) * 1024;
+    // warps sharing a lane quarter split the tile's 32-column chunks
+    constexpr int kColGroups = T::kEpiWarps / 4;
+    constexpr int kCcPer = T::BN / 32 / kColGroups;
+    static_assert(kCcPer >= 1 && (T::BN / 32) % kColGroups == 0, "epilogue column split");
+    const int cc0 = ((warp - 2) / 4) * kCcPer;
     const uint32_t stg_addr = smem_addr(stg);
     uint32_t g = 0;   // accumulation chunk, in the MMA warp's order
     bool ok = true;
@@ -486,7 +497,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
         const bool last = (ci == nchunks - 1);
         const bool have_run = (ci > 0);
   #pragma unroll 1
-        for (int cc = 0; cc < T::BN / 32; ++cc) {
+        for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
           float v[32];
           if constexpr (T::kPromote) {
             // chunk total hh + 2^-11 (hl + lh), plus the running sum of the
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             tmem_ld_32cols(tacc + cc * 32, v);
             tmem_ld_wait();
           }
-          if (cc == T::BN / 32 - 1) {
+          if (cc == cc0 + kCcPer - 1) {
             // this warp's share of the chunk is now in registers / the running sum
             if constexpr (T::kPromote) {
               if (!last) tmem_st_wait();
@@ -578,7 +589,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
   } else {
     // ------------------------------------------------------------ converters
     if constexpr (T::kHasConv) {
-      const int ct = threadIdx.x - 6 * 32;
+      const int ct = threadIdx.x - T::kConvWarp0 * 32;
       constexpr int kChunks = (T::BM + T::BN) * 8;  // 4-element chunks per stage
       constexpr int kPerThread = kChunks / T::kConvThreads;
       static_assert(kChunks % T::kConvThreads == 0, "chunk split");
