@@ -168,7 +168,7 @@ struct PrepassLayout {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 PrepassLayout prepass_layout(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_layout al, mpg_layout bl,
-                             bool split, size_t base) {
+                             bool split_a, bool split_b, size_t base) {
   PrepassLayout L;
   L.a_outer = (al == MPG_ROW_MAJOR) ? m : k;
   L.a_inner = (al == MPG_ROW_MAJOR) ? k : m;
@@ -180,17 +180,21 @@ PrepassLayout prepass_layout(int64_t m, int64_t n, int64_t k, int64_t batch, mpg
   const size_t b_bytes = align256((size_t)batch * L.b_outer * L.b_ld * 2);
   size_t off = align256(base);
   L.off_a_hi = off; off += a_bytes;
-  L.off_a_lo = off; off += split ? a_bytes : 0;
+  L.off_a_lo = off; off += split_a ? a_bytes : 0;
   L.off_b_hi = off; off += b_bytes;
-  L.off_b_lo = off; off += split ? b_bytes : 0;
+  L.off_b_lo = off; off += split_b ? b_bytes : 0;
   L.end = off;
   return L;
 }
 
 bool prepass_mode(mpg_precision mode) {
   return mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC || mode == MPG_SPLIT_FP16_3CHAIN ||
-         mode == MPG_SPLIT_FP16_1CHAIN;
+         mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_A_FP16_2CHAIN;
 }
+
+// Which operands carry hi and lo copies under a conversion.
+bool splits_a(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplitA2; }
+bool splits_b(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1; }
 
 mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
                      float alpha, mpg_precision mode, const mpg_options& o, int sm_count, size_t ws_bytes,
@@ -243,6 +247,11 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       p.conv = Conv::kSplit1;
       p.st = SrcT::kF32;
       break;
+    case MPG_SPLIT_A_FP16_2CHAIN:
+      p.op = Op::kF16;
+      p.conv = Conv::kSplitA2;
+      p.st = SrcT::kF32;
+      break;
     default:
       return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   }
@@ -269,7 +278,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = 128;
   } else if (p.src == Src::kTmaDirect && p.conv == Conv::kNone) {
     bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
-  } else if (p.conv == Conv::kSplit3) {
+  } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2) {
     bn = (n <= 64 || k <= 512) ? 64 : 128;
   } else if (p.conv == Conv::kSplit1) {
     bn = n <= 64 ? 64 : 128;
@@ -288,8 +297,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
 
   int splits = choose_splits(m, n, k, batch, sm_count, o);
   if (p.prepass) {
-    const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout,
-                                           p.conv == Conv::kSplit3 || p.conv == Conv::kSplit1,
+    const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout, splits_a(p.conv), splits_b(p.conv),
                                            splitk_bytes(splits, m, n, batch));
     if (L.end > ws_bytes)
       return fail(MPG_ERR_WORKSPACE, "the separate conversion pass needs %zu workspace bytes, got %zu", L.end,
@@ -318,7 +326,8 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
                 (long long)n, (long long)k, (long long)batch);
   if (m > kMax || n > kMax || k > kMax || batch > kMax)
     return fail(MPG_ERR_INVALID_ARG, "size beyond 2^31-1");
-  if ((int)mode < 0 || (int)mode > (int)MPG_FP32_FFMA) return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
+  if ((int)mode < 0 || (int)mode > (int)MPG_SPLIT_A_FP16_2CHAIN)
+    return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   for (const Operand* x : {&A, &B}) {
     if ((int)x->dt < 0 || (int)x->dt > 2) return fail(MPG_ERR_INVALID_ARG, "unknown dtype %d", (int)x->dt);
     if ((int)x->layout < 0 || (int)x->layout > 1) return fail(MPG_ERR_INVALID_ARG, "unknown layout %d", (int)x->layout);
@@ -432,14 +441,17 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
     if (!b_mn) s = encode_map(&p.map_b, Bx, k, n, batch, BK, bn);
     else s = encode_map(&p.map_b, Bx, n, k, batch, BK, BK);
     if (s != MPG_OK) return s;
-    if (A_lo && B_lo) {
-      // lo halves of pre-split operands: same geometry as the hi halves
-      Operand Al = *A_lo, Bl = *B_lo;
+    // lo halves of pre-split operands: same geometry as the hi halves
+    if (A_lo) {
+      Operand Al = *A_lo;
       Al.stride = a_stride;
-      Bl.stride = b_stride;
       if (!a_mn) s = encode_map(&p.map_a_lo, Al, k, m, batch, BK, BM);
       else s = encode_map(&p.map_a_lo, Al, m, k, batch, BK, BK);
       if (s != MPG_OK) return s;
+    }
+    if (B_lo) {
+      Operand Bl = *B_lo;
+      Bl.stride = b_stride;
       if (!b_mn) s = encode_map(&p.map_b_lo, Bl, k, n, batch, BK, bn);
       else s = encode_map(&p.map_b_lo, Bl, n, k, batch, BK, BK);
       if (s != MPG_OK) return s;
@@ -483,7 +495,7 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.b_vec_ok = vec_ok(B, b_stride);
   p.partial = splits_eff > 1 ? static_cast<float*>(workspace) : nullptr;
   p.p_vec_ok = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(workspace) % 16 == 0);
-  const bool split = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit1);
+  const bool split = splits_a(plan.conv);
   const int sa = split ? o.split_exp_a : 0, sb = split ? o.split_exp_b : 0;
   p.alpha = (float)std::ldexp((double)alpha, -(sa + sb));
   p.beta = beta;
@@ -492,7 +504,7 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.status = dev->status;
   p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
   p.chunk_kb = 0;
-  if (plan.conv == Conv::kSplit3 && o.split_chunk_k >= 0) {
+  if ((plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplitA2) && o.split_chunk_k >= 0) {
     const int64_t chunk_k = o.split_chunk_k > 0 ? o.split_chunk_k : kDefaultSplitChunkK;
     p.chunk_kb = (int32_t)std::min<int64_t>((chunk_k + BK - 1) / BK, p.num_k_blk);
   }
@@ -571,11 +583,12 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   const size_t partials = splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
   if (o.prepass == 1 && prepass_mode(mode)) {
     // layouts are not known here: take the larger of the two line paddings
-    const bool split = (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN);
+    const bool split_b = (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN);
+    const bool split_a = split_b || mode == MPG_SPLIT_A_FP16_2CHAIN;
     size_t worst = 0;
     for (mpg_layout al : {MPG_ROW_MAJOR, MPG_COL_MAJOR})
       for (mpg_layout bl : {MPG_ROW_MAJOR, MPG_COL_MAJOR})
-        worst = std::max(worst, prepass_layout(m, n, k, batch, al, bl, split, partials).end);
+        worst = std::max(worst, prepass_layout(m, n, k, batch, al, bl, split_a, split_b, partials).end);
     return worst;
   }
   return partials;
@@ -638,22 +651,25 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       if (!plan.prepass)
         return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
       // separate conversion pass into the workspace, then the direct path
-      const bool split = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit1);
-      const PrepassLayout L = prepass_layout(m, n, k, batch, a_layout, b_layout, split,
+      const bool sa_ = splits_a(plan.conv), sb_ = splits_b(plan.conv);
+      const PrepassLayout L = prepass_layout(m, n, k, batch, a_layout, b_layout, sa_, sb_,
                                              splitk_bytes(plan.splits, m, n, batch));
       uint8_t* ws = static_cast<uint8_t*>(workspace);
       uint16_t* a_hi = reinterpret_cast<uint16_t*>(ws + L.off_a_hi);
-      uint16_t* a_lo = split ? reinterpret_cast<uint16_t*>(ws + L.off_a_lo) : nullptr;
+      uint16_t* a_lo = sa_ ? reinterpret_cast<uint16_t*>(ws + L.off_a_lo) : nullptr;
       uint16_t* b_hi = reinterpret_cast<uint16_t*>(ws + L.off_b_hi);
-      uint16_t* b_lo = split ? reinterpret_cast<uint16_t*>(ws + L.off_b_lo) : nullptr;
-      const int sa = split ? o.split_exp_a : 0, sb = split ? o.split_exp_b : 0;
+      uint16_t* b_lo = sb_ ? reinterpret_cast<uint16_t*>(ws + L.off_b_lo) : nullptr;
+      const int ea = sa_ ? o.split_exp_a : 0, eb = sa_ ? o.split_exp_b : 0;
+      // the two-chain split splits A only; its B is rounded to fp16
+      const Conv conv_a = (plan.pre_conv == Conv::kSplitA2) ? Conv::kSplit3 : plan.pre_conv;
+      const Conv conv_b = (plan.pre_conv == Conv::kSplitA2) ? Conv::kRoundF16 : plan.pre_conv;
       const int64_t sA = strideA ? strideA : L.a_outer * lda;
       const int64_t sB = strideB ? strideB : L.b_outer * ldb;
-      e = launch_prepass(plan.pre_conv, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi,
-                         a_lo, L.a_ld, std::ldexp(1.0f, sa), dev->sm_count, st);
+      e = launch_prepass(conv_a, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi, a_lo,
+                         L.a_ld, std::ldexp(1.0f, ea), dev->sm_count, st);
       if (e == cudaSuccess)
-        e = launch_prepass(plan.pre_conv, static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi,
-                           b_lo, L.b_ld, std::ldexp(1.0f, sb), dev->sm_count, st);
+        e = launch_prepass(conv_b, static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi, b_lo,
+                           L.b_ld, std::ldexp(1.0f, eb), dev->sm_count, st);
       if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "conversion pass launch: %s", cudaGetErrorString(e));
       const mpg_dtype cdt = (plan.op == Op::kBF16) ? MPG_BF16 : MPG_F16;
       Operand Ah{a_hi, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
@@ -661,7 +677,7 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       Operand Al{a_lo, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
       Operand Bl{b_lo, L.b_ld, L.b_outer * L.b_ld, cdt, b_layout};
       return launch_tc(plan, dev, m, n, k, batch, Ah, Bh, C, ldc, strideC, alpha, beta, o, workspace, st,
-                       split ? &Al : nullptr, split ? &Bl : nullptr);
+                       sa_ ? &Al : nullptr, sb_ ? &Bl : nullptr);
     }
   }
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));

@@ -22,6 +22,7 @@ enum class Conv : int {
   kRoundBF16 = 2, // fp32 -> bf16 round-to-nearest-even
   kSplit3 = 3,    // fp32 -> hi, lo*2^11; three accumulator chains
   kSplit1 = 4,    // fp32 -> hi, lo; one shared accumulator chain
+  kSplitA2 = 5,   // A: fp32 -> hi, lo*2^11; B: fp32 -> fp16; two chains (A_hi B, A_lo B)
 };
 
 // Bits of the device status word.

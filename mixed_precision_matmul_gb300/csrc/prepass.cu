@@ -11,45 +11,72 @@
 namespace mpg {
 namespace {
 
+// Convert 8 consecutive fp32 values into 8 16-bit values (hi) and, for the
+// split, 8 lo values, packed as four 32-bit words each.
+template <Conv CV>
+__device__ __forceinline__ void convert8(const float (&x)[8], float scale, uint4& hi, uint4& lo) {
+  uint32_t w[4], l[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if constexpr (CV == Conv::kRoundF16) {
+      w[j] = pack_f16x2(x[2 * j] * scale, x[2 * j + 1] * scale);   // scale: 1, or 2^s for a split's B
+    } else if constexpr (CV == Conv::kRoundBF16) {
+      w[j] = pack_bf16x2(x[2 * j] * scale, x[2 * j + 1] * scale);
+    } else {
+      constexpr int L = (CV == Conv::kSplit3) ? 11 : 0;
+      split_pair<L>(x[2 * j], x[2 * j + 1], scale, w[j], l[j]);
+    }
+  }
+  hi = make_uint4(w[0], w[1], w[2], w[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// One work item = 8 consecutive elements of one line; each thread handles two
+// items per loop trip, loading both before converting either.
 template <Conv CV>
 __global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ in, int64_t ld_in,
                                                       int64_t stride_in, int64_t outer, int64_t inner,
                                                       int64_t batch, uint16_t* __restrict__ hi,
                                                       uint16_t* __restrict__ lo, int64_t ld_out, float scale,
                                                       int vec) {
-  const int64_t chunks_per_line = (inner + 3) / 4;
-  const int64_t per_batch = outer * chunks_per_line;
+  constexpr bool kSplit = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
+  const int64_t items_per_line = (inner + 7) / 8;
+  const int64_t per_batch = outer * items_per_line;
   const int64_t total = per_batch * batch;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t b = i / per_batch;
-    const int64_t r = i - b * per_batch;
-    const int64_t line = r / chunks_per_line;
-    const int64_t c = (r - line * chunks_per_line) * 4;
-    const float* src = in + b * stride_in + line * ld_in + c;
-    float x[4];
-    if (vec && c + 3 < inner) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    } else {
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total; i0 += 2 * step) {
+    float x[2][8];
+    int64_t o[2];
+    bool live[2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = (c + e < inner) ? __ldg(src + e) : 0.0f;
+    for (int u = 0; u < 2; ++u) {
+      const int64_t i = i0 + u * step;
+      live[u] = i < total;
+      const int64_t ii = live[u] ? i : 0;
+      const int64_t b = ii / per_batch;
+      const int64_t r = ii - b * per_batch;
+      const int64_t line = r / items_per_line;
+      const int64_t c = (r - line * items_per_line) * 8;
+      const float* src = in + b * stride_in + line * ld_in + c;
+      o[u] = b * outer * ld_out + line * ld_out + c;   // ld_out % 8 == 0: 16-byte aligned
+      if (vec && c + 7 < inner) {
+        const float4 v0 = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
+        x[u][0] = v0.x; x[u][1] = v0.y; x[u][2] = v0.z; x[u][3] = v0.w;
+        x[u][4] = v1.x; x[u][5] = v1.y; x[u][6] = v1.z; x[u][7] = v1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[u][e] = (live[u] && c + e < inner) ? __ldg(src + e) : 0.0f;
+      }
     }
-    uint32_t w0, w1, l0 = 0, l1 = 0;
-    if constexpr (CV == Conv::kRoundF16) {
-      w0 = pack_f16x2(x[0], x[1]);
-      w1 = pack_f16x2(x[2], x[3]);
-    } else if constexpr (CV == Conv::kRoundBF16) {
-      w0 = pack_bf16x2(x[0], x[1]);
-      w1 = pack_bf16x2(x[2], x[3]);
-    } else {
-      constexpr int L = (CV == Conv::kSplit3) ? 11 : 0;
-      split_pair<L>(x[0], x[1], scale, w0, l0);
-      split_pair<L>(x[2], x[3], scale, w1, l1);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!live[u]) continue;
+      uint4 h, l;
+      convert8<CV>(x[u], scale, h, l);
+      *reinterpret_cast<uint4*>(hi + o[u]) = h;
+      if constexpr (kSplit) *reinterpret_cast<uint4*>(lo + o[u]) = l;
     }
-    const int64_t o = b * outer * ld_out + line * ld_out + c;   // ld_out % 8 == 0: 8-byte aligned
-    *reinterpret_cast<uint2*>(hi + o) = make_uint2(w0, w1);
-    if constexpr (CV == Conv::kSplit3 || CV == Conv::kSplit1) *reinterpret_cast<uint2*>(lo + o) = make_uint2(l0, l1);
   }
 }
 
@@ -58,8 +85,8 @@ __global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ 
 cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
                            int sm_count, cudaStream_t stream) {
-  const int64_t total = batch * outer * ((inner + 3) / 4);
-  int64_t blocks = (total + 255) / 256;
+  const int64_t total = batch * outer * ((inner + 7) / 8);
+  int64_t blocks = (total + 511) / 512;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
   if (blocks < 1) blocks = 1;
   const int vec = reinterpret_cast<uintptr_t>(in) % 16 == 0 && ld_in % 4 == 0 && (batch == 1 || stride_in % 4 == 0);

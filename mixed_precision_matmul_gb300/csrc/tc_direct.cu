@@ -13,6 +13,8 @@ bool tc_lookup_direct(Conv conv, Op op, int bn, TcKernel* out) {
   MPG_DIRECT_SPLIT(Conv::kSplit3, 64)
   MPG_DIRECT_SPLIT(Conv::kSplit1, 128)
   MPG_DIRECT_SPLIT(Conv::kSplit1, 64)
+  MPG_DIRECT_SPLIT(Conv::kSplitA2, 128)
+  MPG_DIRECT_SPLIT(Conv::kSplitA2, 64)
 #undef MPG_DIRECT_SPLIT
   if (conv != Conv::kNone) return false;
 #define MPG_DIRECT(OPV, STV, BNV)                                                  \

@@ -47,11 +47,14 @@ struct TcTraits {
   static constexpr uint32_t kSwizzle = (kRowBytes == 128) ? kSwizzle128B : kSwizzle64B;
   static constexpr int kKSteps = kRowBytes / 32;   // MMAs of 32 bytes of K each
   static constexpr int kInstrK = 32 / kOpBytes;    // 16 (f16/bf16) or 8 (tf32)
-  static constexpr bool kSplit = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
-  static constexpr int kCopies = kSplit ? 2 : 1;
+  // operands that carry a hi and a lo copy in the stages
+  static constexpr bool kSplitA = (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplitA2);
+  static constexpr bool kSplitB = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
+  static constexpr int kCopiesA = kSplitA ? 2 : 1;
+  static constexpr int kCopiesB = kSplitB ? 2 : 1;
   static constexpr int kATile = BM * kRowBytes;
   static constexpr int kBTile = BN * kRowBytes;
-  static constexpr int kOpStage = kCopies * (kATile + kBTile);
+  static constexpr int kOpStage = kCopiesA * kATile + kCopiesB * kBTile;
   static constexpr bool kStaged = (S == Src::kTmaStaged);
   static constexpr bool kHasConv = (S != Src::kTmaDirect);
   static constexpr int kStgATile = kStaged ? BM * 128 : 0;
@@ -71,8 +74,8 @@ struct TcTraits {
   // The three-chain split accumulates K in chunks: each chunk starts fresh
   // chains, and the epilogue folds hh + 2^-11 (hl + lh) of every chunk into
   // an fp32 running sum (round to nearest) kept in kRunCols extra columns.
-  static constexpr bool kPromote = (CV == Conv::kSplit3);
-  static constexpr int kChainCols = (CV == Conv::kSplit3) ? 3 * BN : BN;
+  static constexpr bool kPromote = (CV == Conv::kSplit3 || CV == Conv::kSplitA2);
+  static constexpr int kChainCols = (CV == Conv::kSplit3) ? 3 * BN : (CV == Conv::kSplitA2) ? 2 * BN : BN;
   static constexpr int kRunCols = kPromote ? BN : 0;
   static constexpr int kAccStride = kPromote ? kChainCols
                                     : kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
@@ -225,7 +228,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // tf32 operands w[0..3] are the fp32 bits.
 template <class T>
 __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned short (&h)[4], float scale,
-                                           uint32_t (&w)[4]) {
+                                           uint32_t (&w)[4], bool isA) {
   if constexpr (T::kOpBytes == 4) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(x[e]);
@@ -241,6 +244,16 @@ __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned s
     w[0] = pack_bf16x2(x[0], x[1]);
     w[1] = pack_bf16x2(x[2], x[3]);
     w[2] = w[3] = 0;
+  } else if constexpr (T::kConv == Conv::kSplitA2) {
+    // A is split (lo scaled by 2^11), B rounded to fp16
+    if (isA) {
+      split_pair<11>(x[0], x[1], scale, w[0], w[2]);
+      split_pair<11>(x[2], x[3], scale, w[1], w[3]);
+    } else {
+      w[0] = pack_f16x2(x[0] * scale, x[1] * scale);
+      w[1] = pack_f16x2(x[2] * scale, x[3] * scale);
+      w[2] = w[3] = 0;
+    }
   } else {
     constexpr int L = (T::kConv == Conv::kSplit3) ? 11 : 0;
     split_pair<L>(x[0], x[1], scale, w[0], w[2]);
@@ -252,7 +265,7 @@ __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned s
 // operand tile(s) at `hi_tile` (and `lo_tile` for the split).
 template <class T>
 __device__ __forceinline__ void store_chunk(const uint32_t (&w)[4], uint32_t hi_tile, uint32_t lo_tile, uint32_t lg,
-                                            uint32_t ch, bool transpose) {
+                                            uint32_t ch, bool transpose, bool isA) {
   if constexpr (T::kOpBytes == 4) {
     if (transpose) {
       // tf32 operands are kept K-major in shared memory: an MN-major source
@@ -273,7 +286,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&w)[4], uint32_t hi_
     // 16-bit operand, 64-byte lines: 4 values = half of a 16-byte chunk
     const uint32_t off = swz_chunk_offset<64>(lg, ch >> 1) + ((ch & 1u) << 3);
     st_shared_v2(hi_tile + off, w[0], w[1]);
-    if constexpr (T::kSplit) st_shared_v2(lo_tile + off, w[2], w[3]);
+    if ((isA && T::kSplitA) || (!isA && T::kSplitB)) st_shared_v2(lo_tile + off, w[2], w[3]);
   }
 }
 
@@ -373,11 +386,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               }
             };
             load_tile(&p.map_a, dst, p.a_mn_major, tc.mb * T::BM, T::BM);
-            if constexpr (T::kSplit && !T::kHasConv) {
-              // pre-split operands: hi and lo halves of A, then of B
+            if constexpr (T::kSplitA && !T::kHasConv) {
+              // pre-split operands: hi and lo halves of A, then of B (B may be single)
               load_tile(&p.map_a_lo, dst + T::kATile, p.a_mn_major, tc.mb * T::BM, T::BM);
               load_tile(&p.map_b, dst + 2 * T::kATile, p.b_mn_major, tc.nb * T::BN, T::BN);
-              load_tile(&p.map_b_lo, dst + 2 * T::kATile + T::kBTile, p.b_mn_major, tc.nb * T::BN, T::BN);
+              if constexpr (T::kSplitB)
+                load_tile(&p.map_b_lo, dst + 2 * T::kATile + T::kBTile, p.b_mn_major, tc.nb * T::BN, T::BN);
             } else {
               load_tile(&p.map_b, dst + kABytes, p.b_mn_major, tc.nb * T::BN, T::BN);
             }
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             tc_fence_after_sync();
             const uint32_t a_hi = op_smem + st * T::kOpStage;
             const uint32_t a_lo = a_hi + T::kATile;                       // split only
-            const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
+            const uint32_t b_hi = a_hi + T::kCopiesA * T::kATile;
             const uint32_t b_lo = b_hi + T::kBTile;                       // split only
 #pragma unroll
             for (int ks = 0; ks < T::kKSteps; ++ks) {
@@ -432,6 +446,10 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
                 // lh = A_lo * B_hi
                 mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
+              } else if constexpr (T::kConv == Conv::kSplitA2) {
+                // two chains: A_hi B and A_lo B (B single)
+                mma_f16(d0, da_hi, db_hi, idesc_n, acc);
+                mma_f16(d0 + T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
               } else if constexpr (T::kConv == Conv::kSplit1) {
                 // one chain: hh, hl and lh all accumulate into the same columns
                 mma_f16(d0, da_hi, db_hi, idesc_n, acc);
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
         for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
           float v[32];
           if constexpr (T::kPromote) {
-            // chunk total hh + 2^-11 (hl + lh), plus the running sum of the
+            // chunk total of the split's chains, plus the running sum of the
             // earlier chunks of this tile
   #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -508,12 +526,14 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               const uint32_t col = cc * 32 + h * 16;
               tmem_ld_16cols(tacc + col, x0);
               tmem_ld_16cols(tacc + T::BN + col, x1);
-              tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
+              if constexpr (T::kConv == Conv::kSplit3) tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
               if (have_run) tmem_ld_16cols(trun + col, r);
               tmem_ld_wait();
   #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const float x = x0[j] + 0x1p-11f * (x1[j] + x2[j]);
+                // three chains: hh + 2^-11 (hl + lh); two chains (A-only split): hb + 2^-11 lb
+                const float x = (T::kConv == Conv::kSplit3) ? x0[j] + 0x1p-11f * (x1[j] + x2[j])
+                                                            : x0[j] + 0x1p-11f * x1[j];
                 v[h * 16 + j] = have_run ? r[j] + x : x;
               }
             }
@@ -671,7 +691,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 }
               }
             }
-            pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, w[i]);
+            pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, w[i], isA);
           }
           if constexpr (T::kStaged) {
             // Every staging value has been consumed by the conversion above,
@@ -683,7 +703,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           if (!warp_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
           // ---- scatter into the swizzled operand tiles
           const uint32_t a_hi = op_smem + st * T::kOpStage;
-          const uint32_t b_hi = a_hi + T::kCopies * T::kATile;
+          const uint32_t b_hi = a_hi + T::kCopiesA * T::kATile;
 #pragma unroll
           for (int i = 0; i < kPerThread; ++i) {
             const int wi = ct + i * T::kConvThreads;
@@ -692,7 +712,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             const uint32_t lg = wl >> 3, ch = wl & 7;
             const uint32_t hi_tile = isA ? a_hi : b_hi;
             const uint32_t lo_tile = hi_tile + (isA ? (uint32_t)T::kATile : (uint32_t)T::kBTile);
-            store_chunk<T>(w[i], hi_tile, lo_tile, lg, ch, isA ? (p.a_mn_major != 0) : (p.b_mn_major != 0));
+            store_chunk<T>(w[i], hi_tile, lo_tile, lg, ch, isA ? (p.a_mn_major != 0) : (p.b_mn_major != 0), isA);
           }
           fence_proxy_async_smem();
           mbar_arrive(&op_full[st]);

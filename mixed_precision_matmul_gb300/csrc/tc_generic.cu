@@ -16,6 +16,7 @@ bool tc_lookup_generic(Conv conv, Op op, SrcT st, int bn, TcKernel* out) {
   MPG_GENERIC(Conv::kRoundBF16, Op::kBF16, SrcT::kF32, 128)
   MPG_GENERIC(Conv::kSplit3, Op::kF16, SrcT::kF32, 128)
   MPG_GENERIC(Conv::kSplit1, Op::kF16, SrcT::kF32, 128)
+  MPG_GENERIC(Conv::kSplitA2, Op::kF16, SrcT::kF32, 128)
 #undef MPG_GENERIC
   return false;
 }

@@ -18,7 +18,10 @@ MODE_Q = {
     mpg.SPLIT_FP16_3CHAIN: oracle.Q_SPLIT3,
     mpg.SPLIT_FP16_1CHAIN: oracle.Q_SPLIT1,
     mpg.FP32_FFMA: oracle.Q_NONE,
+    mpg.SPLIT_A_FP16_2CHAIN: oracle.Q_SPLIT3,    # A: hi + lo*2^-11
 }
+# quantisation of B where it differs from A's
+MODE_QB = {mpg.SPLIT_A_FP16_2CHAIN: oracle.Q_FP16}
 
 TOL = {  # normalised error bars
     "q16": 1e-5,     # fp16 / bf16 against the quantised-input problem
@@ -125,13 +128,15 @@ class Case:
             return 0, 0
         return int(self.opts.split_exp_a), int(self.opts.split_exp_b)
 
-    def reference(self, q, batches=None):
-        """Full-grid oracle (ref, den) per batch for quantisation q."""
+    def reference(self, q, batches=None, qb=None):
+        """Full-grid oracle (ref, den) per batch for quantisation q (of A and,
+        unless qb is given, of B)."""
         sa, sb = self._exps()
+        qb = q if qb is None else qb
         out = []
         for bi in (range(self.batch) if batches is None else batches):
             out.append(oracle.gemm(self.a[bi], self.b[bi], self.c0[bi], self.alpha, self.beta,
-                                   q, q, sa, sb))
+                                   q, qb, sa, sb))
         return out
 
     def reference_points(self, q, bi, rows, cols):
@@ -146,7 +151,7 @@ class Case:
         eR = eQ = 0.0
         q = MODE_Q.get(self.mode)
         refsR = self.reference(oracle.Q_NONE, bl)
-        refsQ = self.reference(q, bl) if q is not None else None
+        refsQ = self.reference(q, bl, MODE_QB.get(self.mode)) if q is not None else None
         for i, bi in enumerate(bl):
             eR = max(eR, oracle.max_rel_err(C[bi], *refsR[i]))
             if refsQ is not None:

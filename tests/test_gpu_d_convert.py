@@ -157,3 +157,18 @@ def test_separate_conversion_pass_needs_workspace():
                       0, 1.0, 0.0, mpg.SPLIT_FP16_3CHAIN, opts=mpg.options(prepass=1), check=False)
     assert st == mpg.ERR_WORKSPACE
     assert mpg.workspace_size(m, n, k, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(prepass=1)) >= 4 * (m * k + k * n)
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES)
+@pytest.mark.parametrize("prepass", [0, 1])
+def test_split_a_two_chain_parity(m, n, k, al, bl, pad, tile_n, prepass):
+    """The Volta page's form: A split into hi and lo, B rounded to fp16, the
+    hi and lo products in separate chains.  Against the problem on the inputs
+    as quantised (A = hi + lo, B = fp16(B))."""
+    mpg.build()
+    opts = mpg.options(tile_n=tile_n if not prepass else 0, prepass=prepass)
+    c = Case(m, n, k, mpg.SPLIT_A_FP16_2CHAIN, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=0.5,
+             opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], (eR, eQ)

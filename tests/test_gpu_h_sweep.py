@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 MODES = [(mpg.FP16_F32ACC, "f32"), (mpg.FP16_F32ACC, "f16"), (mpg.BF16_F32ACC, "f32"),
          (mpg.BF16_F32ACC, "bf16"), (mpg.TF32, "f32"), (mpg.SPLIT_FP16_3CHAIN, "f32"),
-         (mpg.SPLIT_FP16_1CHAIN, "f32"), (mpg.FP32_FFMA, "f32")]
+         (mpg.SPLIT_FP16_1CHAIN, "f32"), (mpg.FP32_FFMA, "f32"), (mpg.SPLIT_A_FP16_2CHAIN, "f32")]
 
 
 def _cases(n=64, seed=20251):

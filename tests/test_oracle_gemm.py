@@ -142,3 +142,24 @@ def test_max_rel_err(orc):
     assert orc.max_rel_err(np.array([1.5, -2.0, 0.0]), ref, den) == 0.25
     assert orc.max_rel_err(np.array([1.0, -2.0, 1e-30]), ref, den) == float("inf")
     assert orc.max_rel_err(np.array([np.nan, -2.0, 0.0]), ref, den) == float("inf")
+
+
+def test_split_of_a_only_with_fp16_b(orc):
+    # A splits exactly into hi + lo (fp16 value plus a small multiple of
+    # 2^-20) and B holds fp16 values: the problem on the quantised inputs of
+    # the A-only split (A = hi + lo, B = fp16(B)) is then the exact product
+    g = np.random.Generator(np.random.PCG64(26))
+    hi = g.integers(1024, 2048, size=(7, 29)) / 1024.0
+    lo = g.integers(-255, 256, size=(7, 29)) * 2.0 ** -20
+    A = (hi + lo).astype(np.float32)
+    B = (g.integers(-2048, 2049, size=(29, 13)) / 256.0).astype(np.float32)   # exact in fp16
+    rR, _ = orc.gemm(A, B)
+    rQ, _ = orc.gemm(A, B, a_q=orc.Q_SPLIT3, b_q=orc.Q_FP16)
+    assert np.array_equal(rR, rQ)
+    # B values that are not fp16 numbers are rounded: the difference is A times
+    # the rounding error of B, which numpy's float16 conversion supplies
+    B2 = synthetic.uniform((29, 13), 27)
+    rR2, _ = orc.gemm(A, B2)
+    rQ2, _ = orc.gemm(A, B2, a_q=orc.Q_SPLIT3, b_q=orc.Q_FP16)
+    expect = A.astype(np.float64) @ (B2.astype(np.float16).astype(np.float64) - B2.astype(np.float64))
+    assert np.max(np.abs((rQ2 - rR2) - expect)) < 1e-12
