@@ -29,7 +29,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 # storage types
 F32, F16, BF16, F64 = 0, 1, 2, 3
 # operand quantisation
-Q_NONE, Q_FP16, Q_BF16, Q_TF32_TRUNC, Q_TF32_RNA, Q_TF32_RNE, Q_SPLIT3, Q_SPLIT1 = range(8)
+Q_NONE, Q_FP16, Q_BF16, Q_TF32_TRUNC, Q_TF32_RNA, Q_TF32_RNE, Q_SPLIT3, Q_SPLIT1, Q_SPLIT4 = range(9)
 
 _lock = threading.Lock()
 _lib = None
@@ -171,7 +171,7 @@ def gemm(A, B, C0=None, alpha: float = 1.0, beta: float = 0.0,
     den = |alpha| * sum_k |q(A)[i,k]| |q(B)[k,j]| + |beta| |C0[i,j]|
 
     where for the split modes q(x) = hi + lo and the product keeps
-    hi*hi + hi*lo + lo*hi.
+    hi*hi + hi*lo + lo*hi (and lo*lo for Q_SPLIT4).
     """
     lib = _load()
     Ahi, Alo = quantize(A, a_q, a_s)
@@ -180,7 +180,7 @@ def gemm(A, B, C0=None, alpha: float = 1.0, beta: float = 0.0,
     k2, n = Bhi.shape
     if k != k2:
         raise ValueError("inner dimensions differ")
-    split = int(a_q in (Q_SPLIT3, Q_SPLIT1))
+    split = 2 if a_q == Q_SPLIT4 else int(a_q in (Q_SPLIT3, Q_SPLIT1))
     ref = np.empty((m, n), dtype=np.float64)
     den = np.empty((m, n), dtype=np.float64)
     if C0 is not None:

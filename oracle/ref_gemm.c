@@ -36,7 +36,8 @@
  *    power-of-two scale and L is 11 for the three-chain form and 0 for the
  *    single-chain form (plain lo = fp16(x - hi) when s = L = 0).  Powers of two
  *    are exact, so they only move the operand out of the FP16 subnormal range.
- *  - The three-chain product keeps hi*hi + hi*lo + lo*hi and drops lo*lo.
+ *  - The three-chain product keeps hi*hi + hi*lo + lo*hi and drops lo*lo;
+ *    the four-chain variant (a next step listed for the split) keeps lo*lo.
  *
  * Everything here is a direct transcription of a definition: a triple loop in
  * the order (row i, column j, k ascending) or the equivalent (i, k, j) axpy
@@ -61,7 +62,8 @@ enum {
   ORC_Q_TF32_RNA = 4,    /* tf32, round half away from zero */
   ORC_Q_TF32_RNE = 5,    /* tf32, round half to even */
   ORC_Q_SPLIT3 = 6,      /* hi/lo split, lo scaled by 2^11 (three chains) */
-  ORC_Q_SPLIT1 = 7       /* hi/lo split, plain lo (single chain) */
+  ORC_Q_SPLIT1 = 7,      /* hi/lo split, plain lo (single chain) */
+  ORC_Q_SPLIT4 = 8       /* hi/lo split, lo scaled by 2^11, lo*lo kept (four chains) */
 };
 
 /* ------------------------------------------------------------------------- */
@@ -169,7 +171,8 @@ static void quant_elem(double x, int q, int s, double* hi, double* lo) {
     case ORC_Q_TF32_TRUNC: *hi = orc_tf32_trunc(x); break;
     case ORC_Q_TF32_RNA: *hi = orc_tf32_rna(x); break;
     case ORC_Q_TF32_RNE: *hi = orc_tf32_rne(x); break;
-    case ORC_Q_SPLIT3: orc_split(x, s, 11, hi, lo); break;
+    case ORC_Q_SPLIT3:
+    case ORC_Q_SPLIT4: orc_split(x, s, 11, hi, lo); break;
     case ORC_Q_SPLIT1: orc_split(x, s, 0, hi, lo); break;
     default: *hi = x; break;
   }
@@ -202,7 +205,7 @@ void orc_quantize(const void* src, int type, int64_t rows, int64_t cols,
 typedef struct {
   int64_t m, n, k;
   const double *Ahi, *Alo, *Bhi, *Blo;  /* logical row-major m*k and k*n */
-  int split;                             /* 1: hi*hi + hi*lo + lo*hi */
+  int split;                             /* 1: hi*hi + hi*lo + lo*hi; 2: also lo*lo */
   const float* C0; int64_t ldc0;
   double alpha, beta;
   double *ref, *den; int64_t ldr;
@@ -225,7 +228,13 @@ static void* full_worker(void* arg) {
       double al = J->split ? J->Alo[i * k + kk] : 0.0;
       double aabs = fabs(ah + al);
       const double* bh = J->Bhi + kk * n;
-      if (J->split) {
+      if (J->split == 2) {
+        const double* bl = J->Blo + kk * n;
+        for (int64_t j = 0; j < n; ++j) {
+          acc[j] += ah * bh[j] + ah * bl[j] + al * bh[j] + al * bl[j];
+          dac[j] += aabs * fabs(bh[j] + bl[j]);
+        }
+      } else if (J->split) {
         const double* bl = J->Blo + kk * n;
         for (int64_t j = 0; j < n; ++j) {
           acc[j] += ah * bh[j] + ah * bl[j] + al * bh[j];
@@ -297,7 +306,8 @@ typedef struct {
 
 static void* pts_worker(void* arg) {
   pts_job* J = (pts_job*)arg;
-  int splitA = (J->a_q == ORC_Q_SPLIT3 || J->a_q == ORC_Q_SPLIT1);
+  int splitA = (J->a_q == ORC_Q_SPLIT3 || J->a_q == ORC_Q_SPLIT1 || J->a_q == ORC_Q_SPLIT4);
+  int four = (J->a_q == ORC_Q_SPLIT4);
   for (int64_t p = J->p_begin; p < J->p_end; ++p) {
     int64_t i = J->rows[p], j = J->cols[p];
     double acc = 0.0, dac = 0.0;
@@ -305,7 +315,8 @@ static void* pts_worker(void* arg) {
       double ah, al, bh, bl;
       quant_elem(load_elem(J->A, J->a_type, elem_index(i, kk, J->lda, J->a_cm)), J->a_q, J->a_s, &ah, &al);
       quant_elem(load_elem(J->B, J->b_type, elem_index(kk, j, J->ldb, J->b_cm)), J->b_q, J->b_s, &bh, &bl);
-      if (splitA) acc += ah * bh + ah * bl + al * bh;
+      if (four) acc += ah * bh + ah * bl + al * bh + al * bl;
+      else if (splitA) acc += ah * bh + ah * bl + al * bh;
       else acc += ah * bh;
       dac += fabs(ah + al) * fabs(bh + bl);
     }

@@ -163,3 +163,23 @@ def test_split_of_a_only_with_fp16_b(orc):
     rQ2, _ = orc.gemm(A, B2, a_q=orc.Q_SPLIT3, b_q=orc.Q_FP16)
     expect = A.astype(np.float64) @ (B2.astype(np.float16).astype(np.float64) - B2.astype(np.float64))
     assert np.max(np.abs((rQ2 - rR2) - expect)) < 1e-12
+
+
+def test_four_chain_split_keeps_lo_lo(orc):
+    # inputs that split exactly into hi + lo: with lo*lo kept the four-term
+    # sum is the exact product; the three-term sum misses exactly sum lo*lo
+    g = np.random.Generator(np.random.PCG64(28))
+    def exact_split(shape):
+        hi = g.integers(1024, 2048, size=shape) / 1024.0 * np.where(g.integers(0, 2, shape) == 0, -1, 1)
+        lo = g.integers(-255, 256, size=shape) * 2.0 ** -20
+        return (hi + lo).astype(np.float32), lo
+    A, Al = exact_split((8, 27))
+    B, Bl = exact_split((27, 10))
+    rR, _ = orc.gemm(A, B)
+    r4, _ = orc.gemm(A, B, a_q=orc.Q_SPLIT4, b_q=orc.Q_SPLIT4)
+    r3, _ = orc.gemm(A, B, a_q=orc.Q_SPLIT3, b_q=orc.Q_SPLIT3)
+    assert np.array_equal(r4, rR)
+    assert np.max(np.abs((r4 - r3) - Al @ Bl)) < 1e-18
+    rows, cols = np.array([0, 3, 7]), np.array([9, 0, 4])
+    p4, _ = orc.gemm_points(A, B, 27, rows, cols, a_q=orc.Q_SPLIT4, b_q=orc.Q_SPLIT4)
+    assert np.array_equal(p4, rR[rows, cols])
