@@ -204,7 +204,8 @@ def mode_cases(torch, mpg, synthetic, device):
     for mn in ("split3", "split1", "tf32", "ffma"):
         yield f"loguniform4096_{mn}", lambda mn=mn: f32_square(4096, "loguniform", mn, "col")
     yield "loguniform4096_split2a", lambda: f32_square(4096, "loguniform", "split2a", "col")
-    for mn in ("split3", "split1", "split2a"):
+    yield "loguniform4096_split4", lambda: f32_square(4096, "loguniform", "split4", "col")
+    for mn in ("split3", "split1", "split2a", "split4"):
         yield f"loguniform4096_{mn}_prepass", lambda mn=mn: f32_square(4096, "loguniform", mn, "col",
                                                                        opts=mpg.options(prepass=1))
     # C2: batched 2048 x (64x4096 * 4096x64), padded leading dims
@@ -516,8 +517,8 @@ def ours(args):
             rate = RATIO.get(mw.mode_name)
             if rate:
                 entry["frac_of_tensor_peak"] = round(tf / (peak_bf16 * rate), 4)
-            elif mw.mode_name in ("split3", "split1", "split2a"):
-                issued = (2.0 if mw.mode_name == "split2a" else 3.0) * tf
+            elif mw.mode_name in ("split3", "split1", "split2a", "split4"):
+                issued = {"split2a": 2.0, "split4": 4.0}.get(mw.mode_name, 3.0) * tf
                 entry["tensor_issued_tflops"] = round(issued, 2)
                 entry["frac_of_tensor_peak"] = round(issued / peak_bf16, 4)
             if mw.algo_bytes:
@@ -530,9 +531,8 @@ def ours(args):
             mw.A = mw.B = None
             torch.cuda.empty_cache()
         ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
-        for lbl in ("loguniform4096_split3", "loguniform4096_split1", "loguniform4096_split2a",
-                    "loguniform4096_split3_prepass", "loguniform4096_split1_prepass",
-                    "loguniform4096_split2a_prepass"):
+        for lbl in [f"loguniform4096_{x}{y}" for x in ("split3", "split1", "split2a", "split4")
+                    for y in ("", "_prepass")]:
             if ffma and lbl in modes:
                 modes[lbl]["x_ffma"] = round(modes[lbl]["tflops"] / ffma, 2)
         result["modes"] = modes
@@ -570,9 +570,8 @@ def ours(args):
             modes[label]["max_rel_err_vs_fp64"] = eR
             if mw.mode_name in qmap:
                 modes[label]["max_rel_err_vs_quantised"] = points_error(orc, mw, Cg, qmap[mw.mode_name])
-        for lbl in ("loguniform4096_split3", "loguniform4096_split1", "loguniform4096_split2a",
-                    "loguniform4096_split3_prepass", "loguniform4096_split1_prepass",
-                    "loguniform4096_split2a_prepass"):
+        for lbl in [f"loguniform4096_{x}{y}" for x in ("split3", "split1", "split2a", "split4")
+                    for y in ("", "_prepass")]:
             if lbl in modes and "loguniform4096_ffma" in modes:
                 f = modes["loguniform4096_ffma"]["max_rel_err_vs_fp64"]
                 modes[lbl]["err_x_ffma"] = round(modes[lbl]["max_rel_err_vs_fp64"] / f, 3) if f else None

@@ -74,7 +74,10 @@ typedef enum { MPG_F32 = 0, MPG_F16 = 1, MPG_BF16 = 2 } mpg_dtype;
  *                on": only A is split into fp16 hi and lo (lo scaled by 2^11),
  *                B is rounded to fp16 (RNE); A_hi*B and A_lo*B accumulate in two
  *                separate chains summed in fp32: acc = hb + 2^-11 * lb (per K
- *                chunk, as for the three-chain split).  fp32 inputs. */
+ *                chunk, as for the three-chain split).  fp32 inputs.
+ *   SPLIT_FP16_4CHAIN  the three-chain split plus the lo*lo product in a
+ *                fourth chain: acc = hh + (2^-11 * (hl + lh) + 2^-22 * ll).
+ *                fp32 inputs; 128 x 64 tiles. */
 typedef enum {
   MPG_FP16_F32ACC = 0,
   MPG_BF16_F32ACC = 1,
@@ -82,7 +85,8 @@ typedef enum {
   MPG_SPLIT_FP16_3CHAIN = 3,
   MPG_SPLIT_FP16_1CHAIN = 4,
   MPG_FP32_FFMA = 5,
-  MPG_SPLIT_A_FP16_2CHAIN = 6
+  MPG_SPLIT_A_FP16_2CHAIN = 6,
+  MPG_SPLIT_FP16_4CHAIN = 7
 } mpg_precision;
 
 typedef enum {
@@ -117,7 +121,7 @@ typedef struct {
    * 0 = default (2 s).  On expiry the kernel stops, records MPG_ERR_TIMEOUT in
    * the device status word and returns without hanging the GPU. */
   int64_t wait_timeout_ns;
-  /* SPLIT_FP16_3CHAIN and SPLIT_A_FP16_2CHAIN: the K loop accumulates in chunks of this many k
+  /* The split modes except the one-chain form: the K loop accumulates in chunks of this many k
    * elements.  Each chunk starts fresh hh / hl / lh accumulators on the tensor
    * cores; the epilogue adds the chunk's hh + 2^-11*(hl + lh) to an fp32
    * running sum with round-to-nearest.  This bounds how long the tensor
@@ -152,7 +156,7 @@ void mpg_options_init(mpg_options* opt);
  *   mode         precision policy; allowed input dtypes per mode:
  *                  FP16_F32ACC: A, B both F32 or both F16
  *                  BF16_F32ACC: A, B both F32 or both BF16
- *                  TF32, SPLIT_* (incl. SPLIT_A_FP16_2CHAIN), FP32_FFMA: A, B both F32
+ *                  TF32, SPLIT_* (all split forms), FP32_FFMA: A, B both F32
  *                anything else returns MPG_ERR_UNSUPPORTED.
  *   workspace    device scratch of at least mpg_gemm_workspace_size(...)
  *                bytes (may be NULL when that size is 0).  Its contents on

@@ -27,11 +27,12 @@ import threading
 from . import _build
 
 # precision modes (mpg_precision)
-FP16_F32ACC, BF16_F32ACC, TF32, SPLIT_FP16_3CHAIN, SPLIT_FP16_1CHAIN, FP32_FFMA, SPLIT_A_FP16_2CHAIN = range(7)
+(FP16_F32ACC, BF16_F32ACC, TF32, SPLIT_FP16_3CHAIN, SPLIT_FP16_1CHAIN, FP32_FFMA, SPLIT_A_FP16_2CHAIN,
+ SPLIT_FP16_4CHAIN) = range(8)
 MODE_NAMES = {
     "fp16": FP16_F32ACC, "bf16": BF16_F32ACC, "tf32": TF32,
     "split3": SPLIT_FP16_3CHAIN, "split1": SPLIT_FP16_1CHAIN, "ffma": FP32_FFMA,
-    "split2a": SPLIT_A_FP16_2CHAIN,
+    "split2a": SPLIT_A_FP16_2CHAIN, "split4": SPLIT_FP16_4CHAIN,
 }
 # storage types (mpg_dtype) and layouts (mpg_layout)
 F32, F16, BF16 = 0, 1, 2

@@ -189,12 +189,14 @@ PrepassLayout prepass_layout(int64_t m, int64_t n, int64_t k, int64_t batch, mpg
 
 bool prepass_mode(mpg_precision mode) {
   return mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC || mode == MPG_SPLIT_FP16_3CHAIN ||
-         mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_A_FP16_2CHAIN;
+         mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_A_FP16_2CHAIN || mode == MPG_SPLIT_FP16_4CHAIN;
 }
 
 // Which operands carry hi and lo copies under a conversion.
-bool splits_a(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplitA2; }
-bool splits_b(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1; }
+bool splits_a(Conv c) {
+  return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplitA2 || c == Conv::kSplit4;
+}
+bool splits_b(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplit4; }
 
 mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
                      float alpha, mpg_precision mode, const mpg_options& o, int sm_count, size_t ws_bytes,
@@ -252,6 +254,11 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       p.conv = Conv::kSplitA2;
       p.st = SrcT::kF32;
       break;
+    case MPG_SPLIT_FP16_4CHAIN:
+      p.op = Op::kF16;
+      p.conv = Conv::kSplit4;
+      p.st = SrcT::kF32;
+      break;
     default:
       return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   }
@@ -274,7 +281,9 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
 
   // tile width along N
   int bn;
-  if (p.src == Src::kGeneric) {
+  if (p.conv == Conv::kSplit4) {
+    bn = 64;   // four chains of 64 columns plus the running sum fill TMEM
+  } else if (p.src == Src::kGeneric) {
     bn = 128;
   } else if (p.src == Src::kTmaDirect && p.conv == Conv::kNone) {
     bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
@@ -326,7 +335,7 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
                 (long long)n, (long long)k, (long long)batch);
   if (m > kMax || n > kMax || k > kMax || batch > kMax)
     return fail(MPG_ERR_INVALID_ARG, "size beyond 2^31-1");
-  if ((int)mode < 0 || (int)mode > (int)MPG_SPLIT_A_FP16_2CHAIN)
+  if ((int)mode < 0 || (int)mode > (int)MPG_SPLIT_FP16_4CHAIN)
     return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   for (const Operand* x : {&A, &B}) {
     if ((int)x->dt < 0 || (int)x->dt > 2) return fail(MPG_ERR_INVALID_ARG, "unknown dtype %d", (int)x->dt);
@@ -504,7 +513,8 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.status = dev->status;
   p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
   p.chunk_kb = 0;
-  if ((plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplitA2) && o.split_chunk_k >= 0) {
+  if ((plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplitA2 || plan.conv == Conv::kSplit4) &&
+      o.split_chunk_k >= 0) {
     const int64_t chunk_k = o.split_chunk_k > 0 ? o.split_chunk_k : kDefaultSplitChunkK;
     p.chunk_kb = (int32_t)std::min<int64_t>((chunk_k + BK - 1) / BK, p.num_k_blk);
   }
@@ -583,7 +593,8 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   const size_t partials = splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
   if (o.prepass == 1 && prepass_mode(mode)) {
     // layouts are not known here: take the larger of the two line paddings
-    const bool split_b = (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN);
+    const bool split_b =
+        (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_FP16_4CHAIN);
     const bool split_a = split_b || mode == MPG_SPLIT_A_FP16_2CHAIN;
     size_t worst = 0;
     for (mpg_layout al : {MPG_ROW_MAJOR, MPG_COL_MAJOR})
@@ -661,8 +672,12 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       uint16_t* b_lo = sb_ ? reinterpret_cast<uint16_t*>(ws + L.off_b_lo) : nullptr;
       const int ea = sa_ ? o.split_exp_a : 0, eb = sa_ ? o.split_exp_b : 0;
       // the two-chain split splits A only; its B is rounded to fp16
-      const Conv conv_a = (plan.pre_conv == Conv::kSplitA2) ? Conv::kSplit3 : plan.pre_conv;
-      const Conv conv_b = (plan.pre_conv == Conv::kSplitA2) ? Conv::kRoundF16 : plan.pre_conv;
+      // the four-chain split uses the three-chain split's halves
+      const Conv conv_a = (plan.pre_conv == Conv::kSplitA2 || plan.pre_conv == Conv::kSplit4) ? Conv::kSplit3
+                                                                                              : plan.pre_conv;
+      const Conv conv_b = (plan.pre_conv == Conv::kSplitA2)  ? Conv::kRoundF16
+                          : (plan.pre_conv == Conv::kSplit4) ? Conv::kSplit3
+                                                             : plan.pre_conv;
       const int64_t sA = strideA ? strideA : L.a_outer * lda;
       const int64_t sB = strideB ? strideB : L.b_outer * ldb;
       e = launch_prepass(conv_a, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi, a_lo,

@@ -23,6 +23,7 @@ enum class Conv : int {
   kSplit3 = 3,    // fp32 -> hi, lo*2^11; three accumulator chains
   kSplit1 = 4,    // fp32 -> hi, lo; one shared accumulator chain
   kSplitA2 = 5,   // A: fp32 -> hi, lo*2^11; B: fp32 -> fp16; two chains (A_hi B, A_lo B)
+  kSplit4 = 6,    // fp32 -> hi, lo*2^11; four chains (hh, hl, lh, ll)
 };
 
 // Bits of the device status word.

@@ -48,8 +48,9 @@ struct TcTraits {
   static constexpr int kKSteps = kRowBytes / 32;   // MMAs of 32 bytes of K each
   static constexpr int kInstrK = 32 / kOpBytes;    // 16 (f16/bf16) or 8 (tf32)
   // operands that carry a hi and a lo copy in the stages
-  static constexpr bool kSplitA = (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplitA2);
-  static constexpr bool kSplitB = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
+  static constexpr bool kSplitA =
+      (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplitA2 || CV == Conv::kSplit4);
+  static constexpr bool kSplitB = (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplit4);
   static constexpr int kCopiesA = kSplitA ? 2 : 1;
   static constexpr int kCopiesB = kSplitB ? 2 : 1;
   static constexpr int kATile = BM * kRowBytes;
@@ -74,8 +75,11 @@ struct TcTraits {
   // The three-chain split accumulates K in chunks: each chunk starts fresh
   // chains, and the epilogue folds hh + 2^-11 (hl + lh) of every chunk into
   // an fp32 running sum (round to nearest) kept in kRunCols extra columns.
-  static constexpr bool kPromote = (CV == Conv::kSplit3 || CV == Conv::kSplitA2);
-  static constexpr int kChainCols = (CV == Conv::kSplit3) ? 3 * BN : (CV == Conv::kSplitA2) ? 2 * BN : BN;
+  static constexpr bool kPromote = (CV == Conv::kSplit3 || CV == Conv::kSplitA2 || CV == Conv::kSplit4);
+  static constexpr int kChainCols = (CV == Conv::kSplit4)   ? 4 * BN
+                                    : (CV == Conv::kSplit3)  ? 3 * BN
+                                    : (CV == Conv::kSplitA2) ? 2 * BN
+                                                             : BN;
   static constexpr int kRunCols = kPromote ? BN : 0;
   static constexpr int kAccStride = kPromote ? kChainCols
                                     : kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
@@ -255,7 +259,7 @@ __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned s
       w[2] = w[3] = 0;
     }
   } else {
-    constexpr int L = (T::kConv == Conv::kSplit3) ? 11 : 0;
+    constexpr int L = (T::kConv == Conv::kSplit1) ? 0 : 11;
     split_pair<L>(x[0], x[1], scale, w[0], w[2]);
     split_pair<L>(x[2], x[3], scale, w[1], w[3]);
   }
@@ -413,8 +417,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       uint32_t it = 0, g = 0;   // k-block iteration; accumulation chunk
       bool ok = true;
       const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::BN);
-      const uint32_t idesc_2n =
-          make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::kConv == Conv::kSplit3 ? 2 * T::BN : T::BN);
+      const uint32_t idesc_2n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM,
+                                           (T::kConv == Conv::kSplit3 || T::kConv == Conv::kSplit4) ? 2 * T::BN
+                                                                                                    : T::BN);
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(p, t);
         const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
@@ -446,6 +451,10 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
                 // lh = A_lo * B_hi
                 mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
+              } else if constexpr (T::kConv == Conv::kSplit4) {
+                // [hh | hl] = A_hi * [B_hi | B_lo];  [lh | ll] = A_lo * [B_hi | B_lo]
+                mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
+                mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_2n, acc);
               } else if constexpr (T::kConv == Conv::kSplitA2) {
                 // two chains: A_hi B and A_lo B (B single)
                 mma_f16(d0, da_hi, db_hi, idesc_n, acc);
@@ -522,18 +531,25 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             // earlier chunks of this tile
   #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              float x0[16], x1[16], x2[16], r[16];
+              float x0[16], x1[16], x2[16], x3[16], r[16];
               const uint32_t col = cc * 32 + h * 16;
               tmem_ld_16cols(tacc + col, x0);
               tmem_ld_16cols(tacc + T::BN + col, x1);
-              if constexpr (T::kConv == Conv::kSplit3) tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
+              if constexpr (T::kConv == Conv::kSplit3 || T::kConv == Conv::kSplit4)
+                tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
+              if constexpr (T::kConv == Conv::kSplit4) tmem_ld_16cols(tacc + 3 * T::BN + col, x3);
               if (have_run) tmem_ld_16cols(trun + col, r);
               tmem_ld_wait();
   #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 // three chains: hh + 2^-11 (hl + lh); two chains (A-only split): hb + 2^-11 lb
-                const float x = (T::kConv == Conv::kSplit3) ? x0[j] + 0x1p-11f * (x1[j] + x2[j])
-                                                            : x0[j] + 0x1p-11f * x1[j];
+                float x;
+                if constexpr (T::kConv == Conv::kSplit4)   // ... + 2^-22 ll
+                  x = x0[j] + (0x1p-11f * (x1[j] + x2[j]) + 0x1p-22f * x3[j]);
+                else if constexpr (T::kConv == Conv::kSplit3)
+                  x = x0[j] + 0x1p-11f * (x1[j] + x2[j]);
+                else
+                  x = x0[j] + 0x1p-11f * x1[j];
                 v[h * 16 + j] = have_run ? r[j] + x : x;
               }
             }

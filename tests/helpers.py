@@ -19,6 +19,7 @@ MODE_Q = {
     mpg.SPLIT_FP16_1CHAIN: oracle.Q_SPLIT1,
     mpg.FP32_FFMA: oracle.Q_NONE,
     mpg.SPLIT_A_FP16_2CHAIN: oracle.Q_SPLIT3,    # A: hi + lo*2^-11
+    mpg.SPLIT_FP16_4CHAIN: oracle.Q_SPLIT4,
 }
 # quantisation of B where it differs from A's
 MODE_QB = {mpg.SPLIT_A_FP16_2CHAIN: oracle.Q_FP16}

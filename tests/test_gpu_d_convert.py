@@ -172,3 +172,15 @@ def test_split_a_two_chain_parity(m, n, k, al, bl, pad, tile_n, prepass):
     c.run()
     eR, eQ = c.errors()
     assert eQ <= TOL["q16"], (eR, eQ)
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES)
+@pytest.mark.parametrize("prepass", [0, 1])
+def test_split_four_chain_parity(m, n, k, al, bl, pad, tile_n, prepass):
+    """hi*hi, hi*lo, lo*hi and lo*lo in four chains (128 x 64 tiles)."""
+    mpg.build()
+    c = Case(m, n, k, mpg.SPLIT_FP16_4CHAIN, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=-0.5,
+             opts=mpg.options(prepass=prepass))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)

@@ -12,7 +12,8 @@ pytestmark = pytest.mark.gpu
 
 MODES = [(mpg.FP16_F32ACC, "f32"), (mpg.FP16_F32ACC, "f16"), (mpg.BF16_F32ACC, "f32"),
          (mpg.BF16_F32ACC, "bf16"), (mpg.TF32, "f32"), (mpg.SPLIT_FP16_3CHAIN, "f32"),
-         (mpg.SPLIT_FP16_1CHAIN, "f32"), (mpg.FP32_FFMA, "f32"), (mpg.SPLIT_A_FP16_2CHAIN, "f32")]
+         (mpg.SPLIT_FP16_1CHAIN, "f32"), (mpg.FP32_FFMA, "f32"), (mpg.SPLIT_A_FP16_2CHAIN, "f32"),
+         (mpg.SPLIT_FP16_4CHAIN, "f32")]
 
 
 def _cases(n=64, seed=20251):
@@ -51,5 +52,5 @@ def test_random_case(case):
         assert eR <= TOL["q16"], eR
     else:
         assert eQ <= TOL["q16"], (eR, eQ)
-    if mode == mpg.SPLIT_FP16_3CHAIN:
+    if mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_4CHAIN):
         assert eR <= TOL["split"], eR
