@@ -260,6 +260,23 @@ int mpg_acc_decode(int offset, int* lane, int* j);
  * row = 32*(warp % 4) + lane and col = col_base + reg.  Returns 0 or -1. */
 int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int* col);
 
+/* ---- operand fragment maps of mma.sync m16n8k16 (f16 / bf16 operands) -----
+ * The cuda-oxide page derives the accumulator numeral and notes that the A
+ * and B operands are different numerals ("Scope").  From the PTX ISA operand
+ * layouts, with group = lane/4 and tig = lane%4:
+ *   A (16x16, row-major): value i in [0,8) of a lane (register i/2, half i%2)
+ *     sits at row = group + 8*((i>>1)&1), col = 2*tig + (i&1) + 8*(i>>2);
+ *     row-major offset = (i&1)*1 + tig*2 + (i>>2)*8 + group*16 + ((i>>1)&1)*128.
+ *   B (16x8, column-major): value i in [0,4) (register i/2, half i%2) sits at
+ *     k = 2*tig + (i&1) + 8*(i>>1), n = group;
+ *     column-major offset = (i&1)*1 + tig*2 + (i>>1)*8 + group*16.
+ * Each is a bijection (256 resp. 128 points).  Return 0, or -1 for an
+ * out-of-range argument. */
+int mpg_frag_a_coords(int lane, int i, int* row, int* col);
+int mpg_frag_a_decode(int row, int col, int* lane, int* i);
+int mpg_frag_b_coords(int lane, int i, int* k, int* n);
+int mpg_frag_b_decode(int k, int n, int* lane, int* i);
+
 /* ---- hardware checks ------------------------------------------------------ */
 
 /* One mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 by one warp.
@@ -270,6 +287,13 @@ int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int
  *      mpg_acc_coords and compare with a host product.
  * Fragments are gathered with the A/B operand layouts of the PTX ISA. */
 mpg_status mpg_probe_mma_m16n8k16(const void* A, const void* B, float* D, void* stream);
+
+/* The same mma.sync with the operand fragments supplied per lane by the
+ * caller: Afrag[lane*4 + r] is A register r of `lane` (two fp16 values, low
+ * half first), Bfrag[lane*2 + r] is B register r.  The kernel loads them
+ * verbatim, so a product equal to the host product checks the caller's
+ * fragment maps on the hardware.  D as above (device pointers, C = 0). */
+mpg_status mpg_probe_mma_m16n8k16_fragments(const uint32_t* Afrag, const uint32_t* Bfrag, float* D, void* stream);
 
 /* Failure-detection self test: launches one kernel whose single wait is on an
  * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then

@@ -124,6 +124,11 @@ def lib():
         L.mpg_tmem_acc_coords.restype = i32
         L.mpg_probe_mma_m16n8k16.argtypes = [vp, vp, vp, vp]
         L.mpg_probe_mma_m16n8k16.restype = i32
+        for nm in ("mpg_frag_a_coords", "mpg_frag_a_decode", "mpg_frag_b_coords", "mpg_frag_b_decode"):
+            getattr(L, nm).argtypes = [i32, i32, pi, pi]
+            getattr(L, nm).restype = i32
+        L.mpg_probe_mma_m16n8k16_fragments.argtypes = [vp, vp, vp, vp]
+        L.mpg_probe_mma_m16n8k16_fragments.restype = i32
         L.mpg_selftest_wait_timeout.argtypes = [i64, vp]
         L.mpg_selftest_wait_timeout.restype = i32
         _lib = L
@@ -309,6 +314,31 @@ def tmem_acc_coords(warp: int, lane: int, reg: int, col_base: int = 0):
     return r.value, c.value
 
 
+def _pair(fn, x, y):
+    u, v = ctypes.c_int(), ctypes.c_int()
+    if fn(x, y, ctypes.byref(u), ctypes.byref(v)) != 0:
+        return None
+    return u.value, v.value
+
+
+def frag_a_coords(lane: int, i: int):
+    """(row, col) of value i (register i//2, half i%2) of an A fragment."""
+    return _pair(lib().mpg_frag_a_coords, lane, i)
+
+
+def frag_a_decode(row: int, col: int):
+    return _pair(lib().mpg_frag_a_decode, row, col)
+
+
+def frag_b_coords(lane: int, i: int):
+    """(k, n) of value i (register i//2, half i%2) of a B fragment."""
+    return _pair(lib().mpg_frag_b_coords, lane, i)
+
+
+def frag_b_decode(k: int, n: int):
+    return _pair(lib().mpg_frag_b_decode, k, n)
+
+
 # ---------------------------------------------------------------------------
 # hardware checks
 # ---------------------------------------------------------------------------
@@ -321,6 +351,18 @@ def probe_mma_m16n8k16(A16, B16, stream=None):
     bt = B16.to(torch.float16).t().contiguous()  # column-major storage of B
     d = torch.empty((32, 4), dtype=torch.float32, device=a.device)
     _check(lib().mpg_probe_mma_m16n8k16(a.data_ptr(), bt.data_ptr(), d.data_ptr(), _stream_handle(stream)))
+    return d
+
+
+def probe_mma_m16n8k16_fragments(a_frag, b_frag, stream=None):
+    """mma.sync m16n8k16 on fragments given per lane: a_frag (32, 4) and
+    b_frag (32, 2) int32 tensors of packed fp16 pairs; returns (32, 4) floats."""
+    torch = _torch()
+    a = a_frag.to(torch.int32).contiguous()
+    b = b_frag.to(torch.int32).contiguous()
+    d = torch.empty((32, 4), dtype=torch.float32, device=a.device)
+    _check(lib().mpg_probe_mma_m16n8k16_fragments(a.data_ptr(), b.data_ptr(), d.data_ptr(),
+                                                   _stream_handle(stream)))
     return d
 
 

@@ -57,6 +57,41 @@ int64_t mpg_acc_matrix_offset(int lane, int j, int64_t tile_row, int64_t tile_co
   return total;
 }
 
+// Operand fragments: numerals built the same way (low digits first).
+int mpg_frag_a_coords(int lane, int i, int* row, int* col) {
+  if (lane < 0 || lane > 31 || i < 0 || i > 7 || !row || !col) return -1;
+  const int off = (i & 1) * 1 + (lane & 3) * 2 + (i >> 2) * 8 + (lane >> 2) * 16 + ((i >> 1) & 1) * 128;
+  *row = off / 16;  // A is 16 columns wide, row-major
+  *col = off % 16;
+  return 0;
+}
+
+int mpg_frag_a_decode(int row, int col, int* lane, int* i) {
+  if (row < 0 || row > 15 || col < 0 || col > 15 || !lane || !i) return -1;
+  const int off = row * 16 + col;
+  const int d0 = off % 2, tig = (off / 2) % 4, d2 = (off / 8) % 2, group = (off / 16) % 8, d4 = off / 128;
+  *lane = group * 4 + tig;
+  *i = d2 * 4 + d4 * 2 + d0;
+  return 0;
+}
+
+int mpg_frag_b_coords(int lane, int i, int* k, int* n) {
+  if (lane < 0 || lane > 31 || i < 0 || i > 3 || !k || !n) return -1;
+  const int off = (i & 1) * 1 + (lane & 3) * 2 + (i >> 1) * 8 + (lane >> 2) * 16;
+  *n = off / 16;    // B is 16 rows (k) tall, column-major
+  *k = off % 16;
+  return 0;
+}
+
+int mpg_frag_b_decode(int k, int n, int* lane, int* i) {
+  if (k < 0 || k > 15 || n < 0 || n > 7 || !lane || !i) return -1;
+  const int off = n * 16 + k;
+  const int d0 = off % 2, tig = (off / 2) % 4, d2 = (off / 8) % 2, group = off / 16;
+  *lane = group * 4 + tig;
+  *i = d2 * 2 + d0;
+  return 0;
+}
+
 int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int* col) {
   if (warp < 0 || lane < 0 || lane > 31 || reg < 0 || col_base < 0 || col_base + reg >= 512 || !row || !col)
     return -1;

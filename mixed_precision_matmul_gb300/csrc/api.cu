@@ -737,6 +737,17 @@ mpg_status mpg_probe_mma_m16n8k16(const void* A, const void* B, float* D, void* 
   return MPG_OK;
 }
 
+mpg_status mpg_probe_mma_m16n8k16_fragments(const uint32_t* Afrag, const uint32_t* Bfrag, float* D, void* stream) {
+  t_err.clear();
+  if (!Afrag || !Bfrag || !D) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = launch_probe_mma_frag(Afrag, Bfrag, D, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
 mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
   t_err.clear();
   if (timeout_ns < 1000000 || timeout_ns > 10000000000ll)

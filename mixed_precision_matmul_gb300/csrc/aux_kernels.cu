@@ -79,6 +79,24 @@ __global__ void probe_mma_kernel(const unsigned short* __restrict__ A, const uns
   D[lane * 4 + 3] = d3;
 }
 
+// The same instruction with the fragments given verbatim per lane.
+__global__ void probe_mma_frag_kernel(const uint32_t* __restrict__ Af, const uint32_t* __restrict__ Bf,
+                                      float* __restrict__ D) {
+  const int lane = threadIdx.x;
+  const uint32_t a0 = Af[lane * 4], a1 = Af[lane * 4 + 1], a2 = Af[lane * 4 + 2], a3 = Af[lane * 4 + 3];
+  const uint32_t b0 = Bf[lane * 2], b1 = Bf[lane * 2 + 1];
+  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  D[lane * 4 + 0] = d0;
+  D[lane * 4 + 1] = d1;
+  D[lane * 4 + 2] = d2;
+  D[lane * 4 + 3] = d3;
+}
+
 // A single bounded wait on an mbarrier that nothing arrives at: the wait must
 // expire, record the timeout in the status word and let the kernel return.
 __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
@@ -125,6 +143,11 @@ cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c,
 cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_t stream) {
   probe_mma_kernel<<<1, 32, 0, stream>>>(static_cast<const unsigned short*>(a),
                                          static_cast<const unsigned short*>(b), d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream) {
+  probe_mma_frag_kernel<<<1, 32, 0, stream>>>(a, b, d);
   return cudaGetLastError();
 }
 

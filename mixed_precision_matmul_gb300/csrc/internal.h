@@ -116,6 +116,7 @@ cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_
 cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
                            int sm_count, cudaStream_t stream);
+cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Device status word of the current device (allocated by the runtime as a

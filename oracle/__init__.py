@@ -80,6 +80,9 @@ def _load():
         lib.orc_gemm_points.restype = i32
         lib.orc_acc_coords.argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.orc_acc_coords.restype = i32
+        for nm in ("orc_frag_a_coords", "orc_frag_b_coords"):
+            getattr(lib, nm).argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            getattr(lib, nm).restype = i32
         _lib = lib
         return lib
 
@@ -252,4 +255,20 @@ def acc_coords(lane: int, j: int) -> tuple[int, int]:
     r, c = ctypes.c_int(), ctypes.c_int()
     if _load().orc_acc_coords(lane, j, ctypes.byref(r), ctypes.byref(c)) != 0:
         raise ValueError("lane or fragment index out of range")
+    return r.value, c.value
+
+
+def frag_a_coords(lane: int, i: int) -> tuple[int, int]:
+    """(row, col) of value i of an m16n8k16 A fragment (PTX operand layout)."""
+    r, c = ctypes.c_int(), ctypes.c_int()
+    if _load().orc_frag_a_coords(lane, i, ctypes.byref(r), ctypes.byref(c)) != 0:
+        raise ValueError("lane or value index out of range")
+    return r.value, c.value
+
+
+def frag_b_coords(lane: int, i: int) -> tuple[int, int]:
+    """(k, n) of value i of an m16n8k16 B fragment (PTX operand layout)."""
+    r, c = ctypes.c_int(), ctypes.c_int()
+    if _load().orc_frag_b_coords(lane, i, ctypes.byref(r), ctypes.byref(c)) != 0:
+        raise ValueError("lane or value index out of range")
     return r.value, c.value

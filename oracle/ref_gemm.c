@@ -372,3 +372,26 @@ int orc_acc_coords(int lane, int j, int* row, int* col) {
   *col = 2 * tig + (j % 2);
   return 0;
 }
+
+/* The m16n8k16 operand fragments, from the PTX ISA operand layouts
+ * (groupID = lane / 4, threadID_in_group = lane % 4):
+ *   A (row): register r of a lane holds two consecutive columns;
+ *     r = 0: row g,   cols 2t, 2t+1      r = 1: row g+8, cols 2t, 2t+1
+ *     r = 2: row g,   cols 2t+8, 2t+9    r = 3: row g+8, cols 2t+8, 2t+9
+ *   B (col): r = 0: rows (k) 2t, 2t+1 of column g; r = 1: rows 2t+8, 2t+9.
+ * Value i of a lane is half i % 2 of register i / 2. */
+int orc_frag_a_coords(int lane, int i, int* row, int* col) {
+  if (lane < 0 || lane > 31 || i < 0 || i > 7) return -1;
+  int g = lane / 4, t = lane % 4, r = i / 2, h = i % 2;
+  *row = g + ((r == 1 || r == 3) ? 8 : 0);
+  *col = 2 * t + h + ((r >= 2) ? 8 : 0);
+  return 0;
+}
+
+int orc_frag_b_coords(int lane, int i, int* k, int* n) {
+  if (lane < 0 || lane > 31 || i < 0 || i > 3) return -1;
+  int g = lane / 4, t = lane % 4, r = i / 2, h = i % 2;
+  *k = 2 * t + h + (r == 1 ? 8 : 0);
+  *n = g;
+  return 0;
+}

@@ -177,3 +177,43 @@ def test_tmem_accumulator_map(L):
     assert rows == set(range(128))
     assert mpg.tmem_acc_coords(0, 32, 0) is None
     assert mpg.tmem_acc_coords(0, 0, 0, 512) is None
+
+
+# ---------------------------------------------------------------- operand fragments
+def test_fragment_maps_match_oracle_definition(L, orc):
+    for lane in range(32):
+        for i in range(8):
+            assert mpg.frag_a_coords(lane, i) == orc.frag_a_coords(lane, i)
+        for i in range(4):
+            assert mpg.frag_b_coords(lane, i) == orc.frag_b_coords(lane, i)
+
+
+def test_fragment_maps_are_bijections_with_inverse(L):
+    seen_a, seen_b = set(), set()
+    for lane in range(32):
+        for i in range(8):
+            r, c = mpg.frag_a_coords(lane, i)
+            assert 0 <= r < 16 and 0 <= c < 16 and (r, c) not in seen_a
+            seen_a.add((r, c))
+            assert mpg.frag_a_decode(r, c) == (lane, i)
+        for i in range(4):
+            k, n = mpg.frag_b_coords(lane, i)
+            assert 0 <= k < 16 and 0 <= n < 8 and (k, n) not in seen_b
+            seen_b.add((k, n))
+            assert mpg.frag_b_decode(k, n) == (lane, i)
+    assert len(seen_a) == 256 and len(seen_b) == 128
+    assert mpg.frag_a_coords(32, 0) is None and mpg.frag_a_coords(0, 8) is None
+    assert mpg.frag_b_coords(0, 4) is None and mpg.frag_b_decode(16, 0) is None
+
+
+def test_fragment_numerals(L):
+    # A: offset = (i&1) + tig*2 + (i>>2)*8 + group*16 + ((i>>1)&1)*128 (row-major)
+    # B: offset = (i&1) + tig*2 + (i>>1)*8 + group*16 (column-major)
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for i in range(8):
+            r, c = mpg.frag_a_coords(lane, i)
+            assert r * 16 + c == (i & 1) + t * 2 + (i >> 2) * 8 + g * 16 + ((i >> 1) & 1) * 128
+        for i in range(4):
+            k, n = mpg.frag_b_coords(lane, i)
+            assert n * 16 + k == (i & 1) + t * 2 + (i >> 1) * 8 + g * 16

@@ -56,3 +56,42 @@ def test_bounded_wait_expires_and_reports():
     x = torch.ones(4, device="cuda") * 2
     torch.cuda.synchronize()
     assert float(x.sum()) == 8.0
+
+
+def _pack_pairs(vals16):
+    """(..., 2) fp16 values -> uint32 words, element 0 in the low half."""
+    bits = vals16.astype(np.float16).view(np.uint16).astype(np.uint32)
+    return (bits[..., 0] | (bits[..., 1] << 16)).astype(np.uint32)
+
+
+def test_operand_fragment_maps_on_hardware(orc):
+    """Fragments packed on the host with the A / B maps, loaded verbatim by
+    one mma.sync: the product must equal the host product exactly, so a wrong
+    map (transposed, half-swapped, registers exchanged) fails."""
+    import torch
+    mpg.build()
+    a = synthetic.asymmetric((16, 16), 63)
+    b = synthetic.asymmetric((16, 8), 64)
+    af = np.zeros((32, 8), np.float32)
+    bf = np.zeros((32, 4), np.float32)
+    for lane in range(32):
+        for i in range(8):
+            r, c = mpg.frag_a_coords(lane, i)
+            af[lane, i] = a[r, c]
+        for i in range(4):
+            k, n = mpg.frag_b_coords(lane, i)
+            bf[lane, i] = b[k, n]
+    A = torch.from_numpy(_pack_pairs(af.reshape(32, 4, 2)).view(np.int32)).cuda()
+    B = torch.from_numpy(_pack_pairs(bf.reshape(32, 2, 2)).view(np.int32)).cuda()
+    d = mpg.probe_mma_m16n8k16_fragments(A, B).cpu().numpy()
+    ref, _ = orc.gemm(a.astype(np.float16), b.astype(np.float16))
+    placed = np.full((16, 8), np.nan)
+    for lane in range(32):
+        for j in range(4):
+            r, c = mpg.acc_coords(lane, j)
+            placed[r, c] = d[lane, j]
+    assert np.array_equal(placed, ref)
+    # the same fragments with A's registers 1 and 2 exchanged give another product
+    A2 = torch.from_numpy(_pack_pairs(af.reshape(32, 4, 2))[:, [0, 2, 1, 3]].copy().view(np.int32)).cuda()
+    d2 = mpg.probe_mma_m16n8k16_fragments(A2, B).cpu().numpy()
+    assert not np.array_equal(d2, d)

@@ -132,3 +132,39 @@ def test_accumulator_rounding_model(capsys):
               f"rz {np.max(np.abs(d_rz - exact)):.4g}")
     # both models bound the error by one ulp per instruction
     assert np.max(np.abs(got - exact)) <= (steps - 1) * 0.125
+
+
+@pytest.mark.parametrize("mode,dt", [(mpg.BF16_F32ACC, "bf16"), (mpg.TF32, "f32"), (mpg.SPLIT_FP16_3CHAIN, "f32")])
+def test_backward_operand_roles_by_layout(mode, dt):
+    """The two products of a backward pass, dA = dC . B^T and dB = A^T . dC,
+    read the forward pass's row-major A (m x k) and B (k x n) buffers in place:
+    B^T is B's storage read column-major (ld n), A^T is A's storage read
+    column-major (ld k).  No transposed copies."""
+    import torch
+    mpg.build()
+    m, n, k = 200, 136, 168
+    import synthetic
+    from helpers import round_to
+    a = round_to(synthetic.normal((m, k), 91), dt)
+    b = round_to(synthetic.normal((k, n), 92), dt)
+    dc = round_to(synthetic.normal((m, n), 93), dt)
+    td = {"bf16": torch.bfloat16, "f32": torch.float32}[dt]
+    code = {"bf16": mpg.BF16, "f32": mpg.F32}[dt]
+    A = torch.from_numpy(a).cuda().to(td)
+    B = torch.from_numpy(b).cuda().to(td)
+    dC = torch.from_numpy(dc).cuda().to(td)
+    dA = torch.zeros((m, k), device="cuda")
+    dB = torch.zeros((k, n), device="cuda")
+    # dA (m x k) = dC (m x n, row-major ld n) . B^T (n x k: B's storage, column-major ld n)
+    mpg.gemm_raw(m, k, n, 1, dC.data_ptr(), n, 0, code, R, B.data_ptr(), n, 0, code, Cm,
+                 dA.data_ptr(), k, 0, 1.0, 0.0, mode)
+    # dB (k x n) = A^T (k x m: A's storage, column-major ld k) . dC (m x n, row-major ld n)
+    mpg.gemm_raw(k, n, m, 1, A.data_ptr(), k, 0, code, Cm, dC.data_ptr(), n, 0, code, R,
+                 dB.data_ptr(), n, 0, 1.0, 0.0, mode)
+    torch.cuda.synchronize()
+    q = {mpg.BF16_F32ACC: oracle.Q_BF16, mpg.TF32: oracle.Q_NONE, mpg.SPLIT_FP16_3CHAIN: oracle.Q_NONE}[mode]
+    tol = {mpg.BF16_F32ACC: TOL["q16"], mpg.TF32: TOL["tf32"], mpg.SPLIT_FP16_3CHAIN: TOL["split"]}[mode]
+    ref, den = oracle.gemm(dc, b.T.copy(), None, 1.0, 0.0, q, q)
+    assert oracle.max_rel_err(dA.cpu().numpy(), ref, den) <= tol
+    ref, den = oracle.gemm(a.T.copy(), dc, None, 1.0, 0.0, q, q)
+    assert oracle.max_rel_err(dB.cpu().numpy(), ref, den) <= tol
