@@ -138,7 +138,15 @@ typedef struct {
    * (4 bytes per operand element for the split, 2 otherwise, plus split-K
    * partials).  0 (default) = convert on the fly in the load stage. */
   int32_t prepass;
-  int32_t reserved[6];
+  /* Storage type of C (an mpg_dtype): MPG_F32 (default), MPG_F16 or MPG_BF16.
+   * With a 16-bit C the `C` argument points to 16-bit storage (ldc and
+   * strideC in its elements); beta*C is read in that type and the fp32
+   * result alpha*acc + beta*C is rounded once, to nearest even, when stored:
+   * the extra rounding stage of a reduced-precision output ("Tensor Core
+   * operands: a matrix instruction still needs a layout contract", third
+   * paragraph). */
+  int32_t c_dtype;
+  int32_t reserved[5];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);
@@ -152,7 +160,8 @@ void mpg_options_init(mpg_options* opt);
  *   strideA      elements between consecutive batch matrices of A; 0 means
  *                packed (m*lda for row-major, k*lda for column-major).
  *   B            likewise with (k x n): ROW_MAJOR ldb >= n, COL_MAJOR ldb >= k.
- *   C            device pointer, row-major fp32, ldc >= n; strideC 0 = m*ldc.
+ *   C            device pointer, row-major fp32 (or 16-bit, see
+ *                mpg_options.c_dtype), ldc >= n; strideC 0 = m*ldc.
  *   mode         precision policy; allowed input dtypes per mode:
  *                  FP16_F32ACC: A, B both F32 or both F16
  *                  BF16_F32ACC: A, B both F32 or both BF16

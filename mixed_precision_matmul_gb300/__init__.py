@@ -61,7 +61,8 @@ class Options(ctypes.Structure):
         ("wait_timeout_ns", ctypes.c_int64),
         ("split_chunk_k", ctypes.c_int32),
         ("prepass", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("c_dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 
@@ -248,8 +249,9 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, works
          opts: Options | None = None, stream=None):
     """C = alpha * A @ B + beta * C on CUDA tensors, in place on C.
 
-    A is (m, k) or (batch, m, k), B is (k, n) or (batch, k, n), C is fp32
-    (m, n) or (batch, m, n) with unit column stride.  ``mode`` is one of the
+    A is (m, k) or (batch, m, k), B is (k, n) or (batch, k, n), C is fp32,
+    fp16 or bf16 (m, n) or (batch, m, n) with unit column stride (a 16-bit C
+    gets one final rounding of the fp32 result).  ``mode`` is one of the
     precision constants (or a name from MODE_NAMES).  A workspace for split-K
     is allocated through torch when the library asks for one and none is
     given.  Returns C.
@@ -263,8 +265,16 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, works
     n = B.shape[-1]
     if B.shape[-2] != k or C.shape[-2] != m or C.shape[-1] != n:
         raise ValueError("shape mismatch")
-    if C.dtype != torch.float32 or C.stride(-1) != 1:
-        raise ValueError("C must be fp32 with unit column stride")
+    if C.dtype not in (torch.float32, torch.float16, torch.bfloat16) or C.stride(-1) != 1:
+        raise ValueError("C must be fp32, fp16 or bf16 with unit column stride")
+    if C.dtype != torch.float32:
+        o = Options()
+        if opts is not None:
+            ctypes.memmove(ctypes.byref(o), ctypes.byref(opts), ctypes.sizeof(Options))
+        else:
+            lib().mpg_options_init(ctypes.byref(o))
+        o.c_dtype = _dtype_code(C)
+        opts = o
     a_layout, lda, sa = _operand(A, m, k)
     b_layout, ldb, sb = _operand(B, k, n)
     ldc = max(C.stride(-2), n, 1)

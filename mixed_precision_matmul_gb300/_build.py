@@ -31,7 +31,7 @@ SOURCES = [
     "tc_generic.cu",
     "prepass.cu",
 ]
-HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -363,9 +363,11 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
     return fail(MPG_ERR_INVALID_ARG, "split exponent outside [-100, 100]");
   if (o.splitk < 0) return fail(MPG_ERR_INVALID_ARG, "negative splitk");
   if (o.wait_timeout_ns < 0) return fail(MPG_ERR_INVALID_ARG, "negative wait timeout");
+  if (o.c_dtype < MPG_F32 || o.c_dtype > MPG_BF16) return fail(MPG_ERR_INVALID_ARG, "unknown C dtype %d", o.c_dtype);
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
-  if (reinterpret_cast<uintptr_t>(C) % 4 != 0) return fail(MPG_ERR_INVALID_ARG, "C not 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 4 : 2) != 0)
+    return fail(MPG_ERR_INVALID_ARG, "C not aligned to its element size");
   if (k > 0 && alpha != 0.0f) {
     if (!A.ptr || !B.ptr) return fail(MPG_ERR_INVALID_ARG, "A or B is NULL");
     if (reinterpret_cast<uintptr_t>(A.ptr) % elem_bytes(A.dt) != 0 ||
@@ -492,7 +494,9 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   if (tiles > 0x7FFFFFFF) return fail(MPG_ERR_INVALID_ARG, "too many tiles");
   p.num_tiles = (int32_t)tiles;
   p.group_m = 16;
-  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (batch == 1 || p.stride_c % 4 == 0);
+  p.c_dtype = o.c_dtype;
+  p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 16 : 8) == 0) && (ldc % 4 == 0) &&
+               (batch == 1 || p.stride_c % 4 == 0);
   // generic loads read 4 consecutive elements as one vector when the base,
   // the leading dimension and the batch stride keep every chunk aligned
   auto vec_ok = [&](const Operand& x, int64_t stride) {
@@ -525,7 +529,8 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   if (splits_eff > 1) {
     // the reduction applies alpha (incl. the split scale) and beta
-    e = launch_splitk_reduce(p.partial, splits_eff, C, ldc, p.stride_c, p.m, p.n, p.batch, p.alpha, beta, stream);
+    e = launch_splitk_reduce(p.partial, splits_eff, C, o.c_dtype, ldc, p.stride_c, p.m, p.n, p.batch, p.alpha, beta,
+                             stream);
     if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
   }
   return MPG_OK;
@@ -634,13 +639,14 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
     case Kind::kNoop:
       return MPG_OK;
     case Kind::kScale:
-      e = launch_scale_c(C, ldc, sc, (int32_t)m, (int32_t)n, (int32_t)batch, beta, st);
+      e = launch_scale_c(C, o.c_dtype, ldc, sc, (int32_t)m, (int32_t)n, (int32_t)batch, beta, st);
       break;
     case Kind::kFfma: {
       FfmaParams fp;
       fp.a = static_cast<const float*>(A);
       fp.b = static_cast<const float*>(B);
       fp.c = C;
+      fp.c_dtype = o.c_dtype;
       fp.lda = lda;
       fp.ldb = ldb;
       fp.ldc = ldc;

@@ -2,6 +2,7 @@
 // (k == 0 or alpha == 0), the split-K reduction, the mma.sync m16n8k16
 // accumulator-layout probe and the bounded-wait self test.
 #include "internal.h"
+#include "outio.cuh"
 #include "ptx.cuh"
 
 namespace mpg {
@@ -18,24 +19,24 @@ uint32_t* status_word_ptr() {
 
 namespace {
 
-__global__ void scale_c_kernel(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
-                               float beta) {
+__global__ void scale_c_kernel(void* c, int c_dtype, int64_t ldc, int64_t stride_c, int32_t m, int32_t n,
+                               int32_t batch, float beta) {
   const int64_t per = (int64_t)m * n;
   const int64_t total = per * batch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t b = i / per;
     const int64_t r = (i - b * per) / n;
     const int64_t col = i - b * per - r * n;
-    float* dst = c + b * stride_c + r * ldc + col;
-    *dst = (beta != 0.0f) ? beta * *dst : 0.0f;
+    const int64_t idx = b * stride_c + r * ldc + col;
+    out_store(c, idx, (beta != 0.0f) ? beta * out_load(c, idx, c_dtype) : 0.0f, c_dtype);
   }
 }
 
 // out = alpha * (partial[0] + partial[1] + ... ) + beta * C, partial sums
 // added in split order.
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int32_t splits, float* c, int64_t ldc,
-                                     int64_t stride_c, int32_t m, int32_t n, int32_t batch, float alpha,
-                                     float beta) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int32_t splits, void* c, int c_dtype,
+                                     int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
+                                     float alpha, float beta) {
   const int64_t per = (int64_t)m * n;
   const int64_t total = per * batch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -44,8 +45,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int32_t 
     const int64_t b = i / per;
     const int64_t r = (i - b * per) / n;
     const int64_t col = i - b * per - r * n;
-    float* dst = c + b * stride_c + r * ldc + col;
-    *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * s) : alpha * s;
+    const int64_t idx = b * stride_c + r * ldc + col;
+    out_store(c, idx, (beta != 0.0f) ? fmaf(beta, out_load(c, idx, c_dtype), alpha * s) : alpha * s, c_dtype);
   }
 }
 
@@ -126,17 +127,18 @@ int grid_for(int64_t total) {
 
 }  // namespace
 
-cudaError_t launch_scale_c(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
-                           float beta, cudaStream_t stream) {
-  scale_c_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(c, ldc, stride_c, m, n, batch, beta);
+cudaError_t launch_scale_c(void* c, int c_dtype, int64_t ldc, int64_t stride_c, int32_t m, int32_t n,
+                           int32_t batch, float beta, cudaStream_t stream) {
+  scale_c_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(c, c_dtype, ldc, stride_c, m, n, batch,
+                                                                        beta);
   return cudaGetLastError();
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c, int64_t ldc, int64_t stride_c,
-                                 int32_t m, int32_t n, int32_t batch, float alpha, float beta,
+cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, void* c, int c_dtype, int64_t ldc,
+                                 int64_t stride_c, int32_t m, int32_t n, int32_t batch, float alpha, float beta,
                                  cudaStream_t stream) {
-  splitk_reduce_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(partial, splits, c, ldc, stride_c, m,
-                                                                                  n, batch, alpha, beta);
+  splitk_reduce_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(partial, splits, c, c_dtype, ldc,
+                                                                                  stride_c, m, n, batch, alpha, beta);
   return cudaGetLastError();
 }
 

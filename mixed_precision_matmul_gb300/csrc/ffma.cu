@@ -12,6 +12,7 @@
 // vectors; edge tiles and unaligned operands load element by element with
 // bounds checks.  Any layout, leading dimension and tail.
 #include "internal.h"
+#include "outio.cuh"
 
 namespace mpg {
 namespace {
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
   for (int bz = blockIdx.z; bz < p.batch; bz += gridDim.z) {
     const float* a = p.a + (int64_t)bz * p.stride_a;
     const float* b = p.b + (int64_t)bz * p.stride_b;
-    float* c = p.c + (int64_t)bz * p.stride_c;
+    void* c = static_cast<uint8_t*>(p.c) + (int64_t)bz * p.stride_c * (p.c_dtype == kOutF32 ? 4 : 2);
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -160,8 +161,10 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
       for (int j = 0; j < 8; ++j) {
         const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
         if (gn >= p.n) continue;
-        float* dst = c + (int64_t)gm * p.ldc + gn;
-        *dst = (p.beta != 0.0f) ? fmaf(p.beta, *dst, p.alpha * acc[i][j]) : p.alpha * acc[i][j];
+        const int64_t idx = (int64_t)gm * p.ldc + gn;
+        out_store(c, idx,
+                  (p.beta != 0.0f) ? fmaf(p.beta, out_load(c, idx, p.c_dtype), p.alpha * acc[i][j]) : p.alpha * acc[i][j],
+                  p.c_dtype);
       }
     }
     __syncthreads();

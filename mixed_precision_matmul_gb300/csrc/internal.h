@@ -46,7 +46,7 @@ struct TcParams {
   const void* a;      // generic path addressing (element units of the source type)
   const void* b;
   int64_t lda, ldb, stride_a, stride_b;
-  float* c;
+  void* c;            // output, element type c_dtype
   int64_t ldc, stride_c;
   float* partial;     // split-K partial sums [split][batch][m][n] (ld = n), or null
   int32_t m, n, k, batch;
@@ -55,7 +55,8 @@ struct TcParams {
   int32_t splits, kb_per_split;
   int32_t num_tiles;
   int32_t group_m;
-  int32_t c_vec_ok;   // C base 16-byte aligned and ldc % 4 == 0
+  int32_t c_dtype;    // 0 fp32, 1 fp16, 2 bf16 (rounded once, to nearest even, when stored)
+  int32_t c_vec_ok;   // 4-element vectors of C are aligned (base, ldc % 4, batch stride % 4)
   int32_t a_vec_ok, b_vec_ok;  // 4-element chunks of A / B are vector-aligned (generic loads)
   int32_t p_vec_ok;   // partial buffer: n % 4 == 0
   float alpha;        // already multiplied by 2^-(split_exp_a + split_exp_b)
@@ -88,7 +89,8 @@ bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out)
 struct FfmaParams {
   const float* a;
   const float* b;
-  float* c;
+  void* c;
+  int32_t c_dtype;
   int64_t lda, ldb, ldc, stride_a, stride_b, stride_c;
   int32_t m, n, k, batch;
   int32_t a_col_major, b_col_major;
@@ -97,12 +99,12 @@ struct FfmaParams {
 cudaError_t launch_ffma(const FfmaParams& p, cudaStream_t stream);
 
 // C = beta * C (beta == 0: C = 0 without reading it).
-cudaError_t launch_scale_c(float* c, int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
-                           float beta, cudaStream_t stream);
+cudaError_t launch_scale_c(void* c, int c_dtype, int64_t ldc, int64_t stride_c, int32_t m, int32_t n,
+                           int32_t batch, float beta, cudaStream_t stream);
 
 // C = alpha * sum_s partial[s] + beta * C, partial laid out [split][batch][m][n].
-cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, float* c, int64_t ldc, int64_t stride_c,
-                                 int32_t m, int32_t n, int32_t batch, float alpha, float beta,
+cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, void* c, int c_dtype, int64_t ldc,
+                                 int64_t stride_c, int32_t m, int32_t n, int32_t batch, float alpha, float beta,
                                  cudaStream_t stream);
 
 cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_t stream);

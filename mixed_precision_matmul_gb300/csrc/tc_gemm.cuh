@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "outio.cuh"
 #include "ptx.cuh"
 
 namespace mpg {
@@ -495,22 +496,25 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       const TileCoord tc = decode_tile(p, t);
       const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
       const int nchunks = (tc.kb1 - tc.kb0 + ck - 1) / ck;
-      float* out;
+      void* out;          // element (r, c) at out[r * ldo + c], type out_dt
       int64_t ldo;
       float alpha, beta;
       bool vec_ok;
+      int out_dt;
       if (p.splits > 1) {
         out = p.partial + ((int64_t)tc.s * p.batch + tc.b) * (int64_t)p.m * p.n;
         ldo = p.n;
         alpha = 1.0f;
         beta = 0.0f;
         vec_ok = p.p_vec_ok != 0;
+        out_dt = kOutF32;
       } else {
-        out = p.c + (int64_t)tc.b * p.stride_c;
+        out = static_cast<uint8_t*>(p.c) + (int64_t)tc.b * p.stride_c * (p.c_dtype == kOutF32 ? 4 : 2);
         ldo = p.ldc;
         alpha = p.alpha;
         beta = p.beta;
         vec_ok = p.c_vec_ok != 0;
+        out_dt = p.c_dtype;
       }
       const int row_base = tc.mb * T::BM + 32 * q;
 #pragma unroll 1
@@ -589,10 +593,10 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
               const int grow = row_base + r;
               if (grow < p.m) {
-                float4* dst = reinterpret_cast<float4*>(out + (int64_t)grow * ldo + col_base + ch * 4);
+                const int64_t idx = (int64_t)grow * ldo + col_base + ch * 4;
                 float4 o;
                 if (beta != 0.0f) {
-                  const float4 c0 = *dst;
+                  const float4 c0 = out_load4(out, idx, out_dt);
                   o.x = fmaf(beta, c0.x, alpha * x.x);
                   o.y = fmaf(beta, c0.y, alpha * x.y);
                   o.z = fmaf(beta, c0.z, alpha * x.z);
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                   o.z = alpha * x.z;
                   o.w = alpha * x.w;
                 }
-                *dst = o;
+                out_store4(out, idx, o, out_dt);
               }
             }
           } else {
@@ -613,8 +617,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
               const int grow = row_base + r;
               if (grow < p.m && gcol < p.n) {
-                float* dst = out + (int64_t)grow * ldo + gcol;
-                *dst = (beta != 0.0f) ? fmaf(beta, *dst, alpha * x) : alpha * x;
+                const int64_t idx = (int64_t)grow * ldo + gcol;
+                out_store(out, idx, (beta != 0.0f) ? fmaf(beta, out_load(out, idx, out_dt), alpha * x) : alpha * x,
+                          out_dt);
               }
             }
           }
