@@ -146,7 +146,15 @@ typedef struct {
    * operands: a matrix instruction still needs a layout contract", third
    * paragraph). */
   int32_t c_dtype;
-  int32_t reserved[5];
+  /* 1 = run 16-bit products on the direct TMA path (FP16 / BF16 operands, or
+   * the copies of the separate conversion pass) on pairs of CTAs: a cluster
+   * of two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
+   * tensor-core instructions, each CTA holding half of A's rows and half of
+   * B's columns.  The same products, accumulated in fp32 on the tensor cores
+   * along K in the same order; other configurations ignore it.  0 (default) = one CTA per
+   * 128-row tile. */
+  int32_t cta_pair;
+  int32_t reserved[4];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);

@@ -62,7 +62,8 @@ class Options(ctypes.Structure):
         ("split_chunk_k", ctypes.c_int32),
         ("prepass", ctypes.c_int32),
         ("c_dtype", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("cta_pair", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -267,7 +268,8 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, works
         raise ValueError("shape mismatch")
     if C.dtype not in (torch.float32, torch.float16, torch.bfloat16) or C.stride(-1) != 1:
         raise ValueError("C must be fp32, fp16 or bf16 with unit column stride")
-    if C.dtype != torch.float32:
+    if C.dtype != torch.float32 or opts is not None:
+        # the output type always follows C's own dtype
         o = Options()
         if opts is not None:
             ctypes.memmove(ctypes.byref(o), ctypes.byref(opts), ctypes.sizeof(Options))

@@ -30,6 +30,7 @@ SOURCES = [
     "tc_staged.cu",
     "tc_generic.cu",
     "prepass.cu",
+    "tc_pair.cu",
 ]
 HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh"]
 

@@ -122,6 +122,7 @@ struct Plan {
   int splits = 1;
   bool prepass = false;       // operands converted by a separate pass into the workspace
   Conv pre_conv = Conv::kNone;
+  bool pair = false;          // 256 x 256 tiles on CTA pairs (cta_group::2)
 };
 
 struct Operand {
@@ -303,6 +304,13 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = o.tile_n;
   }
   p.bn = bn;
+  // CTA pairs: 16-bit operands on the direct path (also the conversion
+  // pass's copies), 256-wide tiles
+  if (o.cta_pair == 1 && p.src == Src::kTmaDirect && p.conv == Conv::kNone && p.op != Op::kTF32 &&
+      (o.tile_n == 0 || o.tile_n == 256)) {
+    p.pair = true;
+    p.bn = 256;
+  }
 
   int splits = choose_splits(m, n, k, batch, sm_count, o);
   if (p.prepass) {
@@ -403,13 +411,47 @@ mpg_status encode_map(CUtensorMap* map, const Operand& x, int64_t inner, int64_t
   return MPG_OK;
 }
 
+// Clusters of two CTAs of the pair kernel that fit on the device at once,
+// asked once per device (both pair kernels have the same launch shape).
+mpg_status pair_clusters(DeviceInfo* dev, const TcKernel& kern, int* out) {
+  static std::mutex mu;
+  static int cached[kMaxDevices];
+  const int devid = (int)(dev - g_devices);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[devid] <= 0) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3((unsigned)kern.block);
+    cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern.fn, &cfg);
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return fail(MPG_ERR_UNSUPPORTED, "no resident cluster of two CTAs for the pair kernel: %s",
+                  e != cudaSuccess ? cudaGetErrorString(e) : "occupancy 0");
+    }
+    cached[devid] = n;
+  }
+  *out = cached[devid];
+  return MPG_OK;
+}
+
 mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, int64_t k, int64_t batch,
                      const Operand& A, const Operand& B, float* C, int64_t ldc, int64_t strideC, float alpha,
                      float beta, const mpg_options& o, void* workspace, cudaStream_t stream,
                      const Operand* A_lo = nullptr, const Operand* B_lo = nullptr) {
   TcKernel kern;
-  if (!mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern))
-    return fail(MPG_ERR_UNSUPPORTED, "no kernel for this configuration");
+  const bool found = plan.pair ? mpg::tc_lookup_pair(plan.op, &kern)
+                               : mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern);
+  if (!found) return fail(MPG_ERR_UNSUPPORTED, "no kernel for this configuration");
   if (kern.smem_bytes > dev->max_smem_optin)
     return fail(MPG_ERR_UNSUPPORTED, "kernel needs %d bytes of shared memory, device offers %d", kern.smem_bytes,
                 dev->max_smem_optin);
@@ -434,8 +476,10 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   const int BK = (plan.src == Src::kTmaDirect) ? (plan.op == Op::kTF32 ? 32 : 64) : 32;
-  const int BM = 128;
+  const int BM = plan.pair ? 256 : 128;   // rows of C per tile (a pair: 128 per CTA)
   const int bn = plan.bn;
+  const int a_box = 128;                  // rows of A per CTA
+  const int b_box = plan.pair ? bn / 2 : bn;   // rows of a K-major B tile per CTA
   const bool a_mn = (A.layout == MPG_COL_MAJOR);
   const bool b_mn = (B.layout == MPG_ROW_MAJOR);
   const int64_t a_stride = A.stride ? A.stride : (a_mn ? k * A.ld : m * A.ld);
@@ -446,24 +490,24 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   if (plan.src != Src::kGeneric) {
     mpg_status s;
     // staged path: fp32 boxes of 32 elements (128 bytes) per line
-    if (!a_mn) s = encode_map(&p.map_a, Ax, k, m, batch, BK, BM);
+    if (!a_mn) s = encode_map(&p.map_a, Ax, k, m, batch, BK, a_box);
     else s = encode_map(&p.map_a, Ax, m, k, batch, BK, BK);
     if (s != MPG_OK) return s;
-    if (!b_mn) s = encode_map(&p.map_b, Bx, k, n, batch, BK, bn);
+    if (!b_mn) s = encode_map(&p.map_b, Bx, k, n, batch, BK, b_box);
     else s = encode_map(&p.map_b, Bx, n, k, batch, BK, BK);
     if (s != MPG_OK) return s;
     // lo halves of pre-split operands: same geometry as the hi halves
     if (A_lo) {
       Operand Al = *A_lo;
       Al.stride = a_stride;
-      if (!a_mn) s = encode_map(&p.map_a_lo, Al, k, m, batch, BK, BM);
+      if (!a_mn) s = encode_map(&p.map_a_lo, Al, k, m, batch, BK, a_box);
       else s = encode_map(&p.map_a_lo, Al, m, k, batch, BK, BK);
       if (s != MPG_OK) return s;
     }
     if (B_lo) {
       Operand Bl = *B_lo;
       Bl.stride = b_stride;
-      if (!b_mn) s = encode_map(&p.map_b_lo, Bl, k, n, batch, BK, bn);
+      if (!b_mn) s = encode_map(&p.map_b_lo, Bl, k, n, batch, BK, b_box);
       else s = encode_map(&p.map_b_lo, Bl, n, k, batch, BK, BK);
       if (s != MPG_OK) return s;
     }
@@ -523,9 +567,31 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
     p.chunk_kb = (int32_t)std::min<int64_t>((chunk_k + BK - 1) / BK, p.num_k_blk);
   }
 
-  const int grid = (int)std::min<int64_t>(tiles, dev->sm_count);
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(kern.fn, dim3(grid), dim3(kern.block), args, kern.smem_bytes, stream);
+  cudaError_t e;
+  if (plan.pair) {
+    // clusters of two CTAs; as many clusters as can be resident at once
+    int clusters = 0;
+    mpg_status cs = pair_clusters(dev, kern, &clusters);
+    if (cs != MPG_OK) return cs;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(tiles, clusters)));
+    cfg.blockDim = dim3((unsigned)kern.block);
+    cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, kern.fn, args);
+  } else {
+    const int grid = (int)std::min<int64_t>(tiles, dev->sm_count);
+    e = cudaLaunchKernel(kern.fn, dim3(grid), dim3(kern.block), args, kern.smem_bytes, stream);
+  }
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   if (splits_eff > 1) {
     // the reduction applies alpha (incl. the split scale) and beta

@@ -85,6 +85,10 @@ struct TcKernel {
 // combination is not instantiated.
 bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out);
 
+// The 16-bit direct product on a CTA pair (cta_group::2, 256 x 256 tiles per
+// cluster of two CTAs); false for operand types it does not cover.
+bool tc_lookup_pair(Op op, TcKernel* out);
+
 // Plain fp32 FFMA comparator.
 struct FfmaParams {
   const float* a;

@@ -58,12 +58,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // global status word and the time limit of a single wait.
 struct WaitCtl {
   volatile int* abort;     // shared memory; non-zero once any role gave up
+  volatile int* peer_abort = nullptr;   // the other CTA's flag in a CTA pair (distributed shared memory)
   uint32_t* status;        // global device status word
   uint64_t limit_ns;
 };
 
 __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t code) {
   *c.abort = 1;
+  if (c.peer_abort) *c.peer_abort = 1;
   atomicOr(c.status, code);
 }
 

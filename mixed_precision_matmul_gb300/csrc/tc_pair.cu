@@ -1,0 +1,409 @@
+// The 16-bit tensor-core product on a pair of CTAs (sm_103a, cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile of C with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256): CTA rank r holds rows
+// 128r .. 128r+127 of the tile's A panel and columns 128r .. 128r+127 of its B
+// panel in shared memory, the tensor cores of the pair read both halves, and
+// each CTA's TMEM receives its own 128 rows x 256 columns of the accumulator.
+// Per SM this halves the B bytes that travel from L2 into shared memory (and
+// that the tensor core reads back) for the same flops, compared with a
+// 128 x 256 tile on one SM.  This is the GB300 counterpart of keeping the
+// accumulator in registers and feeding it from swizzled shared memory
+// ("tile_matmul(): use the cuBLASDx register-accumulator API ...", "Proposed
+// change"): the operands are staged once per pair instead of once per SM.
+//
+// Roles (320 threads per CTA):
+//   warp 0      TMA producer of this CTA's halves.  Both CTAs' copies signal
+//               the rank-0 CTA's "full" barrier (cp.async.bulk.tensor
+//               .cta_group::2), which expects the bytes of both.
+//   warp 1      TMEM allocation (collective over the pair); on rank 0 its
+//               lane 0 issues every MMA of the pair and commits with
+//               multicast to both CTAs' barriers.
+//   warps 2-9   epilogue of this CTA's 128 rows (two warps per TMEM lane
+//               quarter, each taking half of the columns); they hand the
+//               accumulator buffer back to rank 0 with a remote arrive.
+//
+// Every wait is bounded.  A timeout raises the abort flag of both CTAs, so
+// the pair stops together; every role then drains what it has in flight and
+// the pair meets at a final cluster barrier before TMEM is released.
+#include "tc_gemm.cuh"
+
+namespace mpg {
+namespace {
+
+template <Op O>
+struct PairTraits {
+  static constexpr int BM = 128;    // rows of A held by one CTA
+  static constexpr int BMP = 256;   // rows of the pair's tile
+  static constexpr int BN = 256;    // columns of the pair's tile (the instruction's N)
+  static constexpr int BNH = 128;   // columns of B held by one CTA
+  static constexpr int BK = 64;     // one 128-byte line of k per stage
+  static constexpr int kRowBytes = 128;
+  static constexpr uint32_t kSwizzle = kSwizzle128B;
+  static constexpr int kInstrK = 16;
+  static constexpr int kKSteps = BK / kInstrK;
+  static constexpr int kATile = BM * kRowBytes;
+  static constexpr int kBTile = BNH * kRowBytes;
+  static constexpr int kOpStage = kATile + kBTile;   // 32 KB of this CTA's halves
+  static constexpr int kStages = 6;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kAccStride = BN;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
+  static constexpr int kSmemBytes = 1024 + kStages * kOpStage + kEpiBytes + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kAccBufs * kAccStride <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : 1u;
+};
+
+// ---------------------------------------------------------------------------
+// cluster and cta_group::2 forms (used only by this kernel: every tcgen05
+// instruction of one kernel has to name the same CTA group)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Shared-window address of the same shared-memory location in CTA `rank` of
+// the cluster.
+__device__ __forceinline__ uint32_t cluster_smem_addr(uint32_t smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem), "r"(rank));
+  return r;
+}
+// Generic address of the same location in CTA `rank` (distributed shared memory).
+template <class T>
+__device__ __forceinline__ T* cluster_generic_ptr(T* p, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<T*>(r);
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory; completion is signalled on
+// the barrier at `bar_cluster_addr`, which may sit in the peer CTA.
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrival on the barrier at this offset in every CTA of `mask`, once all
+// MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+template <class T>
+__global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Both CTAs run the same code on the same dynamic shared-memory layout, so
+  // every buffer and barrier sits at the same offset in the two CTAs (the
+  // MMA's descriptors and the multicast commits rely on it).
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* op_base = smem;
+  float* epi_base = reinterpret_cast<float*>(op_base + T::kStages * T::kOpStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_base) + T::kEpiBytes);
+  uint64_t* op_full = bars;                         // rank 0: both CTAs' halves of a stage landed
+  uint64_t* op_empty = bars + T::kStages;           // each CTA: the pair's MMAs consumed the stage
+  uint64_t* acc_full = bars + 2 * T::kStages;       // each CTA: accumulator buffer complete
+  uint64_t* acc_empty = acc_full + T::kAccBufs;     // rank 0: both CTAs' epilogues drained it
+  uint64_t* done_bar = acc_empty + T::kAccBufs;     // rank 0: every MMA of the pair finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t cid = cluster_id_x();
+  const uint32_t ncl = num_clusters_x();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < T::kStages; ++i) {
+      mbar_init(&op_full[i], 1);     // the rank-0 producer's arrive.expect_tx
+      mbar_init(&op_empty[i], 1);    // one multicast commit
+    }
+    for (int i = 0; i < T::kAccBufs; ++i) {
+      mbar_init(&acc_full[i], 1);                   // one multicast commit
+      mbar_init(&acc_empty[i], 2 * T::kEpiWarps);   // one arrival per epilogue warp of the pair
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, T::kTmemCols);
+    tmem_relinquish_pair();
+    tc_fence_before_sync();
+  }
+  // barriers, abort flags and the TMEM address of both CTAs are in place
+  // before either CTA touches the other's shared memory
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  WaitCtl ctl;
+  ctl.abort = abort_flag;
+  ctl.peer_abort = cluster_generic_ptr(const_cast<int*>(abort_flag), rank ^ 1u);
+  ctl.status = p.status;
+  ctl.limit_ns = p.wait_limit_ns;
+
+  const uint32_t op_smem = smem_addr(op_base);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.map_a);
+      tma_prefetch_map(&p.map_b);
+      const uint32_t full0 = cluster_smem_addr(smem_addr(op_full), 0);   // rank 0's op_full[0]
+      constexpr int kRegion = T::BK * T::kRowBytes;                      // one MN-major region
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl) {
+        const TileCoord tc = decode_tile(p, t);
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
+          const uint32_t st = it % T::kStages;
+          const uint32_t ph = (it / T::kStages) & 1u;
+          if (!mbar_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(&op_full[st], 2 * T::kOpStage);
+          uint8_t* dst = op_base + st * T::kOpStage;
+          const uint32_t bar = full0 + st * 8u;
+          const int k0 = kb * T::BK;
+          auto load_half = [&](const CUtensorMap* map, uint8_t* d, bool mn, int row0, int rows) {
+            if (!mn) {
+              tma_load_3d_pair(d, map, bar, k0, row0, tc.b);
+            } else {
+              for (int g = 0; g < rows / T::BK; ++g) tma_load_3d_pair(d + g * kRegion, map, bar, row0 + g * T::BK, k0, tc.b);
+            }
+          };
+          load_half(&p.map_a, dst, p.a_mn_major != 0, tc.mb * T::BMP + (int)rank * T::BM, T::BM);
+          load_half(&p.map_b, dst + T::kATile, p.b_mn_major != 0, tc.nb * T::BN + (int)rank * T::BNH, T::BNH);
+        }
+      }
+      // A stage is released (op_empty) only after both halves landed and the
+      // pair's MMAs read them, so waiting for the last releases also covers
+      // this CTA's copies still in flight.
+      const uint32_t n_drain = it < (uint32_t)T::kStages ? it : (uint32_t)T::kStages;
+      for (uint32_t i = it - n_drain; i < it; ++i)
+        drain_wait(&op_empty[i % T::kStages], (i / T::kStages) & 1u, p.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
+      const bool a_mn = p.a_mn_major != 0;
+      const bool b_mn = p.b_mn_major != 0;
+      const uint32_t idesc = make_idesc(T::kAbFormat, a_mn, b_mn, T::BMP, T::BN);
+      uint32_t it = 0, g = 0;
+      bool ok = true;
+      for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl, ++g) {
+        const TileCoord tc = decode_tile(p, t);
+        const uint32_t ab = g % T::kAccBufs;
+        const uint32_t aph = (g / T::kAccBufs) & 1u;
+        if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctl)) { ok = false; break; }
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + ab * T::kAccStride;
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
+          const uint32_t st = it % T::kStages;
+          const uint32_t ph = (it / T::kStages) & 1u;
+          if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_tile = op_smem + st * T::kOpStage;
+          const uint32_t b_tile = a_tile + T::kATile;
+#pragma unroll
+          for (int ks = 0; ks < T::kKSteps; ++ks)
+            mma_f16_pair(d0, operand_desc<T>(a_tile, a_mn, ks), operand_desc<T>(b_tile, b_mn, ks), idesc,
+                         (kb > tc.kb0 || ks > 0) ? 1u : 0u);
+          mma_commit_multicast(&op_empty[st], 0x3);
+        }
+        if (!ok) break;
+        mma_commit_multicast(&acc_full[ab], 0x3);
+      }
+      // every MMA of the pair completes before either CTA releases TMEM
+      mma_commit_multicast(done_bar, 0x1);
+      drain_wait(done_bar, 0, p.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    float* stg = epi_base + (warp - 2) * 1024;
+    const uint32_t stg_addr = smem_addr(stg);
+    constexpr int kColGroups = T::kEpiWarps / 4;
+    constexpr int kCcPer = T::BN / 32 / kColGroups;
+    const int cc0 = ((warp - 2) / 4) * kCcPer;
+    const uint32_t acc_empty0 = cluster_smem_addr(smem_addr(acc_empty), 0);   // rank 0's acc_empty[0]
+    uint32_t g = 0;
+    bool ok = true;
+    for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl, ++g) {
+      const TileCoord tc = decode_tile(p, t);
+      void* out;
+      int64_t ldo;
+      float alpha, beta;
+      bool vec_ok;
+      int out_dt;
+      if (p.splits > 1) {
+        out = p.partial + ((int64_t)tc.s * p.batch + tc.b) * (int64_t)p.m * p.n;
+        ldo = p.n;
+        alpha = 1.0f;
+        beta = 0.0f;
+        vec_ok = p.p_vec_ok != 0;
+        out_dt = kOutF32;
+      } else {
+        out = static_cast<uint8_t*>(p.c) + (int64_t)tc.b * p.stride_c * (p.c_dtype == kOutF32 ? 4 : 2);
+        ldo = p.ldc;
+        alpha = p.alpha;
+        beta = p.beta;
+        vec_ok = p.c_vec_ok != 0;
+        out_dt = p.c_dtype;
+      }
+      const uint32_t ab = g % T::kAccBufs;
+      const uint32_t aph = (g / T::kAccBufs) & 1u;
+      if (!warp_wait(&acc_full[ab], aph, ctl)) { ok = false; break; }
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + lane_off + ab * T::kAccStride;
+      const int row_base = tc.mb * T::BMP + (int)rank * T::BM + 32 * q;
+#pragma unroll 1
+      for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
+        float v[32];
+        tmem_ld_32cols(tacc + cc * 32, v);
+        tmem_ld_wait();
+        if (cc == cc0 + kCcPer - 1) {
+          // this warp's share of the buffer is in registers: hand it back
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty0 + ab * 8u);
+        }
+        const int col_base = tc.nb * T::BN + cc * 32;
+        if (row_base >= p.m || col_base >= p.n) continue;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
+                       __float_as_uint(v[4 * ch + 1]), __float_as_uint(v[4 * ch + 2]), __float_as_uint(v[4 * ch + 3]));
+        }
+        __syncwarp();
+        if (vec_ok && col_base + 32 <= p.n) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = i * 4 + (lane >> 3);
+            const int ch = lane & 7;
+            const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
+            const int grow = row_base + r;
+            if (grow < p.m) {
+              const int64_t idx = (int64_t)grow * ldo + col_base + ch * 4;
+              float4 o;
+              if (beta != 0.0f) {
+                const float4 c0 = out_load4(out, idx, out_dt);
+                o.x = fmaf(beta, c0.x, alpha * x.x);
+                o.y = fmaf(beta, c0.y, alpha * x.y);
+                o.z = fmaf(beta, c0.z, alpha * x.z);
+                o.w = fmaf(beta, c0.w, alpha * x.w);
+              } else {
+                o.x = alpha * x.x;
+                o.y = alpha * x.y;
+                o.z = alpha * x.z;
+                o.w = alpha * x.w;
+              }
+              out_store4(out, idx, o, out_dt);
+            }
+          }
+        } else {
+          const int gcol = col_base + lane;
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
+            const int grow = row_base + r;
+            if (grow < p.m && gcol < p.n) {
+              const int64_t idx = (int64_t)grow * ldo + gcol;
+              out_store(out, idx, (beta != 0.0f) ? fmaf(beta, out_load(out, idx, out_dt), alpha * x) : alpha * x,
+                        out_dt);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+
+  // Neither CTA releases TMEM or exits while the other may still address its
+  // shared memory (remote arrivals, multicast commits, copies signalling rank
+  // 0) or while MMAs of the pair are in flight.
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, T::kTmemCols);
+  }
+}
+
+template <class T>
+void pair_fill(TcKernel* out) {
+  out->fn = reinterpret_cast<const void*>(&tc_pair_kernel<T>);
+  out->block = T::kThreads;
+  out->smem_bytes = T::kSmemBytes;
+  out->bn = T::BN;
+}
+
+}  // namespace
+
+bool tc_lookup_pair(Op op, TcKernel* out) {
+  switch (op) {
+    case Op::kF16: pair_fill<PairTraits<Op::kF16>>(out); return true;
+    case Op::kBF16: pair_fill<PairTraits<Op::kBF16>>(out); return true;
+    default: return false;
+  }
+}
+
+}  // namespace mpg

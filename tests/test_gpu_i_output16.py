@@ -67,3 +67,23 @@ def test_sixteen_bit_output_split_k_and_scale(out):
     assert np.all(np.abs(got - ref) <= _ulp(ref, out) + TOL["split"] * den)
     got, ref, den = _run(mpg.BF16_F32ACC, "bf16", out, 70, 90, 0, beta=-0.75)   # k == 0: C = beta*C
     assert np.all(np.abs(got - ref) <= _ulp(ref, out))
+
+
+def test_torch_api_output_type_follows_c():
+    """gemm() takes the output type from C's dtype, also when the caller's
+    options say otherwise."""
+    import torch
+    mpg.build()
+    m, n, k = 200, 136, 96
+    a = synthetic.normal((m, k), 111)
+    b = synthetic.normal((k, n), 112)
+    A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ref, den = oracle.gemm(a, b, None, 1.0, 0.0, oracle.Q_FP16, oracle.Q_FP16)
+    C16 = torch.zeros((m, n), dtype=torch.bfloat16, device="cuda")
+    mpg.gemm(A, B, C16, mode="fp16")
+    got = C16.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= _ulp(ref, "bf16") + TOL["q16"] * den)
+    C32 = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    mpg.gemm(A, B, C32, mode="fp16", opts=mpg.options(c_dtype=mpg.F16))
+    torch.cuda.synchronize()
+    assert oracle.max_rel_err(C32.cpu().numpy(), ref, den) <= TOL["q16"]
