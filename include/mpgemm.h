@@ -146,13 +146,14 @@ typedef struct {
    * operands: a matrix instruction still needs a layout contract", third
    * paragraph). */
   int32_t c_dtype;
-  /* 1 = run 16-bit products on the direct TMA path (FP16 / BF16 operands, or
-   * the copies of the separate conversion pass) on pairs of CTAs: a cluster
-   * of two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
+  /* CTA pairs for 16-bit products on the direct TMA path (FP16 / BF16
+   * operands, or the copies of the separate conversion pass): a cluster of
+   * two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
    * tensor-core instructions, each CTA holding half of A's rows and half of
-   * B's columns.  The same products, accumulated in fp32 on the tensor cores
-   * along K in the same order; other configurations ignore it.  0 (default) = one CTA per
-   * 128-row tile. */
+   * B's columns; the same products, accumulated in fp32 on the tensor cores
+   * along K in the same order.  0 (default) = used when the 256 x 256 tiles
+   * give every pair of SMs at least one tile, 1 = always where it applies,
+   * -1 = never (one CTA per 128-row tile).  Other configurations ignore it. */
   int32_t cta_pair;
   int32_t reserved[4];
 } mpg_options;
@@ -233,6 +234,41 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
  * Depends only on the sizes, the mode, the options and the current device. */
 size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
                                mpg_precision mode, const mpg_options* opt);
+
+/* The product with A, B and C in HOST memory: the call copies the operands
+ * in, multiplies on the device and copies C back, all enqueued on `stream`.
+ *
+ * The same arguments as mpg_gemm_ex, except that A, B and C are host
+ * pointers (page-locked memory, e.g. from cudaHostAlloc, lets the copies run
+ * asynchronously and overlap; pageable memory works but its copies block the
+ * calling thread).  C's padding columns (n .. ldc-1) are never written.
+ *   workspace   device memory of at least mpg_gemm_host_workspace_size()
+ *               bytes for the same arguments, 16-byte aligned: device copies
+ *               of A, B and C with the caller's leading dimensions and batch
+ *               strides, plus the product's own workspace.
+ * Inside one call the copies overlap the product: B is copied first, then A
+ * and C are processed in chunks of rows (of whole matrices when batch > 1),
+ * the copy of chunk i+1 and the copy back of chunk i-1 running beside the
+ * product of chunk i on two internal copy streams of the library, ordered
+ * against `stream` by events.  When the call returns, the work is enqueued;
+ * C holds the result once `stream` has completed it (e.g. after
+ * cudaStreamSynchronize(stream)).  Calls on different streams with separate
+ * workspaces and host buffers overlap each other's copies and products.
+ * Errors: those of mpg_gemm_ex; MPG_ERR_WORKSPACE if the workspace is too
+ * small.  No counterpart on the pages: this is the library's entry point for
+ * data that lives on the host. */
+size_t mpg_gemm_host_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
+                                    int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
+                                    int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                                    int64_t ldc, int64_t strideC, float alpha, float beta,
+                                    mpg_precision mode, const mpg_options* opt);
+mpg_status mpg_gemm_host(int64_t m, int64_t n, int64_t k, int64_t batch,
+                         const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
+                         const void* B, int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                         void* C, int64_t ldc, int64_t strideC,
+                         float alpha, float beta, mpg_precision mode,
+                         void* workspace, size_t workspace_bytes, void* stream,
+                         const mpg_options* opt);
 
 /* Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns MPG_ERR_TIMEOUT if any kernel since the

@@ -105,6 +105,11 @@ def lib():
         L.mpg_gemm_noalloc.restype = i32
         L.mpg_gemm_workspace_size.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options)]
         L.mpg_gemm_workspace_size.restype = sz
+        L.mpg_gemm_host.argtypes = gemm_args + [ctypes.POINTER(Options)]
+        L.mpg_gemm_host.restype = i32
+        L.mpg_gemm_host_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, i32, i64, i64, i32, i32,
+                                                   i64, i64, f32, f32, i32, ctypes.POINTER(Options)]
+        L.mpg_gemm_host_workspace_size.restype = sz
         L.mpg_options_init.argtypes = [ctypes.POINTER(Options)]
         L.mpg_options_init.restype = None
         L.mpg_device_status.argtypes = [vp]
@@ -192,6 +197,27 @@ def gemm_noalloc_raw(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb,
     if check:
         _check(st)
     return st
+
+
+def gemm_host_raw(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout,
+                  C, ldc, strideC, alpha, beta, mode, workspace, workspace_bytes, stream=0,
+                  opts: Options | None = None, check: bool = True) -> int:
+    """mpg_gemm_host: A, B and C are HOST addresses; the call copies in,
+    multiplies and copies C back, enqueued on `stream` (device workspace of
+    host_workspace_size() bytes)."""
+    st = lib().mpg_gemm_host(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype,
+                             b_layout, C, ldc, strideC, float(alpha), float(beta), mode, workspace or None,
+                             workspace_bytes, stream or None, ctypes.byref(opts) if opts is not None else None)
+    if check:
+        _check(st)
+    return st
+
+
+def host_workspace_size(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, strideB, b_dtype, b_layout,
+                        ldc, strideC, alpha, beta, mode, opts: Options | None = None) -> int:
+    return int(lib().mpg_gemm_host_workspace_size(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, strideB,
+                                                  b_dtype, b_layout, ldc, strideC, float(alpha), float(beta), mode,
+                                                  ctypes.byref(opts) if opts is not None else None))
 
 
 def workspace_size(m, n, k, batch, mode, opts: Options | None = None) -> int:

@@ -305,9 +305,13 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   }
   p.bn = bn;
   // CTA pairs: 16-bit operands on the direct path (also the conversion
-  // pass's copies), 256-wide tiles
-  if (o.cta_pair == 1 && p.src == Src::kTmaDirect && p.conv == Conv::kNone && p.op != Op::kTF32 &&
-      (o.tile_n == 0 || o.tile_n == 256)) {
+  // pass's copies), 256 x 256 tiles.  Chosen by the library when those tiles
+  // give every pair of SMs at least one (a smaller problem keeps the finer
+  // 128-row tiles), or forced with cta_pair = 1.
+  const bool pair_ok = p.src == Src::kTmaDirect && p.conv == Conv::kNone && p.op != Op::kTF32 &&
+                       (o.tile_n == 0 || o.tile_n == 256);
+  const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
+  if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && o.tile_n == 0 && pair_tiles * 2 >= sm_count))) {
     p.pair = true;
     p.bn = 256;
   }
@@ -372,6 +376,7 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (o.splitk < 0) return fail(MPG_ERR_INVALID_ARG, "negative splitk");
   if (o.wait_timeout_ns < 0) return fail(MPG_ERR_INVALID_ARG, "negative wait timeout");
   if (o.c_dtype < MPG_F32 || o.c_dtype > MPG_BF16) return fail(MPG_ERR_INVALID_ARG, "unknown C dtype %d", o.c_dtype);
+  if (o.cta_pair < -1 || o.cta_pair > 1) return fail(MPG_ERR_INVALID_ARG, "cta_pair must be -1, 0 or 1");
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
   if (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 4 : 2) != 0)
@@ -537,7 +542,10 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   const int64_t tiles = (int64_t)splits_eff * batch * p.num_m_blk * p.num_n_blk;
   if (tiles > 0x7FFFFFFF) return fail(MPG_ERR_INVALID_ARG, "too many tiles");
   p.num_tiles = (int32_t)tiles;
-  p.group_m = 16;
+  // rasterisation: groups of tile rows sized so that the tiles resident at
+  // once touch about as many A panels as B panels (tiles of a pair are
+  // twice as tall)
+  p.group_m = plan.pair ? 8 : 16;
   p.c_dtype = o.c_dtype;
   p.c_vec_ok = (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 16 : 8) == 0) && (ldc % 4 == 0) &&
                (batch == 1 || p.stride_c % 4 == 0);
@@ -637,6 +645,136 @@ mpg_status noalloc_scratch(void** out) {
   }
   *out = slot.ptr;
   return MPG_OK;
+}
+
+// --------------------------------------------------------------------------
+// host-buffer entry point: device copies, chunk plan, internal streams
+// --------------------------------------------------------------------------
+// Stored footprint of one operand: `batch` matrices of `outer` lines of
+// `inner` elements, lines `ld` apart, matrices `stride` apart.
+struct Footprint {
+  int64_t outer = 0, inner = 0, ld = 0, stride = 0, batch = 0, es = 0;
+  // elements from the first to the last stored element (padding between
+  // lines included, nothing past the last element)
+  int64_t span() const { return (batch == 0 || outer == 0) ? 0 : (batch - 1) * stride + (outer - 1) * ld + inner; }
+};
+
+constexpr int kMaxHostChunks = 8;
+constexpr int64_t kHostChunkBytes = int64_t(64) << 20;   // input bytes per chunk, about
+
+struct HostPlan {
+  Footprint a, b, c;
+  bool need_ab = false;    // A and B are read (k > 0, alpha != 0)
+  bool need_c0 = false;    // C is read (beta != 0)
+  bool by_batch = false;   // chunks of whole matrices (batch > 1), else of rows of A and C
+  int64_t chunk = 0;       // rows, or matrices, per chunk
+  int nchunks = 0;
+  size_t off_a = 0, off_b = 0, off_c = 0, off_ws = 0, ws_bytes = 0, total = 0;
+};
+
+mpg_status host_plan(int64_t m, int64_t n, int64_t k, int64_t batch, int64_t lda, int64_t strideA, mpg_dtype adt,
+                     mpg_layout al, int64_t ldb, int64_t strideB, mpg_dtype bdt, mpg_layout bl, int64_t ldc,
+                     int64_t strideC, float alpha, float beta, mpg_precision mode, const mpg_options& o,
+                     HostPlan* out) {
+  HostPlan h;
+  const bool a_row = (al == MPG_ROW_MAJOR), b_row = (bl == MPG_ROW_MAJOR);
+  h.a = {a_row ? m : k, a_row ? k : m, lda, 0, batch, elem_bytes(adt)};
+  h.b = {b_row ? k : n, b_row ? n : k, ldb, 0, batch, elem_bytes(bdt)};
+  h.c = {m, n, ldc, 0, batch, o.c_dtype == MPG_F32 ? 4 : 2};
+  h.a.stride = strideA ? strideA : h.a.outer * lda;
+  h.b.stride = strideB ? strideB : h.b.outer * ldb;
+  h.c.stride = strideC ? strideC : m * ldc;
+  h.need_ab = (k > 0 && alpha != 0.0f);
+  h.need_c0 = (beta != 0.0f);
+  const int64_t in_bytes = (h.need_ab ? h.a.span() * h.a.es : 0) + (h.need_c0 ? h.c.span() * h.c.es : 0);
+  int64_t want = std::min<int64_t>(kMaxHostChunks, std::max<int64_t>(1, in_bytes / kHostChunkBytes));
+  h.by_batch = batch > 1;
+  if (h.by_batch) {
+    want = std::min<int64_t>(want, batch);
+    h.chunk = (batch + want - 1) / want;
+    h.nchunks = (int)((batch + h.chunk - 1) / h.chunk);
+  } else {
+    // row chunks in multiples of 256 rows (a whole number of tiles)
+    want = std::min<int64_t>(want, std::max<int64_t>(1, m / 256));
+    h.chunk = ((m + want - 1) / want + 255) / 256 * 256;
+    h.nchunks = (int)((m + h.chunk - 1) / h.chunk);
+  }
+  // product workspace: the larger of a full chunk and the last one
+  auto ws_for = [&](int64_t units) {
+    return h.by_batch ? mpg_gemm_workspace_size(m, n, k, units, mode, &o)
+                      : mpg_gemm_workspace_size(units, n, k, 1, mode, &o);
+  };
+  const int64_t total_units = h.by_batch ? batch : m;
+  const int64_t last = total_units - (int64_t)(h.nchunks - 1) * h.chunk;
+  h.ws_bytes = std::max(ws_for(h.chunk), ws_for(last));
+  size_t off = 0;
+  h.off_a = off; off += align256((size_t)(h.need_ab ? h.a.span() * h.a.es : 0));
+  h.off_b = off; off += align256((size_t)(h.need_ab ? h.b.span() * h.b.es : 0));
+  h.off_c = off; off += align256((size_t)(h.c.span() * h.c.es));
+  h.off_ws = off; off += align256(h.ws_bytes);
+  h.total = off;
+  *out = h;
+  return MPG_OK;
+}
+
+// Internal copy streams of one device and the events that order them against
+// the caller's stream.  One call enqueues at a time (the mutex).
+struct HostStreams {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev[2 + 2 * kMaxHostChunks] = {};
+  std::mutex mu;
+};
+HostStreams g_host[kMaxDevices];
+
+mpg_status host_streams(HostStreams** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(MPG_ERR_NO_DEVICE, "no current CUDA device");
+  }
+  HostStreams& hs = g_host[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!hs.ready) {
+    cudaError_t e = cudaStreamCreateWithFlags(&hs.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hs.out, cudaStreamNonBlocking);
+    for (auto& ev : hs.ev)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "copy streams: %s", cudaGetErrorString(e));
+    hs.ready = true;
+  }
+  *out = &hs;
+  return MPG_OK;
+}
+
+// Lines [l0, l1) of matrices [b0, b1) of one operand, `width` elements of
+// each line, between host and device copies that share the footprint.
+cudaError_t copy_lines(const Footprint& f, void* dst, const void* src, int64_t b0, int64_t b1, int64_t l0, int64_t l1,
+                       int64_t c0, int64_t width, cudaMemcpyKind kind, cudaStream_t st) {
+  const int64_t lines = l1 - l0;
+  if (lines <= 0 || b1 <= b0 || width <= 0) return cudaSuccess;
+  auto at = [&](const void* base, int64_t b) {
+    return static_cast<const uint8_t*>(base) + ((b * f.stride + l0 * f.ld + c0) * f.es);
+  };
+  if (b1 - b0 == 1 || (l0 == 0 && l1 == f.outer && f.stride == f.outer * f.ld)) {
+    // one run of equally spaced lines
+    const int64_t rows = (b1 - b0 == 1) ? lines : (b1 - b0) * f.outer;
+    return cudaMemcpy2DAsync(const_cast<uint8_t*>(at(dst, b0)), (size_t)(f.ld * f.es), at(src, b0),
+                             (size_t)(f.ld * f.es), (size_t)(width * f.es), (size_t)rows, kind, st);
+  }
+  for (int64_t b = b0; b < b1; ++b) {
+    cudaError_t e = cudaMemcpy2DAsync(const_cast<uint8_t*>(at(dst, b)), (size_t)(f.ld * f.es), at(src, b),
+                                      (size_t)(f.ld * f.es), (size_t)(width * f.es), (size_t)lines, kind, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// A contiguous element range [e0, e0 + count) of one operand, host to device.
+cudaError_t copy_span_in(const Footprint& f, void* dst, const void* src, int64_t e0, int64_t count, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + e0 * f.es, static_cast<const uint8_t*>(src) + e0 * f.es,
+                         (size_t)(count * f.es), cudaMemcpyHostToDevice, st);
 }
 
 }  // namespace
@@ -866,6 +1004,119 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch, cons
   return mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout, C,
                      ldc, strideC, alpha, beta, mode, scratch, need > 0 ? (size_t)MPG_NOALLOC_SCRATCH_BYTES : 0,
                      stream, opt);
+}
+
+size_t mpg_gemm_host_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, int64_t lda, int64_t strideA,
+                                    mpg_dtype a_dtype, mpg_layout a_layout, int64_t ldb, int64_t strideB,
+                                    mpg_dtype b_dtype, mpg_layout b_layout, int64_t ldc, int64_t strideC,
+                                    float alpha, float beta, mpg_precision mode, const mpg_options* opt) {
+  mpg_options o;
+  resolve_options(opt, &o);
+  if (m <= 0 || n <= 0 || batch <= 0 || k < 0) return 0;
+  HostPlan h;
+  if (host_plan(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, strideB, b_dtype, b_layout, ldc, strideC,
+                alpha, beta, mode, o, &h) != MPG_OK)
+    return 0;
+  t_err.clear();
+  return h.total;
+}
+
+mpg_status mpg_gemm_host(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
+                         int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B, int64_t ldb,
+                         int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout, void* C, int64_t ldc,
+                         int64_t strideC, float alpha, float beta, mpg_precision mode, void* workspace,
+                         size_t workspace_bytes, void* stream, const mpg_options* opt) {
+  t_err.clear();
+  mpg_options o;
+  resolve_options(opt, &o);
+  Operand Aop{A, lda, strideA, a_dtype, a_layout};
+  Operand Bop{B, ldb, strideB, b_dtype, b_layout};
+  mpg_status s = validate(m, n, k, batch, Aop, Bop, static_cast<const float*>(C), ldc, strideC, alpha, mode, o);
+  if (s != MPG_OK) return s;
+  if (m == 0 || n == 0 || batch == 0) return MPG_OK;
+  HostPlan h;
+  s = host_plan(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, strideB, b_dtype, b_layout, ldc, strideC,
+                alpha, beta, mode, o, &h);
+  if (s != MPG_OK) return s;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return fail(MPG_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
+  if (workspace_bytes < h.total)
+    return fail(MPG_ERR_WORKSPACE, "host-buffer product needs %zu workspace bytes, got %zu", h.total,
+                workspace_bytes);
+  HostStreams* hs = nullptr;
+  s = host_streams(&hs);
+  if (s != MPG_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* dA = ws + h.off_a;
+  uint8_t* dB = ws + h.off_b;
+  uint8_t* dC = ws + h.off_c;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(hs->mu);
+  cudaEvent_t ev_start = hs->ev[0], ev_end = hs->ev[1];
+  // copies start once earlier work of the caller's stream (which may still
+  // use this workspace) is done
+  cudaError_t e = cudaEventRecord(ev_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->out, ev_start, 0);
+  if (e == cudaSuccess && h.need_ab) e = copy_span_in(h.b, dB, B, 0, h.b.span(), hs->in);
+  mpg_status prod = MPG_OK;
+  const bool a_row = (a_layout == MPG_ROW_MAJOR);
+  for (int c = 0; c < h.nchunks && e == cudaSuccess && prod == MPG_OK; ++c) {
+    cudaEvent_t ev_in = hs->ev[2 + 2 * c], ev_cmp = hs->ev[3 + 2 * c];
+    const int64_t u0 = (int64_t)c * h.chunk;
+    const int64_t u1 = std::min<int64_t>(h.by_batch ? batch : m, u0 + h.chunk);
+    // ---- inputs of the chunk
+    if (h.by_batch) {
+      const int64_t nb = u1 - u0;
+      if (h.need_ab) {
+        Footprint fa = h.a;
+        fa.batch = nb;
+        e = copy_span_in(h.a, dA, A, u0 * h.a.stride, fa.span(), hs->in);
+      }
+      if (e == cudaSuccess && h.need_c0) {
+        Footprint fc = h.c;
+        fc.batch = nb;
+        e = copy_span_in(h.c, dC, C, u0 * h.c.stride, fc.span(), hs->in);
+      }
+    } else {
+      if (h.need_ab) {
+        if (a_row) e = copy_span_in(h.a, dA, A, u0 * lda, (u1 - u0 - 1) * lda + k, hs->in);
+        else e = copy_lines(h.a, dA, A, 0, 1, 0, k, u0, u1 - u0, cudaMemcpyHostToDevice, hs->in);
+      }
+      if (e == cudaSuccess && h.need_c0) e = copy_span_in(h.c, dC, C, u0 * ldc, (u1 - u0 - 1) * ldc + n, hs->in);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, hs->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+    if (e != cudaSuccess) break;
+    // ---- the chunk's product on the caller's stream
+    const int64_t es_a = h.a.es, es_c = h.c.es;
+    if (h.by_batch) {
+      prod = mpg_gemm_ex(m, n, k, u1 - u0, dA + u0 * h.a.stride * es_a, lda, h.a.stride, a_dtype, a_layout,
+                         dB + u0 * h.b.stride * h.b.es, ldb, h.b.stride, b_dtype, b_layout, reinterpret_cast<float*>(dC + u0 * h.c.stride * es_c), ldc,
+                         h.c.stride, alpha, beta, mode, ws + h.off_ws, h.ws_bytes, st, &o);
+    } else {
+      const int64_t a_off = a_row ? u0 * lda : u0;
+      prod = mpg_gemm_ex(u1 - u0, n, k, 1, dA + a_off * es_a, lda, 0, a_dtype, a_layout, dB, ldb, 0, b_dtype,
+                         b_layout, reinterpret_cast<float*>(dC + u0 * ldc * es_c), ldc, 0, alpha, beta, mode,
+                         ws + h.off_ws, h.ws_bytes, st, &o);
+    }
+    if (prod != MPG_OK) break;
+    e = cudaEventRecord(ev_cmp, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->out, ev_cmp, 0);
+    // ---- the chunk's C back to the host (n elements of each row: C's
+    //      padding columns are never written)
+    if (e == cudaSuccess) {
+      if (h.by_batch) e = copy_lines(h.c, C, dC, u0, u1, 0, m, 0, n, cudaMemcpyDeviceToHost, hs->out);
+      else e = copy_lines(h.c, C, dC, 0, 1, u0, u1, 0, n, cudaMemcpyDeviceToHost, hs->out);
+    }
+  }
+  // the caller's stream continues after the last copy back, also on error
+  cudaError_t e2 = cudaEventRecord(ev_end, hs->out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, ev_end, 0);
+  if (prod != MPG_OK) return prod;
+  if (e == cudaSuccess) e = e2;
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "host-buffer product: %s", cudaGetErrorString(e));
+  return MPG_OK;
 }
 
 }  // extern "C"

@@ -26,7 +26,8 @@ def test_every_declared_symbol_is_exported(L):
 def test_version_and_options_init(L):
     assert L.mpg_version() >= 100
     o = mpg.options()
-    assert (o.split_exp_a, o.split_exp_b, o.splitk, o.force_generic_load, o.tile_n, o.wait_timeout_ns) == (0,) * 6
+    assert (o.split_exp_a, o.split_exp_b, o.splitk, o.force_generic_load, o.tile_n, o.wait_timeout_ns,
+            o.split_chunk_k, o.prepass, o.c_dtype, o.cta_pair) == (0,) * 10
 
 
 # ---------------------------------------------------------------- validation
@@ -69,6 +70,22 @@ def test_option_ranges_rejected(L):
     assert _call(opts=mpg.options(split_exp_a=101)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(splitk=-2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(wait_timeout_ns=-1)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(cta_pair=2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(cta_pair=-2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(c_dtype=3)) == mpg.ERR_INVALID_ARG
+
+
+def test_host_entry_rejects_a_small_workspace_before_any_copy(L):
+    # host-buffer product: the workspace check precedes every copy and launch
+    need = mpg.host_workspace_size(64, 64, 64, 1, 64, 0, mpg.F32, mpg.ROW_MAJOR, 64, 0, mpg.F32, mpg.ROW_MAJOR,
+                                   64, 0, 1.0, 0.0, mpg.TF32)
+    assert need >= 3 * 64 * 64 * 4
+    st = mpg.gemm_host_raw(64, 64, 64, 1, 16, 64, 0, mpg.F32, mpg.ROW_MAJOR, 16, 64, 0, mpg.F32, mpg.ROW_MAJOR,
+                           16, 64, 0, 1.0, 0.0, mpg.TF32, 256, need - 256, check=False)
+    assert st == mpg.ERR_WORKSPACE and "workspace" in mpg.last_error()
+    st = mpg.gemm_host_raw(64, 64, 64, 1, 16, 63, 0, mpg.F32, mpg.ROW_MAJOR, 16, 64, 0, mpg.F32, mpg.ROW_MAJOR,
+                           16, 64, 0, 1.0, 0.0, mpg.TF32, 256, need, check=False)
+    assert st == mpg.ERR_INVALID_ARG
 
 
 def test_empty_problems_are_noops_without_a_device(L):

@@ -66,18 +66,20 @@ def test_batched_2048_padded(mode, capsys):
         assert eQ <= TOL["q16"]
 
 
-def test_large_bf16_8192_beta(capsys):
+@pytest.mark.parametrize("cta_pair", [0, -1])
+def test_large_bf16_8192_beta(cta_pair, capsys):
+    """The library's choice (CTA pairs at this size) and single CTAs."""
     mpg.build()
     n = 8192
     c = Case(n, n, n, mpg.BF16_F32ACC, in_dtype="bf16", dist="normal", alpha=1.0, beta=0.5,
-             c0=synthetic.normal((n, n), synthetic.SEED_C0))
+             c0=synthetic.normal((n, n), synthetic.SEED_C0), opts=mpg.options(cta_pair=cta_pair))
     c.run()
     C = c.result()
     rows, cols = sample_points(n, n, 3000, 81)
     ref, den = c.reference_points(oracle.Q_NONE, 0, rows, cols)
     err = oracle.max_rel_err(C[0][rows, cols], ref, den)
     err_rows = row_errors(c, C, np.array([0, 4095, 8191]), oracle.Q_NONE)
-    show(capsys, f"bf16 8192^3: sampled {err:.3e}, rows {err_rows:.3e}")
+    show(capsys, f"bf16 8192^3 (cta_pair {cta_pair}): sampled {err:.3e}, rows {err_rows:.3e}")
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
 
 
