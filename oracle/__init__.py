@@ -73,6 +73,8 @@ def _load():
         lib.orc_gemm_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp, i64, dbl, dbl,
                                      vp, vp, i64, i32]
         lib.orc_gemm_f64.restype = i32
+        lib.orc_attention_f64.argtypes = [i64, i64, i64, i64, vp, vp, vp, dbl, vp, vp, i32]
+        lib.orc_attention_f64.restype = i32
         lib.orc_gemm_points.argtypes = [i64,
                                         vp, i32, i64, i32, i32, i32,
                                         vp, i32, i64, i32, i32, i32,
@@ -197,6 +199,42 @@ def gemm(A, B, C0=None, alpha: float = 1.0, beta: float = 0.0,
     if rc != 0:
         raise ValueError("oracle rejected the shape")
     return ref, den
+
+
+def attention(Q, K, V, scale: float, q_q: int = Q_NONE, q_s: int = 0,
+              nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Reference of the prompt-attention pair ("qsa_prompt_attn: ...",
+    section "What's going on": scores q.k, row softmax, then p.v), in
+    binary64.  Q is lq x d, K is lk x d and V is lk x dv (numpy
+    float32/float16/float64 or :class:`Bf16`).  Q is first quantised by q_q (Q_SPLIT3: the value
+    hi + lo of the split); K and V are taken as stored.  Returns (O, den):
+
+    O[i, t]   = sum_j softmax_j(scale * q_i . k_j) V[j, t]
+    den[i, t] = sum_j softmax_j(scale * q_i . k_j) |V[j, t]|
+    """
+    lib = _load()
+    qh, ql = quantize(Q, q_q, q_s)
+    qv = np.ascontiguousarray(qh + ql, dtype=np.float64)
+    kv = _values(K)
+    vv = _values(V)
+    lq, d = qv.shape
+    lk, dv = vv.shape
+    if kv.shape != (lk, d):
+        raise ValueError("attention operand shapes disagree")
+    o = np.empty((lq, dv), dtype=np.float64)
+    den = np.empty((lq, dv), dtype=np.float64)
+    rc = lib.orc_attention_f64(lq, lk, d, dv, qv.ctypes.data, kv.ctypes.data, vv.ctypes.data, float(scale),
+                               o.ctypes.data, den.ctypes.data, nthreads)
+    if rc != 0:
+        raise ValueError("oracle rejected the attention shape")
+    return o, den
+
+
+def _values(X) -> np.ndarray:
+    """Stored values of a matrix as a dense binary64 array (exact)."""
+    if isinstance(X, Bf16):
+        return np.ascontiguousarray(X.to_f64())
+    return np.ascontiguousarray(np.asarray(X).astype(np.float64))
 
 
 def gemm_points(A, B, k: int, rows, cols, C0=None, alpha: float = 1.0, beta: float = 0.0,

@@ -39,6 +39,10 @@
  *  - The three-chain product keeps hi*hi + hi*lo + lo*hi and drops lo*lo;
  *    the four-chain variant (a next step listed for the split) keeps lo*lo.
  *
+ *  - "qsa_prompt_attn: ...", section "What's going on": the prompt-attention
+ *    pair, scores q.k, then the row softmax, then p.v (the definition of
+ *    attention written out in orc_attention_f64 below).
+ *
  * Everything here is a direct transcription of a definition: a triple loop in
  * the order (row i, column j, k ascending) or the equivalent (i, k, j) axpy
  * order for full grids; no blocking, no fused reductions, no fast-math.
@@ -394,4 +398,85 @@ int orc_frag_b_coords(int lane, int i, int* k, int* n) {
   *k = 2 * t + h + (r == 1 ? 8 : 0);
   *n = g;
   return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* attention: scores, row softmax, weighted sum of values                      */
+/* ------------------------------------------------------------------------- */
+/* For every query row i (q is lq x d, k is lk x d, v is lk x dv, all
+ * row-major and dense, values in binary64 after whatever quantisation the
+ * caller applied):
+ *   s_ij   = scale * sum_t q_it k_jt                 (t ascending)
+ *   p_ij   = exp(s_ij - max_j s_ij) / sum_j exp(s_ij - max_j s_ij)
+ *   o_it   = sum_j p_ij v_jt                          (j ascending)
+ *   den_it = sum_j p_ij |v_jt|
+ * The maximum is subtracted before exp so that no term overflows; it cancels
+ * in the quotient. */
+typedef struct {
+  int64_t lq, lk, d, dv, r0, r1;
+  const double *q, *k, *v;
+  double scale;
+  double *o, *den;
+  int ok;
+} att_task;
+
+static void* att_worker(void* arg) {
+  att_task* t = (att_task*)arg;
+  double* s = (double*)malloc((size_t)(t->lk > 0 ? t->lk : 1) * sizeof(double));
+  if (!s) { t->ok = 0; return NULL; }
+  for (int64_t i = t->r0; i < t->r1; ++i) {
+    const double* qi = t->q + i * t->d;
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < t->lk; ++j) {
+      const double* kj = t->k + j * t->d;
+      double acc = 0.0;
+      for (int64_t c = 0; c < t->d; ++c) acc += qi[c] * kj[c];
+      s[j] = t->scale * acc;
+      if (s[j] > mx) mx = s[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < t->lk; ++j) {
+      s[j] = exp(s[j] - mx);
+      sum += s[j];
+    }
+    double* oi = t->o + i * t->dv;
+    double* di = t->den + i * t->dv;
+    for (int64_t c = 0; c < t->dv; ++c) { oi[c] = 0.0; di[c] = 0.0; }
+    for (int64_t j = 0; j < t->lk; ++j) {
+      const double pj = s[j] / sum;
+      const double* vj = t->v + j * t->dv;
+      for (int64_t c = 0; c < t->dv; ++c) {
+        oi[c] += pj * vj[c];
+        di[c] += pj * fabs(vj[c]);
+      }
+    }
+  }
+  free(s);
+  return NULL;
+}
+
+int orc_attention_f64(int64_t lq, int64_t lk, int64_t d, int64_t dv, const double* q, const double* k,
+                      const double* v, double scale, double* o, double* den, int nthreads) {
+  if (lq < 0 || lk < 1 || d < 1 || dv < 1) return -1;
+  int nt = resolve_threads(nthreads);
+  if (nt > lq) nt = (int)(lq > 0 ? lq : 1);
+  att_task* tasks = (att_task*)calloc((size_t)nt, sizeof(att_task));
+  pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+  if (!tasks || !th) { free(tasks); free(th); return -2; }
+  for (int i = 0; i < nt; ++i) {
+    att_task* t = &tasks[i];
+    t->lq = lq; t->lk = lk; t->d = d; t->dv = dv; t->q = q; t->k = k; t->v = v; t->scale = scale;
+    t->o = o; t->den = den; t->ok = 1;
+    t->r0 = lq * i / nt;
+    t->r1 = lq * (i + 1) / nt;
+    pthread_create(&th[i], NULL, att_worker, t);
+  }
+  int ok = 1;
+  for (int i = 0; i < nt; ++i) {
+    pthread_join(th[i], NULL);
+    ok &= tasks[i].ok;
+  }
+  free(tasks);
+  free(th);
+  return ok ? 0 : -2;
 }

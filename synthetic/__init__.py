@@ -92,6 +92,17 @@ def softmax_rows_f64(logits: np.ndarray) -> np.ndarray:
     return z
 
 
+def attention_fused_inputs(lq: int = 2048, lk: int = 32768, d: int = 128):
+    """Operands of the fused prompt attention: Q fp32 N(0,1); K and V drawn
+    N(0,1) and stored as fp16 (the key/value cache's storage type); the
+    softmax scale 2/sqrt(d) gives the logits scale * q.k a standard
+    deviation of 2, the spread of the attention workload's logits."""
+    q = normal((lq, d), SEED_Q)
+    k = normal((lk, d), SEED_K).astype(np.float16)
+    v = normal((lk, d), SEED_V).astype(np.float16)
+    return q, k, v, 2.0 / float(np.sqrt(d))
+
+
 def attention_inputs(lq: int = 2048, lk: int = 32768, d: int = 128):
     q = normal((lq, d), SEED_Q, 1.0 / np.sqrt(d))
     k = normal((lk, d), SEED_K, 1.0 / np.sqrt(d))
