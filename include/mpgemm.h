@@ -270,6 +270,34 @@ mpg_status mpg_gemm_host(int64_t m, int64_t n, int64_t k, int64_t batch,
                          void* workspace, size_t workspace_bytes, void* stream,
                          const mpg_options* opt);
 
+/* Fused prompt attention: O = softmax(scale * Q K^T) V, row by row, with the
+ * scores and probabilities never written to memory ("qsa_prompt_attn: Volta
+ * m8n8k4 kernel - keep the hi and lo halves in separate accumulator chains",
+ * sections "What's going on" and "The fix").
+ *   Q     device, fp32, lq x d row-major (ldq >= d).  Split on load into an
+ *         FP16 hi half and a lo half for q.k.
+ *   K, V  device, fp16 (the key/value cache), lk x d row-major; ldk and ldv
+ *         >= d, multiples of 8, pointers 16-byte aligned (TMA).
+ *   O     device, fp32, lq x d row-major (ldo >= d).
+ *   d     the head dimension; 128 is supported (else MPG_ERR_UNSUPPORTED).
+ *   scale the softmax scale (e.g. 1/sqrt(d)); scores are scale * q.k.
+ *   mode  MPG_ATTN_SPLIT_2CHAIN: q and the probabilities p are split into
+ *         hi = fp16(x) and lo = fp16((x - hi) * 2^11); the hi and lo products
+ *         accumulate in separate tensor-core chains added in fp32 (the fix).
+ *         MPG_ATTN_SPLIT_1CHAIN: lo = fp16(x - hi) accumulated into the same
+ *         chain as hi (the form the fix replaced), for comparison.
+ *   key_splits  0 = chosen by the library: the keys are divided among CTAs
+ *         so that about one CTA per SM works; > 1 forces that many ranges.
+ *         Several ranges need a workspace of mpg_attention_workspace_size()
+ *         bytes for their partial results (a merge kernel combines them);
+ *         with a smaller workspace an automatic choice falls back to one range.
+ * lq == 0 is a no-op; lk must be >= 1. */
+typedef enum { MPG_ATTN_SPLIT_2CHAIN = 0, MPG_ATTN_SPLIT_1CHAIN = 1 } mpg_attn_mode;
+size_t mpg_attention_workspace_size(int64_t lq, int64_t lk, int64_t d, int32_t key_splits);
+mpg_status mpg_attention(int64_t lq, int64_t lk, int64_t d, const float* Q, int64_t ldq, const void* K, int64_t ldk,
+                         const void* V, int64_t ldv, float* O, int64_t ldo, float scale, mpg_attn_mode mode,
+                         int32_t key_splits, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns MPG_ERR_TIMEOUT if any kernel since the
  * last call gave up a bounded wait, MPG_ERR_CUDA if the stream reports an

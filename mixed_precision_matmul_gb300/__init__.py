@@ -105,6 +105,10 @@ def lib():
         L.mpg_gemm_noalloc.restype = i32
         L.mpg_gemm_workspace_size.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options)]
         L.mpg_gemm_workspace_size.restype = sz
+        L.mpg_attention_workspace_size.argtypes = [i64, i64, i64, i32]
+        L.mpg_attention_workspace_size.restype = sz
+        L.mpg_attention.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, i32, i32, vp, sz, vp]
+        L.mpg_attention.restype = i32
         L.mpg_gemm_host.argtypes = gemm_args + [ctypes.POINTER(Options)]
         L.mpg_gemm_host.restype = i32
         L.mpg_gemm_host_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, i32, i64, i64, i32, i32,
@@ -218,6 +222,50 @@ def host_workspace_size(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, st
     return int(lib().mpg_gemm_host_workspace_size(m, n, k, batch, lda, strideA, a_dtype, a_layout, ldb, strideB,
                                                   b_dtype, b_layout, ldc, strideC, float(alpha), float(beta), mode,
                                                   ctypes.byref(opts) if opts is not None else None))
+
+
+ATTN_SPLIT_2CHAIN = 0
+ATTN_SPLIT_1CHAIN = 1
+
+
+def attention_workspace_size(lq, lk, d=128, key_splits=0) -> int:
+    return int(lib().mpg_attention_workspace_size(lq, lk, d, key_splits))
+
+
+def attention_raw(lq, lk, d, Q, ldq, K, ldk, V, ldv, O, ldo, scale, mode=ATTN_SPLIT_2CHAIN, key_splits=0,
+                  workspace=0, workspace_bytes=0, stream=0, check: bool = True) -> int:
+    """mpg_attention on device addresses: O = softmax(scale * Q K^T) V with Q
+    fp32 and K, V fp16 (lq x d, lk x d, lk x d row-major)."""
+    st = lib().mpg_attention(lq, lk, d, Q, ldq, K, ldk, V, ldv, O, ldo, float(scale), mode, key_splits,
+                             workspace or None, workspace_bytes, stream or None)
+    if check:
+        _check(st)
+    return st
+
+
+def attention(Q, K, V, O=None, scale: float | None = None, mode=ATTN_SPLIT_2CHAIN, key_splits=0, stream=None):
+    """Fused prompt attention on CUDA tensors: Q (lq x d) fp32, K and V
+    (lk x d) fp16, O (lq x d) fp32 (allocated when not given); the scale
+    defaults to 1/sqrt(d).  Returns O."""
+    torch = _torch()
+    lq, d = Q.shape
+    lk = K.shape[0]
+    if K.shape[1] != d or V.shape != K.shape:
+        raise ValueError("attention operand shapes disagree")
+    if Q.dtype != torch.float32 or K.dtype != torch.float16 or V.dtype != torch.float16:
+        raise ValueError("Q must be fp32, K and V fp16")
+    if Q.stride(1) != 1 or K.stride(1) != 1 or V.stride(1) != 1:
+        raise ValueError("operands must be row-major with unit column stride")
+    if O is None:
+        O = torch.empty((lq, d), dtype=torch.float32, device=Q.device)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    ws_bytes = attention_workspace_size(lq, lk, d, key_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=Q.device) if ws_bytes else None
+    attention_raw(lq, lk, d, Q.data_ptr(), Q.stride(0), K.data_ptr(), K.stride(0), V.data_ptr(), V.stride(0),
+                  O.data_ptr(), O.stride(0), scale, mode, key_splits, ws.data_ptr() if ws is not None else 0,
+                  ws_bytes, _stream_handle(stream))
+    return O
 
 
 def workspace_size(m, n, k, batch, mode, opts: Options | None = None) -> int:

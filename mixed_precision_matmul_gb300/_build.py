@@ -31,6 +31,7 @@ SOURCES = [
     "tc_generic.cu",
     "prepass.cu",
     "tc_pair.cu",
+    "attention.cu",
 ]
 HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh"]
 

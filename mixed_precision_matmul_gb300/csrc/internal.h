@@ -85,6 +85,27 @@ struct TcKernel {
 // combination is not instantiated.
 bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out);
 
+// Fused prompt attention O = softmax(scale * Q K^T) V (head dimension 128).
+struct AttnParams {
+  CUtensorMap map_k;   // K: fp16 [lk][ldk], box 64 dims x 64 keys
+  CUtensorMap map_v;   // V: fp16 [lk][ldv], same box
+  const float* q;      // fp32 [lq][ldq]
+  int64_t ldq;
+  float* o;            // fp32 [lq][ldo]
+  int64_t ldo;
+  float* part_o;       // key splits > 1: unnormalised partial outputs [split][lq][128]
+  float* part_m;       //   and their row maxima [split][lq] (log2 domain)
+  float* part_l;       //   and row sums [split][lq]
+  int32_t lq, lk;
+  int32_t splits, kb_per_split, num_q_blk;
+  int32_t q_vec_ok;    // Q rows are 16-byte aligned (float4 loads)
+  float scale_log2;    // softmax scale * log2(e)
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_attention(const AttnParams& p, bool two_chain, cudaStream_t stream);
+int attention_smem_bytes();
+
 // The 16-bit direct product on a CTA pair (cta_group::2, 256 x 256 tiles per
 // cluster of two CTAs); false for operand types it does not cover.
 bool tc_lookup_pair(Op op, TcKernel* out);

@@ -234,3 +234,31 @@ def test_fragment_numerals(L):
         for i in range(4):
             k, n = mpg.frag_b_coords(lane, i)
             assert n * 16 + k == (i & 1) + t * 2 + (i >> 1) * 8 + g * 16
+
+
+def test_attention_arguments_rejected_before_launch(L):
+    def call(**kw):
+        a = dict(lq=256, lk=512, d=128, Q=16, ldq=128, K=16, ldk=128, V=16, ldv=128, O=16, ldo=128, scale=0.1,
+                 mode=mpg.ATTN_SPLIT_2CHAIN, key_splits=0)
+        a.update(kw)
+        return mpg.attention_raw(a["lq"], a["lk"], a["d"], a["Q"], a["ldq"], a["K"], a["ldk"], a["V"], a["ldv"],
+                                 a["O"], a["ldo"], a["scale"], a["mode"], a["key_splits"], check=False)
+    assert call(d=64) == mpg.ERR_UNSUPPORTED
+    assert call(mode=2) == mpg.ERR_UNSUPPORTED
+    assert call(lk=0) == mpg.ERR_INVALID_ARG
+    assert call(ldk=120) == mpg.ERR_INVALID_ARG
+    assert call(ldk=132) == mpg.ERR_INVALID_ARG          # not a multiple of 8: TMA rows
+    assert call(K=24) == mpg.ERR_INVALID_ARG             # not 16-byte aligned
+    assert call(Q=0) == mpg.ERR_INVALID_ARG
+    assert call(key_splits=-1) == mpg.ERR_INVALID_ARG
+    assert call(scale=float("inf")) == mpg.ERR_INVALID_ARG
+    assert call(lq=0) == mpg.OK                          # nothing to do
+
+
+def test_attention_workspace_holds_the_partials(L):
+    # forced key ranges: partial outputs (128 floats per row) plus a maximum and
+    # a sum per row for every range
+    ws = mpg.attention_workspace_size(2048, 32768, 128, 8)
+    assert ws >= 8 * 2048 * (128 + 2) * 4
+    assert mpg.attention_workspace_size(2048, 32768, 128, 1) == 0
+    assert mpg.attention_workspace_size(2048, 32768, 64, 0) == 0
