@@ -315,9 +315,27 @@ def one_mode(args):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
+    attn_modes = {"attention_fused_2chain": mpg.ATTN_SPLIT_2CHAIN, "attention_fused_1chain": mpg.ATTN_SPLIT_1CHAIN}
+    if args.mode in attn_modes:
+        # the fused prompt attention, 2048 queries x 32768 keys, d = 128
+        q, k, v, scale = synthetic.attention_fused_inputs()
+        Q = torch.from_numpy(q).to(device)
+        K = torch.from_numpy(k).to(device)
+        V = torch.from_numpy(v).to(device)
+        O = torch.empty((2048, 128), dtype=torch.float32, device=device)
+        wsb = mpg.attention_workspace_size(2048, 32768, 128, 0)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+        fn = lambda: mpg.attention_raw(2048, 32768, 128, Q.data_ptr(), 128, K.data_ptr(), 128, V.data_ptr(), 128,
+                                       O.data_ptr(), 128, scale, attn_modes[args.mode], 0, ws.data_ptr(), wsb, sh)
+        ms = time_steps(torch, fn, args.steps, args.warmup, stream) / args.steps
+        useful = 4.0 * 2048 * 32768 * 128
+        print(json.dumps({"mode": args.mode, "shape": [2048, 32768, 128], "ms": round(ms, 5),
+                          "tflops": round(useful / (ms * 1e-3) / 1e12, 2), "peaks": {**peaks, "source": peak_src}}),
+              flush=True)
+        return
     cases = dict(mode_cases(torch, mpg, synthetic, device))
     if args.mode not in cases:
-        raise SystemExit(f"unknown mode {args.mode}; one of {sorted(cases)}")
+        raise SystemExit(f"unknown mode {args.mode}; one of {sorted(cases) + sorted(attn_modes)}")
     mw = cases[args.mode]()
     Cm = torch.zeros((mw.batch, mw.m, mw.ldc) if mw.batch > 1 else (mw.m, mw.ldc), dtype=torch.float32,
                      device=device)
@@ -511,6 +529,35 @@ def ours(args):
             del Cm, ws
             mw.A = mw.B = None
             torch.cuda.empty_cache()
+        # fused prompt attention, 2048 queries x 32768 keys, d = 128: one kernel
+        # (plus the merge of key ranges) for softmax(scale Q K^T) V, against the
+        # two products S = Q K^T and O = P V above (which leave the softmax out)
+        q_a, k_a, v_a, scale_a = synthetic.attention_fused_inputs()
+        Qd = torch.from_numpy(q_a).to(device)
+        Kd = torch.from_numpy(k_a).to(device)
+        Vd = torch.from_numpy(v_a).to(device)
+        Od = torch.empty((2048, 128), dtype=torch.float32, device=device)
+        aws_b = mpg.attention_workspace_size(2048, 32768, 128, 0)
+        aws = torch.empty(max(aws_b, 16), dtype=torch.uint8, device=device)
+        useful = 4.0 * 2048 * 32768 * 128
+        unfused = [modes.get(x, {}).get("ms") for x in ("attention_qkt_split3_prepass", "attention_pv_split3")]
+        for label, amode in (("attention_fused_2chain", mpg.ATTN_SPLIT_2CHAIN),
+                             ("attention_fused_1chain", mpg.ATTN_SPLIT_1CHAIN)):
+            fn = (lambda am=amode: mpg.attention_raw(2048, 32768, 128, Qd.data_ptr(), 128, Kd.data_ptr(), 128,
+                                                     Vd.data_ptr(), 128, Od.data_ptr(), 128, scale_a, am, 0,
+                                                     aws.data_ptr(), aws_b, sh))
+            ms = time_steps(torch, fn, 100, 5, stream) / 100
+            tf = useful / (ms * 1e-3) / 1e12
+            entry = {"ms": round(ms, 5), "tflops": round(tf, 2), "tensor_issued_tflops": round(2 * tf, 2),
+                     "frac_of_tensor_peak": round(2 * tf / peak_bf16, 4), "shape": [2048, 32768, 128],
+                     "bound": "tensor + softmax (CUDA cores); 18.9 MB of operands"}
+            if all(unfused):
+                entry["x_unfused_gemm_pair"] = round(sum(unfused) / ms, 2)
+            modes[label] = entry
+            fn()
+            torch.cuda.synchronize()
+            mode_outputs[label] = ("attention", (Od.cpu().numpy(), (q_a, k_a, v_a, scale_a)))
+        del Qd, Kd, Vd, Od, aws
         ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
         for lbl in [f"loguniform4096_{x}{y}" for x in ("split3", "split1", "split2a", "split4")
                     for y in ("", "_prepass")]:
@@ -547,6 +594,12 @@ def ours(args):
         # bf16/fp16 modes also against their quantised-input problem)
         qmap = {"fp16": orc.Q_FP16, "bf16": orc.Q_BF16}
         for label, (mw, Cg) in mode_outputs.items():
+            if mw == "attention":
+                Oa, (qa, ka, va, sc) = Cg
+                rows_a = np.arange(0, 2048, 128)
+                ref, den = orc.attention(qa[rows_a], ka, va, sc)
+                modes[label]["max_rel_err_vs_fp64"] = float(np.max(np.abs(Oa[rows_a] - ref) / den))
+                continue
             eR = points_error(orc, mw, Cg, orc.Q_NONE)
             modes[label]["max_rel_err_vs_fp64"] = eR
             if mw.mode_name in qmap:
@@ -615,7 +668,7 @@ def reference(args):
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
-NCU_TRAFFIC = {"gemm_bf16_8192": None}   # the pair kernel is re-captured before a figure is set
+NCU_TRAFFIC = {"gemm_bf16_8192": 1604956928}   # tc_pair_kernel, one --set full capture
 
 
 def main():
