@@ -201,10 +201,12 @@ def mode_cases(torch, mpg, synthetic, device):
     yield "square8192_fp16_prepass", lambda: f32_square(8192, "normal", "fp16", opts=mpg.options(prepass=1))
     # C4: 4096^3 log-uniform: split3 vs split1 vs tf32 vs FFMA (B column-major
     # so that tf32 takes its direct path; every mode sees the same layout)
+    # (the split rows without a suffix convert on load; "_prepass" rows use the separate pass)
+    onload = mpg.options(prepass=-1)
     for mn in ("split3", "split1", "tf32", "ffma"):
-        yield f"loguniform4096_{mn}", lambda mn=mn: f32_square(4096, "loguniform", mn, "col")
-    yield "loguniform4096_split2a", lambda: f32_square(4096, "loguniform", "split2a", "col")
-    yield "loguniform4096_split4", lambda: f32_square(4096, "loguniform", "split4", "col")
+        yield f"loguniform4096_{mn}", lambda mn=mn: f32_square(4096, "loguniform", mn, "col", opts=onload)
+    yield "loguniform4096_split2a", lambda: f32_square(4096, "loguniform", "split2a", "col", opts=onload)
+    yield "loguniform4096_split4", lambda: f32_square(4096, "loguniform", "split4", "col", opts=onload)
     for mn in ("split3", "split1", "split2a", "split4"):
         yield f"loguniform4096_{mn}_prepass", lambda mn=mn: f32_square(4096, "loguniform", mn, "col",
                                                                        opts=mpg.options(prepass=1))
@@ -234,7 +236,7 @@ def make_batched(torch, mpg, synthetic, device, mode_name):
                     {"a": a, "bt": bt}, algo_bytes=algo)
 
 
-def make_attention(torch, mpg, synthetic, device, which, prepass=0):
+def make_attention(torch, mpg, synthetic, device, which, prepass=-1):
     q, kk, p, v = synthetic.attention_inputs()
     if which == "qkt":
         # S = Q K^T: A = Q (2048x128 row-major), B = K^T, i.e. K stored row-major = B column-major

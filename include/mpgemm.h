@@ -129,14 +129,21 @@ typedef struct {
    * see the design notes).  0 = default (256); negative = one chunk covering
    * the whole K range.  Rounded up to a multiple of 32. */
   int32_t split_chunk_k;
-  /* 1 = convert fp32 operands in a separate pass (FP16_F32ACC, BF16_F32ACC
+  /* The separate conversion pass for fp32 operands (FP16_F32ACC, BF16_F32ACC
    * and the split modes): one extra kernel reads A and B once and writes
    * packed 16-bit copies (hi and lo halves for the split) into the caller's
    * workspace, then the product runs on those copies on its direct TMA path.
-   * Same conversions and same results as the default; it needs a workspace
-   * of mpg_gemm_workspace_size() bytes queried with the same options
-   * (4 bytes per operand element for the split, 2 otherwise, plus split-K
-   * partials).  0 (default) = convert on the fly in the load stage. */
+   * Same conversions and same results as converting on the fly in the load
+   * stage; it needs a workspace of mpg_gemm_workspace_size() bytes queried
+   * with the same options (4 bytes per operand element for the split, 2
+   * otherwise, plus split-K partials).
+   *   1  = always (MPG_ERR_WORKSPACE if the workspace is too small);
+   *   0  (default) = the library's choice: the split modes take the pass when
+   *        m >= 256, n >= 256 and m*n*k >= 2^32 (both operands re-read by
+   *        many tiles) and the workspace holds the copies (the workspace
+   *        query then includes them); otherwise, and for the fp16 / bf16
+   *        modes, conversion happens on the fly;
+   *   -1 = never. */
   int32_t prepass;
   /* Storage type of C (an mpg_dtype): MPG_F32 (default), MPG_F16 or MPG_BF16.
    * With a 16-bit C the `C` argument points to 16-bit storage (ldc and

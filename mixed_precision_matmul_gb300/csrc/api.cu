@@ -188,6 +188,19 @@ PrepassLayout prepass_layout(int64_t m, int64_t n, int64_t k, int64_t batch, mpg
   return L;
 }
 
+// The split modes (fp32 inputs) take the separate conversion pass by
+// default when both operands are re-read by many tiles: at least two
+// 128-row tiles each way and 2^32 multiply-adds, where converting every
+// operand element once in HBM costs far less than converting it in shared
+// memory for every tile that reads it.
+bool split_mode(mpg_precision mode) {
+  return mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_A_FP16_2CHAIN ||
+         mode == MPG_SPLIT_FP16_4CHAIN;
+}
+bool auto_prepass_shape(int64_t m, int64_t n, int64_t k) {
+  return m >= 256 && n >= 256 && (double)m * (double)n * (double)k >= 4294967296.0;
+}
+
 bool prepass_mode(mpg_precision mode) {
   return mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC || mode == MPG_SPLIT_FP16_3CHAIN ||
          mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_A_FP16_2CHAIN || mode == MPG_SPLIT_FP16_4CHAIN;
@@ -264,7 +277,16 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       return fail(MPG_ERR_UNSUPPORTED, "unknown precision mode %d", (int)mode);
   }
   const bool tma = !o.force_generic_load && tma_ok(A, batch) && tma_ok(B, batch);
-  if (o.prepass == 1 && p.conv != Conv::kNone) {
+  // split-K is chosen from the sizes alone, before the path
+  int splits = choose_splits(m, n, k, batch, sm_count, o);
+  bool use_pass = (o.prepass == 1 && p.conv != Conv::kNone);
+  if (!use_pass && o.prepass == 0 && split_mode(mode) && auto_prepass_shape(m, n, k)) {
+    // the library's choice: the pass when the workspace holds the copies
+    const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout, splits_a(p.conv), splits_b(p.conv),
+                                           splitk_bytes(splits, m, n, batch));
+    use_pass = (L.end <= ws_bytes);
+  }
+  if (use_pass) {
     // convert in a separate pass; the product reads packed 16-bit copies
     // (always TMA-aligned) on its direct path
     p.prepass = true;
@@ -316,7 +338,6 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     p.bn = 256;
   }
 
-  int splits = choose_splits(m, n, k, batch, sm_count, o);
   if (p.prepass) {
     const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout, splits_a(p.conv), splits_b(p.conv),
                                            splitk_bytes(splits, m, n, batch));
@@ -377,6 +398,7 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (o.wait_timeout_ns < 0) return fail(MPG_ERR_INVALID_ARG, "negative wait timeout");
   if (o.c_dtype < MPG_F32 || o.c_dtype > MPG_BF16) return fail(MPG_ERR_INVALID_ARG, "unknown C dtype %d", o.c_dtype);
   if (o.cta_pair < -1 || o.cta_pair > 1) return fail(MPG_ERR_INVALID_ARG, "cta_pair must be -1, 0 or 1");
+  if (o.prepass < -1 || o.prepass > 1) return fail(MPG_ERR_INVALID_ARG, "prepass must be -1, 0 or 1");
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
   if (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 4 : 2) != 0)
@@ -826,7 +848,8 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
   t_err.clear();
   const size_t partials = splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
-  if (o.prepass == 1 && prepass_mode(mode)) {
+  if ((o.prepass == 1 && prepass_mode(mode)) ||
+      (o.prepass == 0 && split_mode(mode) && auto_prepass_shape(m, n, k))) {
     // layouts are not known here: take the larger of the two line paddings
     const bool split_b =
         (mode == MPG_SPLIT_FP16_3CHAIN || mode == MPG_SPLIT_FP16_1CHAIN || mode == MPG_SPLIT_FP16_4CHAIN);

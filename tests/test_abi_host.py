@@ -262,3 +262,18 @@ def test_attention_workspace_holds_the_partials(L):
     assert ws >= 8 * 2048 * (128 + 2) * 4
     assert mpg.attention_workspace_size(2048, 32768, 128, 1) == 0
     assert mpg.attention_workspace_size(2048, 32768, 64, 0) == 0
+
+
+def test_workspace_includes_the_conversion_pass_when_the_library_takes_it(L):
+    # split modes with both operands re-read by many tiles: the library's
+    # choice is the separate pass, so the query includes the hi/lo copies
+    # (4 bytes per element of A and of B); never (-1) or a skinny / small
+    # problem: no copies
+    n = 4096
+    ws = mpg.workspace_size(n, n, n, 1, mpg.SPLIT_FP16_3CHAIN)
+    assert ws >= 2 * 4 * n * n
+    assert mpg.workspace_size(n, n, n, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(prepass=-1)) == 0
+    assert mpg.workspace_size(256, 256, 256, 1, mpg.SPLIT_FP16_3CHAIN) == 0
+    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC) == 0          # fp16 mode: opt-in only
+    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, mpg.options(prepass=1)) >= 2 * 2 * n * n
+    assert _call(opts=mpg.options(prepass=2)) == mpg.ERR_INVALID_ARG

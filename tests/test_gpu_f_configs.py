@@ -109,13 +109,18 @@ def test_loguniform_4096_split_vs_one_chain_vs_tf32_vs_ffma(capsys):
     b = synthetic.loguniform_signed((n, n), synthetic.SEED_B)
     rows = np.array([0, 1, 2, 1000, 2047, 2048, 3001, 4095])
     errs = {}
+    onload = mpg.options(prepass=-1)
     for mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_1CHAIN, mpg.TF32, mpg.FP32_FFMA):
-        c = Case(n, n, n, mode, a=a, b=b, b_layout=Cm, alpha=1.0, beta=0.0)
+        c = Case(n, n, n, mode, a=a, b=b, b_layout=Cm, alpha=1.0, beta=0.0, opts=onload)
         c.run()
         C = c.result()
         errs[mode] = row_errors(c, C, rows, oracle.Q_NONE)
         if mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_1CHAIN):
             errs[(mode, "Q")] = row_errors(c, C, rows, MODE_Q[mode])
+    # the library's default at this size: the separate conversion pass
+    c = Case(n, n, n, mpg.SPLIT_FP16_3CHAIN, a=a, b=b, b_layout=Cm)
+    c.run()
+    errs["split3 default (conversion pass)"] = row_errors(c, c.result(), rows, oracle.Q_NONE)
     # the three-chain split without chunked accumulation, for the record
     c = Case(n, n, n, mpg.SPLIT_FP16_3CHAIN, a=a, b=b, b_layout=Cm, opts=mpg.options(split_chunk_k=-1))
     c.run()
@@ -124,6 +129,7 @@ def test_loguniform_4096_split_vs_one_chain_vs_tf32_vs_ffma(capsys):
         f"{k}: {v:.3e}" for k, v in errs.items()))
     assert errs[mpg.SPLIT_FP16_3CHAIN] <= TOL["split"]
     assert errs[mpg.SPLIT_FP16_3CHAIN] <= 1.5 * errs[mpg.FP32_FFMA]
+    assert errs["split3 default (conversion pass)"] <= TOL["split"]
     assert errs[mpg.TF32] <= TOL["tf32"]
     assert errs[(mpg.SPLIT_FP16_3CHAIN, "Q")] <= TOL["q16"]
     assert errs[(mpg.SPLIT_FP16_1CHAIN, "Q")] <= TOL["q16"]
@@ -139,6 +145,11 @@ def test_attention_pair_split3(capsys):
     cs.run()
     S = cs.result()
     e_s = row_errors(cs, S, rows, oracle.Q_NONE)
+    # the same product converted on load (the default above takes the separate pass)
+    cl = Case(2048, 32768, 128, mpg.SPLIT_FP16_3CHAIN, a=q, b=np.ascontiguousarray(kk.T), b_layout=Cm,
+              c0=np.zeros((2048, 32768), np.float32), opts=mpg.options(prepass=-1))
+    cl.run()
+    e_sl = row_errors(cl, cl.result(), rows, oracle.Q_NONE)
     # O = P V; P holds probabilities (<= 1): operand scale 2^14 lifts it out
     # of fp16's subnormal range
     co = Case(2048, 128, 32768, mpg.SPLIT_FP16_3CHAIN, a=p, b=v, c0=np.zeros((2048, 128), np.float32),
@@ -151,5 +162,5 @@ def test_attention_pair_split3(capsys):
     cu.run()
     e_u = row_errors(cu, cu.result(), np.arange(0, 2048, 64), oracle.Q_NONE)
     show(capsys, f"attention split3: S {e_s:.3e}, O {e_o:.3e} (O without operand scale {e_u:.3e})")
-    assert e_s <= TOL["split"]
+    assert e_s <= TOL["split"] and e_sl <= TOL["split"]
     assert e_o <= TOL["split"]
