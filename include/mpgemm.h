@@ -305,6 +305,20 @@ mpg_status mpg_attention(int64_t lq, int64_t lk, int64_t d, const float* Q, int6
                          const void* V, int64_t ldv, float* O, int64_t ldo, float scale, mpg_attn_mode mode,
                          int32_t key_splits, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of workspace for this exact call: mpg_gemm_workspace_size() plus,
+ * for 16-bit operands in the FP16 / BF16 modes (and fp32 operands in TF32
+ * with A row-major and B column-major) that TMA cannot describe as given
+ * (base not 16-byte aligned, or a leading dimension or batch stride whose
+ * byte size is not a multiple of 16), room for aligned copies of them.
+ * Given that workspace, mpg_gemm_ex copies such operands (one extra read
+ * and write of each) and multiplies the copies on its TMA path instead of
+ * loading the originals element by element. */
+size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch,
+                                  const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype,
+                                  mpg_layout a_layout, const void* B, int64_t ldb, int64_t strideB,
+                                  mpg_dtype b_dtype, mpg_layout b_layout, mpg_precision mode,
+                                  const mpg_options* opt);
+
 /* Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns MPG_ERR_TIMEOUT if any kernel since the
  * last call gave up a bounded wait, MPG_ERR_CUDA if the stream reports an

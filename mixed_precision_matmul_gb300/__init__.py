@@ -105,6 +105,9 @@ def lib():
         L.mpg_gemm_noalloc.restype = i32
         L.mpg_gemm_workspace_size.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options)]
         L.mpg_gemm_workspace_size.restype = sz
+        L.mpg_gemm_workspace_size_ex.argtypes = [i64, i64, i64, i64, vp, i64, i64, i32, i32, vp, i64, i64, i32, i32,
+                                                 i32, ctypes.POINTER(Options)]
+        L.mpg_gemm_workspace_size_ex.restype = sz
         L.mpg_attention_workspace_size.argtypes = [i64, i64, i64, i32]
         L.mpg_attention_workspace_size.restype = sz
         L.mpg_attention.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, i32, i32, vp, sz, vp]
@@ -268,6 +271,15 @@ def attention(Q, K, V, O=None, scale: float | None = None, mode=ATTN_SPLIT_2CHAI
     return O
 
 
+def workspace_size_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout,
+                      mode, opts: Options | None = None) -> int:
+    """Workspace for this exact call (includes aligned copies of operands
+    TMA cannot describe)."""
+    return int(lib().mpg_gemm_workspace_size_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb,
+                                                strideB, b_dtype, b_layout, mode,
+                                                ctypes.byref(opts) if opts is not None else None))
+
+
 def workspace_size(m, n, k, batch, mode, opts: Options | None = None) -> int:
     return int(lib().mpg_gemm_workspace_size(m, n, k, batch, mode,
                                              ctypes.byref(opts) if opts is not None else None))
@@ -355,7 +367,8 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, works
     b_layout, ldb, sb = _operand(B, k, n)
     ldc = max(C.stride(-2), n, 1)
     sc = C.stride(0) if batched else 0
-    ws_bytes = workspace_size(m, n, k, batch, mode, opts)
+    ws_bytes = workspace_size_ex(m, n, k, batch, A.data_ptr(), lda, sa, _dtype_code(A), a_layout,
+                                 B.data_ptr(), ldb, sb, _dtype_code(B), b_layout, mode, opts)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=C.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0

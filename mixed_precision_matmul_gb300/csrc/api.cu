@@ -123,6 +123,8 @@ struct Plan {
   bool prepass = false;       // operands converted by a separate pass into the workspace
   Conv pre_conv = Conv::kNone;
   bool pair = false;          // 256 x 256 tiles on CTA pairs (cta_group::2)
+  bool copy_a = false;        // operand copied to an aligned layout in the workspace (TMA cannot
+  bool copy_b = false;        //   describe it as given), then multiplied on the direct path
 };
 
 struct Operand {
@@ -199,6 +201,32 @@ bool split_mode(mpg_precision mode) {
 }
 bool auto_prepass_shape(int64_t m, int64_t n, int64_t k) {
   return m >= 256 && n >= 256 && (double)m * (double)n * (double)k >= 4294967296.0;
+}
+
+// Workspace of the aligned copies of operands TMA cannot describe: dense
+// copies in the operand's own type and majorness, lines padded to a
+// multiple of 8 elements, after the split-K partials, 256-byte aligned.
+struct CopyLayout {
+  int64_t a_outer, a_inner, a_ld, b_outer, b_inner, b_ld;
+  size_t off_a, off_b, end;
+};
+
+CopyLayout copy_layout(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
+                       bool ca, bool cb, size_t base) {
+  CopyLayout L;
+  L.a_outer = (A.layout == MPG_ROW_MAJOR) ? m : k;
+  L.a_inner = (A.layout == MPG_ROW_MAJOR) ? k : m;
+  L.b_outer = (B.layout == MPG_ROW_MAJOR) ? k : n;
+  L.b_inner = (B.layout == MPG_ROW_MAJOR) ? n : k;
+  L.a_ld = (L.a_inner + 7) / 8 * 8;
+  L.b_ld = (L.b_inner + 7) / 8 * 8;
+  size_t off = align256(base);
+  L.off_a = off;
+  if (ca) off += align256((size_t)batch * L.a_outer * L.a_ld * elem_bytes(A.dt));
+  L.off_b = off;
+  if (cb) off += align256((size_t)batch * L.b_outer * L.b_ld * elem_bytes(B.dt));
+  L.end = off;
+  return L;
 }
 
 bool prepass_mode(mpg_precision mode) {
@@ -298,9 +326,25 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     } else {
       p.st = SrcT::kF16;
     }
-  } else if (tma && p.conv == Conv::kNone && direct_layout_ok) p.src = Src::kTmaDirect;
-  else if (tma && p.conv != Conv::kNone) p.src = Src::kTmaStaged;
-  else p.src = Src::kGeneric;
+  } else if (tma && p.conv == Conv::kNone && direct_layout_ok) {
+    p.src = Src::kTmaDirect;
+  } else if (tma && p.conv != Conv::kNone) {
+    p.src = Src::kTmaStaged;
+  } else {
+    p.src = Src::kGeneric;
+    // operands TMA cannot describe (unaligned base, leading dimension or
+    // batch stride): copied to an aligned layout when the workspace holds
+    // the copies, then the direct path
+    if (!o.force_generic_load && p.conv == Conv::kNone && direct_layout_ok) {
+      const bool ca = !tma_ok(A, batch), cb = !tma_ok(B, batch);
+      const CopyLayout L = copy_layout(m, n, k, batch, A, B, ca, cb, splitk_bytes(splits, m, n, batch));
+      if (L.end <= ws_bytes) {
+        p.src = Src::kTmaDirect;
+        p.copy_a = ca;
+        p.copy_b = cb;
+      }
+    }
+  }
 
   // tile width along N
   int bn;
@@ -863,6 +907,34 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   return partials;
 }
 
+size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
+                                  int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B,
+                                  int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
+                                  mpg_precision mode, const mpg_options* opt) {
+  mpg_options o;
+  resolve_options(opt, &o);
+  const size_t base = mpg_gemm_workspace_size(m, n, k, batch, mode, opt);
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || o.force_generic_load) return base;
+  // the aligned copies the planner makes for 16-bit (or tf32 K-major)
+  // operands on the direct path that TMA cannot describe as given
+  const bool f16in = (mode == MPG_FP16_F32ACC && a_dtype == MPG_F16 && b_dtype == MPG_F16) ||
+                     (mode == MPG_BF16_F32ACC && a_dtype == MPG_BF16 && b_dtype == MPG_BF16);
+  const bool tf32 = (mode == MPG_TF32 && a_dtype == MPG_F32 && b_dtype == MPG_F32 && a_layout == MPG_ROW_MAJOR &&
+                     b_layout == MPG_COL_MAJOR);
+  if (!f16in && !tf32) return base;
+  Operand Aop{A, lda, strideA, a_dtype, a_layout};
+  Operand Bop{B, ldb, strideB, b_dtype, b_layout};
+  const bool ca = !tma_ok(Aop, batch), cb = !tma_ok(Bop, batch);
+  if (!ca && !cb) return base;
+  DeviceInfo* dev = nullptr;
+  int sm = 152;
+  if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
+  t_err.clear();
+  const CopyLayout L =
+      copy_layout(m, n, k, batch, Aop, Bop, ca, cb, splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch));
+  return std::max(base, L.end);
+}
+
 mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
                        int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B, int64_t ldb,
                        int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout, float* C, int64_t ldc,
@@ -918,6 +990,27 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       break;
     }
     case Kind::kTc: {
+      if (plan.copy_a || plan.copy_b) {
+        // aligned copies in the workspace, then the direct path on them
+        const CopyLayout L = copy_layout(m, n, k, batch, Aop, Bop, plan.copy_a, plan.copy_b,
+                                         splitk_bytes(plan.splits, m, n, batch));
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        Operand Ac = Aop, Bc = Bop;
+        if (plan.copy_a) {
+          const int64_t sA = strideA ? strideA : L.a_outer * lda;
+          e = launch_copy_pad(A, elem_bytes(a_dtype), lda, sA, L.a_outer, L.a_inner, batch, ws + L.off_a, L.a_ld,
+                              dev->sm_count, st);
+          Ac = Operand{ws + L.off_a, L.a_ld, L.a_outer * L.a_ld, a_dtype, a_layout};
+        }
+        if (e == cudaSuccess && plan.copy_b) {
+          const int64_t sB = strideB ? strideB : L.b_outer * ldb;
+          e = launch_copy_pad(B, elem_bytes(b_dtype), ldb, sB, L.b_outer, L.b_inner, batch, ws + L.off_b, L.b_ld,
+                              dev->sm_count, st);
+          Bc = Operand{ws + L.off_b, L.b_ld, L.b_outer * L.b_ld, b_dtype, b_layout};
+        }
+        if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "aligned copy launch: %s", cudaGetErrorString(e));
+        return launch_tc(plan, dev, m, n, k, batch, Ac, Bc, C, ldc, strideC, alpha, beta, o, workspace, st);
+      }
       if (!plan.prepass)
         return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
       // separate conversion pass into the workspace, then the direct path

@@ -85,6 +85,12 @@ struct TcKernel {
 // combination is not instantiated.
 bool tc_kernel_lookup(Src src, Conv conv, Op op, SrcT st, int bn, TcKernel* out);
 
+// Copy into a dense layout with 16-byte aligned lines (ld_out % 8 == 0);
+// elem_bytes 2 or 4.
+cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64_t stride_in, int64_t outer,
+                            int64_t inner, int64_t batch, void* out, int64_t ld_out, int sm_count,
+                            cudaStream_t stream);
+
 // Fused prompt attention O = softmax(scale * Q K^T) V (head dimension 128).
 struct AttnParams {
   CUtensorMap map_k;   // K: fp16 [lk][ldk], box 64 dims x 64 keys

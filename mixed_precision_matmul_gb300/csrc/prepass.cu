@@ -6,6 +6,8 @@
 // HBM for shared-memory traffic in the product kernel ("Tensor Core operands:
 // a matrix instruction still needs a layout contract", fifth paragraph: the
 // cost of input conversion belongs in the measurement).
+#include <type_traits>
+
 #include "tc_gemm.cuh"
 
 namespace mpg {
@@ -80,7 +82,60 @@ __global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ 
   }
 }
 
+// Copy of a matrix TMA cannot describe (unaligned base, leading dimension or
+// batch stride) into a dense layout whose lines start on 16-byte boundaries:
+// `batch` matrices of `outer` lines of `inner` elements of ES bytes, read with
+// ld_in / stride_in, written with ld_out (a multiple of 8 elements) and
+// stride outer * ld_out.  One work item = 8 consecutive elements of a line.
+template <int ES>
+__global__ void __launch_bounds__(256) copy_pad_kernel(const uint8_t* __restrict__ in, int64_t ld_in,
+                                                       int64_t stride_in, int64_t outer, int64_t inner, int64_t batch,
+                                                       uint8_t* __restrict__ out, int64_t ld_out) {
+  using E = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
+  const E* src = reinterpret_cast<const E*>(in);
+  E* dst = reinterpret_cast<E*>(out);
+  const int64_t items_per_line = (inner + 7) / 8;
+  const int64_t per_batch = outer * items_per_line;
+  const int64_t total = per_batch * batch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / per_batch;
+    const int64_t r = i - b * per_batch;
+    const int64_t line = r / items_per_line;
+    const int64_t c = (r - line * items_per_line) * 8;
+    const E* s = src + b * stride_in + line * ld_in + c;
+    E v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (c + e < inner) ? __ldg(s + e) : E(0);
+    E* d = dst + (b * outer + line) * ld_out + c;   // 16-byte aligned (ld_out % 8 == 0)
+    if constexpr (ES == 2) {
+      *reinterpret_cast<uint4*>(d) = make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16),
+                                                v[4] | ((uint32_t)v[5] << 16), v[6] | ((uint32_t)v[7] << 16));
+    } else {
+      reinterpret_cast<uint4*>(d)[0] = make_uint4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<uint4*>(d)[1] = make_uint4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64_t stride_in, int64_t outer,
+                            int64_t inner, int64_t batch, void* out, int64_t ld_out, int sm_count,
+                            cudaStream_t stream) {
+  const int64_t total = batch * outer * ((inner + 7) / 8);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
+  if (blocks < 1) blocks = 1;
+  const uint8_t* src = static_cast<const uint8_t*>(in);
+  uint8_t* dst = static_cast<uint8_t*>(out);
+  if (elem_bytes == 2)
+    copy_pad_kernel<2><<<(int)blocks, 256, 0, stream>>>(src, ld_in, stride_in, outer, inner, batch, dst, ld_out);
+  else if (elem_bytes == 4)
+    copy_pad_kernel<4><<<(int)blocks, 256, 0, stream>>>(src, ld_in, stride_in, outer, inner, batch, dst, ld_out);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,

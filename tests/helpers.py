@@ -97,15 +97,22 @@ class Case:
         cbuf[:, :, :n] = self.c0
         self.C = torch.from_numpy(cbuf).to(dev)
 
-    def run(self, workspace=None, check=True, stream=0):
+    def run(self, workspace=None, check=True, stream=0, exact_ws=False):
+        """exact_ws: size the workspace with the query that sees the operands
+        (it includes aligned copies of operands TMA cannot describe)."""
         import torch
-        ws_bytes = mpg.workspace_size(self.m, self.n, self.k, self.batch, self.mode, self.opts)
+        sa = self.A.stride(0) if self.batch > 1 else 0
+        sb = self.B.stride(0) if self.batch > 1 else 0
+        if exact_ws:
+            ws_bytes = mpg.workspace_size_ex(self.m, self.n, self.k, self.batch, self.A.data_ptr(), self.lda, sa,
+                                             dtype_code(self.in_dtype), self.a_layout, self.B.data_ptr(), self.ldb,
+                                             sb, dtype_code(self.in_dtype), self.b_layout, self.mode, self.opts)
+        else:
+            ws_bytes = mpg.workspace_size(self.m, self.n, self.k, self.batch, self.mode, self.opts)
         if workspace is None and ws_bytes:
             workspace = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         wsp = workspace.data_ptr() if workspace is not None else 0
         wsl = workspace.numel() if workspace is not None else 0
-        sa = self.A.stride(0) if self.batch > 1 else 0
-        sb = self.B.stride(0) if self.batch > 1 else 0
         sc = self.C.stride(0) if self.batch > 1 else 0
         st = mpg.gemm_raw(self.m, self.n, self.k, self.batch,
                           self.A.data_ptr(), self.lda, sa, dtype_code(self.in_dtype), self.a_layout,

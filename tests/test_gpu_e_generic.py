@@ -35,3 +35,29 @@ def test_generic_parity(mode, dt, m, n, k, al, bl, pad, force):
         assert eQ <= TOL["q16"], (eR, eQ)
     if mode == mpg.SPLIT_FP16_3CHAIN:
         assert eR <= TOL["split"], eR
+
+
+@pytest.mark.parametrize("mode,dt", [(mpg.BF16_F32ACC, "bf16"), (mpg.FP16_F32ACC, "f16"), (mpg.TF32, "f32")])
+@pytest.mark.parametrize("m,n,k,al,bl,pad,batch", [
+    (300, 260, 201, R, Cm, (0, 1, 3), 1),    # A's rows of 201 elements: A copied; B too (ldb 202)
+    (300, 260, 200, R, Cm, (0, 3, 0), 1),    # only B unaligned (ldb 203)
+    (200, 130, 130, R, Cm, (1, 0, 2), 3),    # batches with odd strides (lda 131)
+])
+def test_unaligned_operands_copied_to_the_tma_path(mode, dt, m, n, k, al, bl, pad, batch):
+    """With the workspace the exact query asks for, operands TMA cannot
+    describe are copied to aligned lines and multiplied on the direct path."""
+    mpg.build()
+    c = Case(m, n, k, mode, in_dtype=dt, a_layout=al, b_layout=bl, pad=pad, alpha=1.25, beta=-0.5,
+             dist="normal", batch=batch)
+    ws_plain = mpg.workspace_size(m, n, k, batch, mode)
+    c.run(exact_ws=True)
+    eR, eQ = c.errors()
+    if mode == mpg.TF32:
+        assert eR <= TOL["tf32"], eR
+    else:
+        assert eQ <= TOL["q16"], (eR, eQ)
+    ws_exact = mpg.workspace_size_ex(m, n, k, batch, c.A.data_ptr(), c.lda, c.A.stride(0) if batch > 1 else 0,
+                                     {"bf16": mpg.BF16, "f16": mpg.F16, "f32": mpg.F32}[dt], al, c.B.data_ptr(),
+                                     c.ldb, c.B.stride(0) if batch > 1 else 0,
+                                     {"bf16": mpg.BF16, "f16": mpg.F16, "f32": mpg.F32}[dt], bl, mode)
+    assert ws_exact > ws_plain     # room for the copies was asked for

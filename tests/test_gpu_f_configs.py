@@ -83,22 +83,25 @@ def test_large_bf16_8192_beta(cta_pair, capsys):
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
 
 
-def test_large_bf16_tail_unpadded(capsys):
+@pytest.mark.parametrize("exact_ws", [False, True])
+def test_large_bf16_tail_unpadded(exact_ws, capsys):
     """8191 x 8177 x 8183 with unpadded leading dimensions: row pitches of
-    16366 / 16354 bytes are not multiples of 16, so no TMA descriptor exists
-    and the generic-load path runs."""
+    16366 / 16354 bytes are not multiples of 16, so no TMA descriptor exists:
+    without a workspace the generic-load path runs; with the workspace the
+    exact query asks for, the operands are copied to aligned lines and
+    multiplied on the TMA path."""
     mpg.build()
     m, n, k = 8191, 8177, 8183
     c = Case(m, n, k, mpg.BF16_F32ACC, in_dtype="bf16", dist="normal", alpha=1.0, beta=0.5,
              c0=synthetic.normal((m, n), synthetic.SEED_C0))
     assert c.lda == k and c.ldb == n and c.ldc == n
-    c.run()
+    c.run(exact_ws=exact_ws)
     C = c.result()
     rows, cols = sample_points(m, n, 3000, 82)
     ref, den = c.reference_points(oracle.Q_NONE, 0, rows, cols)
     err = oracle.max_rel_err(C[0][rows, cols], ref, den)
     err_rows = row_errors(c, C, np.array([0, 8064, 8190]), oracle.Q_NONE)
-    show(capsys, f"bf16 tail: sampled {err:.3e}, rows {err_rows:.3e}")
+    show(capsys, f"bf16 tail (aligned copies {exact_ws}): sampled {err:.3e}, rows {err_rows:.3e}")
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
 
 
