@@ -180,7 +180,7 @@ def time_steps(torch, fn, steps, warmup, stream):
 # ---------------------------------------------------------------------------
 def mode_cases(torch, mpg, synthetic, device):
     """Yield (label, Workload) for the per-mode table; built lazily."""
-    def f32_square(n_, seed_dist, mode_name, b_layout="row", opts=None):
+    def f32_square(n_, seed_dist, mode_name, b_layout="row", opts=None, exact_ws=False):
         if seed_dist == "uniform":
             a = synthetic.uniform((n_, n_), synthetic.SEED_A)
             b = synthetic.uniform((n_, n_), synthetic.SEED_B)
@@ -200,13 +200,16 @@ def mode_cases(torch, mpg, synthetic, device):
         algo = 4 * n_ * n_ * 2 + 4 * n_ * n_
         return Workload(f"{seed_dist}_{n_}", n_, n_, n_, 1, mode_name, A, B, None, n_, ldb, n_, 0, 0, 0,
                         mpg.ROW_MAJOR, bl, mpg.F32, 1.0, 0.0,
-                        {"a": a, "b": b, "b_col": b_layout == "col"}, opts=opts, algo_bytes=algo)
+                        {"a": a, "b": b, "b_col": b_layout == "col", "exact_ws": exact_ws}, opts=opts,
+                        algo_bytes=algo)
 
     # C1: 256^3 uniform, four modes
     for mn in ("fp16", "bf16", "tf32", "split3"):
         yield f"square256_{mn}", lambda mn=mn: f32_square(256, "uniform", mn)
     # C3-shaped 8192^3 in the other precisions
     yield "square8192_tf32", lambda: f32_square(8192, "normal", "tf32", "col")
+    # tf32 with a row-major B: transposed copy of B, then the direct path
+    yield "square8192_tf32_rowB", lambda: f32_square(8192, "normal", "tf32", "row", exact_ws=True)
     yield "square8192_fp16_onload", lambda: f32_square(8192, "normal", "fp16")
     yield "square8192_fp16_prepass", lambda: f32_square(8192, "normal", "fp16", opts=mpg.options(prepass=1))
     # C4: 4096^3 log-uniform: split3 vs split1 vs tf32 vs FFMA (B column-major

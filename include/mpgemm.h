@@ -305,11 +305,12 @@ mpg_status mpg_attention(int64_t lq, int64_t lk, int64_t d, const float* Q, int6
                          const void* V, int64_t ldv, float* O, int64_t ldo, float scale, mpg_attn_mode mode,
                          int32_t key_splits, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace for this exact call: mpg_gemm_workspace_size() plus,
- * for 16-bit operands in the FP16 / BF16 modes (and fp32 operands in TF32
- * with A row-major and B column-major) that TMA cannot describe as given
- * (base not 16-byte aligned, or a leading dimension or batch stride whose
- * byte size is not a multiple of 16), room for aligned copies of them.
+/* Bytes of workspace for this exact call: mpg_gemm_workspace_size() plus
+ * room for copies of the operands the TMA path cannot take as given:
+ * 16-bit operands (FP16 / BF16 modes) and fp32 operands (TF32) whose base is
+ * not 16-byte aligned or whose leading dimension or batch stride is not a
+ * multiple of 16 bytes, and in TF32 a column-major A or a row-major B (the
+ * tensor cores take tf32 tiles K-major only; those copies are transposed).
  * Given that workspace, mpg_gemm_ex copies such operands (one extra read
  * and write of each) and multiplies the copies on its TMA path instead of
  * loading the originals element by element. */

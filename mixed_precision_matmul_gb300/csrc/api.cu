@@ -203,21 +203,26 @@ bool auto_prepass_shape(int64_t m, int64_t n, int64_t k) {
   return m >= 256 && n >= 256 && (double)m * (double)n * (double)k >= 4294967296.0;
 }
 
-// Workspace of the aligned copies of operands TMA cannot describe: dense
-// copies in the operand's own type and majorness, lines padded to a
-// multiple of 8 elements, after the split-K partials, 256-byte aligned.
+// Workspace of the copies of operands the TMA path cannot take as given:
+// dense copies in the operand's own type, in the layout the direct path
+// needs (the source's own, or for tf32 A row-major and B column-major, whose
+// tiles are K-major), lines padded to a multiple of 8 elements, after the
+// split-K partials, 256-byte aligned.
 struct CopyLayout {
+  mpg_layout a_layout, b_layout;                 // layouts of the copies
   int64_t a_outer, a_inner, a_ld, b_outer, b_inner, b_ld;
   size_t off_a, off_b, end;
 };
 
 CopyLayout copy_layout(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
-                       bool ca, bool cb, size_t base) {
+                       bool ca, bool cb, size_t base, mpg_layout a_out, mpg_layout b_out) {
   CopyLayout L;
-  L.a_outer = (A.layout == MPG_ROW_MAJOR) ? m : k;
-  L.a_inner = (A.layout == MPG_ROW_MAJOR) ? k : m;
-  L.b_outer = (B.layout == MPG_ROW_MAJOR) ? k : n;
-  L.b_inner = (B.layout == MPG_ROW_MAJOR) ? n : k;
+  L.a_layout = a_out;
+  L.b_layout = b_out;
+  L.a_outer = (a_out == MPG_ROW_MAJOR) ? m : k;
+  L.a_inner = (a_out == MPG_ROW_MAJOR) ? k : m;
+  L.b_outer = (b_out == MPG_ROW_MAJOR) ? k : n;
+  L.b_inner = (b_out == MPG_ROW_MAJOR) ? n : k;
   L.a_ld = (L.a_inner + 7) / 8 * 8;
   L.b_ld = (L.b_inner + 7) / 8 * 8;
   size_t off = align256(base);
@@ -333,11 +338,17 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   } else {
     p.src = Src::kGeneric;
     // operands TMA cannot describe (unaligned base, leading dimension or
-    // batch stride): copied to an aligned layout when the workspace holds
-    // the copies, then the direct path
-    if (!o.force_generic_load && p.conv == Conv::kNone && direct_layout_ok) {
-      const bool ca = !tma_ok(A, batch), cb = !tma_ok(B, batch);
-      const CopyLayout L = copy_layout(m, n, k, batch, A, B, ca, cb, splitk_bytes(splits, m, n, batch));
+    // batch stride), and tf32 operands in the wrong majorness, are copied
+    // to aligned lines in the layout the direct path needs when the
+    // workspace holds the copies, then the direct path multiplies them
+    if (!o.force_generic_load && p.conv == Conv::kNone) {
+      const bool tf32 = (p.op == Op::kTF32);
+      const mpg_layout a_out = tf32 ? MPG_ROW_MAJOR : A.layout;
+      const mpg_layout b_out = tf32 ? MPG_COL_MAJOR : B.layout;
+      const bool ca = !tma_ok(A, batch) || A.layout != a_out;
+      const bool cb = !tma_ok(B, batch) || B.layout != b_out;
+      const CopyLayout L =
+          copy_layout(m, n, k, batch, A, B, ca, cb, splitk_bytes(splits, m, n, batch), a_out, b_out);
       if (L.end <= ws_bytes) {
         p.src = Src::kTmaDirect;
         p.copy_a = ca;
@@ -919,19 +930,19 @@ size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch
   // operands on the direct path that TMA cannot describe as given
   const bool f16in = (mode == MPG_FP16_F32ACC && a_dtype == MPG_F16 && b_dtype == MPG_F16) ||
                      (mode == MPG_BF16_F32ACC && a_dtype == MPG_BF16 && b_dtype == MPG_BF16);
-  const bool tf32 = (mode == MPG_TF32 && a_dtype == MPG_F32 && b_dtype == MPG_F32 && a_layout == MPG_ROW_MAJOR &&
-                     b_layout == MPG_COL_MAJOR);
+  const bool tf32 = (mode == MPG_TF32 && a_dtype == MPG_F32 && b_dtype == MPG_F32);
   if (!f16in && !tf32) return base;
   Operand Aop{A, lda, strideA, a_dtype, a_layout};
   Operand Bop{B, ldb, strideB, b_dtype, b_layout};
-  const bool ca = !tma_ok(Aop, batch), cb = !tma_ok(Bop, batch);
+  const mpg_layout a_out = tf32 ? MPG_ROW_MAJOR : a_layout, b_out = tf32 ? MPG_COL_MAJOR : b_layout;
+  const bool ca = !tma_ok(Aop, batch) || a_layout != a_out, cb = !tma_ok(Bop, batch) || b_layout != b_out;
   if (!ca && !cb) return base;
   DeviceInfo* dev = nullptr;
   int sm = 152;
   if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
   t_err.clear();
-  const CopyLayout L =
-      copy_layout(m, n, k, batch, Aop, Bop, ca, cb, splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch));
+  const CopyLayout L = copy_layout(m, n, k, batch, Aop, Bop, ca, cb,
+                                   splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch), a_out, b_out);
   return std::max(base, L.end);
 }
 
@@ -992,21 +1003,30 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
     case Kind::kTc: {
       if (plan.copy_a || plan.copy_b) {
         // aligned copies in the workspace, then the direct path on them
+        const bool tf32 = (plan.op == Op::kTF32);
         const CopyLayout L = copy_layout(m, n, k, batch, Aop, Bop, plan.copy_a, plan.copy_b,
-                                         splitk_bytes(plan.splits, m, n, batch));
+                                         splitk_bytes(plan.splits, m, n, batch),
+                                         tf32 ? MPG_ROW_MAJOR : a_layout, tf32 ? MPG_COL_MAJOR : b_layout);
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         Operand Ac = Aop, Bc = Bop;
+        // one copy: same layout (aligned lines) or transposed (32-bit elements)
+        auto copy = [&](const void* src, mpg_dtype dt, mpg_layout src_layout, int64_t ld, int64_t stride,
+                        mpg_layout dst_layout, int64_t dst_outer, int64_t dst_inner, int64_t dst_ld,
+                        uint8_t* dst) -> cudaError_t {
+          const int64_t src_outer = (src_layout == dst_layout) ? dst_outer : dst_inner;
+          const int64_t s = stride ? stride : src_outer * ld;
+          if (src_layout == dst_layout)
+            return launch_copy_pad(src, elem_bytes(dt), ld, s, dst_outer, dst_inner, batch, dst, dst_ld,
+                                   dev->sm_count, st);
+          return launch_transpose32(src, ld, s, dst_inner, dst_outer, batch, dst, dst_ld, st);
+        };
         if (plan.copy_a) {
-          const int64_t sA = strideA ? strideA : L.a_outer * lda;
-          e = launch_copy_pad(A, elem_bytes(a_dtype), lda, sA, L.a_outer, L.a_inner, batch, ws + L.off_a, L.a_ld,
-                              dev->sm_count, st);
-          Ac = Operand{ws + L.off_a, L.a_ld, L.a_outer * L.a_ld, a_dtype, a_layout};
+          e = copy(A, a_dtype, a_layout, lda, strideA, L.a_layout, L.a_outer, L.a_inner, L.a_ld, ws + L.off_a);
+          Ac = Operand{ws + L.off_a, L.a_ld, L.a_outer * L.a_ld, a_dtype, L.a_layout};
         }
         if (e == cudaSuccess && plan.copy_b) {
-          const int64_t sB = strideB ? strideB : L.b_outer * ldb;
-          e = launch_copy_pad(B, elem_bytes(b_dtype), ldb, sB, L.b_outer, L.b_inner, batch, ws + L.off_b, L.b_ld,
-                              dev->sm_count, st);
-          Bc = Operand{ws + L.off_b, L.b_ld, L.b_outer * L.b_ld, b_dtype, b_layout};
+          e = copy(B, b_dtype, b_layout, ldb, strideB, L.b_layout, L.b_outer, L.b_inner, L.b_ld, ws + L.off_b);
+          Bc = Operand{ws + L.off_b, L.b_ld, L.b_outer * L.b_ld, b_dtype, L.b_layout};
         }
         if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "aligned copy launch: %s", cudaGetErrorString(e));
         return launch_tc(plan, dev, m, n, k, batch, Ac, Bc, C, ldc, strideC, alpha, beta, o, workspace, st);

@@ -91,6 +91,11 @@ cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64
                             int64_t inner, int64_t batch, void* out, int64_t ld_out, int sm_count,
                             cudaStream_t stream);
 
+// Transposed copy of 32-bit elements: `outer` lines of `inner` become `inner`
+// lines of `outer` (ld_out % 8 == 0, padding columns zeroed).
+cudaError_t launch_transpose32(const void* in, int64_t ld_in, int64_t stride_in, int64_t outer, int64_t inner,
+                               int64_t batch, void* out, int64_t ld_out, cudaStream_t stream);
+
 // Fused prompt attention O = softmax(scale * Q K^T) V (head dimension 128).
 struct AttnParams {
   CUtensorMap map_k;   // K: fp16 [lk][ldk], box 64 dims x 64 keys

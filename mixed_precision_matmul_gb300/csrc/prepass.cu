@@ -117,7 +117,46 @@ __global__ void __launch_bounds__(256) copy_pad_kernel(const uint8_t* __restrict
   }
 }
 
+// Transposed copy of 32-bit elements: `batch` matrices of `outer` lines of
+// `inner` elements (ld_in, stride_in) become `inner` lines of `outer`
+// elements with ld_out (a multiple of 8) and stride inner * ld_out.  32 x 32
+// tiles through shared memory (one padding column against bank conflicts),
+// both global sides coalesced.
+__global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __restrict__ in, int64_t ld_in,
+                                                          int64_t stride_in, int64_t outer, int64_t inner,
+                                                          uint32_t* __restrict__ out, int64_t ld_out) {
+  __shared__ uint32_t tile[32][33];
+  const int64_t b = blockIdx.z;
+  const int64_t o0 = (int64_t)blockIdx.y * 32, i0 = (int64_t)blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+  const uint32_t* src = in + b * stride_in;
+  uint32_t* dst = out + b * inner * ld_out;
+#pragma unroll
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t o = o0 + r, i = i0 + tx;
+    tile[r][tx] = (o < outer && i < inner) ? __ldg(src + o * ld_in + i) : 0u;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t i = i0 + r, o = o0 + tx;
+    // the padding columns of each output line (outer .. ld_out-1) are zero
+    if (i < inner && o < ld_out) dst[i * ld_out + o] = (o < outer) ? tile[tx][r] : 0u;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose32(const void* in, int64_t ld_in, int64_t stride_in, int64_t outer, int64_t inner,
+                               int64_t batch, void* out, int64_t ld_out, cudaStream_t stream) {
+  if (batch > 65535 || (outer + 31) / 32 > 65535) return cudaErrorInvalidValue;
+  // blocks along the output lines also cover their padding columns
+  const int64_t out_cols = (ld_out > outer) ? ld_out : outer;
+  dim3 grid((unsigned)((inner + 31) / 32), (unsigned)((out_cols + 31) / 32), (unsigned)batch);
+  transpose32_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint32_t*>(in), ld_in, stride_in, outer, inner,
+                                               static_cast<uint32_t*>(out), ld_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64_t stride_in, int64_t outer,
                             int64_t inner, int64_t batch, void* out, int64_t ld_out, int sm_count,

@@ -61,3 +61,23 @@ def test_unaligned_operands_copied_to_the_tma_path(mode, dt, m, n, k, al, bl, pa
                                      c.ldb, c.B.stride(0) if batch > 1 else 0,
                                      {"bf16": mpg.BF16, "f16": mpg.F16, "f32": mpg.F32}[dt], bl, mode)
     assert ws_exact > ws_plain     # room for the copies was asked for
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,batch", [
+    (300, 260, 200, R, R, (0, 0, 0), 1),     # B row-major: transposed copy of B
+    (300, 260, 200, Cm, Cm, (0, 0, 0), 1),   # A column-major: transposed copy of A
+    (257, 131, 99, Cm, R, (1, 3, 2), 2),     # both transposed, odd leading dims, batches
+])
+def test_tf32_operands_transposed_to_the_direct_path(m, n, k, al, bl, pad, batch):
+    """tf32 tiles are K-major: with the exact workspace, a column-major A or a
+    row-major B is copied transposed and the direct tf32 path multiplies it."""
+    mpg.build()
+    c = Case(m, n, k, mpg.TF32, in_dtype="f32", a_layout=al, b_layout=bl, pad=pad, alpha=0.75, beta=0.5,
+             dist="normal", batch=batch)
+    c.run(exact_ws=True)
+    eR, _ = c.errors()
+    assert eR <= TOL["tf32"], eR
+    ws_exact = mpg.workspace_size_ex(m, n, k, batch, c.A.data_ptr(), c.lda, c.A.stride(0) if batch > 1 else 0,
+                                     mpg.F32, al, c.B.data_ptr(), c.ldb, c.B.stride(0) if batch > 1 else 0,
+                                     mpg.F32, bl, mpg.TF32)
+    assert ws_exact > mpg.workspace_size(m, n, k, batch, mpg.TF32)
