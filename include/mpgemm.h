@@ -138,11 +138,12 @@ typedef struct {
    * with the same options (4 bytes per operand element for the split, 2
    * otherwise, plus split-K partials).
    *   1  = always (MPG_ERR_WORKSPACE if the workspace is too small);
-   *   0  (default) = the library's choice: the split modes take the pass when
-   *        m >= 256, n >= 256 and m*n*k >= 2^32 (both operands re-read by
-   *        many tiles) and the workspace holds the copies (the workspace
-   *        query then includes them); otherwise, and for the fp16 / bf16
-   *        modes, conversion happens on the fly;
+   *   0  (default) = the library's choice: the pass when m >= 256,
+   *        n >= 256 and m*n*k >= 2^32 (both operands re-read by many tiles)
+   *        and the workspace holds the copies; mpg_gemm_workspace_size
+   *        includes them for the split modes, mpg_gemm_workspace_size_ex
+   *        (which sees the operand types) also for fp16 / bf16 modes on
+   *        fp32 operands; otherwise conversion happens on the fly;
    *   -1 = never. */
   int32_t prepass;
   /* Storage type of C (an mpg_dtype): MPG_F32 (default), MPG_F16 or MPG_BF16.

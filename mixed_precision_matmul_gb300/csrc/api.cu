@@ -313,7 +313,11 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   // split-K is chosen from the sizes alone, before the path
   int splits = choose_splits(m, n, k, batch, sm_count, o);
   bool use_pass = (o.prepass == 1 && p.conv != Conv::kNone);
-  if (!use_pass && o.prepass == 0 && split_mode(mode) && auto_prepass_shape(m, n, k)) {
+  // the library's choice: every mode that converts fp32 operands (split,
+  // and fp16 / bf16 on fp32 inputs), when the workspace holds the copies
+  // (the sizes-only query includes them for the split modes, the exact one
+  // for all)
+  if (!use_pass && o.prepass == 0 && p.conv != Conv::kNone && auto_prepass_shape(m, n, k)) {
     // the library's choice: the pass when the workspace holds the copies
     const PrepassLayout L = prepass_layout(m, n, k, batch, A.layout, B.layout, splits_a(p.conv), splits_b(p.conv),
                                            splitk_bytes(splits, m, n, batch));
@@ -931,6 +935,18 @@ size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch
   const bool f16in = (mode == MPG_FP16_F32ACC && a_dtype == MPG_F16 && b_dtype == MPG_F16) ||
                      (mode == MPG_BF16_F32ACC && a_dtype == MPG_BF16 && b_dtype == MPG_BF16);
   const bool tf32 = (mode == MPG_TF32 && a_dtype == MPG_F32 && b_dtype == MPG_F32);
+  // fp16 / bf16 modes on fp32 operands: the conversion pass on large products
+  const bool round_f32 = (mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC) && a_dtype == MPG_F32 &&
+                         b_dtype == MPG_F32;
+  if (round_f32 && o.prepass == 0 && auto_prepass_shape(m, n, k)) {
+    DeviceInfo* dev = nullptr;
+    int sm = 152;
+    if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
+    t_err.clear();
+    const PrepassLayout L = prepass_layout(m, n, k, batch, a_layout, b_layout, false, false,
+                                           splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch));
+    return std::max(base, L.end);
+  }
   if (!f16in && !tf32) return base;
   Operand Aop{A, lda, strideA, a_dtype, a_layout};
   Operand Bop{B, ldb, strideB, b_dtype, b_layout};

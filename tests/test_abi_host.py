@@ -277,3 +277,17 @@ def test_workspace_includes_the_conversion_pass_when_the_library_takes_it(L):
     assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC) == 0          # fp16 mode: opt-in only
     assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, mpg.options(prepass=1)) >= 2 * 2 * n * n
     assert _call(opts=mpg.options(prepass=2)) == mpg.ERR_INVALID_ARG
+
+
+def test_exact_query_includes_the_pass_for_fp16_modes_on_fp32_operands(L):
+    n = 4096
+    plain = mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC)
+    exact = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
+                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC)
+    assert plain == 0 and exact >= 2 * 2 * n * n            # fp16 copies of A and B
+    exact16 = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F16, mpg.ROW_MAJOR, 256, n, 0, mpg.F16,
+                                    mpg.ROW_MAJOR, mpg.FP16_F32ACC)
+    assert exact16 == 0                                      # fp16 operands: nothing to convert
+    never = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
+                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC, mpg.options(prepass=-1))
+    assert never == 0

@@ -1,10 +1,12 @@
 """GPU: fp32 operands converted on load (TMA staging + converter warps):
 fp16 / bf16 rounding and the hi/lo split in its three-chain and one-chain
 forms, against both oracle modes."""
+import numpy as np
 import pytest
 
 import mixed_precision_matmul_gb300 as mpg
-from helpers import TOL, Case
+import oracle
+from helpers import TOL, Case, sample_points
 
 pytestmark = pytest.mark.gpu
 
@@ -184,3 +186,30 @@ def test_split_four_chain_parity(m, n, k, al, bl, pad, tile_n, prepass):
     c.run()
     eR, eQ = c.errors()
     assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
+
+
+@pytest.mark.parametrize("mode,q", [(mpg.FP16_F32ACC, oracle.Q_FP16), (mpg.BF16_F32ACC, oracle.Q_BF16)])
+def test_fp16_modes_on_fp32_take_the_pass_with_the_exact_workspace(mode, q):
+    """2048 x 2048 x 1024 (2^32 multiply-adds): with the workspace the exact
+    query asks for, fp32 operands are converted by the separate pass; the
+    result equals the on-load conversion's within the mode's bar."""
+    import torch
+    mpg.build()
+    m = n = 2048
+    k = 1024
+    c = Case(m, n, k, mode, b_layout=Cm, alpha=1.0, beta=0.5, dist="normal")
+    c.run(exact_ws=True)
+    rows, cols = sample_points(m, n, 1500, 91)
+    ref, den = c.reference_points(q, 0, rows, cols)
+    err = oracle.max_rel_err(c.result()[0][rows, cols], ref, den)
+    assert err <= TOL["q16"], err
+    # the torch wrapper sizes its workspace with the exact query
+    A = torch.from_numpy(c.a[0]).cuda()
+    B = torch.from_numpy(c.b[0]).cuda()
+    C = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    mpg.gemm(A, B, C, mode=mode)
+    torch.cuda.synchronize()
+    ref, den = c.reference_points(q, 0, rows, cols)
+    ref0 = ref - 0.5 * c.c0[0][rows, cols].astype(np.float64)   # the wrapper call used beta = 0
+    den0 = den - 0.5 * np.abs(c.c0[0][rows, cols].astype(np.float64))
+    assert oracle.max_rel_err(C.cpu().numpy()[rows, cols], ref0, den0) <= TOL["q16"]
