@@ -160,6 +160,22 @@ def run_step(mpg, w, C, ws=0, ws_bytes=0, stream=0):
                  w.alpha, w.beta, mpg.MODE_NAMES[w.mode_name], ws, ws_bytes, stream, w.opts)
 
 
+def slowest_rank(torch, dist, device, ms_local):
+    """Time of the slowest rank (max over ranks; this rank's time alone
+    without a process group)."""
+    if dist is None:
+        return ms_local
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, flops_per_rank, ms_per_step):
+    """Whole-job TFLOP/s of N independent replicas: the work of every rank in
+    one step divided by the slowest rank's step time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def time_steps(torch, fn, steps, warmup, stream):
     """Device time of `steps` back-to-back calls (CUDA events on `stream`)."""
     for _ in range(warmup):
@@ -440,17 +456,13 @@ def ours(args):
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank(torch, dist, device, elapsed_ms)
     status = mpg.device_status()
     if status != mpg.OK:
         raise RuntimeError(f"device status {mpg.STATUS.get(status)} after the timed region")
 
     ms_per_step = elapsed_ms / args.steps
-    per_rank_tflops = w.flops / (ms_per_step * 1e-3) / 1e12
-    value = per_rank_tflops * world
+    value = job_throughput(world, w.flops, ms_per_step)
     peak_bf16 = peaks["bf16_tflops"]
 
     result = {
@@ -526,12 +538,9 @@ def ours(args):
         st = mpg.device_status()
         if st != mpg.OK:
             raise RuntimeError(f"e2e steps reported status {st}: {mpg.last_error()}")
-        if dist:
-            t = torch.tensor([e2e_ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = slowest_rank(torch, dist, device, e2e_ms)
         h2d = (hA.numel() + hB.numel()) * hA.element_size() + hC[0].numel() * 4
-        result["e2e"] = {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        result["e2e"] = {"value": round(job_throughput(world, w.flops, e2e_ms), 2), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC[0].numel() * 4,
                          "ms_per_step": round(e2e_ms, 4),
                          "api": "mpg_gemm_host (host buffers in, host C out, one call per step)",
