@@ -251,9 +251,10 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
  * asynchronously and overlap; pageable memory works but its copies block the
  * calling thread).  C's padding columns (n .. ldc-1) are never written.
  *   workspace   device memory of at least mpg_gemm_host_workspace_size()
- *               bytes for the same arguments, 16-byte aligned: device copies
- *               of A, B and C with the caller's leading dimensions and batch
- *               strides, plus the product's own workspace.
+ *               bytes for the same arguments, 16-byte aligned: packed device
+ *               copies of A, B and C with lines padded to 16 bytes (so the
+ *               product takes the TMA path whatever the host leading
+ *               dimensions), plus the product's own workspace.
  * Inside one call the copies overlap the product: B is copied first, then A
  * and C are processed in chunks of rows (of whole matrices when batch > 1),
  * the copy of chunk i+1 and the copy back of chunk i-1 running beside the

@@ -151,3 +151,15 @@ def test_host_k_zero_scales_c():
     c0 = synthetic.normal((1, 40, 50), 171)
     got = run_host(a, b, c0, mpg.FP32_FFMA, dt="f32", pad=(1, 0, 3), beta=-2.0)
     assert np.array_equal(got[0], (-2.0 * c0[0].astype(np.float32)).astype(np.float64))
+
+
+def test_host_odd_leading_dimensions_run_on_aligned_device_copies():
+    """bf16 host operands with odd leading dimensions: the device copies are
+    padded to 16-byte lines, so the product takes the TMA path (checked here
+    for values; the padding of host C is checked by run_host)."""
+    mpg.build()
+    a = round_to(synthetic.normal((1, 520, 301), 181), "bf16")
+    b = round_to(synthetic.normal((1, 301, 263), 182), "bf16")
+    c0 = synthetic.normal((1, 520, 263), 183)
+    got = run_host(a, b, c0, mpg.BF16_F32ACC, al=R, bl=Cm, pad=(0, 0, 1), alpha=1.0, beta=0.5)
+    _check(got, a, b, c0, oracle.Q_BF16, 1.0, 0.5, TOL["q16"])
