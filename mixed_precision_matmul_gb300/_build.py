@@ -23,6 +23,10 @@ INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = [
     "api.cu",
+    "host_common.cu",
+    "plan.cu",
+    "host_api.cu",
+    "attention_api.cu",
     "acc_layout.cpp",
     "aux_kernels.cu",
     "ffma.cu",
@@ -33,7 +37,7 @@ SOURCES = [
     "tc_pair.cu",
     "attention.cu",
 ]
-HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh", "host.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
