@@ -379,6 +379,51 @@ def gemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, works
     return C
 
 
+def gemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, mode=BF16_F32ACC, opts: Options | None = None,
+              device=None, stream=None):
+    """C = alpha * A @ B + beta * C on CPU tensors (page-locked ones, e.g.
+    from ``tensor.pin_memory()``, let the copies run asynchronously), through
+    mpg_gemm_host: the call copies A, B and C to the device, multiplies, and
+    copies C back into the same host tensor.  The device workspace is
+    allocated through torch on ``device`` (default: the current CUDA device).
+    Returns C once the product has completed (the stream is synchronised)."""
+    torch = _torch()
+    if isinstance(mode, str):
+        mode = MODE_NAMES[mode]
+    for t in (A, B, C):
+        if t.is_cuda:
+            raise ValueError("gemm_host takes host (CPU) tensors")
+    batched = C.dim() == 3
+    batch = C.shape[0] if batched else 1
+    m, k = A.shape[-2], A.shape[-1]
+    n = B.shape[-1]
+    if B.shape[-2] != k or C.shape[-2] != m or C.shape[-1] != n:
+        raise ValueError("shape mismatch")
+    if C.dtype not in (torch.float32, torch.float16, torch.bfloat16) or C.stride(-1) != 1:
+        raise ValueError("C must be fp32, fp16 or bf16 with unit column stride")
+    o = Options()
+    if opts is not None:
+        ctypes.memmove(ctypes.byref(o), ctypes.byref(opts), ctypes.sizeof(Options))
+    else:
+        lib().mpg_options_init(ctypes.byref(o))
+    o.c_dtype = _dtype_code(C)
+    a_layout, lda, sa = _operand(A, m, k)
+    b_layout, ldb, sb = _operand(B, k, n)
+    ldc = max(C.stride(-2), n, 1)
+    sc = C.stride(0) if batched else 0
+    ws_bytes = host_workspace_size(m, n, k, batch, lda, sa, _dtype_code(A), a_layout, ldb, sb, _dtype_code(B),
+                                   b_layout, ldc, sc, alpha, beta, mode, o)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = torch.cuda.current_stream() if stream is None else stream
+        gemm_host_raw(m, n, k, batch, A.data_ptr(), lda, sa, _dtype_code(A), a_layout, B.data_ptr(), ldb, sb,
+                      _dtype_code(B), b_layout, C.data_ptr(), ldc, sc, alpha, beta, mode, ws.data_ptr(), ws_bytes,
+                      st.cuda_stream, o)
+        st.synchronize()
+    return C
+
+
 # ---------------------------------------------------------------------------
 # accumulator fragment decode (host)
 # ---------------------------------------------------------------------------

@@ -163,3 +163,18 @@ def test_host_odd_leading_dimensions_run_on_aligned_device_copies():
     c0 = synthetic.normal((1, 520, 263), 183)
     got = run_host(a, b, c0, mpg.BF16_F32ACC, al=R, bl=Cm, pad=(0, 0, 1), alpha=1.0, beta=0.5)
     _check(got, a, b, c0, oracle.Q_BF16, 1.0, 0.5, TOL["q16"])
+
+
+def test_torch_gemm_host_on_cpu_tensors():
+    import torch
+    mpg.build()
+    a = round_to(synthetic.normal((300, 200), 191), "bf16")
+    b = round_to(synthetic.normal((200, 260), 192), "bf16")
+    c0 = synthetic.normal((300, 260), 193)
+    A = torch.from_numpy(a).to(torch.bfloat16).pin_memory()
+    B = torch.from_numpy(b).to(torch.bfloat16).t().contiguous().t()     # column-major view
+    C = torch.from_numpy(c0.copy())
+    out = mpg.gemm_host(A, B, C, alpha=1.0, beta=0.5, mode="bf16")
+    assert out is C and not C.is_cuda
+    ref, den = oracle.gemm(a, b, c0, 1.0, 0.5, oracle.Q_BF16, oracle.Q_BF16)
+    assert oracle.max_rel_err(C.numpy(), ref, den) <= TOL["q16"]
