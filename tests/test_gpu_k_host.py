@@ -178,3 +178,25 @@ def test_torch_gemm_host_on_cpu_tensors():
     assert out is C and not C.is_cuda
     ref, den = oracle.gemm(a, b, c0, 1.0, 0.5, oracle.Q_BF16, oracle.Q_BF16)
     assert oracle.max_rel_err(C.numpy(), ref, den) <= TOL["q16"]
+
+
+def test_host_full_size_bf16_8192_beta(capsys):
+    """The end-to-end configuration of the benchmark: 8192^3 bf16 with beta =
+    0.5 from page-locked host buffers through mpg_gemm_host (row chunks
+    pipelined against the product); sampled elements and whole rows at chunk
+    boundaries against the oracle."""
+    mpg.build()
+    n = 8192
+    a = round_to(synthetic.normal((1, n, n), synthetic.SEED_A), "bf16")
+    b = round_to(synthetic.normal((1, n, n), synthetic.SEED_B), "bf16")
+    c0 = synthetic.normal((1, n, n), synthetic.SEED_C0)
+    got = run_host(a, b, c0, mpg.BF16_F32ACC, beta=0.5)
+    rows, cols = sample_points(n, n, 2000, 195)
+    ref, den = oracle.gemm_points(a[0], b[0], n, rows, cols, c0[0], 1.0, 0.5, oracle.Q_BF16, oracle.Q_BF16)
+    err = oracle.max_rel_err(got[0][rows, cols], ref, den)
+    edge = np.array([0, 1535, 1536, 4607, 4608, 8191])
+    refr, denr = oracle.gemm(a[0][edge], b[0], c0[0][edge], 1.0, 0.5, oracle.Q_BF16, oracle.Q_BF16)
+    err_rows = oracle.max_rel_err(got[0][edge], refr, denr)
+    with capsys.disabled():
+        print(f"\n[host 8192^3 bf16: sampled {err:.3e}, rows {err_rows:.3e}]")
+    assert err <= TOL["q16"] and err_rows <= TOL["q16"]
