@@ -18,17 +18,18 @@
 //                 S_j = [Q_hi ; Q_lo] K_j^T   (M 128, N 64, K 128) -> 2 chains
 //                 O_j = [P_hi ; P_lo] V_j     (M 128, N 128, K 64) -> 2 chains
 //               with S double-buffered, so S_{j+2} runs beside softmax_{j+1}
-//   warps 2-9   softmax and correction.  Warps w and w+4 read the same TMEM
-//               lanes (query rows); each takes half of a row: 32 of the
-//               block's keys for the softmax and 64 of the output dims for
-//               the correction.
+//   warps 2-17  softmax and correction, four warps per TMEM lane quarter
+//               (32 query rows); each of the four takes a quarter of a row:
+//               16 of the block's keys for the softmax and 32 of the output
+//               dims for the correction.
 //               softmax of block j: s = (S_hi + 2^-11 S_lo) * scale * log2(e);
-//               the two halves exchange their maxima (shared memory and a
-//               64-arrival mbarrier per lane quarter, waited on with the same
-//               bounded wait as every other handoff), so both compute the same running
-//               maximum and the same rescale factor; p = 2^(s - max), split
-//               into hi/lo fp16 and written to shared memory as the A operand
-//               of the next MMA; each half keeps its own running sum.
+//               the four parts exchange their maxima (shared memory and an
+//               mbarrier per lane quarter that all four parts arrive on,
+//               waited on with the same bounded wait as every other handoff),
+//               so all compute the same running maximum and the same rescale
+//               factor; p = 2^(s - max), split into hi/lo fp16 and written to
+//               shared memory as the A operand of the next MMA; each part
+//               keeps its own running sum.
 //               correction of block j: O_run = O_run * 2^(max_old - max_new)
 //               + (O_hi + 2^-11 O_lo) in fp32 (round to nearest), in
 //               registers.  A warp runs the softmax of block j+1 before the
@@ -36,7 +37,7 @@
 //               next block's work.  At the end O = O_run / sum (or the
 //               unnormalised partial with its max and sum when the keys are
 //               split across CTAs; a merge kernel combines the partials).
-// First, warps 2-9 load the CTA's 128 x 128 fp32 block of Q and split it into
+// First, the compute warps load the CTA's 128 x 128 fp32 block of Q and split it into
 // the swizzled hi/lo operand tiles.  Every wait is bounded.
 #include "tc_gemm.cuh"
 
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   uint64_t* o_empty = o_full + 1;
   uint64_t* q_ready = o_full + 2;
   uint64_t* done_bar = q_ready + 1;
-  uint64_t* xchg = done_bar + 1;            // [4]: the two warps of a lane quarter exchange values
+  uint64_t* xchg = done_bar + 1;            // [4]: the parts of a lane quarter exchange values
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
