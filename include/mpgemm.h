@@ -163,7 +163,26 @@ typedef struct {
    * give every pair of SMs at least one tile, 1 = always where it applies,
    * -1 = never (one CTA per 128-row tile).  Other configurations ignore it. */
   int32_t cta_pair;
-  int32_t reserved[4];
+  /* Split tail for the CTA-pair kernel.  A persistent grid of P clusters
+   * takes tiles in rounds of P; when the last round holds R < P tiles, the
+   * other clusters would idle for a whole tile.  With the split tail each of
+   * those R tiles is cut in two along K at the middle k-block: 2R workers
+   * each multiply one half, write their fp32 partial sums to the workspace,
+   * and the second half to arrive adds the two (fp32, round to nearest: the
+   * same sum in either order) and applies alpha, beta and C's type, so the
+   * result does not depend on timing.  Needs the workspace that
+   * mpg_gemm_workspace_size reports (at most 128 x 256 x 4 bytes per SM plus
+   * counters) and clears its counters with one cudaMemsetAsync per call.
+   *   0 (default) = where it pays on a GB300: 1 to 6 full rounds, then
+   *       1 <= R <= P/2 tiles, and k >= 8192 (half a tile's time outweighs
+   *       waiting for the later of two clusters and exchanging the partial
+   *       sums, about 16 us), when the workspace holds it;
+   *   1 = whenever the tile count is not a multiple of P (all tiles when
+   *       there are fewer than P) and K has two k-blocks
+   *       (MPG_ERR_WORKSPACE if the workspace is too small);
+   *   -1 = never.  Other kernels ignore it. */
+  int32_t tail_split;
+  int32_t reserved[3];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);
@@ -229,7 +248,10 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch,
  *   - Every call on a device shares the one scratch array, and each call
  *     overwrites the part it uses: calls that can overlap on the GPU
  *     (different streams without ordering) race.  Order them on one stream.
- * Results equal mpg_gemm_ex's for the same arguments and options. */
+ *   - The split tail (mpg_options.tail_split) is never taken here: its
+ *     partial sums can outgrow the scratch.
+ * Results equal mpg_gemm_ex's for the same arguments and options with
+ * tail_split = -1. */
 #define MPG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
                             const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
@@ -239,7 +261,11 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
                             const mpg_options* opt);
 
 /* Bytes of workspace mpg_gemm / mpg_gemm_ex need for this problem (0 if none).
- * Depends only on the sizes, the mode, the options and the current device. */
+ * Depends only on the sizes, the mode, the options and the current device.
+ * For the fp16 / bf16 modes it includes the split tail's partial sums
+ * (mpg_options.tail_split) when the library may take it (1 to 6 full rounds
+ * of 256 x 256 tiles on SMs / 2 clusters, k >= 8192): up to SMs / 4 tiles x
+ * 512 KiB, about 20 MB on 152 SMs. */
 size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
                                mpg_precision mode, const mpg_options* opt);
 

@@ -63,7 +63,8 @@ class Options(ctypes.Structure):
         ("prepass", ctypes.c_int32),
         ("c_dtype", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("tail_split", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 

@@ -61,8 +61,9 @@ int mpg_version(void) { return 100; }
 
 const char* mpg_last_error_string(void) { return t_err.c_str(); }
 
-size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode,
-                               const mpg_options* opt) {
+namespace {
+// Workspace of everything but the split tail, from the sizes alone.
+size_t regions_bytes(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, const mpg_options* opt) {
   mpg_options o;
   resolve_options(opt, &o);
   if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || mode == MPG_FP32_FFMA) return 0;
@@ -86,14 +87,36 @@ size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, m
   return partials;
 }
 
+// Split-tail bound for these sizes (0 when it cannot apply).
+size_t tail_region(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, const mpg_options* opt) {
+  mpg_options o;
+  resolve_options(opt, &o);
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0) return 0;
+  DeviceInfo* dev = nullptr;
+  int sm = 152;
+  if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
+  t_err.clear();
+  return tail_bound(m, n, k, batch, mode, sm, o);
+}
+}  // namespace
+
+size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode,
+                               const mpg_options* opt) {
+  const size_t r = regions_bytes(m, n, k, batch, mode, opt);
+  const size_t t = tail_region(m, n, k, batch, mode, opt);
+  return t ? align256(r) + t : r;
+}
+
 size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
                                   int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout, const void* B,
                                   int64_t ldb, int64_t strideB, mpg_dtype b_dtype, mpg_layout b_layout,
                                   mpg_precision mode, const mpg_options* opt) {
   mpg_options o;
   resolve_options(opt, &o);
-  const size_t base = mpg_gemm_workspace_size(m, n, k, batch, mode, opt);
-  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || o.force_generic_load) return base;
+  const size_t base = regions_bytes(m, n, k, batch, mode, opt);
+  const size_t tail = tail_region(m, n, k, batch, mode, opt);
+  auto with_tail = [&](size_t r) { return tail ? align256(r) + tail : r; };
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || o.force_generic_load) return with_tail(base);
   // the aligned copies the planner makes for 16-bit (or tf32 K-major)
   // operands on the direct path that TMA cannot describe as given
   const bool f16in = (mode == MPG_FP16_F32ACC && a_dtype == MPG_F16 && b_dtype == MPG_F16) ||
@@ -109,21 +132,21 @@ size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch
     t_err.clear();
     const PrepassLayout L = prepass_layout(m, n, k, batch, a_layout, b_layout, false, false,
                                            splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch));
-    return std::max(base, L.end);
+    return with_tail(std::max(base, L.end));
   }
-  if (!f16in && !tf32) return base;
+  if (!f16in && !tf32) return with_tail(base);
   Operand Aop{A, lda, strideA, a_dtype, a_layout};
   Operand Bop{B, ldb, strideB, b_dtype, b_layout};
   const mpg_layout a_out = tf32 ? MPG_ROW_MAJOR : a_layout, b_out = tf32 ? MPG_COL_MAJOR : b_layout;
   const bool ca = !tma_ok(Aop, batch) || a_layout != a_out, cb = !tma_ok(Bop, batch) || b_layout != b_out;
-  if (!ca && !cb) return base;
+  if (!ca && !cb) return with_tail(base);
   DeviceInfo* dev = nullptr;
   int sm = 152;
   if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
   t_err.clear();
   const CopyLayout L = copy_layout(m, n, k, batch, Aop, Bop, ca, cb,
                                    splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch), a_out, b_out);
-  return std::max(base, L.end);
+  return with_tail(std::max(base, L.end));
 }
 
 mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const void* A, int64_t lda,
@@ -343,9 +366,12 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch, cons
     s = noalloc_scratch(&scratch);
     if (s != MPG_OK) return s;
   }
+  // the split tail's partial sums would need more than the scratch holds
+  // for the largest products: this entry never takes it
+  o.tail_split = -1;
   return mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout, C,
                      ldc, strideC, alpha, beta, mode, scratch, need > 0 ? (size_t)MPG_NOALLOC_SCRATCH_BYTES : 0,
-                     stream, opt);
+                     stream, &o);
 }
 
 }  // extern "C"

@@ -57,6 +57,8 @@ struct Plan {
   bool pair = false;          // 256 x 256 tiles on CTA pairs (cta_group::2)
   bool copy_a = false;        // operand copied to an aligned layout in the workspace (TMA cannot
   bool copy_b = false;        //   describe it as given), then multiplied on the direct path
+  size_t tail_off = 0;        // workspace offset of the split tail's partial sums and counters
+  size_t tail_avail = 0;      // workspace bytes from tail_off on
 };
 
 struct Operand {
@@ -76,6 +78,13 @@ mpg_status encode_map(CUtensorMap* map, const Operand& x, int64_t inner, int64_t
 
 int choose_splits(int64_t m, int64_t n, int64_t k, int64_t batch, int sm_count, const mpg_options& o);
 size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch);
+// Workspace of the CTA-pair kernel's split tail for `tiles` tiles: two
+// halves of fp32 partial sums per 256 x 256 tile, then one counter per
+// epilogue warp piece; and its bound for the workspace queries.
+size_t tail_bytes(int64_t tiles);
+size_t tail_bound(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, int sm_count,
+                  const mpg_options& o);
+bool tail_auto(int64_t tiles, int64_t clusters, int64_t num_k_blk);
 struct PrepassLayout {
   int64_t a_outer, a_inner, a_ld, b_outer, b_inner, b_ld;
   size_t off_a_hi, off_a_lo, off_b_hi, off_b_lo, end;

@@ -65,6 +65,15 @@ struct TcParams {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t chunk_kb;   // k-blocks per accumulation chunk (0: the whole k range of a tile)
+  // split tail (CTA-pair kernel): work items from tail_first on are halves
+  // of the k range of the last tiles, cut at k-block tail_kb_mid; each half
+  // writes its partial sums to tail_ws and counts itself in tail_cnt (zero
+  // at launch); the second half to arrive adds the first's and stores C.
+  // tail_first = num_tiles: no split tail.
+  int32_t tail_first;
+  int32_t tail_kb_mid;
+  float* tail_ws;
+  uint32_t* tail_cnt;
 };
 
 struct LaunchInfo {

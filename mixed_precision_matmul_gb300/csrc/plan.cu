@@ -37,6 +37,39 @@ size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch) {
   return splits > 1 ? (size_t)splits * (size_t)batch * (size_t)m * (size_t)n * sizeof(float) : 0;
 }
 
+size_t tail_bytes(int64_t tiles) {
+  return align256((size_t)tiles * 2 * 256 * 256 * sizeof(float)) + align256((size_t)tiles * 16 * sizeof(uint32_t));
+}
+
+// The library's choice of the split tail for `tiles` pair tiles on P
+// clusters and num_k_blk k-blocks of 64.  Cutting the last round's tiles in
+// two saves half a tile's time but pairs two clusters' halves: the second
+// half waits for the later of the two (the clusters drift apart over the
+// earlier rounds) and then exchanges 128 KB of partial sums per CTA, about
+// 16 us in all on a GB300.  So: at least 128 k-blocks (k >= 8192: a tile
+// takes about 50 us), at most 6 full rounds before the tail (more, and the
+// one partial round is a small share of the time), and a last round of at
+// most P / 2 tiles, so that every half finds a cluster.
+bool tail_auto(int64_t tiles, int64_t P, int64_t num_k_blk) {
+  const int64_t full = tiles / P, rem = tiles % P;
+  return full >= 1 && full <= 6 && rem >= 1 && 2 * rem <= P && num_k_blk >= 128;
+}
+
+// The most split-tail workspace a call may take: at most a quarter of the
+// SMs' worth of tiles by default (2R <= P <= SMs / 2 clusters), half with
+// tail_split = 1; only the fp16 / bf16 modes reach the pair kernel.
+size_t tail_bound(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, int sm_count,
+                  const mpg_options& o) {
+  if (o.tail_split < 0 || (mode != MPG_FP16_F32ACC && mode != MPG_BF16_F32ACC) || o.cta_pair < 0) return 0;
+  if (o.tail_split == 1) return tail_bytes(std::max(sm_count / 2, 1));
+  // the clusters resident at launch are at most SMs / 2, so a product this
+  // query leaves out has more than 6 full rounds at launch too
+  const int64_t P = std::max(sm_count / 2, 1);
+  const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
+  if (pair_tiles < P || pair_tiles / P > 6 || (k + 63) / 64 < 128) return 0;
+  return tail_bytes(std::max(sm_count / 4, 1));
+}
+
 // Workspace of the separate conversion pass: packed 16-bit copies of A and B
 // (hi and lo for the split) after the split-K partials, each 256-byte aligned.
 // A copy keeps its operand's majorness; its lines are padded to a multiple of
@@ -180,6 +213,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   const bool tma = !o.force_generic_load && tma_ok(A, batch) && tma_ok(B, batch);
   // split-K is chosen from the sizes alone, before the path
   int splits = choose_splits(m, n, k, batch, sm_count, o);
+  size_t copies_end = 0;   // end of the conversion pass's or the aligned copies' region
   bool use_pass = (o.prepass == 1 && p.conv != Conv::kNone);
   // the library's choice: every mode that converts fp32 operands (split,
   // and fp16 / bf16 on fp32 inputs), when the workspace holds the copies
@@ -225,6 +259,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
         p.src = Src::kTmaDirect;
         p.copy_a = ca;
         p.copy_b = cb;
+        copies_end = L.end;
       }
     }
   }
@@ -271,6 +306,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     if (L.end > ws_bytes)
       return fail(MPG_ERR_WORKSPACE, "the separate conversion pass needs %zu workspace bytes, got %zu", L.end,
                   ws_bytes);
+    copies_end = L.end;
   }
   if (splits > 1 && splitk_bytes(splits, m, n, batch) > ws_bytes) {
     if (o.splitk > 0)
@@ -279,6 +315,9 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     splits = 1;  // automatic choice: no workspace, no split
   }
   p.splits = splits;
+  // the split tail's partial sums follow everything else in the workspace
+  p.tail_off = align256(std::max(copies_end, splitk_bytes(splits, m, n, batch)));
+  p.tail_avail = ws_bytes > p.tail_off ? ws_bytes - p.tail_off : 0;
   *plan = p;
   return MPG_OK;
 }
@@ -325,6 +364,7 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (o.wait_timeout_ns < 0) return fail(MPG_ERR_INVALID_ARG, "negative wait timeout");
   if (o.c_dtype < MPG_F32 || o.c_dtype > MPG_BF16) return fail(MPG_ERR_INVALID_ARG, "unknown C dtype %d", o.c_dtype);
   if (o.cta_pair < -1 || o.cta_pair > 1) return fail(MPG_ERR_INVALID_ARG, "cta_pair must be -1, 0 or 1");
+  if (o.tail_split < -1 || o.tail_split > 1) return fail(MPG_ERR_INVALID_ARG, "tail_split must be -1, 0 or 1");
   if (o.prepass < -1 || o.prepass > 1) return fail(MPG_ERR_INVALID_ARG, "prepass must be -1, 0 or 1");
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
@@ -465,6 +505,37 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   const int64_t tiles = (int64_t)splits_eff * batch * p.num_m_blk * p.num_n_blk;
   if (tiles > 0x7FFFFFFF) return fail(MPG_ERR_INVALID_ARG, "too many tiles");
   p.num_tiles = (int32_t)tiles;
+  p.tail_first = p.num_tiles;
+  // clusters of the pair kernel resident at once
+  int clusters = 0;
+  if (plan.pair) {
+    mpg_status cs = pair_clusters(dev, kern, &clusters);
+    if (cs != MPG_OK) return cs;
+  }
+  // split tail: the last round's R tiles become 2R halves of their k range
+  int64_t tail_tiles = 0;
+  if (plan.pair && splits_eff == 1 && o.tail_split >= 0 && p.num_k_blk >= 2 && tiles > 0) {
+    const int64_t P = clusters;
+    const int64_t full = tiles / P, rem = tiles % P;
+    if (o.tail_split == 1) {
+      tail_tiles = full == 0 ? tiles : rem;
+    } else if (tail_auto(tiles, P, p.num_k_blk) && tail_bytes(rem) <= plan.tail_avail) {
+      tail_tiles = rem;
+    }
+    if (tail_tiles > 0 && tail_bytes(tail_tiles) > plan.tail_avail)
+      return fail(MPG_ERR_WORKSPACE, "the split tail needs %zu workspace bytes after offset %zu, got %zu",
+                  tail_bytes(tail_tiles), plan.tail_off, plan.tail_avail);
+  }
+  if (tail_tiles > 0) {
+    uint8_t* base = static_cast<uint8_t*>(workspace) + plan.tail_off;
+    p.tail_first = (int32_t)(tiles - tail_tiles);
+    p.num_tiles = (int32_t)(tiles + tail_tiles);
+    p.tail_kb_mid = p.num_k_blk / 2;
+    p.tail_ws = reinterpret_cast<float*>(base);
+    p.tail_cnt = reinterpret_cast<uint32_t*>(base + align256((size_t)tail_tiles * 2 * 256 * 256 * sizeof(float)));
+    cudaError_t me = cudaMemsetAsync(p.tail_cnt, 0, (size_t)tail_tiles * 16 * sizeof(uint32_t), stream);
+    if (me != cudaSuccess) return fail(MPG_ERR_CUDA, "split tail counters: %s", cudaGetErrorString(me));
+  }
   // rasterisation: groups of tile rows sized so that the tiles resident at
   // once touch about as many A panels as B panels (tiles of a pair are
   // twice as tall)
@@ -502,12 +573,9 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   cudaError_t e;
   if (plan.pair) {
     // clusters of two CTAs; as many clusters as can be resident at once
-    int clusters = 0;
-    mpg_status cs = pair_clusters(dev, kern, &clusters);
-    if (cs != MPG_OK) return cs;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(tiles, clusters)));
+    cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(p.num_tiles, clusters)));
     cfg.blockDim = dim3((unsigned)kern.block);
     cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
     cfg.stream = stream;

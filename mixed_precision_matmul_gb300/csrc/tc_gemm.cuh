@@ -102,6 +102,8 @@ struct TcTraits {
 
 struct TileCoord {
   int s, b, mb, nb, kb0, kb1;
+  int tail;   // index among the tiles whose k range is cut in two, or -1
+  int half;   // which half of the k range (0: [kb0, mid), 1: [mid, kb1))
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const TcParams& p, int t) {
@@ -122,6 +124,23 @@ __device__ __forceinline__ TileCoord decode_tile(const TcParams& p, int t) {
   c.nb = within / gm;
   c.kb0 = c.s * p.kb_per_split;
   c.kb1 = min(p.num_k_blk, c.kb0 + p.kb_per_split);
+  c.tail = -1;
+  c.half = 0;
+  return c;
+}
+
+// Work item t of a persistent loop.  Items below tail_first are whole tiles
+// in decode_tile's order; from tail_first on, each remaining tile is two
+// items, the halves of its k range, so that the last round of tiles spreads
+// over twice as many workers.
+__device__ __forceinline__ TileCoord decode_item(const TcParams& p, int t) {
+  if (t < p.tail_first) return decode_tile(p, t);
+  const int h = t - p.tail_first;
+  TileCoord c = decode_tile(p, p.tail_first + (h >> 1));
+  c.tail = h >> 1;
+  c.half = h & 1;
+  if (c.half == 0) c.kb1 = p.tail_kb_mid;
+  else c.kb0 = p.tail_kb_mid;
   return c;
 }
 

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
       uint32_t it = 0;
       bool ok = true;
       for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl) {
-        const TileCoord tc = decode_tile(p, t);
+        const TileCoord tc = decode_item(p, t);
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
           const uint32_t st = it % T::kStages;
           const uint32_t ph = (it / T::kStages) & 1u;
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
       uint32_t it = 0, g = 0;
       bool ok = true;
       for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl, ++g) {
-        const TileCoord tc = decode_tile(p, t);
+        const TileCoord tc = decode_item(p, t);
         const uint32_t ab = g % T::kAccBufs;
         const uint32_t aph = (g / T::kAccBufs) & 1u;
         if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctl)) { ok = false; break; }
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
     uint32_t g = 0;
     bool ok = true;
     for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl, ++g) {
-      const TileCoord tc = decode_tile(p, t);
+      const TileCoord tc = decode_item(p, t);
       void* out;
       int64_t ldo;
       float alpha, beta;
@@ -315,19 +315,18 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
       tc_fence_after_sync();
       const uint32_t tacc = tmem_base + lane_off + ab * T::kAccStride;
       const int row_base = tc.mb * T::BMP + (int)rank * T::BM + 32 * q;
-#pragma unroll 1
-      for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
-        float v[32];
-        tmem_ld_32cols(tacc + cc * 32, v);
-        tmem_ld_wait();
-        if (cc == cc0 + kCcPer - 1) {
-          // this warp's share of the buffer is in registers: hand it back
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty0 + ab * 8u);
-        }
+      // hand this warp's share of the accumulator buffer back to rank 0
+      auto release = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0 + ab * 8u);
+      };
+      // one 32-column chunk of this warp's 32 rows: alpha * v + beta * C
+      // stored in C's type, rows staged through shared memory so that each
+      // store instruction writes whole lines
+      auto store_chunk = [&](const float* v, int cc) {
         const int col_base = tc.nb * T::BN + cc * 32;
-        if (row_base >= p.m || col_base >= p.n) continue;
+        if (row_base >= p.m || col_base >= p.n) return;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
@@ -373,6 +372,62 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
           }
         }
         __syncwarp();
+      };
+      if (tc.tail < 0) {
+#pragma unroll 1
+        for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
+          float v[32];
+          tmem_ld_32cols(tacc + cc * 32, v);
+          tmem_ld_wait();
+          // the last chunk of this warp's share is in registers
+          if (cc == cc0 + kCcPer - 1) release();
+          store_chunk(v, cc);
+        }
+        continue;
+      }
+      // Half of the k range of a tile of the split tail.  Each warp writes
+      // its 32 x 128 piece of partial sums (chunk-major, one float4 per lane
+      // per store: whole lines) and counts itself; the second of the two
+      // halves to arrive adds the first's piece to its own and stores C.
+      // Both orders give the same sum (fp32 addition commutes).
+      const size_t piece = ((size_t)tc.tail * 2 + rank) * T::kEpiWarps + (size_t)(warp - 2);
+      constexpr int kPieceF4 = kCcPer * 8 * 32;
+      float4* own = reinterpret_cast<float4*>(p.tail_ws) + (piece * 2 + (size_t)tc.half) * kPieceF4;
+      const float4* other = reinterpret_cast<const float4*>(p.tail_ws) + (piece * 2 + (size_t)(tc.half ^ 1)) * kPieceF4;
+#pragma unroll 1
+      for (int j = 0; j < kCcPer; ++j) {
+        float v[32];
+        tmem_ld_32cols(tacc + (cc0 + j) * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          own[(j * 8 + i) * 32 + lane] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+      __threadfence();
+      __syncwarp();
+      uint32_t prev = 0;
+      if (lane == 0) prev = atomicAdd(p.tail_cnt + piece, 1u);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == 0) {
+        release();   // the other half finishes this piece
+        continue;
+      }
+      __threadfence();
+#pragma unroll 1
+      for (int j = 0; j < kCcPer; ++j) {
+        float v[32];
+        tmem_ld_32cols(tacc + (cc0 + j) * 32, v);
+        tmem_ld_wait();
+        if (j == kCcPer - 1) release();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 o = __ldcg(other + (j * 8 + i) * 32 + lane);
+          v[4 * i] += o.x;
+          v[4 * i + 1] += o.y;
+          v[4 * i + 2] += o.z;
+          v[4 * i + 3] += o.w;
+        }
+        store_chunk(v, cc0 + j);
       }
     }
   }

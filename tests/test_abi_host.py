@@ -27,7 +27,7 @@ def test_version_and_options_init(L):
     assert L.mpg_version() >= 100
     o = mpg.options()
     assert (o.split_exp_a, o.split_exp_b, o.splitk, o.force_generic_load, o.tile_n, o.wait_timeout_ns,
-            o.split_chunk_k, o.prepass, o.c_dtype, o.cta_pair) == (0,) * 10
+            o.split_chunk_k, o.prepass, o.c_dtype, o.cta_pair, o.tail_split) == (0,) * 11
 
 
 # ---------------------------------------------------------------- validation
@@ -73,6 +73,8 @@ def test_option_ranges_rejected(L):
     assert _call(opts=mpg.options(cta_pair=2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(cta_pair=-2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(c_dtype=3)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(tail_split=2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(tail_split=-2)) == mpg.ERR_INVALID_ARG
 
 
 def test_host_entry_rejects_a_small_workspace_before_any_copy(L):
@@ -102,10 +104,51 @@ def test_alpha_zero_does_not_need_operands(L):
     assert st in (mpg.OK, mpg.ERR_NO_DEVICE)
 
 
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def _tail_bytes(tiles):
+    # two halves of fp32 partial sums per 256 x 256 tile, one counter per
+    # epilogue warp piece (16 per tile)
+    return _align256(tiles * 2 * 256 * 256 * 4) + _align256(tiles * 16 * 4)
+
+
+SMS = 152   # the queries' SM count without a device
+
+
 def test_workspace_size_is_zero_for_large_problems(L):
-    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC) == 0
+    # nothing but the split tail's partial sums, which tail_split = -1 drops
+    never = mpg.options(tail_split=-1)
+    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC, never) == 0
+    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.TF32) == 0
     assert mpg.workspace_size(0, 8, 8, 1, mpg.TF32) == 0
     assert mpg.workspace_size(64, 64, 64, 1, mpg.FP32_FFMA) == 0
+
+
+def test_workspace_holds_the_split_tail(L):
+    # fp16 / bf16 products with 1 to 6 full rounds of 256 x 256 tiles on
+    # SMs / 2 clusters and k >= 8192: up to SMs / 4 tiles cut in two
+    q = _tail_bytes(SMS // 4)
+    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC) == q      # 100 tiles
+    assert mpg.workspace_size(4096, 4096, 8192, 1, mpg.FP16_F32ACC) == q      # 256 tiles
+    assert mpg.workspace_size(4096, 4096, 8191, 1, mpg.FP16_F32ACC) == q      # 128 k-blocks
+    assert mpg.workspace_size(4096, 4096, 8128, 1, mpg.FP16_F32ACC) == 0      # 127 k-blocks
+    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC) == 0      # 13 rounds
+    assert mpg.workspace_size(2048, 2048, 8192, 1, mpg.BF16_F32ACC) == 0      # 64 tiles: no full round
+    # forced: up to SMs / 2 tiles, at any size
+    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC,
+                              mpg.options(tail_split=1)) == _tail_bytes(SMS // 2)
+    assert mpg.workspace_size(512, 512, 256, 1, mpg.BF16_F32ACC, mpg.options(tail_split=1)) > 0
+    # never; single-CTA tiles only (cta_pair = -1); a mode that never takes pairs
+    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC, mpg.options(tail_split=-1)) == 0
+    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC, mpg.options(cta_pair=-1)) == 0
+    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.SPLIT_FP16_1CHAIN, mpg.options(prepass=-1)) == 0
+    # the tail follows the other regions: the conversion pass's copies first
+    with_pass = mpg.workspace_size(2560, 2560, 8192, 1, mpg.FP16_F32ACC, mpg.options(prepass=1))
+    pass_only = mpg.workspace_size(2560, 2560, 8192, 1, mpg.FP16_F32ACC, mpg.options(prepass=1, tail_split=-1))
+    assert pass_only >= 2 * 2 * 2560 * 8192
+    assert with_pass == _align256(pass_only) + q
 
 
 def test_workspace_size_for_skinny_long_k(L):
@@ -274,20 +317,29 @@ def test_workspace_includes_the_conversion_pass_when_the_library_takes_it(L):
     assert ws >= 2 * 4 * n * n
     assert mpg.workspace_size(n, n, n, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(prepass=-1)) == 0
     assert mpg.workspace_size(256, 256, 256, 1, mpg.SPLIT_FP16_3CHAIN) == 0
-    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC) == 0          # fp16 mode: opt-in only
+    never = mpg.options(tail_split=-1)
+    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, never) == 0   # fp16 mode: opt-in only
     assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, mpg.options(prepass=1)) >= 2 * 2 * n * n
     assert _call(opts=mpg.options(prepass=2)) == mpg.ERR_INVALID_ARG
 
 
 def test_exact_query_includes_the_pass_for_fp16_modes_on_fp32_operands(L):
     n = 4096
-    plain = mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC)
+    nt = mpg.options(tail_split=-1)     # without the split tail's partial sums
+    plain = mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, nt)
     exact = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
-                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC)
+                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC, nt)
     assert plain == 0 and exact >= 2 * 2 * n * n            # fp16 copies of A and B
     exact16 = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F16, mpg.ROW_MAJOR, 256, n, 0, mpg.F16,
-                                    mpg.ROW_MAJOR, mpg.FP16_F32ACC)
+                                    mpg.ROW_MAJOR, mpg.FP16_F32ACC, nt)
     assert exact16 == 0                                      # fp16 operands: nothing to convert
     never = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
-                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC, mpg.options(prepass=-1))
+                                  mpg.ROW_MAJOR, mpg.FP16_F32ACC, mpg.options(prepass=-1, tail_split=-1))
     assert never == 0
+    # with the split tail (k >= 8192): it follows the copies
+    k = 8192
+    copies = mpg.workspace_size_ex(n, n, k, 1, 256, k, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
+                                   mpg.ROW_MAJOR, mpg.FP16_F32ACC, nt)
+    full = mpg.workspace_size_ex(n, n, k, 1, 256, k, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
+                                 mpg.ROW_MAJOR, mpg.FP16_F32ACC)
+    assert copies >= 2 * (n * k + k * n) and full == _align256(copies) + _tail_bytes(SMS // 4)

@@ -95,3 +95,93 @@ def test_pair_full_size_bf16_8192_beta(capsys):
     with capsys.disabled():
         print(f"\n[pair bf16 8192^3: sampled {err:.3e}, rows {err_rows:.3e}]")
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
+
+
+# ---------------------------------------------------------------- split tail
+@pytest.mark.parametrize("m,n,k,mode,dt,al,bl,batch", [
+    (300, 520, 200, mpg.BF16_F32ACC, "bf16", R, R, 1),     # ragged k: 4 k-blocks, cut after 2
+    (520, 300, 1000, mpg.FP16_F32ACC, "f16", Cm, R, 1),
+    (200, 300, 520, mpg.BF16_F32ACC, "bf16", R, Cm, 3),
+    (256, 256, 128, mpg.FP16_F32ACC, "f16", Cm, Cm, 2),    # two k-blocks: one each
+])
+def test_pair_split_tail_forced(m, n, k, mode, dt, al, bl, batch):
+    """tail_split = 1 with fewer tiles than clusters: every tile is cut in
+    two along K and the second half to finish adds the first's partial sums."""
+    mpg.build()
+    c = Case(m, n, k, mode, batch=batch, in_dtype=dt, a_layout=al, b_layout=bl, pad=(8, 0, 4), alpha=1.5,
+             beta=-0.5, dist="normal", opts=pair(tail_split=1))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"], eQ
+
+
+def test_pair_split_tail_is_deterministic_and_sixteen_bit_output():
+    import torch
+    mpg.build()
+    m, n, k = 300, 520, 700
+    a = synthetic.normal((m, k), 131)
+    b = synthetic.normal((k, n), 132)
+    A = torch.from_numpy(a).cuda().to(torch.bfloat16)
+    B = torch.from_numpy(b).cuda().to(torch.bfloat16)
+    outs = []
+    for _ in range(3):
+        C = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+        mpg.gemm(A, B, C, mode="bf16", opts=pair(tail_split=1))
+        outs.append(C.cpu().numpy())
+    # the two halves meet in either order with the same sum
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
+    ref, den = oracle.gemm(A.float().cpu().numpy(), B.float().cpu().numpy())
+    assert oracle.max_rel_err(outs[0], ref, den) <= TOL["q16"]
+    # a 16-bit C: alpha * (half + half) + beta * C rounded once
+    c0 = synthetic.uniform((m, n), 133).astype(np.float16)
+    C16 = torch.from_numpy(c0).cuda()
+    mpg.gemm(A, B, C16, alpha=0.75, beta=0.5, mode="bf16", opts=pair(tail_split=1))
+    got = C16.float().cpu().numpy().astype(np.float64)
+    ref, den = oracle.gemm(A.float().cpu().numpy(), B.float().cpu().numpy(), c0.astype(np.float32), 0.75, 0.5)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -14))) - 10)
+    assert np.all(np.abs(got - ref) <= ulp + TOL["q16"] * den)
+
+
+def test_pair_split_tail_needs_its_workspace():
+    import torch
+    mpg.build()
+    A = torch.zeros((300, 200), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((200, 520), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((300, 520), dtype=torch.float32, device="cuda")
+    st = mpg.gemm_raw(300, 520, 200, 1, A.data_ptr(), 200, 0, mpg.BF16, R, B.data_ptr(), 520, 0, mpg.BF16, R,
+                      C.data_ptr(), 520, 0, 1.0, 0.0, mpg.BF16_F32ACC, opts=pair(tail_split=1), check=False)
+    assert st == mpg.ERR_WORKSPACE and "split tail" in mpg.last_error()
+
+
+def test_pair_split_tail_by_default_on_the_last_round(capsys):
+    """2560 x 2560 x 8192 bf16: 100 tiles of 256 x 256, one full round on the
+    device's clusters and a partial last round, which the library cuts in two
+    along K by default (k >= 8192).  Against tail_split = -1 the tiles of the
+    full round agree bit for bit, those of the last round differ in rounding
+    only, and both products meet the oracle's bar on sampled points, among
+    them 64 in every tile that was cut."""
+    mpg.build()
+    m = n = 2560
+    k = 8192
+    out = {}
+    for ts in (0, -1):
+        c = Case(m, n, k, mpg.BF16_F32ACC, in_dtype="bf16", dist="normal", beta=0.5, opts=pair(tail_split=ts))
+        c.run()
+        out[ts] = c.result()[0]
+    tiles = m // 256
+    cut = [(i, j) for i in range(tiles) for j in range(tiles)
+           if not np.array_equal(out[0][256 * i:256 * (i + 1), 256 * j:256 * (j + 1)].view(np.uint32),
+                                 out[-1][256 * i:256 * (i + 1), 256 * j:256 * (j + 1)].view(np.uint32))]
+    # R tiles after W >= 1 full rounds of P clusters, 2R <= P: R <= 100 / 3
+    assert 1 <= len(cut) and 3 * len(cut) <= tiles * tiles, len(cut)
+    rows, cols = sample_points(m, n, 2000, 141)
+    g = np.random.Generator(np.random.PCG64(142))
+    for (i, j) in cut:
+        rows = np.concatenate([rows, 256 * i + g.integers(0, 256, 64)])
+        cols = np.concatenate([cols, 256 * j + g.integers(0, 256, 64)])
+    ref, den = c.reference_points(oracle.Q_NONE, 0, rows, cols)
+    errs = {ts: oracle.max_rel_err(out[ts][rows, cols], ref, den) for ts in out}
+    with capsys.disabled():
+        print(f"\n[split tail 2560^2 x 8192: {len(cut)} tiles cut; errors {errs}]")
+    assert max(errs.values()) <= TOL["q16"], errs
