@@ -154,9 +154,10 @@ typedef struct {
    * operands: a matrix instruction still needs a layout contract", third
    * paragraph). */
   int32_t c_dtype;
-  /* CTA pairs for 16-bit products on the direct TMA path (FP16 / BF16
-   * operands, or the copies of the separate conversion pass): a cluster of
-   * two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
+  /* CTA pairs for 16-bit and TF32 products on the direct TMA path (FP16 /
+   * BF16 operands, TF32 with a row-major A and a column-major B, or the
+   * copies made by the conversion pass or the aligned-copy path): a cluster
+   * of two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
    * tensor-core instructions, each CTA holding half of A's rows and half of
    * B's columns; the same products, accumulated in fp32 on the tensor cores
    * along K in the same order.  0 (default) = used when the 256 x 256 tiles
@@ -174,7 +175,8 @@ typedef struct {
    * mpg_gemm_workspace_size reports (at most 128 x 256 x 4 bytes per SM plus
    * counters) and clears its counters with one cudaMemsetAsync per call.
    *   0 (default) = where it pays on a GB300: 1 to 6 full rounds, then
-   *       1 <= R <= P/2 tiles, and k >= 8192 (half a tile's time outweighs
+   *       1 <= R <= P/2 tiles, and at least 128 k-blocks (k >= 8192, tf32
+   *       k >= 4096: half a tile's time outweighs
    *       waiting for the later of two clusters and exchanging the partial
    *       sums, about 16 us), when the workspace holds it;
    *   1 = whenever the tile count is not a multiple of P (all tiles when
@@ -262,10 +264,10 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
 
 /* Bytes of workspace mpg_gemm / mpg_gemm_ex need for this problem (0 if none).
  * Depends only on the sizes, the mode, the options and the current device.
- * For the fp16 / bf16 modes it includes the split tail's partial sums
+ * For the fp16 / bf16 / tf32 modes it includes the split tail's partial sums
  * (mpg_options.tail_split) when the library may take it (1 to 6 full rounds
- * of 256 x 256 tiles on SMs / 2 clusters, k >= 8192): up to SMs / 4 tiles x
- * 512 KiB, about 20 MB on 152 SMs. */
+ * of 256 x 256 tiles on SMs / 2 clusters, k >= 8192, tf32 k >= 4096): up to
+ * SMs / 4 tiles x 512 KiB, about 20 MB on 152 SMs. */
 size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch,
                                mpg_precision mode, const mpg_options* opt);
 

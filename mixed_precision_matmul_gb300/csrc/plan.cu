@@ -42,12 +42,13 @@ size_t tail_bytes(int64_t tiles) {
 }
 
 // The library's choice of the split tail for `tiles` pair tiles on P
-// clusters and num_k_blk k-blocks of 64.  Cutting the last round's tiles in
-// two saves half a tile's time but pairs two clusters' halves: the second
+// clusters and num_k_blk k-blocks (64 elements, 32 for tf32).  Cutting the
+// last round's tiles in two saves half a tile's time but pairs two
+// clusters' halves: the second
 // half waits for the later of the two (the clusters drift apart over the
 // earlier rounds) and then exchanges 128 KB of partial sums per CTA, about
-// 16 us in all on a GB300.  So: at least 128 k-blocks (k >= 8192: a tile
-// takes about 50 us), at most 6 full rounds before the tail (more, and the
+// 16 us in all on a GB300.  So: at least 128 k-blocks (k >= 8192 for 16-bit
+// operands, 4096 for tf32: a tile takes about 50 us), at most 6 full rounds before the tail (more, and the
 // one partial round is a small share of the time), and a last round of at
 // most P / 2 tiles, so that every half finds a cluster.
 bool tail_auto(int64_t tiles, int64_t P, int64_t num_k_blk) {
@@ -57,16 +58,20 @@ bool tail_auto(int64_t tiles, int64_t P, int64_t num_k_blk) {
 
 // The most split-tail workspace a call may take: at most a quarter of the
 // SMs' worth of tiles by default (2R <= P <= SMs / 2 clusters), half with
-// tail_split = 1; only the fp16 / bf16 modes reach the pair kernel.
+// tail_split = 1; only the fp16 / bf16 / tf32 modes reach the pair kernel
+// (k-blocks of 64 elements, 32 for tf32).
 size_t tail_bound(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, int sm_count,
                   const mpg_options& o) {
-  if (o.tail_split < 0 || (mode != MPG_FP16_F32ACC && mode != MPG_BF16_F32ACC) || o.cta_pair < 0) return 0;
+  if (o.tail_split < 0 || (mode != MPG_FP16_F32ACC && mode != MPG_BF16_F32ACC && mode != MPG_TF32) ||
+      o.cta_pair < 0)
+    return 0;
+  const int64_t bk = (mode == MPG_TF32) ? 32 : 64;
   if (o.tail_split == 1) return tail_bytes(std::max(sm_count / 2, 1));
   // the clusters resident at launch are at most SMs / 2, so a product this
   // query leaves out has more than 6 full rounds at launch too
   const int64_t P = std::max(sm_count / 2, 1);
   const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
-  if (pair_tiles < P || pair_tiles / P > 6 || (k + 63) / 64 < 128) return 0;
+  if (pair_tiles < P || pair_tiles / P > 6 || (k + bk - 1) / bk < 128) return 0;
   return tail_bytes(std::max(sm_count / 4, 1));
 }
 
@@ -288,12 +293,12 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = o.tile_n;
   }
   p.bn = bn;
-  // CTA pairs: 16-bit operands on the direct path (also the conversion
-  // pass's copies), 256 x 256 tiles.  Chosen by the library when those tiles
-  // give every pair of SMs at least one (a smaller problem keeps the finer
-  // 128-row tiles), or forced with cta_pair = 1.
-  const bool pair_ok = p.src == Src::kTmaDirect && p.conv == Conv::kNone && p.op != Op::kTF32 &&
-                       (o.tile_n == 0 || o.tile_n == 256);
+  // CTA pairs: 16-bit or tf32 operands on the direct path (also the
+  // conversion pass's and the aligned copies), 256 x 256 tiles.  Chosen by
+  // the library when those tiles give every pair of SMs at least one (a
+  // smaller problem keeps the finer 128-row tiles), or forced with
+  // cta_pair = 1.
+  const bool pair_ok = p.src == Src::kTmaDirect && p.conv == Conv::kNone && (o.tile_n == 0 || o.tile_n == 256);
   const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
   if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && o.tile_n == 0 && pair_tiles * 2 >= sm_count))) {
     p.pair = true;

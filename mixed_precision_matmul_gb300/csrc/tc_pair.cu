@@ -1,4 +1,5 @@
-// The 16-bit tensor-core product on a pair of CTAs (sm_103a, cta_group::2).
+// The 16-bit and tf32 tensor-core product on a pair of CTAs (sm_103a,
+// cta_group::2).
 //
 // A cluster of two CTAs on two SMs computes one 256 x 256 tile of C with
 // tcgen05.mma.cta_group::2 (M = 256, N = 256): CTA rank r holds rows
@@ -33,14 +34,16 @@ namespace {
 
 template <Op O>
 struct PairTraits {
+  static constexpr Op kOp = O;
   static constexpr int BM = 128;    // rows of A held by one CTA
   static constexpr int BMP = 256;   // rows of the pair's tile
   static constexpr int BN = 256;    // columns of the pair's tile (the instruction's N)
   static constexpr int BNH = 128;   // columns of B held by one CTA
-  static constexpr int BK = 64;     // one 128-byte line of k per stage
+  static constexpr int kOpBytes = (O == Op::kTF32) ? 4 : 2;
+  static constexpr int BK = 128 / kOpBytes;   // one 128-byte line of k per stage (64, tf32 32)
   static constexpr int kRowBytes = 128;
   static constexpr uint32_t kSwizzle = kSwizzle128B;
-  static constexpr int kInstrK = 16;
+  static constexpr int kInstrK = 32 / kOpBytes;   // k of one MMA: 16 (tf32 8)
   static constexpr int kKSteps = BK / kInstrK;
   static constexpr int kATile = BM * kRowBytes;
   static constexpr int kBTile = BNH * kRowBytes;
@@ -56,7 +59,7 @@ struct PairTraits {
   static constexpr int kSmemBytes = 1024 + kStages * kOpStage + kEpiBytes + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kAccBufs * kAccStride <= kTmemCols, "TMEM budget");
-  static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : 1u;
+  static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : (O == Op::kBF16) ? 1u : 2u;
 };
 
 // ---------------------------------------------------------------------------
@@ -126,14 +129,24 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+template <Op O>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  if constexpr (O == Op::kTF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // One arrival on the barrier at this offset in every CTA of `mask`, once all
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
           const uint32_t b_tile = a_tile + T::kATile;
 #pragma unroll
           for (int ks = 0; ks < T::kKSteps; ++ks)
-            mma_f16_pair(d0, operand_desc<T>(a_tile, a_mn, ks), operand_desc<T>(b_tile, b_mn, ks), idesc,
+            mma_pair<T::kOp>(d0, operand_desc<T>(a_tile, a_mn, ks), operand_desc<T>(b_tile, b_mn, ks), idesc,
                          (kb > tc.kb0 || ks > 0) ? 1u : 0u);
           mma_commit_multicast(&op_empty[st], 0x3);
         }
@@ -457,6 +470,7 @@ bool tc_lookup_pair(Op op, TcKernel* out) {
   switch (op) {
     case Op::kF16: pair_fill<PairTraits<Op::kF16>>(out); return true;
     case Op::kBF16: pair_fill<PairTraits<Op::kBF16>>(out); return true;
+    case Op::kTF32: pair_fill<PairTraits<Op::kTF32>>(out); return true;
     default: return false;
   }
 }

@@ -135,6 +135,8 @@ def test_workspace_holds_the_split_tail(L):
     assert mpg.workspace_size(4096, 4096, 8191, 1, mpg.FP16_F32ACC) == q      # 128 k-blocks
     assert mpg.workspace_size(4096, 4096, 8128, 1, mpg.FP16_F32ACC) == 0      # 127 k-blocks
     assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC) == 0      # 13 rounds
+    assert mpg.workspace_size(4096, 4096, 4096, 1, mpg.TF32) == q             # tf32: 128 k-blocks of 32
+    assert mpg.workspace_size(4096, 4096, 4064, 1, mpg.TF32) == 0
     assert mpg.workspace_size(2048, 2048, 8192, 1, mpg.BF16_F32ACC) == 0      # 64 tiles: no full round
     # forced: up to SMs / 2 tiles, at any size
     assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC,

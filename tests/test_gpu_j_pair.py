@@ -185,3 +185,31 @@ def test_pair_split_tail_by_default_on_the_last_round(capsys):
     with capsys.disabled():
         print(f"\n[split tail 2560^2 x 8192: {len(cut)} tiles cut; errors {errs}]")
     assert max(errs.values()) <= TOL["q16"], errs
+
+
+# ---------------------------------------------------------------- tf32 pairs
+@pytest.mark.parametrize("al,bl", [(R, Cm), (R, R), (Cm, Cm)])
+@pytest.mark.parametrize("m,n,k,batch", [(300, 520, 200, 1), (520, 272, 1000, 2), (256, 256, 32, 1)])
+def test_pair_tf32(al, bl, m, n, k, batch):
+    """tf32 on CTA pairs (cta_group::2, kind::tf32), row-major A and column-
+    major B on the direct path, other layouts through the transposed copies."""
+    mpg.build()
+    c = Case(m, n, k, mpg.TF32, batch=batch, a_layout=al, b_layout=bl, pad=(4, 8, 4), alpha=1.5, beta=-0.5,
+             dist="normal", opts=pair())
+    c.run(exact_ws=True)
+    eR, _ = c.errors()
+    assert eR <= TOL["tf32"], eR
+
+
+@pytest.mark.parametrize("mode,dt", [(mpg.TF32, "f32"), (mpg.BF16_F32ACC, "bf16")])
+def test_pair_matches_single_cta_bit_for_bit(mode, dt):
+    """The pair form multiplies the same products in the same K order as
+    the one-CTA form: the results agree bit for bit."""
+    mpg.build()
+    out = {}
+    for cp in (1, -1):
+        c = Case(520, 784, 1000, mode, in_dtype=dt, a_layout=R, b_layout=Cm, beta=0.5, dist="normal",
+                 opts=mpg.options(cta_pair=cp))
+        c.run(exact_ws=True)
+        out[cp] = c.result()
+    assert np.array_equal(out[1].view(np.uint32), out[-1].view(np.uint32))
