@@ -160,8 +160,10 @@ typedef struct {
    * of two CTAs on two SMs computes a 256 x 256 tile with cta_group::2
    * tensor-core instructions, each CTA holding half of A's rows and half of
    * B's columns; the same products, accumulated in fp32 on the tensor cores
-   * along K in the same order.  0 (default) = used when the 256 x 256 tiles
-   * give every pair of SMs at least one tile, 1 = always where it applies,
+   * along K in the same order.  0 (default) = used when m > 128, n > 128
+   * and the 256 x 256 tiles give every pair of SMs at least one tile (many
+   * small batched products keep the finer one-CTA tiles), 1 = always where
+   * it applies,
    * -1 = never (one CTA per 128-row tile).  Other configurations ignore it. */
   int32_t cta_pair;
   /* Split tail for the CTA-pair kernel.  A persistent grid of P clusters

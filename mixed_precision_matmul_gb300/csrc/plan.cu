@@ -71,7 +71,7 @@ size_t tail_bound(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision 
   // query leaves out has more than 6 full rounds at launch too
   const int64_t P = std::max(sm_count / 2, 1);
   const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
-  if (pair_tiles < P || pair_tiles / P > 6 || (k + bk - 1) / bk < 128) return 0;
+  if (m <= 128 || n <= 128 || pair_tiles < P || pair_tiles / P > 6 || (k + bk - 1) / bk < 128) return 0;
   return tail_bytes(std::max(sm_count / 4, 1));
 }
 
@@ -295,12 +295,15 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   p.bn = bn;
   // CTA pairs: 16-bit or tf32 operands on the direct path (also the
   // conversion pass's and the aligned copies), 256 x 256 tiles.  Chosen by
-  // the library when those tiles give every pair of SMs at least one (a
-  // smaller problem keeps the finer 128-row tiles), or forced with
-  // cta_pair = 1.
+  // the library when those tiles give every pair of SMs at least one and
+  // the product is wider and taller than 128 (where the one-CTA kernel
+  // would take 128 x 256 tiles too: narrower products, e.g. many small
+  // batched ones, keep the finer tiles instead of multiplying padding), or
+  // forced with cta_pair = 1.
   const bool pair_ok = p.src == Src::kTmaDirect && p.conv == Conv::kNone && (o.tile_n == 0 || o.tile_n == 256);
   const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
-  if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && o.tile_n == 0 && pair_tiles * 2 >= sm_count))) {
+  if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && o.tile_n == 0 && m > 128 && n > 128 &&
+                                      pair_tiles * 2 >= sm_count))) {
     p.pair = true;
     p.bn = 256;
   }
