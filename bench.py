@@ -191,22 +191,27 @@ def time_steps(torch, fn, steps, warmup, stream):
     return start.elapsed_time(end)  # ms
 
 
-def time_graph(torch, fn, calls, reps, stream):
+def time_graph(torch, launch, calls, reps):
     """Device time per call of `calls` back-to-back calls captured once in a
-    CUDA graph and replayed `reps` times (CUDA events on `stream`): the
-    launch cost of small products without the host's per-call work."""
+    CUDA graph and replayed `reps` times (CUDA events on the capture stream):
+    the launch cost of small products without the host's per-call work.
+    `launch(stream_handle)` issues one call on the given stream."""
+    stream = torch.cuda.Stream()    # capture needs a stream other than the default one
+    launch(stream.cuda_stream)      # outside the capture: one-time setup of the call
+    torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for _ in range(calls):
-            fn()
-    g.replay()
-    torch.cuda.synchronize()
+            launch(stream.cuda_stream)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):   # replays launch on the current stream
         g.replay()
-    end.record(stream)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / (calls * reps)
 
@@ -599,8 +604,7 @@ def ours(args):
                 # (argument checks, planning, tensor maps, the launch): the
                 # same calls replayed from a CUDA graph show the device time
                 try:
-                    gms = time_graph(torch, lambda: run_step(mpg, mw, Cm, ws.data_ptr(), ws_bytes, sh), 20, 10,
-                                     stream)
+                    gms = time_graph(torch, lambda h: run_step(mpg, mw, Cm, ws.data_ptr(), ws_bytes, h), 20, 10)
                     entry["graph_ms"] = round(gms, 5)
                     entry["graph_tflops"] = round(mw.flops / (gms * 1e-3) / 1e12, 2)
                 except RuntimeError as e:

@@ -430,6 +430,20 @@ mpg_status mpg_probe_mma_m16n8k16(const void* A, const void* B, float* D, void* 
  * fragment maps on the hardware.  D as above (device pointers, C = 0). */
 mpg_status mpg_probe_mma_m16n8k16_fragments(const uint32_t* Afrag, const uint32_t* Bfrag, float* D, void* stream);
 
+/* Probe of the epilogue's shared-memory staging, for measuring its bank
+ * conflicts apart from the tensor core's and TMA's shared-memory traffic
+ * (the swizzled shared layouts of "tile_matmul(): use the cuBLASDx
+ * register-accumulator API ...", "Proposed change").  `blocks` blocks of
+ * 32 x 32 fp32 (row-major, packed, 4 KB each) are copied from `in` to `out`
+ * through the staging buffer of one warp, with the product epilogues' own
+ * code: each lane writes one row, then the warp reads the block back by
+ * 16-byte chunks of rows (scalar = 0, the vector-store path) or by columns
+ * (scalar = 1, the scalar path of unaligned destinations).  out equals in on
+ * return.  in, out: device pointers, 16-byte aligned, blocks * 1024 floats
+ * each, not overlapping; blocks in [0, 2^40].  MPG_ERR_INVALID_ARG for bad
+ * arguments, before any launch. */
+mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t blocks, int scalar, void* stream);
+
 /* Failure-detection self test: launches one kernel whose single wait is on an
  * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then
  * synchronises.  Returns MPG_ERR_TIMEOUT when the kernel gave up the wait and

@@ -144,6 +144,8 @@ def lib():
             getattr(L, nm).restype = i32
         L.mpg_probe_mma_m16n8k16_fragments.argtypes = [vp, vp, vp, vp]
         L.mpg_probe_mma_m16n8k16_fragments.restype = i32
+        L.mpg_probe_epilogue_staging.argtypes = [vp, vp, ctypes.c_int64, i32, vp]
+        L.mpg_probe_epilogue_staging.restype = i32
         L.mpg_selftest_wait_timeout.argtypes = [i64, vp]
         L.mpg_selftest_wait_timeout.restype = i32
         _lib = L
@@ -509,6 +511,19 @@ def probe_mma_m16n8k16_fragments(a_frag, b_frag, stream=None):
     _check(lib().mpg_probe_mma_m16n8k16_fragments(a.data_ptr(), b.data_ptr(), d.data_ptr(),
                                                    _stream_handle(stream)))
     return d
+
+
+def probe_epilogue_staging(blocks_in, scalar=False, stream=None):
+    """Copy (nblocks, 32, 32) fp32 blocks through the epilogue's staging
+    layout (mpg_probe_epilogue_staging); returns the copy."""
+    torch = _torch()
+    x = blocks_in.to(torch.float32).contiguous()
+    if x.numel() % 1024 != 0:
+        raise ValueError("blocks of 32 x 32 floats expected")
+    out = torch.empty_like(x)
+    _check(lib().mpg_probe_epilogue_staging(x.data_ptr(), out.data_ptr(), x.numel() // 1024, 1 if scalar else 0,
+                                            _stream_handle(stream)))
+    return out
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> int:

@@ -323,6 +323,22 @@ mpg_status mpg_probe_mma_m16n8k16_fragments(const uint32_t* Afrag, const uint32_
   return MPG_OK;
 }
 
+mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t blocks, int scalar, void* stream) {
+  t_err.clear();
+  if (blocks < 0 || blocks > ((int64_t)1 << 40)) return fail(MPG_ERR_INVALID_ARG, "blocks outside [0, 2^40]");
+  if (blocks == 0) return MPG_OK;
+  if (!in || !out) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(in) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 16 != 0)
+    return fail(MPG_ERR_INVALID_ARG, "in and out must be 16-byte aligned");
+  if (scalar != 0 && scalar != 1) return fail(MPG_ERR_INVALID_ARG, "scalar must be 0 or 1");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = launch_probe_staging(in, out, blocks, scalar, dev->sm_count, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
 mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
   t_err.clear();
   if (timeout_ns < 1000000 || timeout_ns > 10000000000ll)

@@ -1,9 +1,13 @@
 // Small kernels around the main product: the device status word, C = beta*C
 // (k == 0 or alpha == 0), the split-K reduction, the mma.sync m16n8k16
-// accumulator-layout probe and the bounded-wait self test.
+// accumulator-layout probe, the epilogue-staging probe and the bounded-wait
+// self test.
+#include <algorithm>
+
 #include "internal.h"
 #include "outio.cuh"
 #include "ptx.cuh"
+#include "staging.cuh"
 
 namespace mpg {
 
@@ -150,6 +154,54 @@ cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_
 
 cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream) {
   probe_mma_frag_kernel<<<1, 32, 0, stream>>>(a, b, d);
+  return cudaGetLastError();
+}
+
+// Epilogue-staging probe: warp w of the grid moves blocks of 32 x 32 fp32
+// (row-major, packed, 4 KB each) from `in` to `out` through its staging
+// buffer exactly as the product epilogues do after tcgen05.ld: lane l holds
+// row l and writes it, then the warp reads the block back by 16-byte chunks
+// of rows (vector stores) or by columns (scalar stores).  Nothing else uses
+// shared memory meanwhile, so the profiler's bank-conflict counters see the
+// staging pattern alone.
+__global__ void __launch_bounds__(256) probe_staging_kernel(const float* __restrict__ in, float* __restrict__ out,
+                                                             int64_t blocks, int scalar) {
+  __shared__ __align__(16) float stg_all[8][1024];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t stg = smem_addr(stg_all[warp]);
+  for (int64_t b = (int64_t)blockIdx.x * 8 + warp; b < blocks; b += (int64_t)gridDim.x * 8) {
+    const float* src = in + b * 1024;
+    float* dst = out + b * 1024;
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(src + lane * 32 + 4 * c));
+      v[4 * c] = x.x;
+      v[4 * c + 1] = x.y;
+      v[4 * c + 2] = x.z;
+      v[4 * c + 3] = x.w;
+    }
+    stage_write_row(stg, lane, v);
+    __syncwarp();
+    if (!scalar) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = i * 4 + (lane >> 3);
+        *reinterpret_cast<float4*>(dst + r * 32 + (lane & 7) * 4) = stage_read_chunk(stg, lane, i);
+      }
+    } else {
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) dst[r * 32 + lane] = stage_read_elem(stg, lane, r);
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, int scalar, int sm_count,
+                                 cudaStream_t stream) {
+  const int64_t grid = std::min<int64_t>((blocks + 7) / 8, (int64_t)sm_count * 8);
+  if (grid <= 0) return cudaSuccess;
+  probe_staging_kernel<<<(unsigned)grid, 256, 0, stream>>>(in, out, blocks, scalar);
   return cudaGetLastError();
 }
 

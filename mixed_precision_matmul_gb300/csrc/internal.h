@@ -164,6 +164,8 @@ cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t st
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
                            int sm_count, cudaStream_t stream);
 cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream);
+cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, int scalar, int sm_count,
+                                 cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Device status word of the current device (allocated by the runtime as a

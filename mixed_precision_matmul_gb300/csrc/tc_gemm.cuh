@@ -29,6 +29,7 @@
 #include "internal.h"
 #include "outio.cuh"
 #include "ptx.cuh"
+#include "staging.cuh"
 
 namespace mpg {
 
@@ -597,19 +598,14 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           if (row_base >= p.m || col_base >= p.n) continue;
           // transpose through a per-warp swizzled 32x32 staging tile so that
           // global stores are row-contiguous
-  #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            st_shared_v4(stg_addr + (uint32_t)((lane * 8 + (ch ^ (lane & 7))) * 16), __float_as_uint(v[4 * ch]),
-                         __float_as_uint(v[4 * ch + 1]), __float_as_uint(v[4 * ch + 2]),
-                         __float_as_uint(v[4 * ch + 3]));
-          }
+          stage_write_row(stg_addr, lane, v);
           __syncwarp();
           if (vec_ok && col_base + 32 <= p.n) {
   #pragma unroll
             for (int it = 0; it < 8; ++it) {
               const int r = it * 4 + (lane >> 3);
               const int ch = lane & 7;
-              const float4 x = ld_shared_f4(stg_addr + (uint32_t)((r * 8 + (ch ^ (r & 7))) * 16));
+              const float4 x = stage_read_chunk(stg_addr, lane, it);
               const int grow = row_base + r;
               if (grow < p.m) {
                 const int64_t idx = (int64_t)grow * ldo + col_base + ch * 4;
@@ -633,7 +629,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             const int gcol = col_base + lane;
   #pragma unroll 4
             for (int r = 0; r < 32; ++r) {
-              const float x = stg[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
+              const float x = stage_read_elem(stg_addr, lane, r);
               const int grow = row_base + r;
               if (grow < p.m && gcol < p.n) {
                 const int64_t idx = (int64_t)grow * ldo + gcol;

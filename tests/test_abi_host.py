@@ -77,6 +77,13 @@ def test_option_ranges_rejected(L):
     assert _call(opts=mpg.options(tail_split=-2)) == mpg.ERR_INVALID_ARG
 
 
+def test_staging_probe_arguments_rejected_before_launch(L):
+    assert L.mpg_probe_epilogue_staging(None, None, -1, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_epilogue_staging(None, None, 1, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_epilogue_staging(16, 32, 1, 5, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_epilogue_staging(None, None, 0, 0, None) == mpg.OK    # nothing to do
+
+
 def test_host_entry_rejects_a_small_workspace_before_any_copy(L):
     # host-buffer product: the workspace check precedes every copy and launch
     need = mpg.host_workspace_size(64, 64, 64, 1, 64, 0, mpg.F32, mpg.ROW_MAJOR, 64, 0, mpg.F32, mpg.ROW_MAJOR,
