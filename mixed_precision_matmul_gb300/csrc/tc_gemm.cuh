@@ -653,6 +653,79 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       using E = typename SE::type;
       const E* __restrict__ ga = reinterpret_cast<const E*>(p.a);
       const E* __restrict__ gb = reinterpret_cast<const E*>(p.b);
+      // Raw source values of one stage for this thread: fp32 values, or
+      // 16-bit codes (4 per chunk).
+      struct Raw {
+        float x[kPerThread][4];
+        unsigned short h[kPerThread][4];
+      };
+      // Generic source: read this thread's chunks of stage (tc, kb) from
+      // global memory (zero outside the matrix).
+      auto gather = [&](const TileCoord& tc, int kb, Raw& raw) {
+        const int k0 = kb * T::BK;
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+          const int wi = ct + i * T::kConvThreads;
+          const bool isA = wi < T::BM * 8;
+          const int wl = isA ? wi : wi - T::BM * 8;
+          const uint32_t lg = wl >> 3, ch = wl & 7;
+          const bool mn = isA ? p.a_mn_major : p.b_mn_major;
+          const int rows_lim = isA ? p.m : p.n;
+          const int row0 = isA ? tc.mb * T::BM : tc.nb * T::BN;
+          const int64_t ld = isA ? p.lda : p.ldb;
+          const E* g = (isA ? ga : gb) + (int64_t)tc.b * (isA ? p.stride_a : p.stride_b);
+          // the chunk's 4 elements are consecutive in memory: (row r0,
+          // k kk0..kk0+3) for K-major, (rows r0..r0+3, k kk0) for MN-major
+          int r0, kk0;
+          if (!mn) {
+            r0 = row0 + (int)lg;
+            kk0 = k0 + (int)ch * 4;
+          } else {
+            r0 = row0 + (int)(lg / T::BK) * T::BK + (int)ch * 4;
+            kk0 = k0 + (int)(lg % T::BK);
+          }
+          const int64_t idx0 = mn ? (int64_t)kk0 * ld + r0 : (int64_t)r0 * ld + kk0;
+          const bool whole = mn ? (r0 + 3 < rows_lim && kk0 < p.k) : (r0 < rows_lim && kk0 + 3 < p.k);
+          if (whole && (isA ? p.a_vec_ok : p.b_vec_ok)) {
+            // one aligned vector load (16 bytes of fp32, 8 of 16-bit codes)
+            if constexpr (T::kSrcT == SrcT::kF32) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(g + idx0));
+              raw.x[i][0] = v.x; raw.x[i][1] = v.y; raw.x[i][2] = v.z; raw.x[i][3] = v.w;
+              raw.h[i][0] = raw.h[i][1] = raw.h[i][2] = raw.h[i][3] = 0;
+            } else {
+              const uint2 v = __ldg(reinterpret_cast<const uint2*>(g + idx0));
+              raw.h[i][0] = (unsigned short)(v.x & 0xFFFFu); raw.h[i][1] = (unsigned short)(v.x >> 16);
+              raw.h[i][2] = (unsigned short)(v.y & 0xFFFFu); raw.h[i][3] = (unsigned short)(v.y >> 16);
+              raw.x[i][0] = raw.x[i][1] = raw.x[i][2] = raw.x[i][3] = 0.0f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = mn ? r0 + e : r0;
+              const int kk = mn ? kk0 : kk0 + e;
+              const bool in = (r < rows_lim) && (kk < p.k);
+              const int64_t idx = idx0 + e;
+              if constexpr (T::kSrcT == SrcT::kF32) {
+                raw.x[i][e] = in ? SE::load(g + idx) : 0.0f;
+                raw.h[i][e] = 0;
+              } else {
+                raw.h[i][e] = in ? SE::load(g + idx) : (unsigned short)0;
+                raw.x[i][e] = 0.0f;
+              }
+            }
+          }
+        }
+      };
+      // The generic source issues the next stage's loads before converting
+      // and storing the current one, so that one stage's global-memory
+      // latency overlaps the work of the previous stage.
+      Raw cur, nxt;
+      if constexpr (T::kSrc == Src::kGeneric) {
+        if ((int)blockIdx.x < p.num_tiles) {
+          const TileCoord tc = decode_tile(p, blockIdx.x);
+          if (tc.kb0 < tc.kb1) gather(tc, tc.kb0, cur);
+        }
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -660,13 +733,23 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
           const uint32_t st = it % T::kStages;
           const uint32_t ph = (it / T::kStages) & 1u;
+          if constexpr (T::kSrc == Src::kGeneric) {
+            if (kb + 1 < tc.kb1) {
+              gather(tc, kb + 1, nxt);
+            } else {
+              const int tn = t + (int)gridDim.x;
+              if (tn < p.num_tiles) {
+                const TileCoord tcn = decode_tile(p, tn);
+                if (tcn.kb0 < tcn.kb1) gather(tcn, tcn.kb0, nxt);
+              }
+            }
+          }
           if constexpr (T::kStaged) {
             if (!warp_wait(&stg_full[st], ph, ctl)) { ok = false; break; }
           }
           uint32_t w[kPerThread][4];
-          const int k0 = kb * T::BK;
-          // ---- gather (staging written by TMA, 128B-swizzled fp32; or
-          //      global memory) and convert into packed operand words
+          // ---- convert (staging written by TMA, 128B-swizzled fp32; or the
+          //      values gathered from global memory) into packed operand words
 #pragma unroll
           for (int i = 0; i < kPerThread; ++i) {
             const int wi = ct + i * T::kConvThreads;
@@ -681,54 +764,15 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
               h[0] = h[1] = h[2] = h[3] = 0;
             } else {
-              const bool mn = isA ? p.a_mn_major : p.b_mn_major;
-              const int rows_lim = isA ? p.m : p.n;
-              const int row0 = isA ? tc.mb * T::BM : tc.nb * T::BN;
-              const int64_t ld = isA ? p.lda : p.ldb;
-              const E* g = (isA ? ga : gb) + (int64_t)tc.b * (isA ? p.stride_a : p.stride_b);
-              // the chunk's 4 elements are consecutive in memory: (row r0,
-              // k kk0..kk0+3) for K-major, (rows r0..r0+3, k kk0) for MN-major
-              int r0, kk0;
-              if (!mn) {
-                r0 = row0 + (int)lg;
-                kk0 = k0 + (int)ch * 4;
-              } else {
-                r0 = row0 + (int)(lg / T::BK) * T::BK + (int)ch * 4;
-                kk0 = k0 + (int)(lg % T::BK);
-              }
-              const int64_t idx0 = mn ? (int64_t)kk0 * ld + r0 : (int64_t)r0 * ld + kk0;
-              const bool whole = mn ? (r0 + 3 < rows_lim && kk0 < p.k) : (r0 < rows_lim && kk0 + 3 < p.k);
-              if (whole && (isA ? p.a_vec_ok : p.b_vec_ok)) {
-                // one aligned vector load (16 bytes of fp32, 8 of 16-bit codes)
-                if constexpr (T::kSrcT == SrcT::kF32) {
-                  const float4 v = __ldg(reinterpret_cast<const float4*>(g + idx0));
-                  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-                  h[0] = h[1] = h[2] = h[3] = 0;
-                } else {
-                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(g + idx0));
-                  h[0] = (unsigned short)(v.x & 0xFFFFu); h[1] = (unsigned short)(v.x >> 16);
-                  h[2] = (unsigned short)(v.y & 0xFFFFu); h[3] = (unsigned short)(v.y >> 16);
-                  x[0] = x[1] = x[2] = x[3] = 0.0f;
-                }
-              } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int r = mn ? r0 + e : r0;
-                  const int kk = mn ? kk0 : kk0 + e;
-                  const bool in = (r < rows_lim) && (kk < p.k);
-                  const int64_t idx = idx0 + e;
-                  if constexpr (T::kSrcT == SrcT::kF32) {
-                    x[e] = in ? SE::load(g + idx) : 0.0f;
-                    h[e] = 0;
-                  } else {
-                    h[e] = in ? SE::load(g + idx) : (unsigned short)0;
-                    x[e] = 0.0f;
-                  }
-                }
+              for (int e = 0; e < 4; ++e) {
+                x[e] = cur.x[i][e];
+                h[e] = cur.h[i][e];
               }
             }
             pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, w[i], isA);
           }
+          if constexpr (T::kSrc == Src::kGeneric) cur = nxt;
           if constexpr (T::kStaged) {
             // Every staging value has been consumed by the conversion above,
             // so the reads are complete; order them before the TMA's
