@@ -37,7 +37,7 @@ SOURCES = [
     "tc_pair.cu",
     "attention.cu",
 ]
-HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh", "host.h"]
+HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh", "host.h", "staging.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
