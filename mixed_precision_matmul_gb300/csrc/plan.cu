@@ -278,7 +278,13 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   } else if (p.src == Src::kTmaDirect && p.conv == Conv::kNone) {
     bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
   } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2) {
-    bn = (n <= 64 || k <= 512) ? 64 : 128;
+    // 128-wide tiles hold one TMEM accumulator (chains and running sum
+    // fill the 512 columns), 64-wide tiles two.  Short K with few tiles
+    // (e.g. 256^3) takes the 64-wide ones for twice the tiles; short K with
+    // many tiles (the attention scores, 2048 x 32768 x 128: 16 % faster)
+    // and long K take the 128-wide ones, which read A once per 128 columns.
+    const int64_t tiles128 = batch * ((m + 127) / 128) * ((n + 127) / 128);
+    bn = (n <= 64 || (k <= 512 && tiles128 < sm_count)) ? 64 : 128;
   } else if (p.conv == Conv::kSplit1) {
     bn = n <= 64 ? 64 : 128;
   } else {
