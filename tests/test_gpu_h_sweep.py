@@ -54,3 +54,44 @@ def test_random_case(case):
         assert eQ <= TOL["q16"], (eR, eQ)
     if mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_4CHAIN):
         assert eR <= TOL["split"], eR
+
+
+PAIR_MODES = [(mpg.FP16_F32ACC, "f16"), (mpg.BF16_F32ACC, "bf16"), (mpg.TF32, "f32"), (mpg.FP16_F32ACC, "f32"),
+              (mpg.BF16_F32ACC, "f32")]
+
+
+def _pair_cases(n=30, seed=20252):
+    """Cases that take the CTA-pair kernel (cta_pair = 1) whenever their path
+    allows it, with the split tail forced, automatic or off."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for i in range(n):
+        mode, dt = PAIR_MODES[i % len(PAIR_MODES)]
+        m = int(g.integers(1, 700))
+        nn = int(g.integers(1, 700))
+        k = int(g.integers(1, 700))
+        batch = int(g.choice([1, 1, 2, 3]))
+        al = int(g.integers(0, 2))
+        bl = int(g.integers(0, 2))
+        pad = tuple(int(x) for x in g.choice([0, 0, 1, 8], size=3))
+        alpha = float(g.choice([1.0, -0.5, 2.0]))
+        beta = float(g.choice([0.0, 1.0, -0.75]))
+        tail = int(g.choice([-1, 0, 1]))
+        prepass = int(dt == "f32" and mode != mpg.TF32 and g.random() < 0.5)
+        out.append((i, mode, dt, m, nn, k, batch, al, bl, pad, alpha, beta, tail, prepass))
+    return out
+
+
+@pytest.mark.parametrize("case", _pair_cases(), ids=lambda c: f"p{c[0]}")
+def test_random_pair_case(case):
+    i, mode, dt, m, n, k, batch, al, bl, pad, alpha, beta, tail, prepass = case
+    mpg.build()
+    opts = mpg.options(cta_pair=1, tail_split=tail, prepass=prepass)
+    c = Case(m, n, k, mode, batch=batch, in_dtype=dt, a_layout=al, b_layout=bl, pad=pad,
+             alpha=alpha, beta=beta, seed=100 + i, dist="normal", opts=opts)
+    c.run(exact_ws=True)
+    eR, eQ = c.errors()
+    if mode == mpg.TF32:
+        assert eR <= TOL["tf32"], eR
+    else:
+        assert eQ <= TOL["q16"], (eR, eQ)
