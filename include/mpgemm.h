@@ -125,9 +125,11 @@ typedef struct {
    * elements.  Each chunk starts fresh hh / hl / lh accumulators on the tensor
    * cores; the epilogue adds the chunk's hh + 2^-11*(hl + lh) to an fp32
    * running sum with round-to-nearest.  This bounds how long the tensor
-   * cores' own fp32 accumulation runs (its rounding is not round-to-nearest,
-   * see the design notes).  0 = default (256); negative = one chunk covering
-   * the whole K range.  Rounded up to a multiple of 32. */
+   * cores' own fp32 accumulation runs (its rounding is not round-to-nearest).
+   * 0 = default: 512 for the three- and four-chain splits, one chunk for the
+   * A-only two-chain split (whose error is set by B's fp16 rounding);
+   * negative = one chunk covering the whole K range.  Rounded up to a
+   * multiple of the k-block (32 or 64). */
   int32_t split_chunk_k;
   /* The separate conversion pass for fp32 operands (FP16_F32ACC, BF16_F32ACC
    * and the split modes): one extra kernel reads A and B once and writes

@@ -22,7 +22,10 @@ mpg_status fail(mpg_status s, const char* fmt, ...);
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
-constexpr int64_t kDefaultSplitChunkK = 256;
+// K chunk of the three- and four-chain splits' accumulation: measured on
+// the log-uniform 4096^3 product, error vs FFMA 0.25x / 0.45x / 0.66x / 1.33x
+// for chunks of 256 / 512 / 1024 / 2048, speed 361 / 408 / 431 / 445 TFLOP/s.
+constexpr int64_t kDefaultSplitChunkK = 512;
 
 
 struct DeviceInfo {

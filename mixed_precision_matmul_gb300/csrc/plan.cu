@@ -577,8 +577,14 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.status = dev->status;
   p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
   p.chunk_kb = 0;
-  if ((plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplitA2 || plan.conv == Conv::kSplit4) &&
-      o.split_chunk_k >= 0) {
+  // K chunks of the split's accumulation: the default for the three- and
+  // four-chain splits; the A-only split takes one chunk by default (its
+  // error is set by B's fp16 rounding, 100x the tensor cores' accumulation
+  // error over the whole K), any of them the caller's chunk when given
+  const bool chunked = (plan.conv == Conv::kSplit3 || plan.conv == Conv::kSplit4) ? o.split_chunk_k >= 0
+                       : plan.conv == Conv::kSplitA2                             ? o.split_chunk_k > 0
+                                                                                 : false;
+  if (chunked) {
     const int64_t chunk_k = o.split_chunk_k > 0 ? o.split_chunk_k : kDefaultSplitChunkK;
     p.chunk_kb = (int32_t)std::min<int64_t>((chunk_k + BK - 1) / BK, p.num_k_blk);
   }
