@@ -564,6 +564,13 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               if constexpr (T::kConv == Conv::kSplit4) tmem_ld_16cols(tacc + 3 * T::BN + col, x3);
               if (have_run) tmem_ld_16cols(trun + col, r);
               tmem_ld_wait();
+              if (h == 1 && cc == cc0 + kCcPer - 1) {
+                // this warp's share of the chains is in registers: the next
+                // chunk's MMAs may overwrite them while the running sum (in
+                // columns of its own) is updated
+                tc_fence_before_sync();
+                mbar_arrive(&acc_empty[ab]);
+              }
   #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 // three chains: hh + 2^-11 (hl + lh); two chains (A-only split): hb + 2^-11 lb
@@ -580,18 +587,17 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             if (!last) {
               tmem_st_16cols(trun + cc * 32, v);
               tmem_st_16cols(trun + cc * 32 + 16, v + 16);
+              // the next fold reads these columns back
+              if (cc == cc0 + kCcPer - 1) tmem_st_wait();
             }
           } else {
             tmem_ld_32cols(tacc + cc * 32, v);
             tmem_ld_wait();
-          }
-          if (cc == cc0 + kCcPer - 1) {
-            // this warp's share of the chunk is now in registers / the running sum
-            if constexpr (T::kPromote) {
-              if (!last) tmem_st_wait();
+            if (cc == cc0 + kCcPer - 1) {
+              // this warp's share of the accumulator is in registers
+              tc_fence_before_sync();
+              mbar_arrive(&acc_empty[ab]);
             }
-            tc_fence_before_sync();
-            mbar_arrive(&acc_empty[ab]);
           }
           if (!last) continue;   // chunk folded into the running sum; nothing to store yet
           const int col_base = tc.nb * T::BN + cc * 32;
