@@ -26,6 +26,10 @@
  *     library never frees or retains them after the call returns.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Compute calls are asynchronous on that stream.
+ *   - Compute calls launch only stream-ordered work (kernels, and one
+ *     cudaMemsetAsync for the split tail), so they can be captured in CUDA
+ *     graphs; make the first call on a device outside a capture (it sets
+ *     kernel attributes and queries cluster occupancy once).
  *   - Every call returns an mpg_status; on failure the reason is available
  *     from mpg_last_error_string() (thread-local, valid until the next call
  *     on the same thread).  Argument errors are detected on the host before
