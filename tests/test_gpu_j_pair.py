@@ -217,3 +217,21 @@ def test_pair_matches_single_cta_bit_for_bit(mode, dt):
         c.run(exact_ws=True)
         out[cp] = c.result()
     assert np.array_equal(out[1].view(np.uint32), out[-1].view(np.uint32))
+
+
+@pytest.mark.parametrize("mode,dt,tail", [(mpg.BF16_F32ACC, "bf16", -1), (mpg.BF16_F32ACC, "bf16", 1),
+                                          (mpg.TF32, "f32", -1), (mpg.TF32, "f32", 1)])
+def test_pair_beta_zero_does_not_read_c(mode, dt, tail):
+    """beta == 0 on CTA pairs, whole tiles and split tail: NaN in C must not
+    leak into the result (C is written, never read)."""
+    mpg.build()
+    c = Case(300, 520, 400, mode, batch=2, in_dtype=dt, a_layout=R, b_layout=Cm, pad=(8, 8, 4), alpha=2.0,
+             beta=0.0, dist="normal", opts=pair(tail_split=tail))
+    c.C[:, :, :c.n] = float("nan")
+    c.c0[...] = 0.0
+    c.run(exact_ws=True)
+    eR, eQ = c.errors()
+    if mode == mpg.TF32:
+        assert eR <= TOL["tf32"], eR
+    else:
+        assert eQ <= TOL["q16"], eQ
