@@ -85,6 +85,7 @@ size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch);
 // halves of fp32 partial sums per 256 x 256 tile, then one counter per
 // epilogue warp piece; and its bound for the workspace queries.
 size_t tail_bytes(int64_t tiles);
+int pick_bn(int64_t m, int64_t n, int64_t batch, int splits, int sm_count, int widest);
 size_t tail_bound(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, int sm_count,
                   const mpg_options& o);
 bool tail_auto(int64_t tiles, int64_t clusters, int64_t num_k_blk);

@@ -37,6 +37,27 @@ size_t splitk_bytes(int splits, int64_t m, int64_t n, int64_t batch) {
   return splits > 1 ? (size_t)splits * (size_t)batch * (size_t)m * (size_t)n * sizeof(float) : 0;
 }
 
+// Tile width along N among widest, widest / 2, ... 64 (no wider than N
+// needs): the least (rounds of tiles over the SMs) x (128 + width), a model
+// of the time when every tile loads a 128-row A tile and a width-wide B tile
+// per k-block; ties keep the wider tile.  Large products keep the widest
+// tiles; products with fewer tiles than SMs take narrower, more numerous
+// ones (256^3 fp16 on fp32 operands: 14 -> 7.5 us; 512^3 17 -> 11 us).
+int pick_bn(int64_t m, int64_t n, int64_t batch, int splits, int sm_count, int widest) {
+  int top = n <= 64 ? 64 : (n <= 128 ? std::min(widest, 128) : widest);
+  int best = top;
+  int64_t best_cost = -1;
+  for (int w = top; w >= 64; w /= 2) {
+    const int64_t tiles = batch * ((m + 127) / 128) * ((n + w - 1) / w) * std::max(splits, 1);
+    const int64_t cost = ((tiles + sm_count - 1) / sm_count) * (128 + w);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = w;
+    }
+  }
+  return best;
+}
+
 size_t tail_bytes(int64_t tiles) {
   return align256((size_t)tiles * 2 * 256 * 256 * sizeof(float)) + align256((size_t)tiles * 16 * sizeof(uint32_t));
 }
@@ -275,22 +296,14 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = 64;   // four chains of 64 columns plus the running sum fill TMEM
   } else if (p.src == Src::kGeneric) {
     bn = 128;
-  } else if (p.src == Src::kTmaDirect && p.conv == Conv::kNone) {
-    bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
-  } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2) {
-    // 128-wide tiles hold one TMEM accumulator (chains and running sum
-    // fill the 512 columns), 64-wide tiles two.  Short K with few tiles
-    // (e.g. 256^3) takes the 64-wide ones for twice the tiles; short K with
-    // many tiles (the attention scores, 2048 x 32768 x 128: 16 % faster)
-    // and long K take the 128-wide ones, which read A once per 128 columns.
-    const int64_t tiles128 = batch * ((m + 127) / 128) * ((n + 127) / 128);
-    bn = (n <= 64 || (k <= 512 && tiles128 < sm_count)) ? 64 : 128;
-  } else if (p.conv == Conv::kSplit1) {
-    bn = n <= 64 ? 64 : 128;
+  } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2 || p.conv == Conv::kSplit1) {
+    // 128-wide tiles read A once per 128 columns; for the three-chain and
+    // A-only splits they hold one TMEM accumulator, 64-wide tiles two
+    bn = pick_bn(m, n, batch, splits, sm_count, 128);
   } else {
-    // fp32 -> fp16 / bf16 on load: the widest tile converts the fewest
-    // source bytes per flop
-    bn = n <= 64 ? 64 : (n <= 128 ? 128 : 256);
+    // direct 16-bit / tf32, and fp32 -> fp16 / bf16 on load (the widest
+    // tile converts the fewest source bytes per flop)
+    bn = pick_bn(m, n, batch, splits, sm_count, 256);
   }
   if (o.tile_n != 0) {
     TcKernel probe;
