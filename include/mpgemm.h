@@ -207,7 +207,10 @@ void mpg_options_init(mpg_options* opt);
  *                packed (m*lda for row-major, k*lda for column-major).
  *   B            likewise with (k x n): ROW_MAJOR ldb >= n, COL_MAJOR ldb >= k.
  *   C            device pointer, row-major fp32 (or 16-bit, see
- *                mpg_options.c_dtype), ldc >= n; strideC 0 = m*ldc.
+ *                mpg_options.c_dtype), ldc >= n; strideC 0 = m*ldc; with
+ *                batch > 1 a nonzero strideC must keep the batch matrices
+ *                of C apart (strideC >= (m-1)*ldc + n), else
+ *                MPG_ERR_INVALID_ARG.
  *   mode         precision policy; allowed input dtypes per mode:
  *                  FP16_F32ACC: A, B both F32 or both F16
  *                  BF16_F32ACC: A, B both F32 or both BF16

@@ -385,6 +385,10 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (B.ld < b_min) return fail(MPG_ERR_INVALID_ARG, "ldb=%lld smaller than %lld", (long long)B.ld, (long long)b_min);
   if (ldc < std::max<int64_t>(n, 1)) return fail(MPG_ERR_INVALID_ARG, "ldc=%lld smaller than n", (long long)ldc);
   if (A.stride < 0 || B.stride < 0 || strideC < 0) return fail(MPG_ERR_INVALID_ARG, "negative batch stride");
+  // batches of C written concurrently must not share elements
+  if (batch > 1 && strideC > 0 && m > 0 && n > 0 && strideC < (m - 1) * ldc + n)
+    return fail(MPG_ERR_INVALID_ARG, "strideC=%lld makes the batch matrices of C overlap (one spans %lld elements)",
+                (long long)strideC, (long long)((m - 1) * ldc + n));
   if (o.split_exp_a < -100 || o.split_exp_a > 100 || o.split_exp_b < -100 || o.split_exp_b > 100)
     return fail(MPG_ERR_INVALID_ARG, "split exponent outside [-100, 100]");
   if (o.splitk < 0) return fail(MPG_ERR_INVALID_ARG, "negative splitk");

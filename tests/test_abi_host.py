@@ -49,6 +49,7 @@ def _call(m=64, n=64, k=64, batch=1, A=16, lda=64, sA=0, adt=mpg.F32, alay=mpg.R
     (dict(blay=mpg.COL_MAJOR, k=70, lda=70, ldb=69), mpg.ERR_INVALID_ARG),
     (dict(ldc=63), mpg.ERR_INVALID_ARG),
     (dict(sA=-1), mpg.ERR_INVALID_ARG),
+    (dict(batch=2, sC=64 * 63 + 63), mpg.ERR_INVALID_ARG),        # batch matrices of C overlap
     (dict(adt=mpg.F16, bdt=mpg.F16, mode=mpg.TF32), mpg.ERR_UNSUPPORTED),
     (dict(adt=mpg.BF16, bdt=mpg.BF16, mode=mpg.FP16_F32ACC), mpg.ERR_UNSUPPORTED),
     (dict(adt=mpg.F16, bdt=mpg.F16, mode=mpg.SPLIT_FP16_3CHAIN), mpg.ERR_UNSUPPORTED),
