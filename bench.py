@@ -244,9 +244,11 @@ def mode_cases(torch, mpg, synthetic, device):
                         {"a": a, "b": b, "b_col": b_layout == "col", "exact_ws": exact_ws}, opts=opts,
                         algo_bytes=algo)
 
-    # C1: 256^3 uniform, four modes
+    # C1: 256^3 uniform, four modes; workspace from the query that sees the
+    # operands, as the torch wrapper sizes it (tf32's row-major B is copied
+    # transposed, then multiplied on the direct path)
     for mn in ("fp16", "bf16", "tf32", "split3"):
-        yield f"square256_{mn}", lambda mn=mn: f32_square(256, "uniform", mn)
+        yield f"square256_{mn}", lambda mn=mn: f32_square(256, "uniform", mn, exact_ws=True)
     # C3-shaped 8192^3 in the other precisions
     yield "square8192_tf32", lambda: f32_square(8192, "normal", "tf32", "col")
     # tf32 with a row-major B: transposed copy of B, then the direct path

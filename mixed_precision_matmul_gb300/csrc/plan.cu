@@ -295,7 +295,7 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   if (p.conv == Conv::kSplit4) {
     bn = 64;   // four chains of 64 columns plus the running sum fill TMEM
   } else if (p.src == Src::kGeneric) {
-    bn = 128;
+    bn = pick_bn(m, n, batch, splits, sm_count, 128);
   } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2 || p.conv == Conv::kSplit1) {
     // 128-wide tiles read A once per 128 columns; for the three-chain and
     // A-only splits they hold one TMEM accumulator, 64-wide tiles two
