@@ -8,19 +8,20 @@
 // separate TMEM chains that are added in plain fp32 (the two-chain form), or
 // in one chain (the single-chain form the fix replaced).
 //
-// One CTA takes 128 queries and a range of keys, in blocks of 64 keys:
-//   warp 0      TMA producer: K and V blocks (64 keys x 128 dims, fp16,
-//               128-byte swizzle) into separate rings (K 4 stages, released
-//               once S_j has read it; V 3 stages, released after O_j), K one
-//               block ahead of V, so K loads start about three blocks before
-//               their product
+// One CTA takes 128 queries and a range of keys, in blocks of 96 keys:
+//   warp 0      TMA producer: K and V blocks (96 keys x 128 dims, fp16,
+//               128-byte swizzle) into separate rings of 2 stages (K released
+//               once S_j has read it, V after O_j), K one block ahead of V
 //   warp 1      TMEM allocation; lane 0 issues every MMA:
-//                 S_j = [Q_hi ; Q_lo] K_j^T   (M 128, N 64, K 128) -> 2 chains
-//                 O_j = [P_hi ; P_lo] V_j     (M 128, N 128, K 64) -> 2 chains
-//               with S double-buffered, so S_{j+2} runs beside softmax_{j+1}
+//                 S_j = [Q_hi ; Q_lo] K_j^T   (M 128, N 96, K 128) -> 2 chains
+//                 O_j = [P_hi ; P_lo] V_j     (M 128, N 128, K 96) -> 2 chains
+//               in the order S_(j+1), O_j: S has one TMEM buffer, and S_(j+1)
+//               goes in as soon as the compute warps have read S_j, while
+//               O_(j-1) still runs.  P's first 64 keys sit in a 128-byte
+//               swizzled atom column, the last 32 in a 64-byte swizzled one.
 //   warps 2-17  softmax and correction, four warps per TMEM lane quarter
 //               (32 query rows); each of the four takes a quarter of a row:
-//               16 of the block's keys for the softmax and 32 of the output
+//               24 of the block's keys for the softmax and 32 of the output
 //               dims for the correction.
 //               softmax of block j: s = (S_hi + 2^-11 S_lo) * scale * log2(e);
 //               the four parts exchange their maxima (shared memory and an
@@ -47,13 +48,18 @@ namespace {
 template <bool kTwoChain, int PARTS>
 struct AttnTraits {
   static constexpr int BM = 128;     // queries per CTA
-  static constexpr int BKEY = 64;    // keys per block
+  static constexpr int BKEY = kAttnKeyBlock;   // keys per block (96)
+  static_assert(BKEY == 96, "the P tile's two swizzle regions and the 24-key parts assume 96");
   static constexpr int D = 128;      // head dimension (q.k and v)
-  static constexpr int kKStages = 4;
-  static constexpr int kVStages = 3;
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = 2;
   static constexpr int kQTile = BM * D * 2;          // 32 KB per half (hi or lo)
-  static constexpr int kKVTile = BKEY * D * 2;       // 16 KB (K or V block)
-  static constexpr int kPTile = BM * BKEY * 2;       // 16 KB per half
+  static constexpr int kKVTile = BKEY * D * 2;       // 24 KB (K or V block): two 64-dim halves
+  // P, the A operand of O = P V (K-major, keys contiguous): keys 0-63 in a
+  // 128-byte swizzled atom column (16 KB), keys 64-95 in a 64-byte swizzled
+  // one (8 KB)
+  static constexpr int kPCol0 = BM * 128;
+  static constexpr int kPTile = BM * 128 + BM * 64;  // 24 KB per half
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTile;
   static constexpr int kOffV = kOffK + kKStages * kKVTile;
@@ -67,12 +73,12 @@ struct AttnTraits {
   static constexpr int kOffMax = kOffP + 2 * kPTile;            // [block parity][part][128] partial maxima
   static constexpr int kOffSum = kOffMax + 2 * PARTS * BM * 4;  // [part][128] partial sums
   static constexpr int kOffBars = kOffSum + PARTS * BM * 4;
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 1 + 1 + 4;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 1 + 1 + 2 + 2 + 1 + 1 + 4;
   static constexpr int kSmemBytes = 1024 + kOffBars + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr int kThreads = 64 + kComputeThreads;
   // TMEM columns
-  static constexpr uint32_t kColS = 0;      // S buffer b: hi at 128 b, lo at 128 b + 64
+  static constexpr uint32_t kColS = 0;      // S: hi at 0, lo at BKEY
   static constexpr uint32_t kColOhi = 256;
   static constexpr uint32_t kColOlo = 384;
   static constexpr int kL = kTwoChain ? 11 : 0;   // lo scale exponent of the split
@@ -96,9 +102,16 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, uint32_t rows, in
   return make_smem_desc(base + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u, 16u, 1024u,
                         kSwizzle128B);
 }
-// MN-major (N contiguous) B tile: regions of 64 N x 64 k-lines, 8 KB apart.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int ks) {
-  return make_smem_desc(base + (uint32_t)ks * 16u * 128u, 64u * 128u, 1024u, kSwizzle128B);
+// MN-major (N contiguous) B tile: regions of 64 N x `lines` k-lines, one
+// after the other.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t lines, int ks) {
+  return make_smem_desc(base + (uint32_t)ks * 16u * 128u, lines * 128u, 1024u, kSwizzle128B);
+}
+// K-major A tile of 128 rows whose first 64 k sit in a 128-byte swizzled
+// atom column and the rest in a 64-byte swizzled one (the P tile).
+__device__ __forceinline__ uint64_t p_desc(uint32_t base, uint32_t col0_bytes, int ks) {
+  if (ks < 4) return make_smem_desc(base + (uint32_t)ks * 32u, 16u, 1024u, kSwizzle128B);
+  return make_smem_desc(base + col0_bytes + (uint32_t)(ks - 4) * 32u, 16u, 512u, kSwizzle64B);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1) {
@@ -110,9 +123,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_tiles = smem + T::kOffQ;      // [hi | lo], each [2 atom columns][128 rows][128 B]
-  uint8_t* k_tiles = smem + T::kOffK;      // stage s of each ring: [2 dim halves][64 keys][128 B]
+  uint8_t* k_tiles = smem + T::kOffK;      // stage s of each ring: [2 dim halves][BKEY keys][128 B]
   uint8_t* v_tiles = smem + T::kOffV;
-  uint8_t* p_tiles = smem + T::kOffP;      // [hi | lo], each [128 rows][128 B]
+  uint8_t* p_tiles = smem + T::kOffP;      // [hi | lo], each [128 rows][128 B] + [128 rows][64 B]
   float* part_max = reinterpret_cast<float*>(smem + T::kOffMax);
   float* part_sum = reinterpret_cast<float*>(smem + T::kOffSum);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBars);
@@ -121,8 +134,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   uint64_t* v_full = k_empty + T::kKStages;
   uint64_t* v_empty = v_full + T::kVStages;
   uint64_t* s_full = v_empty + T::kVStages;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;           // [0] p_full, [1] p_empty
+  uint64_t* s_empty = s_full + 1;
+  uint64_t* p_full = s_empty + 1;           // [0] p_full, [1] p_empty
   uint64_t* p_empty = p_full + 1;
   uint64_t* o_full = p_full + 2;            // [0] o_full, [1] o_empty
   uint64_t* o_empty = o_full + 1;
@@ -149,10 +162,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], T::kComputeThreads);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, T::kComputeThreads);
     mbar_init(p_full, T::kComputeThreads);
     mbar_init(p_empty, 1);
     mbar_init(o_full, 1);
@@ -220,31 +231,31 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = make_idesc(0u, false, false, 128, 64);
+      const uint32_t idesc_s = make_idesc(0u, false, false, 128, T::BKEY);
       const uint32_t idesc_o = make_idesc(0u, false, true, 128, 128);
       const uint32_t q_hi = q_smem, q_lo = q_smem + T::kQTile;
       const uint32_t p_hi = p_smem, p_lo = p_smem + T::kPTile;
       bool ok = mbar_wait(q_ready, 0, ctl);
       tc_fence_after_sync();
+      // one S buffer: S_j is issued once the compute warps have read S_(j-1)
       auto issue_s = [&](int j) -> bool {
         const uint32_t st = j % T::kKStages;
-        const uint32_t b = j & 1;
         if (!mbar_wait(&k_full[st], (j / T::kKStages) & 1u, ctl)) return false;
-        if (!mbar_wait(&s_empty[b], ((j >> 1) & 1u) ^ 1u, ctl)) return false;
+        if (!mbar_wait(s_empty, (j & 1u) ^ 1u, ctl)) return false;
         tc_fence_after_sync();
         const uint32_t kt = k_smem + st * T::kKVTile;
-        const uint32_t d_hi = tmem_base + T::kColS + 128u * b;
+        const uint32_t d_hi = tmem_base + T::kColS;
 #pragma unroll
         for (int ks = 0; ks < T::D / 16; ++ks) {
-          const uint64_t bk = kmajor_desc(kt, 64, ks);
+          const uint64_t bk = kmajor_desc(kt, T::BKEY, ks);
           mma_f16(d_hi, kmajor_desc(q_hi, 128, ks), bk, idesc_s, ks > 0 ? 1u : 0u);
           if constexpr (T::kL == 11) {
-            mma_f16(d_hi + 64, kmajor_desc(q_lo, 128, ks), bk, idesc_s, ks > 0 ? 1u : 0u);
+            mma_f16(d_hi + T::BKEY, kmajor_desc(q_lo, 128, ks), bk, idesc_s, ks > 0 ? 1u : 0u);
           } else {
             mma_f16(d_hi, kmajor_desc(q_lo, 128, ks), bk, idesc_s, 1u);
           }
         }
-        mma_commit(&s_full[b]);
+        mma_commit(s_full);
         mma_commit(&k_empty[st]);
         return true;
       };
@@ -258,12 +269,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         const uint32_t d_hi = tmem_base + T::kColOhi, d_lo = tmem_base + T::kColOlo;
 #pragma unroll
         for (int ks = 0; ks < T::BKEY / 16; ++ks) {
-          const uint64_t bv = mnmajor_desc(vt, ks);
-          mma_f16(d_hi, kmajor_desc(p_hi, 128, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
+          const uint64_t bv = mnmajor_desc(vt, T::BKEY, ks);
+          mma_f16(d_hi, p_desc(p_hi, T::kPCol0, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
           if constexpr (T::kL == 11) {
-            mma_f16(d_lo, kmajor_desc(p_lo, 128, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
+            mma_f16(d_lo, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
           } else {
-            mma_f16(d_hi, kmajor_desc(p_lo, 128, ks), bv, idesc_o, 1u);
+            mma_f16(d_hi, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, 1u);
           }
         }
         mma_commit(o_full);
@@ -271,11 +282,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         mma_commit(&v_empty[st]);
         return true;
       };
+      // S_(j+1) goes in as soon as the compute warps have read S_j (while
+      // O_(j-1) runs), then O_j once P_j is written
       if (ok) ok = issue_s(0);
-      if (ok && nb > 1) ok = issue_s(1);
       for (int j = 0; j < nb && ok; ++j) {
-        ok = issue_o(j);
-        if (ok && j + 2 < nb) ok = issue_s(j + 2);
+        if (j + 1 < nb) ok = issue_s(j + 1);
+        if (ok) ok = issue_o(j);
       }
       mma_commit(done_bar);
       drain_wait(done_bar, 0, p.wait_limit_ns);
@@ -335,28 +347,28 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       if (t < nb) {
         // ---------------------------------------------------------- softmax of block t
         const int j = t;
-        const uint32_t b = j & 1;
-        if (!warp_wait(&s_full[b], (j >> 1) & 1u, ctl)) { ok = false; break; }
+        if (!warp_wait(s_full, j & 1u, ctl)) { ok = false; break; }
         tc_fence_after_sync();
         float s[KP];
-        const uint32_t t_hi = tmem_base + lane_off + T::kColS + 128u * b + (uint32_t)(KP * part);
+        const uint32_t t_hi = tmem_base + lane_off + T::kColS + (uint32_t)(KP * part);
         {
-          float a[KP];
-          if constexpr (KP == 32) tmem_ld_32cols(t_hi, a); else tmem_ld_16cols(t_hi, a);
+#pragma unroll
+          for (int c = 0; c < KP / 8; ++c) tmem_ld_8cols(t_hi + 8 * c, s + 8 * c);
           if constexpr (T::kL == 11) {
-            float c[KP];
-            if constexpr (KP == 32) tmem_ld_32cols(t_hi + 64, c); else tmem_ld_16cols(t_hi + 64, c);
+            float lo[KP];
+#pragma unroll
+            for (int c = 0; c < KP / 8; ++c) tmem_ld_8cols(t_hi + T::BKEY + 8 * c, lo + 8 * c);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < KP; ++i) s[i] = (a[i] + kLoScale * c[i]) * p.scale_log2;
+            for (int i = 0; i < KP; ++i) s[i] = (s[i] + kLoScale * lo[i]) * p.scale_log2;
           } else {
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < KP; ++i) s[i] = a[i] * p.scale_log2;
+            for (int i = 0; i < KP; ++i) s[i] = s[i] * p.scale_log2;
           }
         }
         tc_fence_before_sync();
-        mbar_arrive(&s_empty[b]);
+        mbar_arrive(s_empty);
         // keys past the end of the sequence score -inf (only the last block
         // of the sequence has any)
         const int valid = p.lk - (kb0 + j) * T::BKEY - KP * part;
@@ -365,16 +377,18 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
           for (int i = 0; i < KP; ++i)
             if (i >= valid) s[i] = -INFINITY;
         }
-        // pairwise (tree) maximum
-        float tr[KP / 2];
+        // maximum over this part's keys: eight running maxima, then a tree
+        float tr[8];
 #pragma unroll
-        for (int i = 0; i < KP / 2; ++i) tr[i] = fmaxf(s[i], s[i + KP / 2]);
+        for (int i = 0; i < 8; ++i) tr[i] = s[i];
 #pragma unroll
-        for (int w = KP / 4; w >= 1; w >>= 1)
+        for (int i = 8; i < KP; ++i) tr[i & 7] = fmaxf(tr[i & 7], s[i]);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) tr[i] = fmaxf(tr[i], tr[i + w]);
         // the parts of the row agree on the block's maximum
-        float* mx = part_max + (b * NP) * T::BM;
+        float* mx = part_max + ((j & 1) * NP) * T::BM;
         mx[part * T::BM + r] = tr[0];
         mbar_arrive(&xchg[q4]);
         if (!warp_wait(&xchg[q4], nx & 1u, ctl)) { ok = false; break; }
@@ -386,16 +400,20 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         alpha_cur = exp2_approx(m_run - m_new);   // 0 on the first block
 #pragma unroll
         for (int i = 0; i < KP; ++i) s[i] = exp2_approx(s[i] - m_new);
-        // pairwise sum
+        // sum: eight running sums, then a tree
 #pragma unroll
-        for (int i = 0; i < KP / 2; ++i) tr[i] = s[i] + s[i + KP / 2];
+        for (int i = 0; i < 8; ++i) tr[i] = s[i];
 #pragma unroll
-        for (int w = KP / 4; w >= 1; w >>= 1)
+        for (int i = 8; i < KP; ++i) tr[i & 7] += s[i];
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) tr[i] += tr[i + w];
         l_part = l_part * alpha_cur + tr[0];
         m_run = m_new;
-        // p split into hi/lo fp16: this part's chunks of row r of the A tiles
+        // p split into hi/lo fp16: this part's 8-key chunks of row r of the A
+        // tiles (chunks 0-7 in the 128-byte swizzled column, 8-11 in the
+        // 64-byte swizzled one)
         if (!warp_wait(p_empty, (j & 1u) ^ 1u, ctl)) { ok = false; break; }
         const uint32_t p_hi = p_smem, p_lo = p_smem + T::kPTile;
 #pragma unroll
@@ -404,7 +422,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             split_pair<T::kL>(s[8 * cc + 2 * e], s[8 * cc + 2 * e + 1], 1.0f, h[e], l[e]);
-          const uint32_t off = swz_chunk_offset<128>((uint32_t)r, (uint32_t)((KP / 8) * part + cc));
+          const uint32_t c = (uint32_t)((KP / 8) * part + cc);
+          const uint32_t off = c < 8 ? swz_chunk_offset<128>((uint32_t)r, c)
+                                     : (uint32_t)T::kPCol0 + swz_chunk_offset<64>((uint32_t)r, c - 8);
           st_shared_v4(p_hi + off, h[0], h[1], h[2], h[3]);
           st_shared_v4(p_lo + off, l[0], l[1], l[2], l[3]);
         }

@@ -20,7 +20,7 @@ struct AttnSplit {
 
 AttnSplit attention_split(int64_t lq, int64_t lk, int32_t key_splits, int sm_count) {
   AttnSplit a;
-  const int64_t nkb = (lk + 63) / 64;
+  const int64_t nkb = (lk + kAttnKeyBlock - 1) / kAttnKeyBlock;
   const int64_t nqb = (lq + 127) / 128;
   int64_t s = key_splits > 0 ? key_splits : std::max<int64_t>(1, sm_count / std::max<int64_t>(nqb, 1));
   s = std::max<int64_t>(1, std::min<int64_t>(s, nkb));
@@ -84,9 +84,9 @@ mpg_status mpg_attention(int64_t lq, int64_t lk, int64_t d, const float* Q, int6
   std::memset(&p, 0, sizeof(p));
   Operand Kop{K, ldk, 0, MPG_F16, MPG_ROW_MAJOR};
   Operand Vop{V, ldv, 0, MPG_F16, MPG_ROW_MAJOR};
-  s = encode_map(&p.map_k, Kop, d, lk, 1, 64, 64);
+  s = encode_map(&p.map_k, Kop, d, lk, 1, 64, kAttnKeyBlock);
   if (s != MPG_OK) return s;
-  s = encode_map(&p.map_v, Vop, d, lk, 1, 64, 64);
+  s = encode_map(&p.map_v, Vop, d, lk, 1, 64, kAttnKeyBlock);
   if (s != MPG_OK) return s;
   p.q = Q;
   p.ldq = ldq;
