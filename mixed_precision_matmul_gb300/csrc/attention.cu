@@ -19,24 +19,30 @@
 //               goes in as soon as the compute warps have read S_j, while
 //               O_(j-1) still runs.  P's first 64 keys sit in a 128-byte
 //               swizzled atom column, the last 32 in a 64-byte swizzled one.
-//   warps 2-17  softmax and correction, four warps per TMEM lane quarter
+//   warps 2-17  softmax and folds of O, four warps per TMEM lane quarter
 //               (32 query rows); each of the four takes a quarter of a row:
 //               24 of the block's keys for the softmax and 32 of the output
-//               dims for the correction.
+//               dims for the folds.
 //               softmax of block j: s = (S_hi + 2^-11 S_lo) * scale * log2(e);
 //               the four parts exchange their maxima (shared memory and an
 //               mbarrier per lane quarter that all four parts arrive on,
 //               waited on with the same bounded wait as every other handoff),
-//               so all compute the same running maximum and the same rescale
-//               factor; p = 2^(s - max), split into hi/lo fp16 and written to
-//               shared memory as the A operand of the next MMA; each part
-//               keeps its own running sum.
-//               correction of block j: O_run = O_run * 2^(max_old - max_new)
-//               + (O_hi + 2^-11 O_lo) in fp32 (round to nearest), in
-//               registers.  A warp runs the softmax of block j+1 before the
-//               correction of block j, so the tensor core always has the
-//               next block's work.  At the end O = O_run / sum (or the
-//               unnormalised partial with its max and sum when the keys are
+//               so all compute the same reference maximum m_ref.  m_ref
+//               moves only when a block's maximum exceeds it by more than 8
+//               (lazy rescaling: p = 2^(s - m_ref) <= 2^8, well inside
+//               fp16); p is split into hi/lo fp16 and written to shared
+//               memory as the A operand of the next MMA; each part keeps its
+//               own running sum.
+//               The O chains in TMEM accumulate the products of successive
+//               blocks (all relative to m_ref).  A fold adds them to the fp32
+//               running output in registers, O_run = O_run * 2^(r - m_ref) +
+//               (O_hi + 2^-11 O_lo) * 2^(m_old - m_ref) (round to nearest),
+//               and zeroes them; a warp folds after every fourth block, before
+//               a block whose softmax moved m_ref in any of its rows, and at
+//               the end.  A warp runs the softmax of block j+1 before the
+//               fold of block j, so the tensor core always has the next
+//               block's work.  At the end O = O_run / sum (or the
+//               unnormalised partial with its m_ref and sum when the keys are
 //               split across CTAs; a merge kernel combines the partials).
 // First, the compute warps load the CTA's 128 x 128 fp32 block of Q and split it into
 // the swizzled hi/lo operand tiles.  Every wait is bounded.
@@ -85,6 +91,13 @@ struct AttnTraits {
 };
 
 constexpr float kLoScale = 0x1p-11f;
+// Lazy rescaling of the online softmax: the reference maximum moves only
+// when a block's maximum exceeds it by more than kLazyLog2, so p <= 2^8.
+constexpr float kLazyLog2 = 8.0f;
+// Blocks of products the O chains accumulate in TMEM between folds into the
+// fp32 running output (384 keys: the tensor cores' own accumulation stays
+// short, like the split GEMM's K chunks).
+constexpr int kFoldBlocks = 4;
 
 // 2^x by the hardware's approximate base-2 exponential (ex2.approx, results
 // below 2^-126 flushed to zero: such probabilities add nothing to a sum
@@ -270,9 +283,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
 #pragma unroll
         for (int ks = 0; ks < T::BKEY / 16; ++ks) {
           const uint64_t bv = mnmajor_desc(vt, T::BKEY, ks);
-          mma_f16(d_hi, p_desc(p_hi, T::kPCol0, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
+          // O accumulates across blocks: the compute warps fold it into
+          // registers (and zero it) every few blocks
+          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+          mma_f16(d_hi, p_desc(p_hi, T::kPCol0, ks), bv, idesc_o, acc);
           if constexpr (T::kL == 11) {
-            mma_f16(d_lo, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, ks > 0 ? 1u : 0u);
+            mma_f16(d_lo, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, acc);
           } else {
             mma_f16(d_hi, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, 1u);
           }
@@ -338,12 +354,17 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
     float o[DP];
 #pragma unroll
     for (int i = 0; i < DP; ++i) o[i] = 0.0f;
-    float m_run = -INFINITY, l_part = 0.0f, alpha_prev = 0.0f;
+    // m_ref: the reference maximum of the probabilities (p = 2^(s - m_ref))
+    // and of the O chains accumulating in TMEM; it moves only when a block's
+    // maximum exceeds it by more than kLazyLog2 (p stays <= 2^kLazyLog2).
+    // o (registers) holds the folded blocks relative to r_reg.
+    float m_ref = -INFINITY, r_reg = -INFINITY, l_part = 0.0f;
     uint32_t nx = 0;   // exchanges with the other parts of the rows so far
     bool ok = true;
     // step t: softmax of block t (t < nb), then correction of block t-1 (t >= 1)
     for (int t = 0; t <= nb && ok; ++t) {
-      float alpha_cur = 0.0f;
+      bool rescale = false;        // softmax of block t moved m_ref
+      float o_ref = m_ref;         // the reference of the O chains in TMEM
       if (t < nb) {
         // ---------------------------------------------------------- softmax of block t
         const int j = t;
@@ -396,10 +417,13 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         float m_blk = mx[r];
 #pragma unroll
         for (int k = 1; k < NP; ++k) m_blk = fmaxf(m_blk, mx[k * T::BM + r]);
-        const float m_new = fmaxf(m_run, m_blk);
-        alpha_cur = exp2_approx(m_run - m_new);   // 0 on the first block
+        if (m_blk > m_ref + kLazyLog2) {   // always on the first block
+          rescale = true;
+          m_ref = m_blk;
+        }
+        const float alpha_l = exp2_approx(o_ref - m_ref);   // 1 unless m_ref moved; 0 on the first block
 #pragma unroll
-        for (int i = 0; i < KP; ++i) s[i] = exp2_approx(s[i] - m_new);
+        for (int i = 0; i < KP; ++i) s[i] = exp2_approx(s[i] - m_ref);
         // sum: eight running sums, then a tree
 #pragma unroll
         for (int i = 0; i < 8; ++i) tr[i] = s[i];
@@ -409,8 +433,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) tr[i] += tr[i + w];
-        l_part = l_part * alpha_cur + tr[0];
-        m_run = m_new;
+        l_part = l_part * alpha_l + tr[0];
         // p split into hi/lo fp16: this part's 8-key chunks of row r of the A
         // tiles (chunks 0-7 in the 128-byte swizzled column, 8-11 in the
         // 64-byte swizzled one)
@@ -432,33 +455,58 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         mbar_arrive(p_full);
       }
       if (t >= 1) {
-        // ---------------------------------------------------------- correction of block t-1
+        // ---------------------------------------------------------- fold after block t-1
+        // The O chains hold the blocks since the last fold, relative to
+        // o_ref.  They are added to the registers (round to nearest, the
+        // hi and lo chains summed in fp32) and zeroed every kFoldBlocks
+        // blocks (bounding how long the tensor cores accumulate), before
+        // block t's products when m_ref moved, and at the end; otherwise
+        // the next block's products accumulate on top of them.
         const int j = t - 1;
         if (!warp_wait(o_full, j & 1u, ctl)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint32_t t_hi = tmem_base + lane_off + T::kColOhi + (uint32_t)(DP * part);
-        const uint32_t t_lo = tmem_base + lane_off + T::kColOlo + (uint32_t)(DP * part);
-        constexpr int CW = DP / 2;   // columns per TMEM load
+        // tcgen05.ld/st are warp-collective: the warp folds all its rows when
+        // any of them moved its reference (for the others a_tm is 1)
+        const bool fold = __any_sync(0xffffffffu, rescale) || t % kFoldBlocks == 0 || t == nb;
+        if (fold) {
+          tc_fence_after_sync();
+          const uint32_t t_hi = tmem_base + lane_off + T::kColOhi + (uint32_t)(DP * part);
+          const uint32_t t_lo = tmem_base + lane_off + T::kColOlo + (uint32_t)(DP * part);
+          const float a_reg = exp2_approx(r_reg - m_ref);   // 0 before the first fold
+          const float a_tm = exp2_approx(o_ref - m_ref);
+          constexpr int CW = DP / 2;   // columns per TMEM load
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float a[CW];
-          if constexpr (CW == 32) tmem_ld_32cols(t_hi + CW * c, a); else tmem_ld_16cols(t_hi + CW * c, a);
-          if constexpr (T::kL == 11) {
-            float e[CW];
-            if constexpr (CW == 32) tmem_ld_32cols(t_lo + CW * c, e); else tmem_ld_16cols(t_lo + CW * c, e);
-            tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            float a[CW];
+            if constexpr (CW == 32) tmem_ld_32cols(t_hi + CW * c, a); else tmem_ld_16cols(t_hi + CW * c, a);
+            if constexpr (T::kL == 11) {
+              float e[CW];
+              if constexpr (CW == 32) tmem_ld_32cols(t_lo + CW * c, e); else tmem_ld_16cols(t_lo + CW * c, e);
+              tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], alpha_prev, a[i] + kLoScale * e[i]);
-          } else {
-            tmem_ld_wait();
+              for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], a_reg, (a[i] + kLoScale * e[i]) * a_tm);
+            } else {
+              tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], alpha_prev, a[i]);
+              for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], a_reg, a[i] * a_tm);
+            }
+          }
+          r_reg = m_ref;
+          if (t < nb) {
+            // the next block's products start the chains again
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.0f;
+#pragma unroll
+            for (int c = 0; c < DP / 16; ++c) {
+              tmem_st_16cols(t_hi + 16 * c, z);
+              if constexpr (T::kL == 11) tmem_st_16cols(t_lo + 16 * c, z);
+            }
+            tmem_st_wait();
           }
         }
         tc_fence_before_sync();
         mbar_arrive(o_empty);
       }
-      alpha_prev = alpha_cur;
     }
     // the row's sum is the sum of its parts' sums
     if (ok) {
@@ -483,7 +531,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < DP; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
         if (part == 0) {
-          p.part_m[(int64_t)split * p.lq + grow] = m_run;
+          p.part_m[(int64_t)split * p.lq + grow] = m_ref;
           p.part_l[(int64_t)split * p.lq + grow] = l_row;
         }
       }

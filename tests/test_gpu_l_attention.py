@@ -112,3 +112,30 @@ def test_attention_full_size_sampled_rows(capsys):
     with capsys.disabled():
         print(f"\n[attention 2048 x 32768: {err:.3e} vs exact q, {errq:.3e} vs split q]")
     assert err <= TOL_2CHAIN
+
+
+def _jump_inputs(lq, lk, seed):
+    """Rows whose running maximum jumps at chosen keys for even rows only: q
+    has a component a_r along dim 0 (1 on even rows, 1/20 on odd rows) and a
+    few keys carry large values in dim 0, so within each warp of 32 rows
+    half the rows move their reference maximum on those blocks and half do
+    not."""
+    q = 0.02 * synthetic.normal((lq, 128), 600 + seed)
+    q[:, 0] += np.where(np.arange(lq) % 2 == 0, 1.0, 0.05).astype(np.float32)
+    k = (0.02 * synthetic.normal((lk, 128), 700 + seed)).astype(np.float16)
+    v = synthetic.normal((lk, 128), 800 + seed).astype(np.float16)
+    for key, val in ((200, 20.0), (500, 40.0), (lk - 3, 60.0)):
+        if key < lk:
+            k[key, 0] = val
+    return q.astype(np.float32), k, v
+
+
+@pytest.mark.parametrize("lq,lk,splits", [(256, 1000, 1), (256, 1000, 2), (160, 4100, 1)])
+def test_attention_rows_of_a_warp_rescale_apart(lq, lk, splits):
+    """Some rows of a warp move their reference maximum on a block and the
+    others do not (the fold then runs for the whole warp)."""
+    mpg.build()
+    q, k, v = _jump_inputs(lq, lk, lq + lk)
+    O = run(q, k, v, 0.5, key_splits=splits)
+    ref, den = oracle.attention(q, k, v, 0.5)
+    assert _err(O, ref, den) <= TOL_2CHAIN
