@@ -8,86 +8,85 @@
 // separate TMEM chains that are added in plain fp32 (the two-chain form), or
 // in one chain (the single-chain form the fix replaced).
 //
-// One CTA takes 128 queries and a range of keys, in blocks of 96 keys:
-//   warp 0      TMA producer: K and V blocks (96 keys x 128 dims, fp16,
-//               128-byte swizzle) into separate rings of 2 stages (K released
-//               once S_j has read it, V after O_j), K one block ahead of V
-//   warp 1      TMEM allocation; lane 0 issues every MMA:
-//                 S_j = [Q_hi ; Q_lo] K_j^T   (M 128, N 96, K 128) -> 2 chains
-//                 O_j = [P_hi ; P_lo] V_j     (M 128, N 128, K 96) -> 2 chains
-//               in the order S_(j+1), O_j: S has one TMEM buffer, and S_(j+1)
-//               goes in as soon as the compute warps have read S_j, while
-//               O_(j-1) still runs.  P's first 64 keys sit in a 128-byte
-//               swizzled atom column, the last 32 in a 64-byte swizzled one.
-//   warps 2-17  softmax and folds of O, four warps per TMEM lane quarter
-//               (32 query rows); each of the four takes a quarter of a row:
-//               24 of the block's keys for the softmax and 32 of the output
-//               dims for the folds.
-//               softmax of block j: s = (S_hi + 2^-11 S_lo) * scale * log2(e);
-//               the four parts exchange their maxima (shared memory and an
-//               mbarrier per lane quarter that all four parts arrive on,
-//               waited on with the same bounded wait as every other handoff),
-//               so all compute the same reference maximum m_ref.  m_ref
-//               moves only when a block's maximum exceeds it by more than 8
-//               (lazy rescaling: p = 2^(s - m_ref) <= 2^8, well inside
-//               fp16); p is split into hi/lo fp16 and written to shared
-//               memory as the A operand of the next MMA; each part keeps its
-//               own running sum.
-//               The O chains in TMEM accumulate the products of successive
-//               blocks (all relative to m_ref).  A fold adds them to the fp32
-//               running output in registers, O_run = O_run * 2^(r - m_ref) +
-//               (O_hi + 2^-11 O_lo) * 2^(m_old - m_ref) (round to nearest),
-//               and zeroes them; a warp folds after every fourth block, before
-//               a block whose softmax moved m_ref in any of its rows, and at
-//               the end.  A warp runs the softmax of block j+1 before the
-//               fold of block j, so the tensor core always has the next
-//               block's work.  At the end O = O_run / sum (or the
-//               unnormalised partial with its m_ref and sum when the keys are
-//               split across CTAs; a merge kernel combines the partials).
-// First, the compute warps load the CTA's 128 x 128 fp32 block of Q and split it into
-// the swizzled hi/lo operand tiles.  Every wait is bounded.
+// Both products are computed transposed, keys and head dimensions on the
+// M side and the queries on the N side:
+//     S^T = K [Q_hi ; Q_lo]^T     M 128 keys, N 256 = 128 queries x (hi, lo), K 128 dims
+//     O^T = V^T [P_hi ; P_lo]^T   M 128 dims, N 256 = 128 queries x (hi, lo), K 128 keys
+// so that the hi and lo chains of one k-step are a single N = 256
+// instruction (the tensor core's full rate; instructions with N <= 128 cost
+// about as much as N = 256 ones), 8 instructions per product and block.  The
+// single-chain form issues the hi and lo halves as two N = 128 instructions
+// into one accumulator.
+//
+// One CTA takes 128 queries and a range of keys, in blocks of 128 keys:
+//   warp 0      TMA producer: one ring of five 16 KB slots that K and V
+//               share, filled in the order the MMAs read them: K_(j+1) (two
+//               64-dim halves), then V_j (two 64-key halves).
+//   warp 1      TMEM allocation; lane 0 issues every MMA, in the order S_(j+1),
+//               O_j: S^T has one TMEM buffer (columns 0-255), and S_(j+1) goes
+//               in as soon as the compute warps have read S_j; O^T
+//               (columns 256-511) accumulates the blocks between folds.
+//   warps 2-17  softmax and folds of O.  Warp w reads TMEM lane quarter
+//               w % 4 (32 keys of S^T, 32 dims of O^T) and one of four 32-query
+//               column groups; lane l holds one key (or dim) for 32 queries.
+//               softmax of block j: s = S_hi + 2^-11 S_lo (q was scaled by
+//               scale * log2(e) before the split), x = s - m_ref per query;
+//               m_ref (one per query, the same in the four warps of a column
+//               group) moves only when a block's maximum exceeds it by more
+//               than 8 (lazy rescaling, p = 2^x <= 2^8).  The four warps of a
+//               column group exchange one flag per block (shared memory and
+//               an mbarrier, waited on with the bounded wait); only when one
+//               is raised do they exchange per-query maxima (warp maxima by
+//               redux.sync) and move m_ref.  p = 2^x is split into hi/lo
+//               fp16 and written to shared memory as P^T (keys x queries,
+//               the B operand of O^T); each warp sums p over its 32 keys per
+//               query (a shuffle reduce-scatter leaves query l's sum in lane l).
+//               fold: O_run += O_hi + 2^-11 O_lo (round to nearest, in
+//               registers; times 2^(m_old - m_new) per query when m_ref
+//               moved), then the O^T chains are zeroed; after every fourth
+//               block, before a block whose softmax moved m_ref, and at the
+//               end.  Order within block j: read S_j (S_(j+1) may go in),
+//               the exchange, p = 2^x; once O_(j-1) has completed, the fold
+//               when due and the release of the chains; the P^T write (O_j
+//               may go in); the sums, while O_j runs.
+//   At the end O = O_run / sum, or the unnormalised partial with its m_ref
+//   and sum when the keys are split across CTAs (attn_merge_kernel combines
+//   the partials).
+// First, the compute warps load the CTA's 128 x 128 fp32 block of Q, scale
+// it and split it into the swizzled hi/lo operand tile.  Every wait is
+// bounded.
 #include "tc_gemm.cuh"
 
 namespace mpg {
 namespace {
 
-template <bool kTwoChain, int PARTS>
+template <bool kTwoChain>
 struct AttnTraits {
-  static constexpr int BM = 128;     // queries per CTA
-  static constexpr int BKEY = kAttnKeyBlock;   // keys per block (96)
-  static_assert(BKEY == 96, "the P tile's two swizzle regions and the 24-key parts assume 96");
-  static constexpr int D = 128;      // head dimension (q.k and v)
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
-  static constexpr int kQTile = BM * D * 2;          // 32 KB per half (hi or lo)
-  static constexpr int kKVTile = BKEY * D * 2;       // 24 KB (K or V block): two 64-dim halves
-  // P, the A operand of O = P V (K-major, keys contiguous): keys 0-63 in a
-  // 128-byte swizzled atom column (16 KB), keys 64-95 in a 64-byte swizzled
-  // one (8 KB)
-  static constexpr int kPCol0 = BM * 128;
-  static constexpr int kPTile = BM * 128 + BM * 64;  // 24 KB per half
+  static constexpr int BQ = 128;                 // queries per CTA
+  static constexpr int BKEY = kAttnKeyBlock;     // keys per block
+  static_assert(BKEY == 128, "the ring's half-block slots and the four 32-key quarters assume 128");
+  static constexpr int kRing = 5;                // K/V ring slots
+  static constexpr int kSlot = 16384;            // one slot: half a K block (64 dims) or half a V block (64 keys)
+  // Q: [2 dim halves][256 lines: q_hi of queries 0-127, q_lo of 0-127][128 B], 128-byte swizzle
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQTile;
-  static constexpr int kOffV = kOffK + kKStages * kKVTile;
-  static constexpr int kOffP = kOffV + kVStages * kKVTile;
-  // compute warps: PARTS warps share each TMEM lane quarter (32 query rows);
-  // each takes KP of a block's keys and DP of the output dims of its rows
-  static constexpr int kParts = PARTS;
-  static constexpr int kComputeThreads = 4 * PARTS * 32;
-  static constexpr int KP = BKEY / PARTS;
-  static constexpr int DP = D / PARTS;
-  static constexpr int kOffMax = kOffP + 2 * kPTile;            // [block parity][part][128] partial maxima
-  static constexpr int kOffSum = kOffMax + 2 * PARTS * BM * 4;  // [part][128] partial sums
-  static constexpr int kOffBars = kOffSum + PARTS * BM * 4;
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 1 + 1 + 2 + 2 + 1 + 1 + 4;
+  static constexpr int kOffRing = kOffQ + 2 * 256 * 128;
+  // P^T: [4 atoms: hi queries 0-63, hi 64-127, lo 0-63, lo 64-127][128 keys][128 B]
+  static constexpr int kOffP = kOffRing + kRing * kSlot;
+  static constexpr int kOffMax = kOffP + 4 * BKEY * 128;        // [2][4 groups][4 quarters][32] maxima
+  static constexpr int kOffFlag = kOffMax + 2 * 4 * 4 * 32 * 4;  // [2][4 groups][4 quarters] flags
+  static constexpr int kOffSum = kOffFlag + 2 * 4 * 4 * 4;       // [4 groups][4 quarters][32] sums
+  static constexpr int kOffWarp = kOffSum + 4 * 4 * 32 * 4;      // [16 warps][3][32] per-query values
+  static constexpr int kOffBars = kOffWarp + 16 * 3 * 32 * 4;
+  static constexpr int kNumBars = 2 * kRing + 7 + 4;
   static constexpr int kSmemBytes = 1024 + kOffBars + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr int kComputeThreads = 512;
   static constexpr int kThreads = 64 + kComputeThreads;
-  // TMEM columns
-  static constexpr uint32_t kColS = 0;      // S: hi at 0, lo at BKEY
-  static constexpr uint32_t kColOhi = 256;
-  static constexpr uint32_t kColOlo = 384;
-  static constexpr int kL = kTwoChain ? 11 : 0;   // lo scale exponent of the split
+  // TMEM columns: S^T at 0 (hi 0-127, lo 128-255), O^T at 256 (hi 256-383, lo 384-511)
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kN = kTwoChain ? 256 : 128;   // N of each MMA
+  static constexpr int kL = kTwoChain ? 11 : 0;           // lo scale exponent of the split
 };
 
 constexpr float kLoScale = 0x1p-11f;
@@ -95,36 +94,118 @@ constexpr float kLoScale = 0x1p-11f;
 // when a block's maximum exceeds it by more than kLazyLog2, so p <= 2^8.
 constexpr float kLazyLog2 = 8.0f;
 // Blocks of products the O chains accumulate in TMEM between folds into the
-// fp32 running output (384 keys: the tensor cores' own accumulation stays
+// fp32 running output (512 keys: the tensor cores' own accumulation stays
 // short, like the split GEMM's K chunks).
 constexpr int kFoldBlocks = 4;
 
 // 2^x by the hardware's approximate base-2 exponential (ex2.approx, results
 // below 2^-126 flushed to zero: such probabilities add nothing to a sum
-// of terms of which the largest is 1).
+// of terms of which the largest is at least 1).
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// K-major operand tile of `rows` lines whose K extent spans 128-byte atom
-// columns stored one after another (each rows x 128 bytes); k-step `ks` of
-// 16 fp16 elements.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, uint32_t rows, int ks) {
-  return make_smem_desc(base + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u, 16u, 1024u,
-                        kSwizzle128B);
+// Two fp32 lanes per instruction (the packed f32x2 forms): d = a * b + c,
+// a + b, a - b, a * b, each rounded to nearest like its scalar form.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
-// MN-major (N contiguous) B tile: regions of 64 N x `lines` k-lines, one
-// after the other.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t lines, int ks) {
-  return make_smem_desc(base + (uint32_t)ks * 16u * 128u, lines * 128u, 1024u, kSwizzle128B);
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
-// K-major A tile of 128 rows whose first 64 k sit in a 128-byte swizzled
-// atom column and the rest in a 64-byte swizzled one (the P tile).
-__device__ __forceinline__ uint64_t p_desc(uint32_t base, uint32_t col0_bytes, int ks) {
-  if (ks < 4) return make_smem_desc(base + (uint32_t)ks * 32u, 16u, 1024u, kSwizzle128B);
-  return make_smem_desc(base + col0_bytes + (uint32_t)(ks - 4) * 32u, 16u, 512u, kSwizzle64B);
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// p = (p0, p1) split into fp16 hi = RN(p) and lo = RN((p - hi) * 2^L), each
+// pair packed into one 32-bit word (the split the operand tiles use).
+template <int L>
+__device__ __forceinline__ void split2(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(p0, p1);
+  const float2 hb = __half22float2(h);
+  float2 r = fsub2(make_float2(p0, p1), hb);
+  if constexpr (L == 11) r = fmul2(r, make_float2(2048.0f, 2048.0f));
+  const __half2 l = __floats2half2_rn(r.x, r.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Maximum of v over the warp's 32 lanes (every lane gets it).
+__device__ __forceinline__ float warp_max(float v) {
+  float m;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
+}
+
+// Reduce-scatter of 32 values over the warp: afterwards lane l returns the
+// sum over all lanes of v[l] (v is overwritten).  Step w halves the values
+// a lane keeps: lanes with bit w set keep the upper half and send the lower
+// one to their partner (lane ^ w), which keeps the lower half.
+__device__ __forceinline__ float reduce_scatter_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+    float keep[16], recv[16];
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      keep[i] = up ? v[i + w] : v[i];
+      recv[i] = __shfl_xor_sync(0xffffffffu, send, w);
+    }
+    if (w == 1) {
+      v[0] = keep[0] + recv[0];
+    } else {
+#pragma unroll
+      for (int i = 0; i < w; i += 2) {
+        const float2 d = fadd2(make_float2(keep[i], keep[i + 1]), make_float2(recv[i], recv[i + 1]));
+        v[i] = d.x;
+        v[i + 1] = d.y;
+      }
+    }
+  }
+  return v[0];
+}
+
+// 128-byte swizzled K-major tile (lines of 128 bytes, 8-line groups 1024
+// bytes apart), k-step `kk` (16 fp16 = 32 bytes) within one atom column.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return make_smem_desc(base + (uint32_t)kk * 32u, 16u, 1024u, kSwizzle128B);
+}
+// 128-byte swizzled MN-major tile: atoms of 64 M/N values x `lines` k-lines
+// stored `lines * 128` bytes apart; k-step `kk` covers 16 k-lines.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t lines, int kk) {
+  return make_smem_desc(base + (uint32_t)kk * 2048u, lines * 128u, 1024u, kSwizzle128B);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1) {
@@ -135,26 +216,22 @@ template <class T>
 __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_tiles = smem + T::kOffQ;      // [hi | lo], each [2 atom columns][128 rows][128 B]
-  uint8_t* k_tiles = smem + T::kOffK;      // stage s of each ring: [2 dim halves][BKEY keys][128 B]
-  uint8_t* v_tiles = smem + T::kOffV;
-  uint8_t* p_tiles = smem + T::kOffP;      // [hi | lo], each [128 rows][128 B] + [128 rows][64 B]
+  uint8_t* ring = smem + T::kOffRing;
   float* part_max = reinterpret_cast<float*>(smem + T::kOffMax);
+  int* flags = reinterpret_cast<int*>(smem + T::kOffFlag);
   float* part_sum = reinterpret_cast<float*>(smem + T::kOffSum);
+  float* warp_vals = reinterpret_cast<float*>(smem + T::kOffWarp);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBars);
-  uint64_t* k_full = bars;
-  uint64_t* k_empty = k_full + T::kKStages;
-  uint64_t* v_full = k_empty + T::kKStages;
-  uint64_t* v_empty = v_full + T::kVStages;
-  uint64_t* s_full = v_empty + T::kVStages;
+  uint64_t* ring_full = bars;
+  uint64_t* ring_empty = bars + T::kRing;
+  uint64_t* s_full = bars + 2 * T::kRing;
   uint64_t* s_empty = s_full + 1;
-  uint64_t* p_full = s_empty + 1;           // [0] p_full, [1] p_empty
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* o_full = p_full + 2;            // [0] o_full, [1] o_empty
-  uint64_t* o_empty = o_full + 1;
-  uint64_t* q_ready = o_full + 2;
-  uint64_t* done_bar = q_ready + 1;
-  uint64_t* xchg = done_bar + 1;            // [4]: the parts of a lane quarter exchange values
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = s_full + 3;            // O_j complete (which also frees the P^T tile)
+  uint64_t* o_empty = s_full + 4;
+  uint64_t* q_ready = s_full + 5;
+  uint64_t* done_bar = s_full + 6;
+  uint64_t* xchg = s_full + 7;              // [4]: the four warps of a column group exchange values
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -167,23 +244,18 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   const int nb = kb1 - kb0;                    // >= 1 (the host never launches an empty range)
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < T::kKStages; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < T::kVStages; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+    for (int i = 0; i < T::kRing; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_empty, T::kComputeThreads);
     mbar_init(p_full, T::kComputeThreads);
-    mbar_init(p_empty, 1);
     mbar_init(o_full, 1);
     mbar_init(o_empty, T::kComputeThreads);
     mbar_init(q_ready, T::kComputeThreads);
     mbar_init(done_bar, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xchg[i], 32 * T::kParts);
+    for (int i = 0; i < 4; ++i) mbar_init(&xchg[i], 128);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -201,105 +273,111 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   ctl.status = p.status;
   ctl.limit_ns = p.wait_limit_ns;
 
-  const uint32_t q_smem = smem_addr(q_tiles);
-  const uint32_t k_smem = smem_addr(k_tiles);
-  const uint32_t v_smem = smem_addr(v_tiles);
-  const uint32_t p_smem = smem_addr(p_tiles);
+  const uint32_t q_smem = smem_addr(smem + T::kOffQ);
+  const uint32_t ring_smem = smem_addr(ring);
+  const uint32_t p_smem = smem_addr(smem + T::kOffP);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&p.map_k);
       tma_prefetch_map(&p.map_v);
-      // one block of a ring: wait for the stage, then the two 64-dim halves
-      auto load = [&](const CUtensorMap* map, uint8_t* tiles, uint64_t* full, uint64_t* empty, int stages,
-                      int j) -> bool {
-        const int st = j % stages;
-        if (!mbar_wait(&empty[st], ((j / stages) & 1u) ^ 1u, ctl)) return false;
+      uint32_t r = 0;   // ring slots filled so far
+      // half `h` of block j: K's dims 64h..64h+63 (all 128 keys), or V's keys
+      // 64h..64h+63 (both 64-dim halves)
+      auto load = [&](bool is_k, int j, int h) -> bool {
+        const uint32_t slot = r % T::kRing;
+        if (!mbar_wait(&ring_empty[slot], ((r / T::kRing) & 1u) ^ 1u, ctl)) return false;
+        uint8_t* dst = ring + slot * T::kSlot;
         const int key0 = (kb0 + j) * T::BKEY;
-        uint8_t* dst = tiles + st * T::kKVTile;
-        mbar_arrive_expect_tx(&full[st], T::kKVTile);
-        tma_load_2d(dst, map, &full[st], 0, key0);
-        tma_load_2d(dst + T::kKVTile / 2, map, &full[st], 64, key0);
+        mbar_arrive_expect_tx(&ring_full[slot], T::kSlot);
+        if (is_k) {
+          tma_load_2d(dst, &p.map_k, &ring_full[slot], 64 * h, key0);
+        } else {
+          tma_load_2d(dst, &p.map_v, &ring_full[slot], 0, key0 + 64 * h);
+          tma_load_2d(dst + T::kSlot / 2, &p.map_v, &ring_full[slot], 64, key0 + 64 * h);
+        }
+        ++r;
         return true;
       };
-      int nk = 0, nv = 0;   // blocks issued on each ring
-      bool ok = load(&p.map_k, k_tiles, k_full, k_empty, T::kKStages, 0);
-      if (ok) nk = 1;
+      bool ok = load(true, 0, 0) && load(true, 0, 1);
       for (int j = 0; j < nb && ok; ++j) {
-        if (j + 1 < nb) {
-          ok = load(&p.map_k, k_tiles, k_full, k_empty, T::kKStages, j + 1);
-          if (!ok) break;
-          nk = j + 2;
-        }
-        ok = load(&p.map_v, v_tiles, v_full, v_empty, T::kVStages, j);
-        if (ok) nv = j + 1;
+        if (j + 1 < nb) ok = load(true, j + 1, 0) && load(true, j + 1, 1);
+        if (ok) ok = load(false, j, 0) && load(false, j, 1);
       }
       // copies issued must land before the CTA may exit
-      for (int i = nk > T::kKStages ? nk - T::kKStages : 0; i < nk; ++i)
-        drain_wait(&k_full[i % T::kKStages], (i / T::kKStages) & 1u, p.wait_limit_ns);
-      for (int i = nv > T::kVStages ? nv - T::kVStages : 0; i < nv; ++i)
-        drain_wait(&v_full[i % T::kVStages], (i / T::kVStages) & 1u, p.wait_limit_ns);
+      for (uint32_t i = r > (uint32_t)T::kRing ? r - T::kRing : 0u; i < r; ++i)
+        drain_wait(&ring_full[i % T::kRing], (i / T::kRing) & 1u, p.wait_limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = make_idesc(0u, false, false, 128, T::BKEY);
-      const uint32_t idesc_o = make_idesc(0u, false, true, 128, 128);
-      const uint32_t q_hi = q_smem, q_lo = q_smem + T::kQTile;
-      const uint32_t p_hi = p_smem, p_lo = p_smem + T::kPTile;
+      const uint32_t idesc_s = make_idesc(0u, false, false, 128, T::kN);   // K K-major, Q K-major
+      const uint32_t idesc_o = make_idesc(0u, true, true, 128, T::kN);     // V^T MN-major, P^T MN-major
+      const uint32_t t_s = tmem_base + T::kColS, t_o = tmem_base + T::kColO;
+      uint32_t r = 0;   // ring slots consumed so far (the producer's order)
       bool ok = mbar_wait(q_ready, 0, ctl);
       tc_fence_after_sync();
-      // one S buffer: S_j is issued once the compute warps have read S_(j-1)
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t st = j % T::kKStages;
-        if (!mbar_wait(&k_full[st], (j / T::kKStages) & 1u, ctl)) return false;
-        if (!mbar_wait(s_empty, (j & 1u) ^ 1u, ctl)) return false;
+      auto take_slot = [&](uint32_t& base) -> bool {
+        const uint32_t slot = r % T::kRing;
+        if (!mbar_wait(&ring_full[slot], (r / T::kRing) & 1u, ctl)) return false;
         tc_fence_after_sync();
-        const uint32_t kt = k_smem + st * T::kKVTile;
-        const uint32_t d_hi = tmem_base + T::kColS;
+        base = ring_smem + slot * T::kSlot;
+        return true;
+      };
+      auto release_slot = [&]() {
+        mma_commit(&ring_empty[r % T::kRing]);
+        ++r;
+      };
+      // S^T_j: A = K_j (keys x dims, K-major), B = [Q_hi ; Q_lo] (K-major)
+      auto issue_s = [&](int j) -> bool {
+        if (!mbar_wait(s_empty, (j & 1u) ^ 1u, ctl)) return false;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t kt;
+          if (!take_slot(kt)) return false;
 #pragma unroll
-        for (int ks = 0; ks < T::D / 16; ++ks) {
-          const uint64_t bk = kmajor_desc(kt, T::BKEY, ks);
-          mma_f16(d_hi, kmajor_desc(q_hi, 128, ks), bk, idesc_s, ks > 0 ? 1u : 0u);
-          if constexpr (T::kL == 11) {
-            mma_f16(d_hi + T::BKEY, kmajor_desc(q_lo, 128, ks), bk, idesc_s, ks > 0 ? 1u : 0u);
-          } else {
-            mma_f16(d_hi, kmajor_desc(q_lo, 128, ks), bk, idesc_s, 1u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = kmajor_desc(kt, kk);
+            const uint32_t qh = q_smem + (uint32_t)h * 32768u;
+            const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (T::kL == 11) {
+              mma_f16(t_s, a, kmajor_desc(qh, kk), idesc_s, acc);
+            } else {
+              mma_f16(t_s, a, kmajor_desc(qh, kk), idesc_s, acc);
+              mma_f16(t_s, a, kmajor_desc(qh + 16384u, kk), idesc_s, 1u);
+            }
           }
+          release_slot();
         }
         mma_commit(s_full);
-        mma_commit(&k_empty[st]);
         return true;
       };
+      // O^T_j (+)= V_j^T P_j^T: A = V^T (dims x keys, MN-major), B = [P_hi ; P_lo]^T (MN-major)
       auto issue_o = [&](int j) -> bool {
-        const uint32_t st = j % T::kVStages;
         if (!mbar_wait(p_full, j & 1u, ctl)) return false;
-        if (!mbar_wait(&v_full[st], (j / T::kVStages) & 1u, ctl)) return false;
         if (!mbar_wait(o_empty, (j & 1u) ^ 1u, ctl)) return false;
         tc_fence_after_sync();
-        const uint32_t vt = v_smem + st * T::kKVTile;
-        const uint32_t d_hi = tmem_base + T::kColOhi, d_lo = tmem_base + T::kColOlo;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t vt;
+          if (!take_slot(vt)) return false;
 #pragma unroll
-        for (int ks = 0; ks < T::BKEY / 16; ++ks) {
-          const uint64_t bv = mnmajor_desc(vt, T::BKEY, ks);
-          // O accumulates across blocks: the compute warps fold it into
-          // registers (and zero it) every few blocks
-          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-          mma_f16(d_hi, p_desc(p_hi, T::kPCol0, ks), bv, idesc_o, acc);
-          if constexpr (T::kL == 11) {
-            mma_f16(d_lo, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, acc);
-          } else {
-            mma_f16(d_hi, p_desc(p_lo, T::kPCol0, ks), bv, idesc_o, 1u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const int ks = 4 * h + kk;
+            const uint64_t a = mnmajor_desc(vt, 64, kk);
+            // the chains restart after a fold zeroed them (j = 0: nothing to keep)
+            const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+            if constexpr (T::kL == 11) {
+              mma_f16(t_o, a, mnmajor_desc(p_smem, T::BKEY, ks), idesc_o, acc);
+            } else {
+              mma_f16(t_o, a, mnmajor_desc(p_smem, T::BKEY, ks), idesc_o, acc);
+              mma_f16(t_o, a, mnmajor_desc(p_smem + 2u * T::BKEY * 128u, T::BKEY, ks), idesc_o, 1u);
+            }
           }
+          release_slot();
         }
         mma_commit(o_full);
-        mma_commit(p_empty);
-        mma_commit(&v_empty[st]);
         return true;
       };
-      // S_(j+1) goes in as soon as the compute warps have read S_j (while
-      // O_(j-1) runs), then O_j once P_j is written
       if (ok) ok = issue_s(0);
       for (int j = 0; j < nb && ok; ++j) {
         if (j + 1 < nb) ok = issue_s(j + 1);
@@ -311,15 +389,14 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   } else {
     // ------------------------------------------------------------ Q split (compute warps)
     {
-      // 128 rows x 16 chunks of 8 dims; each thread takes CPT consecutive chunks of one row
-      constexpr int CPT = 2048 / T::kComputeThreads;
+      // 128 rows x 16 chunks of 8 dims; each thread takes 4 consecutive chunks of one row
       const int ct = threadIdx.x - 64;
-      const int row = ct / (16 / CPT);
-      const int c0 = (ct % (16 / CPT)) * CPT;
-      const int64_t grow = (int64_t)qb * T::BM + row;
+      const int row = ct >> 2;
+      const int c0 = (ct & 3) * 4;
+      const int64_t grow = (int64_t)qb * T::BQ + row;
       const float* src = p.q + grow * p.ldq;
 #pragma unroll 1
-      for (int c = c0; c < c0 + CPT; ++c) {
+      for (int c = c0; c < c0 + 4; ++c) {
         float x[8];
         if (grow < p.lq) {
           if (p.q_vec_ok) {
@@ -334,205 +411,251 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.0f;
         }
+        // q * scale * log2(e), split: the scores come out in base-2 units
         uint32_t h[4], l[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_pair<T::kL>(x[2 * e], x[2 * e + 1], 1.0f, h[e], l[e]);
-        // dims 8c..8c+7: atom column c / 8, 16-byte chunk c % 8 of row `row`
-        const uint32_t hi_base = q_smem + (uint32_t)(c >> 3) * T::BM * 128u;
+        for (int e = 0; e < 4; ++e) split_pair<T::kL>(x[2 * e], x[2 * e + 1], p.scale_log2, h[e], l[e]);
+        // dims 8c..8c+7: dim half c / 8, chunk c % 8 of line `row` (hi) and `128 + row` (lo)
+        const uint32_t base = q_smem + (uint32_t)(c >> 3) * 32768u;
         const uint32_t off = swz_chunk_offset<128>((uint32_t)row, (uint32_t)(c & 7));
-        st_shared_v4(hi_base + off, h[0], h[1], h[2], h[3]);
-        st_shared_v4(hi_base + T::kQTile + off, l[0], l[1], l[2], l[3]);
+        st_shared_v4(base + off, h[0], h[1], h[2], h[3]);
+        st_shared_v4(base + 16384u + off, l[0], l[1], l[2], l[3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
     }
-    constexpr int KP = T::KP, DP = T::DP, NP = T::kParts;
-    const int q4 = warp & 3;                      // TMEM lane quarter of this warp
-    const int part = (warp - 2) >> 2;             // keys KP*part.., dims DP*part.. of the rows
-    const int r = 32 * q4 + lane;                 // query row within the block
+    const int cw = warp - 2;
+    const int q4 = warp & 3;                      // TMEM lane quarter: keys (S^T) and dims (O^T) 32*q4..
+    const int grp = cw >> 2;                      // query columns 32*grp .. 32*grp+31
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    float o[DP];
+    float* m_w = warp_vals + cw * 96;             // m_ref of the group's 32 queries
+    float* f_w = m_w + 32;                        // factor of the last move of m_ref (1 / sum at the end)
+    float* d_w = m_w + 64;                        // the last move of m_ref
+    float* pmax = part_max + grp * 128;           // + exchange parity * 512: [quarter][32]
+    int* pflag = flags + grp * 4;                 // + exchange parity * 16: [quarter]
+    float o[32];   // O_run of dim 32*q4 + lane for the group's 32 queries, relative to m_ref
 #pragma unroll
-    for (int i = 0; i < DP; ++i) o[i] = 0.0f;
-    // m_ref: the reference maximum of the probabilities (p = 2^(s - m_ref))
-    // and of the O chains accumulating in TMEM; it moves only when a block's
-    // maximum exceeds it by more than kLazyLog2 (p stays <= 2^kLazyLog2).
-    // o (registers) holds the folded blocks relative to r_reg.
-    float m_ref = -INFINITY, r_reg = -INFINITY, l_part = 0.0f;
-    uint32_t nx = 0;   // exchanges with the other parts of the rows so far
+    for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+    // lane l keeps the reference maximum (base 2) and this quarter's sum of
+    // query 32*grp + l; the first block always sets the reference
+    float m_l = 0.0f, l_l = 0.0f;
+    m_w[lane] = 0.0f;
+    __syncwarp();
+    uint32_t nx = 0;   // exchanges of the column group so far
     bool ok = true;
-    // step t: softmax of block t (t < nb), then correction of block t-1 (t >= 1)
-    for (int t = 0; t <= nb && ok; ++t) {
-      bool rescale = false;        // softmax of block t moved m_ref
-      float o_ref = m_ref;         // the reference of the O chains in TMEM
-      if (t < nb) {
-        // ---------------------------------------------------------- softmax of block t
-        const int j = t;
-        if (!warp_wait(s_full, j & 1u, ctl)) { ok = false; break; }
-        tc_fence_after_sync();
-        float s[KP];
-        const uint32_t t_hi = tmem_base + lane_off + T::kColS + (uint32_t)(KP * part);
-        {
+    // Fold of the O^T chains into the registers: the chains hold the blocks
+    // since the last fold, relative to the m_ref before the current block.
+    // They are added (hi and lo summed in fp32) and, when the current block
+    // moved m_ref, registers and chains are scaled by 2^(m_old - m_new) per
+    // query; `zero` restarts the chains for the next block's products.
+    auto fold = [&](bool moved, bool zero) {
+      tc_fence_after_sync();
+      const uint32_t to = tmem_base + lane_off + T::kColO + 32u * grp;
 #pragma unroll
-          for (int c = 0; c < KP / 8; ++c) tmem_ld_8cols(t_hi + 8 * c, s + 8 * c);
-          if constexpr (T::kL == 11) {
-            float lo[KP];
+      for (int c = 0; c < 8; ++c) {
+        float a[4];
+        tmem_ld_4cols(to + 4 * c, a);
+        if constexpr (T::kL == 11) {
+          float b[4];
+          tmem_ld_4cols(to + 128 + 4 * c, b);
+          tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < KP / 8; ++c) tmem_ld_8cols(t_hi + T::BKEY + 8 * c, lo + 8 * c);
-            tmem_ld_wait();
+          for (int i = 0; i < 4; i += 2) {
+            const float2 d = ffma2(make_float2(b[i], b[i + 1]), make_float2(kLoScale, kLoScale),
+                                   make_float2(a[i], a[i + 1]));
+            a[i] = d.x;
+            a[i + 1] = d.y;
+          }
+        } else {
+          tmem_ld_wait();
+        }
+        if (moved) {
+          const float4 f = reinterpret_cast<const float4*>(f_w)[c];
+          o[4 * c] = (o[4 * c] + a[0]) * f.x;
+          o[4 * c + 1] = (o[4 * c + 1] + a[1]) * f.y;
+          o[4 * c + 2] = (o[4 * c + 2] + a[2]) * f.z;
+          o[4 * c + 3] = (o[4 * c + 3] + a[3]) * f.w;
+        } else {
 #pragma unroll
-            for (int i = 0; i < KP; ++i) s[i] = (s[i] + kLoScale * lo[i]) * p.scale_log2;
-          } else {
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < KP; ++i) s[i] = s[i] * p.scale_log2;
+          for (int i = 0; i < 4; i += 2) {
+            const float2 d = fadd2(make_float2(o[4 * c + i], o[4 * c + i + 1]), make_float2(a[i], a[i + 1]));
+            o[4 * c + i] = d.x;
+            o[4 * c + i + 1] = d.y;
           }
         }
-        tc_fence_before_sync();
-        mbar_arrive(s_empty);
-        // keys past the end of the sequence score -inf (only the last block
-        // of the sequence has any)
-        const int valid = p.lk - (kb0 + j) * T::BKEY - KP * part;
-        if (valid < KP) {
-#pragma unroll
-          for (int i = 0; i < KP; ++i)
-            if (i >= valid) s[i] = -INFINITY;
-        }
-        // maximum over this part's keys: eight running maxima, then a tree
-        float tr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) tr[i] = s[i];
-#pragma unroll
-        for (int i = 8; i < KP; ++i) tr[i & 7] = fmaxf(tr[i & 7], s[i]);
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) tr[i] = fmaxf(tr[i], tr[i + w]);
-        // the parts of the row agree on the block's maximum
-        float* mx = part_max + ((j & 1) * NP) * T::BM;
-        mx[part * T::BM + r] = tr[0];
-        mbar_arrive(&xchg[q4]);
-        if (!warp_wait(&xchg[q4], nx & 1u, ctl)) { ok = false; break; }
-        ++nx;
-        float m_blk = mx[r];
-#pragma unroll
-        for (int k = 1; k < NP; ++k) m_blk = fmaxf(m_blk, mx[k * T::BM + r]);
-        if (m_blk > m_ref + kLazyLog2) {   // always on the first block
-          rescale = true;
-          m_ref = m_blk;
-        }
-        const float alpha_l = exp2_approx(o_ref - m_ref);   // 1 unless m_ref moved; 0 on the first block
-#pragma unroll
-        for (int i = 0; i < KP; ++i) s[i] = exp2_approx(s[i] - m_ref);
-        // sum: eight running sums, then a tree
-#pragma unroll
-        for (int i = 0; i < 8; ++i) tr[i] = s[i];
-#pragma unroll
-        for (int i = 8; i < KP; ++i) tr[i & 7] += s[i];
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) tr[i] += tr[i + w];
-        l_part = l_part * alpha_l + tr[0];
-        // p split into hi/lo fp16: this part's 8-key chunks of row r of the A
-        // tiles (chunks 0-7 in the 128-byte swizzled column, 8-11 in the
-        // 64-byte swizzled one)
-        if (!warp_wait(p_empty, (j & 1u) ^ 1u, ctl)) { ok = false; break; }
-        const uint32_t p_hi = p_smem, p_lo = p_smem + T::kPTile;
-#pragma unroll
-        for (int cc = 0; cc < KP / 8; ++cc) {
-          uint32_t h[4], l[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split_pair<T::kL>(s[8 * cc + 2 * e], s[8 * cc + 2 * e + 1], 1.0f, h[e], l[e]);
-          const uint32_t c = (uint32_t)((KP / 8) * part + cc);
-          const uint32_t off = c < 8 ? swz_chunk_offset<128>((uint32_t)r, c)
-                                     : (uint32_t)T::kPCol0 + swz_chunk_offset<64>((uint32_t)r, c - 8);
-          st_shared_v4(p_hi + off, h[0], h[1], h[2], h[3]);
-          st_shared_v4(p_lo + off, l[0], l[1], l[2], l[3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(p_full);
       }
-      if (t >= 1) {
-        // ---------------------------------------------------------- fold after block t-1
-        // The O chains hold the blocks since the last fold, relative to
-        // o_ref.  They are added to the registers (round to nearest, the
-        // hi and lo chains summed in fp32) and zeroed every kFoldBlocks
-        // blocks (bounding how long the tensor cores accumulate), before
-        // block t's products when m_ref moved, and at the end; otherwise
-        // the next block's products accumulate on top of them.
-        const int j = t - 1;
-        if (!warp_wait(o_full, j & 1u, ctl)) { ok = false; break; }
-        // tcgen05.ld/st are warp-collective: the warp folds all its rows when
-        // any of them moved its reference (for the others a_tm is 1)
-        const bool fold = __any_sync(0xffffffffu, rescale) || t % kFoldBlocks == 0 || t == nb;
-        if (fold) {
-          tc_fence_after_sync();
-          const uint32_t t_hi = tmem_base + lane_off + T::kColOhi + (uint32_t)(DP * part);
-          const uint32_t t_lo = tmem_base + lane_off + T::kColOlo + (uint32_t)(DP * part);
-          const float a_reg = exp2_approx(r_reg - m_ref);   // 0 before the first fold
-          const float a_tm = exp2_approx(o_ref - m_ref);
-          constexpr int CW = DP / 2;   // columns per TMEM load
+      if (zero) {
+        float z[16];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            float a[CW];
-            if constexpr (CW == 32) tmem_ld_32cols(t_hi + CW * c, a); else tmem_ld_16cols(t_hi + CW * c, a);
-            if constexpr (T::kL == 11) {
-              float e[CW];
-              if constexpr (CW == 32) tmem_ld_32cols(t_lo + CW * c, e); else tmem_ld_16cols(t_lo + CW * c, e);
-              tmem_ld_wait();
+        for (int i = 0; i < 16; ++i) z[i] = 0.0f;
 #pragma unroll
-              for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], a_reg, (a[i] + kLoScale * e[i]) * a_tm);
-            } else {
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < CW; ++i) o[CW * c + i] = fmaf(o[CW * c + i], a_reg, a[i] * a_tm);
-            }
-          }
-          r_reg = m_ref;
-          if (t < nb) {
-            // the next block's products start the chains again
-            float z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < DP / 16; ++c) {
-              tmem_st_16cols(t_hi + 16 * c, z);
-              if constexpr (T::kL == 11) tmem_st_16cols(t_lo + 16 * c, z);
-            }
-            tmem_st_wait();
-          }
+        for (int c = 0; c < 2; ++c) {
+          tmem_st_16cols(to + 16 * c, z);
+          if constexpr (T::kL == 11) tmem_st_16cols(to + 128 + 16 * c, z);
         }
+        tmem_st_wait();
+      }
+    };
+    // Block j: read S_j (S_(j+1) may then go in), x = s - m_ref and the
+    // group's agreement on m_ref, p = 2^x; then, once O_(j-1) has completed
+    // (which also frees the P^T tile), the fold when it is due and the
+    // release of the O^T chains; then P_j, which lets O_j go in; then the
+    // sums, while O_j runs.
+    for (int j = 0; j < nb && ok; ++j) {
+      if (!warp_wait(s_full, j & 1u, ctl)) { ok = false; break; }
+      tc_fence_after_sync();
+      float x[32];
+      const uint32_t ts = tmem_base + lane_off + T::kColS + 32u * grp;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float a[8];
+        tmem_ld_8cols(ts + 8 * h, a);
+        if constexpr (T::kL == 11) {
+          float b[8];
+          tmem_ld_8cols(ts + 128 + 8 * h, b);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float2 d = ffma2(make_float2(b[i], b[i + 1]), make_float2(kLoScale, kLoScale),
+                                   make_float2(a[i], a[i + 1]));
+            x[8 * h + i] = d.x;
+            x[8 * h + i + 1] = d.y;
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[8 * h + i] = a[i];
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(s_empty);
+      // keys past the end of the sequence score -inf (only the block that
+      // crosses the end has any); x = s - m_ref
+      if ((kb0 + j + 1) * T::BKEY > p.lk && (kb0 + j) * T::BKEY + 32 * q4 + lane >= p.lk) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
+      }
+      float xm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 m = reinterpret_cast<const float4*>(m_w)[i / 4];
+        const float2 d0 = fsub2(make_float2(x[i], x[i + 1]), make_float2(m.x, m.y));
+        const float2 d1 = fsub2(make_float2(x[i + 2], x[i + 3]), make_float2(m.z, m.w));
+        x[i] = d0.x;
+        x[i + 1] = d0.y;
+        x[i + 2] = d1.x;
+        x[i + 3] = d1.y;
+        xm = fmax3(xm, fmax3(x[i], x[i + 1], x[i + 2]), x[i + 3]);
+      }
+      // the group's four warps agree whether any of its queries needs a new reference
+      const bool raise = (j == 0) || __any_sync(0xffffffffu, xm > kLazyLog2);
+      int* fl = pflag + (nx & 1u) * 16;
+      if (lane == 0) fl[q4] = raise ? 1 : 0;
+      mbar_arrive(&xchg[grp]);
+      if (!warp_wait(&xchg[grp], nx & 1u, ctl)) { ok = false; break; }
+      ++nx;
+      const int4 fv = *reinterpret_cast<const int4*>(fl);
+      bool moved = false;   // block j moved m_ref of one of the group's queries (same in its four warps)
+      if ((fv.x | fv.y | fv.z | fv.w) != 0) {
+        // per-query maxima of x over the group's 128 keys: warp maxima, exchanged
+        float* pm = pmax + (nx & 1u) * 512;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float a0 = warp_max(x[i]), a1 = warp_max(x[i + 1]);
+          const float a2 = warp_max(x[i + 2]), a3 = warp_max(x[i + 3]);
+          if (lane == 0) reinterpret_cast<float4*>(pm + q4 * 32)[i / 4] = make_float4(a0, a1, a2, a3);
+        }
+        mbar_arrive(&xchg[grp]);
+        if (!warp_wait(&xchg[grp], nx & 1u, ctl)) { ok = false; break; }
+        ++nx;
+        const float mb = fmaxf(fmaxf(pm[lane], pm[32 + lane]), fmaxf(pm[64 + lane], pm[96 + lane]));
+        const bool mv = (j == 0) || mb > kLazyLog2;
+        const float dm = mv ? mb : 0.0f;
+        // 2^(m_old - m_new); nothing is kept before the first block
+        const float fac = (j == 0) ? 0.0f : (mv ? exp2_approx(-mb) : 1.0f);
+        m_l += dm;
+        l_l *= fac;
+        moved = __any_sync(0xffffffffu, mv);
+        m_w[lane] = m_l;
+        f_w[lane] = fac;
+        d_w[lane] = dm;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 d = reinterpret_cast<const float4*>(d_w)[i / 4];
+          const float2 d0 = fsub2(make_float2(x[i], x[i + 1]), make_float2(d.x, d.y));
+          const float2 d1 = fsub2(make_float2(x[i + 2], x[i + 3]), make_float2(d.z, d.w));
+          x[i] = d0.x;
+          x[i + 1] = d0.y;
+          x[i + 2] = d1.x;
+          x[i + 3] = d1.y;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = exp2_approx(x[i]);
+      if (j >= 1) {
+        // O_(j-1) has completed: fold after every kFoldBlocks blocks and
+        // before products relative to a moved m_ref, then release the chains
+        if (!warp_wait(o_full, (j - 1) & 1u, ctl)) { ok = false; break; }
+        if (moved || j % kFoldBlocks == 0) fold(moved, true);
         tc_fence_before_sync();
         mbar_arrive(o_empty);
       }
-    }
-    // the row's sum is the sum of its parts' sums
-    if (ok) {
-      part_sum[part * T::BM + r] = l_part;
-      mbar_arrive(&xchg[q4]);
-      ok = warp_wait(&xchg[q4], nx & 1u, ctl);
-    }
-    float l_row = 0.0f;
-    if (ok) {
+      // P^T: this lane's key (line), the group's 32 queries as 4 chunks of
+      // 8 in atom grp / 2 (hi) and 2 + grp / 2 (lo)
+      {
+        const uint32_t key = (uint32_t)(32 * q4 + lane);
+        const uint32_t line = p_smem + (uint32_t)(grp >> 1) * (T::BKEY * 128u) + key * 128u;
 #pragma unroll
-      for (int k = 0; k < NP; ++k) l_row += part_sum[k * T::BM + r];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2<T::kL>(x[8 * c + 2 * e], x[8 * c + 2 * e + 1], h[e], l[e]);
+          const uint32_t off = (((uint32_t)((grp & 1) * 4 + c)) ^ (key & 7u)) << 4;
+          st_shared_v4(line + off, h[0], h[1], h[2], h[3]);
+          st_shared_v4(line + 2u * T::BKEY * 128u + off, l[0], l[1], l[2], l[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(p_full);
+      // this quarter's sum of p per query: query 32*grp + l in lane l
+      l_l += reduce_scatter_sum(x, lane);
     }
-    const int64_t grow = (int64_t)qb * T::BM + r;
-    if (ok && grow < p.lq) {
+    // the last fold, once the last block's products have completed
+    if (ok) {
+      ok = warp_wait(o_full, (nb - 1) & 1u, ctl);
+      if (ok) fold(false, false);
+    }
+    // the query's sum is the sum of its four quarters' sums
+    float* ps = part_sum + grp * 128;
+    if (ok) {
+      ps[q4 * 32 + lane] = l_l;
+      mbar_arrive(&xchg[grp]);
+      ok = warp_wait(&xchg[grp], nx & 1u, ctl);
+      ++nx;
+    }
+    if (ok) {
+      const float lsum = (ps[lane] + ps[32 + lane]) + (ps[64 + lane] + ps[96 + lane]);
+      const int64_t q0 = (int64_t)qb * T::BQ + 32 * grp;
+      const int dim = 32 * q4 + lane;
       if (p.splits == 1) {
-        const float inv = 1.0f / l_row;
-        float* dst = p.o + grow * p.ldo + DP * part;
+        f_w[lane] = 1.0f / lsum;
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < DP; ++i) dst[i] = o[i] * inv;
+        for (int i = 0; i < 32; i += 4) {
+          const float4 f = reinterpret_cast<const float4*>(f_w)[i / 4];
+          const float fs[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (q0 + i + e < p.lq) p.o[(q0 + i + e) * p.ldo + dim] = o[i + e] * fs[e];
+        }
       } else {
-        float* dst = p.part_o + ((int64_t)split * p.lq + grow) * 128 + DP * part;
 #pragma unroll
-        for (int i = 0; i < DP; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-        if (part == 0) {
-          p.part_m[(int64_t)split * p.lq + grow] = m_ref;
-          p.part_l[(int64_t)split * p.lq + grow] = l_row;
+        for (int i = 0; i < 32; ++i)
+          if (q0 + i < p.lq) p.part_o[((int64_t)split * p.lq + q0 + i) * 128 + dim] = o[i];
+        if (q4 == 0 && q0 + lane < p.lq) {
+          p.part_m[(int64_t)split * p.lq + q0 + lane] = m_l;
+          p.part_l[(int64_t)split * p.lq + q0 + lane] = lsum;
         }
       }
     }
@@ -582,14 +705,11 @@ cudaError_t launch_kernel(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// warps per TMEM lane quarter of the compute warpgroups
-constexpr int kAttnParts = 4;
-
-int attention_smem_bytes() { return AttnTraits<true, kAttnParts>::kSmemBytes; }
+int attention_smem_bytes() { return AttnTraits<true>::kSmemBytes; }
 
 cudaError_t launch_attention(const AttnParams& p, bool two_chain, cudaStream_t stream) {
-  cudaError_t e = two_chain ? launch_kernel<AttnTraits<true, kAttnParts>>(p, stream)
-                            : launch_kernel<AttnTraits<false, kAttnParts>>(p, stream);
+  cudaError_t e = two_chain ? launch_kernel<AttnTraits<true>>(p, stream)
+                            : launch_kernel<AttnTraits<false>>(p, stream);
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t items = (int64_t)p.lq * 32;
   attn_merge_kernel<<<(unsigned)((items + 255) / 256), 256, 0, stream>>>(p);

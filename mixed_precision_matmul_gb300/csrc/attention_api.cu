@@ -86,7 +86,7 @@ mpg_status mpg_attention(int64_t lq, int64_t lk, int64_t d, const float* Q, int6
   Operand Vop{V, ldv, 0, MPG_F16, MPG_ROW_MAJOR};
   s = encode_map(&p.map_k, Kop, d, lk, 1, 64, kAttnKeyBlock);
   if (s != MPG_OK) return s;
-  s = encode_map(&p.map_v, Vop, d, lk, 1, 64, kAttnKeyBlock);
+  s = encode_map(&p.map_v, Vop, d, lk, 1, 64, kAttnKeyBlock / 2);
   if (s != MPG_OK) return s;
   p.q = Q;
   p.ldq = ldq;

@@ -107,11 +107,11 @@ cudaError_t launch_transpose32(const void* in, int64_t ld_in, int64_t stride_in,
 
 // Fused prompt attention O = softmax(scale * Q K^T) V (head dimension 128).
 // Keys per block of the fused attention (the K and V tensor maps' box).
-constexpr int kAttnKeyBlock = 96;
+constexpr int kAttnKeyBlock = 128;
 
 struct AttnParams {
   CUtensorMap map_k;   // K: fp16 [lk][ldk], box 64 dims x kAttnKeyBlock keys
-  CUtensorMap map_v;   // V: fp16 [lk][ldv], same box
+  CUtensorMap map_v;   // V: fp16 [lk][ldv], box 64 dims x kAttnKeyBlock / 2 keys
   const float* q;      // fp32 [lq][ldq]
   int64_t ldq;
   float* o;            // fp32 [lq][ldo]

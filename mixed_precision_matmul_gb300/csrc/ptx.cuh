@@ -212,6 +212,17 @@ __device__ __forceinline__ void tmem_ld_8cols(uint32_t taddr, float* v) {
   for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 32 lanes x 4 consecutive 32-bit columns (same lane/column mapping).
+__device__ __forceinline__ void tmem_ld_4cols(uint32_t taddr, float* v) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 // Store 16 consecutive 32-bit columns of the warp's 32 lanes.
 __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const float* v) {
   asm volatile(
