@@ -8,47 +8,49 @@
 // separate TMEM chains that are added in plain fp32 (the two-chain form), or
 // in one chain (the single-chain form the fix replaced).
 //
-// Both products are computed transposed, keys and head dimensions on the
-// M side and the queries on the N side:
-//     S^T = K [Q_hi ; Q_lo]^T     M 128 keys, N 256 = 128 queries x (hi, lo), K 128 dims
+// The scores are computed with the queries on the M side, the output
+// transposed (head dimensions on M, queries on N):
+//     S   = [Q_hi ; Q_lo] K^T     two chains of M 128 queries, N 128 keys, K 128 dims
 //     O^T = V^T [P_hi ; P_lo]^T   M 128 dims, N 256 = 128 queries x (hi, lo), K 128 keys
-// so that the hi and lo chains of one k-step are a single N = 256
-// instruction (the tensor core's full rate; instructions with N <= 128 cost
-// about as much as N = 256 ones), 8 instructions per product and block.  The
-// single-chain form issues the hi and lo halves as two N = 128 instructions
-// into one accumulator.
+// S keeps a query's scores in one TMEM lane, so the softmax's maxima and
+// sums stay inside a thread; O^T puts the hi and lo chains of one k-step in a
+// single N = 256 instruction (the tensor core's full rate), and P, written
+// row by row, is its K-major B operand.  The single-chain form accumulates
+// the hi and lo halves in one chain: S's lo products into the hi chain, O^T
+// as two N = 128 instructions into one accumulator.
 //
 // One CTA takes 128 queries and a range of keys, in blocks of 128 keys:
 //   warp 0      TMA producer: one ring of five 16 KB slots that K and V
 //               share, filled in the order the MMAs read them: K_(j+1) (two
 //               64-dim halves), then V_j (two 64-key halves).
 //   warp 1      TMEM allocation; lane 0 issues every MMA, in the order S_(j+1),
-//               O_j: S^T has one TMEM buffer (columns 0-255), and S_(j+1) goes
-//               in as soon as the compute warps have read S_j; O^T
-//               (columns 256-511) accumulates the blocks between folds.
-//   warps 2-17  softmax and folds of O.  Warp w reads TMEM lane quarter
-//               w % 4 (32 keys of S^T, 32 dims of O^T) and one of four 32-query
-//               column groups; lane l holds one key (or dim) for 32 queries.
+//               O_j: S has one TMEM buffer (hi chain in columns 0-127, lo in
+//               128-255), and S_(j+1) goes in as soon as the compute warps have
+//               read S_j; O^T (columns 256-511) accumulates the blocks between
+//               folds.  Per 64-dim half of K, S's hi chain takes its four
+//               k-steps before the lo chain's.
+//   warps 2-17  softmax and folds of O.  Warp w reads TMEM lane quarter w % 4
+//               (32 query rows of S, 32 dims of O^T); its part w / 4 - 1 picks
+//               32 of a block's keys (softmax) and 32 query columns (folds).
 //               softmax of block j: s = S_hi + 2^-11 S_lo (q was scaled by
-//               scale * log2(e) before the split), x = s - m_ref per query;
-//               m_ref (one per query, the same in the four warps of a column
-//               group) moves only when a block's maximum exceeds it by more
-//               than 8 (lazy rescaling, p = 2^x <= 2^8).  The four warps of a
-//               column group exchange one flag per block (shared memory and
-//               an mbarrier, waited on with the bounded wait); only when one
-//               is raised do they exchange per-query maxima (warp maxima by
-//               redux.sync) and move m_ref.  p = 2^x is split into hi/lo
-//               fp16 and written to shared memory as P^T (keys x queries,
-//               the B operand of O^T); each warp sums p over its 32 keys per
-//               query (a shuffle reduce-scatter leaves query l's sum in lane l).
+//               scale * log2(e) before the split), x = s - m_ref of the row;
+//               m_ref (the same in the four parts of a row) moves only when a
+//               block's maximum exceeds it by more than 8 (lazy rescaling,
+//               p = 2^x <= 2^8).  The compute warps exchange one flag per
+//               block (shared memory and an mbarrier, waited on with the
+//               bounded wait); only when one is raised do they exchange the
+//               parts' maxima and move m_ref.  p = 2^x is split into hi/lo
+//               fp16 and written to shared memory as P (queries x keys, the B
+//               operand of O^T); each part sums p over its keys.
 //               fold: O_run += O_hi + 2^-11 O_lo (round to nearest, in
-//               registers; times 2^(m_old - m_new) per query when m_ref
-//               moved), then the O^T chains are zeroed; after every fourth
-//               block, before a block whose softmax moved m_ref, and at the
-//               end.  Order within block j: read S_j (S_(j+1) may go in),
-//               the exchange, p = 2^x; once O_(j-1) has completed, the fold
-//               when due and the release of the chains; the P^T write (O_j
-//               may go in); the sums, while O_j runs.
+//               registers; times 2^(m_old - m_new) per query when m_ref moved,
+//               the factors recomputed from the exchanged maxima), then the
+//               O^T chains are zeroed; after every fourth block, before a
+//               block whose softmax moved m_ref, and at the end.  Order within
+//               block j: read S_j (S_(j+1) may go in), the exchange, p = 2^x
+//               and the sums; once O_(j-1) has completed, the P write (O_j may
+//               go in once the chains are released), then the fold when due
+//               and the release.
 //   At the end O = O_run / sum, or the unnormalised partial with its m_ref
 //   and sum when the keys are split across CTAs (attn_merge_kernel combines
 //   the partials).
@@ -70,14 +72,14 @@ struct AttnTraits {
   // Q: [2 dim halves][256 lines: q_hi of queries 0-127, q_lo of 0-127][128 B], 128-byte swizzle
   static constexpr int kOffQ = 0;
   static constexpr int kOffRing = kOffQ + 2 * 256 * 128;
-  // P^T: [4 atoms: hi queries 0-63, hi 64-127, lo 0-63, lo 64-127][128 keys][128 B]
+  // P: [2 key columns: keys 0-63, 64-127][256 lines: p_hi of queries 0-127, p_lo of 0-127][128 B]
   static constexpr int kOffP = kOffRing + kRing * kSlot;
-  static constexpr int kOffMax = kOffP + 4 * BKEY * 128;        // [2][4 groups][4 quarters][32] maxima
-  static constexpr int kOffFlag = kOffMax + 2 * 4 * 4 * 32 * 4;  // [2][4 groups][4 quarters] flags
-  static constexpr int kOffSum = kOffFlag + 2 * 4 * 4 * 4;       // [4 groups][4 quarters][32] sums
-  static constexpr int kOffWarp = kOffSum + 4 * 4 * 32 * 4;      // [16 warps][3][32] per-query values
-  static constexpr int kOffBars = kOffWarp + 16 * 3 * 32 * 4;
-  static constexpr int kNumBars = 2 * kRing + 7 + 4;
+  static constexpr int kOffMax = kOffP + 2 * 256 * 128;         // [2][4 parts][128 rows] maxima
+  static constexpr int kOffFlag = kOffMax + 2 * 4 * 128 * 4;     // [2][16 warps] flags
+  static constexpr int kOffSum = kOffFlag + 2 * 16 * 4;          // [4 parts][128 rows] sums
+  static constexpr int kOffWarp = kOffSum + 4 * 128 * 4;         // [16 warps][32] per-query factors
+  static constexpr int kOffBars = kOffWarp + 16 * 32 * 4;
+  static constexpr int kNumBars = 2 * kRing + 7 + 1;
   static constexpr int kSmemBytes = 1024 + kOffBars + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr int kComputeThreads = 512;
@@ -161,42 +163,6 @@ __device__ __forceinline__ void split2(float p0, float p1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Maximum of v over the warp's 32 lanes (every lane gets it).
-__device__ __forceinline__ float warp_max(float v) {
-  float m;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
-  return m;
-}
-
-// Reduce-scatter of 32 values over the warp: afterwards lane l returns the
-// sum over all lanes of v[l] (v is overwritten).  Step w halves the values
-// a lane keeps: lanes with bit w set keep the upper half and send the lower
-// one to their partner (lane ^ w), which keeps the lower half.
-__device__ __forceinline__ float reduce_scatter_sum(float (&v)[32], int lane) {
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool up = (lane & w) != 0;
-    float keep[16], recv[16];
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = up ? v[i] : v[i + w];
-      keep[i] = up ? v[i + w] : v[i];
-      recv[i] = __shfl_xor_sync(0xffffffffu, send, w);
-    }
-    if (w == 1) {
-      v[0] = keep[0] + recv[0];
-    } else {
-#pragma unroll
-      for (int i = 0; i < w; i += 2) {
-        const float2 d = fadd2(make_float2(keep[i], keep[i + 1]), make_float2(recv[i], recv[i + 1]));
-        v[i] = d.x;
-        v[i + 1] = d.y;
-      }
-    }
-  }
-  return v[0];
-}
-
 // 128-byte swizzled K-major tile (lines of 128 bytes, 8-line groups 1024
 // bytes apart), k-step `kk` (16 fp16 = 32 bytes) within one atom column.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
@@ -231,8 +197,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   uint64_t* o_empty = s_full + 4;
   uint64_t* q_ready = s_full + 5;
   uint64_t* done_bar = s_full + 6;
-  uint64_t* xchg = s_full + 7;              // [4]: the four warps of a column group exchange values
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 4);
+  uint64_t* xchg = s_full + 7;              // the compute warps exchange flags, maxima and sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -255,7 +221,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
     mbar_init(o_empty, T::kComputeThreads);
     mbar_init(q_ready, T::kComputeThreads);
     mbar_init(done_bar, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xchg[i], 128);
+    mbar_init(xchg, T::kComputeThreads);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -312,8 +278,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = make_idesc(0u, false, false, 128, T::kN);   // K K-major, Q K-major
-      const uint32_t idesc_o = make_idesc(0u, true, true, 128, T::kN);     // V^T MN-major, P^T MN-major
+      const uint32_t idesc_s = make_idesc(0u, false, false, 128, 128);     // Q K-major, K K-major
+      const uint32_t idesc_o = make_idesc(0u, true, false, 128, T::kN);    // V^T MN-major, P K-major
       const uint32_t t_s = tmem_base + T::kColS, t_o = tmem_base + T::kColO;
       uint32_t r = 0;   // ring slots consumed so far (the producer's order)
       bool ok = mbar_wait(q_ready, 0, ctl);
@@ -329,22 +295,25 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         mma_commit(&ring_empty[r % T::kRing]);
         ++r;
       };
-      // S^T_j: A = K_j (keys x dims, K-major), B = [Q_hi ; Q_lo] (K-major)
+      // S_j = [Q_hi ; Q_lo] K_j^T: the hi chain in columns 0-127, the lo chain
+      // in 128-255 (one chain: both into 0-127); per 64-dim half of K_j, the
+      // hi chain's four k-steps, then the lo chain's
       auto issue_s = [&](int j) -> bool {
         if (!mbar_wait(s_empty, (j & 1u) ^ 1u, ctl)) return false;
         for (int h = 0; h < 2; ++h) {
           uint32_t kt;
           if (!take_slot(kt)) return false;
+          const uint32_t qh = q_smem + (uint32_t)h * 32768u;   // Q_hi dims 64h..64h+63; Q_lo 16 KB on
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(t_s, kmajor_desc(qh, kk), kmajor_desc(kt, kk), idesc_s, (h > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = kmajor_desc(kt, kk);
-            const uint32_t qh = q_smem + (uint32_t)h * 32768u;
-            const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
             if constexpr (T::kL == 11) {
-              mma_f16(t_s, a, kmajor_desc(qh, kk), idesc_s, acc);
+              mma_f16(t_s + 128u, kmajor_desc(qh + 16384u, kk), kmajor_desc(kt, kk), idesc_s,
+                      (h > 0 || kk > 0) ? 1u : 0u);
             } else {
-              mma_f16(t_s, a, kmajor_desc(qh, kk), idesc_s, acc);
-              mma_f16(t_s, a, kmajor_desc(qh + 16384u, kk), idesc_s, 1u);
+              mma_f16(t_s, kmajor_desc(qh + 16384u, kk), kmajor_desc(kt, kk), idesc_s, 1u);
             }
           }
           release_slot();
@@ -352,7 +321,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         mma_commit(s_full);
         return true;
       };
-      // O^T_j (+)= V_j^T P_j^T: A = V^T (dims x keys, MN-major), B = [P_hi ; P_lo]^T (MN-major)
+      // O^T_j (+)= V_j^T [P_hi ; P_lo]^T: A = V^T (dims x keys, MN-major),
+      // B = P (256 lines: hi of queries 0-127, lo of 0-127; K-major)
       auto issue_o = [&](int j) -> bool {
         if (!mbar_wait(p_full, j & 1u, ctl)) return false;
         if (!mbar_wait(o_empty, (j & 1u) ^ 1u, ctl)) return false;
@@ -360,17 +330,17 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         for (int h = 0; h < 2; ++h) {
           uint32_t vt;
           if (!take_slot(vt)) return false;
+          const uint32_t pc = p_smem + (uint32_t)h * 32768u;   // keys 64h..64h+63 of P
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const int ks = 4 * h + kk;
             const uint64_t a = mnmajor_desc(vt, 64, kk);
             // the chains restart after a fold zeroed them (j = 0: nothing to keep)
-            const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+            const uint32_t acc = (j > 0 || h > 0 || kk > 0) ? 1u : 0u;
             if constexpr (T::kL == 11) {
-              mma_f16(t_o, a, mnmajor_desc(p_smem, T::BKEY, ks), idesc_o, acc);
+              mma_f16(t_o, a, kmajor_desc(pc, kk), idesc_o, acc);
             } else {
-              mma_f16(t_o, a, mnmajor_desc(p_smem, T::BKEY, ks), idesc_o, acc);
-              mma_f16(t_o, a, mnmajor_desc(p_smem + 2u * T::BKEY * 128u, T::BKEY, ks), idesc_o, 1u);
+              mma_f16(t_o, a, kmajor_desc(pc, kk), idesc_o, acc);
+              mma_f16(t_o, a, kmajor_desc(pc + 16384u, kk), idesc_o, 1u);
             }
           }
           release_slot();
@@ -425,32 +395,27 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       mbar_arrive(q_ready);
     }
     const int cw = warp - 2;
-    const int q4 = warp & 3;                      // TMEM lane quarter: keys (S^T) and dims (O^T) 32*q4..
-    const int grp = cw >> 2;                      // query columns 32*grp .. 32*grp+31
+    const int q4 = warp & 3;                      // TMEM lane quarter: query rows (S), dims (O^T) 32*q4..
+    const int part = cw >> 2;                     // S: keys 32*part.. of each block; O^T: queries 32*part..
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    float* m_w = warp_vals + cw * 96;             // m_ref of the group's 32 queries
-    float* f_w = m_w + 32;                        // factor of the last move of m_ref (1 / sum at the end)
-    float* d_w = m_w + 64;                        // the last move of m_ref
-    float* pmax = part_max + grp * 128;           // + exchange parity * 512: [quarter][32]
-    int* pflag = flags + grp * 4;                 // + exchange parity * 16: [quarter]
-    float o[32];   // O_run of dim 32*q4 + lane for the group's 32 queries, relative to m_ref
+    const int row = 32 * q4 + lane;               // this thread's query row of S
+    float* f_w = warp_vals + cw * 32;             // per-query factors of this warp's O^T columns
+    float o[32];   // O_run of dim 32*q4 + lane for queries 32*part.., relative to m_ref
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-    // lane l keeps the reference maximum (base 2) and this quarter's sum of
-    // query 32*grp + l; the first block always sets the reference
-    float m_l = 0.0f, l_l = 0.0f;
-    m_w[lane] = 0.0f;
-    __syncwarp();
-    uint32_t nx = 0;   // exchanges of the column group so far
+    // the row's reference maximum (base 2; the four parts of a row hold the
+    // same) and this part's sum; the first block always sets the reference
+    float m_row = 0.0f, l_row = 0.0f;
+    uint32_t nx = 0;   // exchanges of the compute warps so far
     bool ok = true;
     // Fold of the O^T chains into the registers: the chains hold the blocks
     // since the last fold, relative to the m_ref before the current block.
     // They are added (hi and lo summed in fp32) and, when the current block
     // moved m_ref, registers and chains are scaled by 2^(m_old - m_new) per
-    // query; `zero` restarts the chains for the next block's products.
+    // query (f_w); `zero` restarts the chains for the next block's products.
     auto fold = [&](bool moved, bool zero) {
       tc_fence_after_sync();
-      const uint32_t to = tmem_base + lane_off + T::kColO + 32u * grp;
+      const uint32_t to = tmem_base + lane_off + T::kColO + 32u * part;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         float a[4];
@@ -496,16 +461,16 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         tmem_st_wait();
       }
     };
-    // Block j: read S_j (S_(j+1) may then go in), x = s - m_ref and the
-    // group's agreement on m_ref, p = 2^x; then, once O_(j-1) has completed
-    // (which also frees the P^T tile), the fold when it is due and the
-    // release of the O^T chains; then P_j, which lets O_j go in; then the
-    // sums, while O_j runs.
+    // Block j: read this part of the row's S_j (S_(j+1) may then go in),
+    // x = s - m_ref, the compute warps' agreement on m_ref, p = 2^x; once
+    // O_(j-1) has completed (which also frees the P tile), the fold when it
+    // is due and the release of the O^T chains; then P_j, which lets O_j go
+    // in; then the row's sum, while O_j runs.
     for (int j = 0; j < nb && ok; ++j) {
       if (!warp_wait(s_full, j & 1u, ctl)) { ok = false; break; }
       tc_fence_after_sync();
       float x[32];
-      const uint32_t ts = tmem_base + lane_off + T::kColS + 32u * grp;
+      const uint32_t ts = tmem_base + lane_off + T::kColS + 32u * part;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         float a[8];
@@ -529,117 +494,119 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       }
       tc_fence_before_sync();
       mbar_arrive(s_empty);
-      // keys past the end of the sequence score -inf (only the block that
-      // crosses the end has any); x = s - m_ref
-      if ((kb0 + j + 1) * T::BKEY > p.lk && (kb0 + j) * T::BKEY + 32 * q4 + lane >= p.lk) {
+      // keys past the end of the sequence score -inf (the same keys in every lane)
+      const int key0 = (kb0 + j) * T::BKEY + 32 * part;
+      if (key0 + 32 > p.lk) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
+        for (int i = 0; i < 32; ++i)
+          if (key0 + i >= p.lk) x[i] = -INFINITY;
       }
+      // x = s - m_ref and its maximum over this part of the row
       float xm = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 m = reinterpret_cast<const float4*>(m_w)[i / 4];
-        const float2 d0 = fsub2(make_float2(x[i], x[i + 1]), make_float2(m.x, m.y));
-        const float2 d1 = fsub2(make_float2(x[i + 2], x[i + 3]), make_float2(m.z, m.w));
-        x[i] = d0.x;
-        x[i + 1] = d0.y;
-        x[i + 2] = d1.x;
-        x[i + 3] = d1.y;
-        xm = fmax3(xm, fmax3(x[i], x[i + 1], x[i + 2]), x[i + 3]);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 d = fsub2(make_float2(x[i], x[i + 1]), make_float2(m_row, m_row));
+        x[i] = d.x;
+        x[i + 1] = d.y;
+        xm = fmax3(xm, d.x, d.y);
       }
-      // the group's four warps agree whether any of its queries needs a new reference
+      // all compute warps agree whether any row needs a new reference
       const bool raise = (j == 0) || __any_sync(0xffffffffu, xm > kLazyLog2);
-      int* fl = pflag + (nx & 1u) * 16;
-      if (lane == 0) fl[q4] = raise ? 1 : 0;
-      mbar_arrive(&xchg[grp]);
-      if (!warp_wait(&xchg[grp], nx & 1u, ctl)) { ok = false; break; }
+      int* fl = flags + (nx & 1u) * 16;
+      if (lane == 0) fl[cw] = raise ? 1 : 0;
+      mbar_arrive(xchg);
+      if (!warp_wait(xchg, nx & 1u, ctl)) { ok = false; break; }
       ++nx;
-      const int4 fv = *reinterpret_cast<const int4*>(fl);
-      bool moved = false;   // block j moved m_ref of one of the group's queries (same in its four warps)
-      if ((fv.x | fv.y | fv.z | fv.w) != 0) {
-        // per-query maxima of x over the group's 128 keys: warp maxima, exchanged
-        float* pm = pmax + (nx & 1u) * 512;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float a0 = warp_max(x[i]), a1 = warp_max(x[i + 1]);
-          const float a2 = warp_max(x[i + 2]), a3 = warp_max(x[i + 3]);
-          if (lane == 0) reinterpret_cast<float4*>(pm + q4 * 32)[i / 4] = make_float4(a0, a1, a2, a3);
-        }
-        mbar_arrive(&xchg[grp]);
-        if (!warp_wait(&xchg[grp], nx & 1u, ctl)) { ok = false; break; }
+      const int4 f0 = reinterpret_cast<const int4*>(fl)[0], f1 = reinterpret_cast<const int4*>(fl)[1];
+      const int4 f2 = reinterpret_cast<const int4*>(fl)[2], f3 = reinterpret_cast<const int4*>(fl)[3];
+      const bool moved = ((f0.x | f0.y | f0.z | f0.w) | (f1.x | f1.y | f1.z | f1.w) | (f2.x | f2.y | f2.z | f2.w) |
+                          (f3.x | f3.y | f3.z | f3.w)) != 0;   // the same in every compute warp
+      const float* pm = part_max + (nx & 1u) * 512;   // [part][row] maxima of x, when moved
+      if (moved) {
+        part_max[(nx & 1u) * 512 + part * 128 + row] = xm;
+        mbar_arrive(xchg);
+        if (!warp_wait(xchg, nx & 1u, ctl)) { ok = false; break; }
         ++nx;
-        const float mb = fmaxf(fmaxf(pm[lane], pm[32 + lane]), fmaxf(pm[64 + lane], pm[96 + lane]));
+        const float mb = fmaxf(fmaxf(pm[row], pm[128 + row]), fmaxf(pm[256 + row], pm[384 + row]));
         const bool mv = (j == 0) || mb > kLazyLog2;
         const float dm = mv ? mb : 0.0f;
+        m_row += dm;
         // 2^(m_old - m_new); nothing is kept before the first block
-        const float fac = (j == 0) ? 0.0f : (mv ? exp2_approx(-mb) : 1.0f);
-        m_l += dm;
-        l_l *= fac;
-        moved = __any_sync(0xffffffffu, mv);
-        m_w[lane] = m_l;
-        f_w[lane] = fac;
-        d_w[lane] = dm;
-        __syncwarp();
+        l_row *= (j == 0) ? 0.0f : (mv ? exp2_approx(-mb) : 1.0f);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 d = reinterpret_cast<const float4*>(d_w)[i / 4];
-          const float2 d0 = fsub2(make_float2(x[i], x[i + 1]), make_float2(d.x, d.y));
-          const float2 d1 = fsub2(make_float2(x[i + 2], x[i + 3]), make_float2(d.z, d.w));
-          x[i] = d0.x;
-          x[i + 1] = d0.y;
-          x[i + 2] = d1.x;
-          x[i + 3] = d1.y;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 d = fsub2(make_float2(x[i], x[i + 1]), make_float2(dm, dm));
+          x[i] = d.x;
+          x[i + 1] = d.y;
         }
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = exp2_approx(x[i]);
-      if (j >= 1) {
-        // O_(j-1) has completed: fold after every kFoldBlocks blocks and
-        // before products relative to a moved m_ref, then release the chains
-        if (!warp_wait(o_full, (j - 1) & 1u, ctl)) { ok = false; break; }
-        if (moved || j % kFoldBlocks == 0) fold(moved, true);
-        tc_fence_before_sync();
-        mbar_arrive(o_empty);
-      }
-      // P^T: this lane's key (line), the group's 32 queries as 4 chunks of
-      // 8 in atom grp / 2 (hi) and 2 + grp / 2 (lo)
+      // this part's sum of p over the row's keys
       {
-        const uint32_t key = (uint32_t)(32 * q4 + lane);
-        const uint32_t line = p_smem + (uint32_t)(grp >> 1) * (T::BKEY * 128u) + key * 128u;
+        float2 s0 = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          s0 = fadd2(s0, make_float2(x[i], x[i + 1]));
+          s1 = fadd2(s1, make_float2(x[i + 2], x[i + 3]));
+        }
+        l_row += (s0.x + s0.y) + (s1.x + s1.y);
+      }
+      // O_(j-1) has completed: the P tile is free and the O^T chains hold
+      // every block up to j-1
+      if (j >= 1 && !warp_wait(o_full, (j - 1) & 1u, ctl)) { ok = false; break; }
+      // P, the K-major B operand of O^T: line `row` (hi) and 128 + row (lo)
+      // of key column part / 2, this part's 32 keys as 4 chunks of 8
+      {
+        const uint32_t line = p_smem + (uint32_t)(part >> 1) * 32768u + (uint32_t)row * 128u;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t h[4], l[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) split2<T::kL>(x[8 * c + 2 * e], x[8 * c + 2 * e + 1], h[e], l[e]);
-          const uint32_t off = (((uint32_t)((grp & 1) * 4 + c)) ^ (key & 7u)) << 4;
+          const uint32_t off = (((uint32_t)((part & 1) * 4 + c)) ^ ((uint32_t)row & 7u)) << 4;
           st_shared_v4(line + off, h[0], h[1], h[2], h[3]);
-          st_shared_v4(line + 2u * T::BKEY * 128u + off, l[0], l[1], l[2], l[3]);
+          st_shared_v4(line + 16384u + off, l[0], l[1], l[2], l[3]);
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(p_full);
-      // this quarter's sum of p per query: query 32*grp + l in lane l
-      l_l += reduce_scatter_sum(x, lane);
+      if (j >= 1) {
+        // fold after every kFoldBlocks blocks and before products relative
+        // to a moved m_ref, then release the chains (O_j waits for both)
+        if (moved || j % kFoldBlocks == 0) {
+          if (moved) {
+            // the factors of this warp's query columns, from the exchanged maxima
+            const int qc = 32 * part + lane;
+            const float mq = fmaxf(fmaxf(pm[qc], pm[128 + qc]), fmaxf(pm[256 + qc], pm[384 + qc]));
+            f_w[lane] = mq > kLazyLog2 ? exp2_approx(-mq) : 1.0f;
+            __syncwarp();
+          }
+          fold(moved, true);
+        }
+        tc_fence_before_sync();
+        mbar_arrive(o_empty);
+      }
     }
     // the last fold, once the last block's products have completed
     if (ok) {
       ok = warp_wait(o_full, (nb - 1) & 1u, ctl);
       if (ok) fold(false, false);
     }
-    // the query's sum is the sum of its four quarters' sums
-    float* ps = part_sum + grp * 128;
+    // the row's sum is the sum of its four parts' sums
     if (ok) {
-      ps[q4 * 32 + lane] = l_l;
-      mbar_arrive(&xchg[grp]);
-      ok = warp_wait(&xchg[grp], nx & 1u, ctl);
+      part_sum[part * 128 + row] = l_row;
+      mbar_arrive(xchg);
+      ok = warp_wait(xchg, nx & 1u, ctl);
       ++nx;
     }
     if (ok) {
-      const float lsum = (ps[lane] + ps[32 + lane]) + (ps[64 + lane] + ps[96 + lane]);
-      const int64_t q0 = (int64_t)qb * T::BQ + 32 * grp;
+      const int64_t q0 = (int64_t)qb * T::BQ + 32 * part;   // this warp's output queries
       const int dim = 32 * q4 + lane;
+      const int qc = 32 * part + lane;
+      const float lq_sum = (part_sum[qc] + part_sum[128 + qc]) + (part_sum[256 + qc] + part_sum[384 + qc]);
       if (p.splits == 1) {
-        f_w[lane] = 1.0f / lsum;
+        f_w[lane] = 1.0f / lq_sum;
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -653,9 +620,11 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (q0 + i < p.lq) p.part_o[((int64_t)split * p.lq + q0 + i) * 128 + dim] = o[i];
-        if (q4 == 0 && q0 + lane < p.lq) {
-          p.part_m[(int64_t)split * p.lq + q0 + lane] = m_l;
-          p.part_l[(int64_t)split * p.lq + q0 + lane] = lsum;
+        const int64_t grow = (int64_t)qb * T::BQ + row;
+        if (part == 0 && grow < p.lq) {
+          const float l_all = (part_sum[row] + part_sum[128 + row]) + (part_sum[256 + row] + part_sum[384 + row]);
+          p.part_m[(int64_t)split * p.lq + grow] = m_row;
+          p.part_l[(int64_t)split * p.lq + grow] = l_all;
         }
       }
     }
