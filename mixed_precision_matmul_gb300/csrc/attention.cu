@@ -365,26 +365,33 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       const int c0 = (ct & 3) * 4;
       const int64_t grow = (int64_t)qb * T::BQ + row;
       const float* src = p.q + grow * p.ldq;
-#pragma unroll 1
-      for (int c = c0; c < c0 + 4; ++c) {
-        float x[8];
+      // all four chunks' loads in flight at once, then the splits
+      float x[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + i;
         if (grow < p.lq) {
           if (p.q_vec_ok) {
             const float4 a = __ldg(reinterpret_cast<const float4*>(src + 8 * c));
             const float4 b = __ldg(reinterpret_cast<const float4*>(src + 8 * c + 4));
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            x[i][0] = a.x; x[i][1] = a.y; x[i][2] = a.z; x[i][3] = a.w;
+            x[i][4] = b.x; x[i][5] = b.y; x[i][6] = b.z; x[i][7] = b.w;
           } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __ldg(src + 8 * c + e);
+            for (int e = 0; e < 8; ++e) x[i][e] = __ldg(src + 8 * c + e);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+          for (int e = 0; e < 8; ++e) x[i][e] = 0.0f;
         }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + i;
         // q * scale * log2(e), split: the scores come out in base-2 units
         uint32_t h[4], l[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_pair<T::kL>(x[2 * e], x[2 * e + 1], p.scale_log2, h[e], l[e]);
+        for (int e = 0; e < 4; ++e) split_pair<T::kL>(x[i][2 * e], x[i][2 * e + 1], p.scale_log2, h[e], l[e]);
         // dims 8c..8c+7: dim half c / 8, chunk c % 8 of line `row` (hi) and `128 + row` (lo)
         const uint32_t base = q_smem + (uint32_t)(c >> 3) * 32768u;
         const uint32_t off = swz_chunk_offset<128>((uint32_t)row, (uint32_t)(c & 7));
