@@ -322,8 +322,10 @@ mpg_status mpg_gemm_host(int64_t m, int64_t n, int64_t k, int64_t batch,
  * scores and probabilities never written to memory ("qsa_prompt_attn: Volta
  * m8n8k4 kernel - keep the hi and lo halves in separate accumulator chains",
  * sections "What's going on" and "The fix").
- *   Q     device, fp32, lq x d row-major (ldq >= d).  Split on load into an
- *         FP16 hi half and a lo half for q.k.
+ *   Q     device, fp32, lq x d row-major (ldq >= d).  Multiplied by
+ *         scale * log2(e) in fp32 on load (the scores come out in base-2
+ *         units for the base-2 exponential) and split into an FP16 hi half
+ *         and a lo half for q.k.
  *   K, V  device, fp16 (the key/value cache), lk x d row-major; ldk and ldv
  *         >= d, multiples of 8, pointers 16-byte aligned (TMA).
  *   O     device, fp32, lq x d row-major (ldo >= d).
@@ -335,7 +337,8 @@ mpg_status mpg_gemm_host(int64_t m, int64_t n, int64_t k, int64_t batch,
  *         MPG_ATTN_SPLIT_1CHAIN: lo = fp16(x - hi) accumulated into the same
  *         chain as hi (the form the fix replaced), for comparison.
  *   key_splits  0 = chosen by the library: the keys are divided among CTAs
- *         so that about one CTA per SM works; > 1 forces that many ranges.
+ *         so that about one CTA per SM works; > 1 forces that many ranges
+ *         (at most one per block of 128 keys).
  *         Several ranges need a workspace of mpg_attention_workspace_size()
  *         bytes for their partial results (a merge kernel combines them);
  *         with a smaller workspace an automatic choice falls back to one range.
