@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         ++r;
         return true;
       };
-      bool ok = load(true, 0, 0) && load(true, 0, 1);
+      // K_0 first; the rest of the ring only once Q is in (the first S
+      // product needs Q and K_0, and every CTA loads them at once)
+      bool ok = load(true, 0, 0) && load(true, 0, 1) && mbar_wait(q_ready, 0, ctl);
       for (int j = 0; j < nb && ok; ++j) {
         if (j + 1 < nb) ok = load(true, j + 1, 0) && load(true, j + 1, 1);
         if (ok) ok = load(false, j, 0) && load(false, j, 1);
@@ -359,44 +361,37 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
   } else {
     // ------------------------------------------------------------ Q split (compute warps)
     {
-      // 128 rows x 16 chunks of 8 dims; each thread takes 4 consecutive chunks of one row
-      const int ct = threadIdx.x - 64;
-      const int row = ct >> 2;
-      const int c0 = (ct & 3) * 4;
-      const int64_t grow = (int64_t)qb * T::BQ + row;
-      const float* src = p.q + grow * p.ldq;
-      // all four chunks' loads in flight at once, then the splits
-      float x[4][8];
+      // 128 rows: compute warp w takes rows 8w..8w+7, one row per load (lane
+      // l: dims 4l..4l+3, so that a warp reads the row's 512 bytes at once)
+      const int w0 = warp - 2;
+      float4 xq[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = c0 + i;
+      for (int i = 0; i < 8; ++i) {
+        const int64_t grow = (int64_t)qb * T::BQ + 8 * w0 + i;
+        const float* src = p.q + grow * p.ldq + 4 * lane;
         if (grow < p.lq) {
           if (p.q_vec_ok) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(src + 8 * c));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(src + 8 * c + 4));
-            x[i][0] = a.x; x[i][1] = a.y; x[i][2] = a.z; x[i][3] = a.w;
-            x[i][4] = b.x; x[i][5] = b.y; x[i][6] = b.z; x[i][7] = b.w;
+            xq[i] = __ldg(reinterpret_cast<const float4*>(src));
           } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[i][e] = __ldg(src + 8 * c + e);
+            xq[i] = make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
           }
         } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[i][e] = 0.0f;
+          xq[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = c0 + i;
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t row = (uint32_t)(8 * w0 + i);
         // q * scale * log2(e), split: the scores come out in base-2 units
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split_pair<T::kL>(x[i][2 * e], x[i][2 * e + 1], p.scale_log2, h[e], l[e]);
-        // dims 8c..8c+7: dim half c / 8, chunk c % 8 of line `row` (hi) and `128 + row` (lo)
-        const uint32_t base = q_smem + (uint32_t)(c >> 3) * 32768u;
-        const uint32_t off = swz_chunk_offset<128>((uint32_t)row, (uint32_t)(c & 7));
-        st_shared_v4(base + off, h[0], h[1], h[2], h[3]);
-        st_shared_v4(base + 16384u + off, l[0], l[1], l[2], l[3]);
+        uint32_t h0, l0, h1, l1;
+        split_pair<T::kL>(xq[i].x, xq[i].y, p.scale_log2, h0, l0);
+        split_pair<T::kL>(xq[i].z, xq[i].w, p.scale_log2, h1, l1);
+        // dims 4l..4l+3: dim half l / 16, 8-byte half (l & 1) of chunk (l / 2) % 8
+        // of line `row` (hi) and `128 + row` (lo)
+        const uint32_t addr = q_smem + (uint32_t)(lane >> 4) * 32768u +
+                              swz_chunk_offset<128>(row, (uint32_t)((lane >> 1) & 7)) + (uint32_t)(lane & 1) * 8u;
+        st_shared_v2(addr, h0, h1);
+        st_shared_v2(addr + 16384u, l0, l1);
       }
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
