@@ -27,8 +27,9 @@
 //               O_j: S has one TMEM buffer (hi chain in columns 0-127, lo in
 //               128-255), and S_(j+1) goes in as soon as the compute warps have
 //               read S_j; O^T (columns 256-511) accumulates the blocks between
-//               folds.  Per 64-dim half of K, S's hi chain takes its four
-//               k-steps before the lo chain's.
+//               folds.  S's hi chain takes all eight k-steps of K_j (both
+//               64-dim halves held) before the lo chain's: the accumulator
+//               changes once per block.
 //   warps 2-17  softmax and folds of O.  Warp w reads TMEM lane quarter w % 4
 //               (32 query rows of S, 32 dims of O^T); its part w / 4 - 1 picks
 //               32 of a block's keys (softmax) and 32 query columns (folds).
@@ -302,24 +303,33 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       // hi chain's four k-steps, then the lo chain's
       auto issue_s = [&](int j) -> bool {
         if (!mbar_wait(s_empty, (j & 1u) ^ 1u, ctl)) return false;
+        // both 64-dim halves of K_j, then each chain's eight k-steps in turn
+        uint32_t kt[2];
         for (int h = 0; h < 2; ++h) {
-          uint32_t kt;
-          if (!take_slot(kt)) return false;
-          const uint32_t qh = q_smem + (uint32_t)h * 32768u;   // Q_hi dims 64h..64h+63; Q_lo 16 KB on
+          const uint32_t q = r + (uint32_t)h;
+          if (!mbar_wait(&ring_full[q % T::kRing], (q / T::kRing) & 1u, ctl)) return false;
+          kt[h] = ring_smem + (q % T::kRing) * T::kSlot;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(t_s, kmajor_desc(qh, kk), kmajor_desc(kt, kk), idesc_s, (h > 0 || kk > 0) ? 1u : 0u);
+            mma_f16(t_s, kmajor_desc(q_smem + (uint32_t)h * 32768u, kk), kmajor_desc(kt[h], kk), idesc_s,
+                    (h > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t aq = kmajor_desc(q_smem + (uint32_t)h * 32768u + 16384u, kk);   // Q_lo
             if constexpr (T::kL == 11) {
-              mma_f16(t_s + 128u, kmajor_desc(qh + 16384u, kk), kmajor_desc(kt, kk), idesc_s,
-                      (h > 0 || kk > 0) ? 1u : 0u);
+              mma_f16(t_s + 128u, aq, kmajor_desc(kt[h], kk), idesc_s, (h > 0 || kk > 0) ? 1u : 0u);
             } else {
-              mma_f16(t_s, kmajor_desc(qh + 16384u, kk), kmajor_desc(kt, kk), idesc_s, 1u);
+              mma_f16(t_s, aq, kmajor_desc(kt[h], kk), idesc_s, 1u);
             }
           }
-          release_slot();
-        }
+        release_slot();
+        release_slot();
         mma_commit(s_full);
         return true;
       };
