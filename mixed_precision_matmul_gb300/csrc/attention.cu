@@ -67,7 +67,7 @@ template <bool kTwoChain>
 struct AttnTraits {
   static constexpr int BQ = 128;                 // queries per CTA
   static constexpr int BKEY = kAttnKeyBlock;     // keys per block
-  static_assert(BKEY == 128, "the ring's half-block slots and the four 32-key quarters assume 128");
+  static_assert(BKEY == 128, "the ring's half-block slots and the four 32-key parts assume 128");
   static constexpr int kRing = 5;                // K/V ring slots
   static constexpr int kSlot = 16384;            // one slot: half a K block (64 dims) or half a V block (64 keys)
   // Q: [2 dim halves][256 lines: q_hi of queries 0-127, q_lo of 0-127][128 B], 128-byte swizzle
@@ -85,7 +85,8 @@ struct AttnTraits {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr int kComputeThreads = 512;
   static constexpr int kThreads = 64 + kComputeThreads;
-  // TMEM columns: S^T at 0 (hi 0-127, lo 128-255), O^T at 256 (hi 256-383, lo 384-511)
+  // TMEM: S at column 0 (lanes = queries; hi chain in columns 0-127, lo in 128-255, one per
+  // key), O^T at 256 (lanes = dims; hi 256-383, lo 384-511, one per query)
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kN = kTwoChain ? 256 : 128;   // N of each MMA
