@@ -139,3 +139,59 @@ def test_attention_rows_of_a_warp_rescale_apart(lq, lk, splits):
     O = run(q, k, v, 0.5, key_splits=splits)
     ref, den = oracle.attention(q, k, v, 0.5)
     assert _err(O, ref, den) <= TOL_2CHAIN
+
+
+@pytest.mark.parametrize("lq,lk,splits", [(1, 1, 0), (1, 129, 0), (129, 1, 1), (1, 3000, 0)])
+def test_attention_degenerate_sizes(lq, lk, splits):
+    """One query and/or one key; a single query over many keys (the library
+    then divides the keys among many CTAs)."""
+    mpg.build()
+    q, k, v = inputs(lq, lk, 7 * lq + lk)
+    scale = 2.0 / np.sqrt(128)
+    O = run(q, k, v, scale, key_splits=splits)
+    ref, den = oracle.attention(q, k, v, scale)
+    assert _err(O, ref, den) <= TOL_2CHAIN
+    if lk == 1:
+        # softmax over one key: O is that key's V row
+        np.testing.assert_allclose(O, np.broadcast_to(v[0].astype(np.float32), O.shape), rtol=1e-6, atol=1e-7)
+
+
+def test_attention_more_ranges_than_blocks():
+    """50 key ranges asked for 1000 keys (8 blocks of 128): one range per block."""
+    mpg.build()
+    q, k, v = inputs(200, 1000, 91)
+    scale = 2.0 / np.sqrt(128)
+    O = run(q, k, v, scale, key_splits=50)
+    ref, den = oracle.attention(q, k, v, scale)
+    assert _err(O, ref, den) <= TOL_2CHAIN
+
+
+def test_attention_one_dominant_key():
+    """One key's score exceeds every other by far more than the lazy
+    reference's threshold: O is that key's V row to within the split's
+    precision, whichever block and key range holds it."""
+    mpg.build()
+    lq, lk = 128, 2000
+    q, k, v = inputs(lq, lk, 17)
+    k = (0.01 * k.astype(np.float32)).astype(np.float16)
+    k[1337] = (q[0] / np.linalg.norm(q[0]) * 8.0).astype(np.float16)   # dominant for row 0
+    # the split q's score error grows with |scale q.k| (the peaked test's
+    # reading): the bar scales with the largest logit
+    logit = float(np.max(np.abs(q.astype(np.float64) @ k.astype(np.float64).T)))
+    ref, den = oracle.attention(q, k, v, 1.0)
+    for splits in (1, 5):
+        O = run(q, k, v, 1.0, key_splits=splits)
+        assert _err(O, ref, den) <= TOL_2CHAIN * max(1.0, logit / 2)
+        # every other key of row 0 lies more than 80 below: p underflows to 0
+        np.testing.assert_allclose(O[0], v[1337].astype(np.float32), rtol=1e-6, atol=1e-7)
+
+
+def test_attention_is_reproducible():
+    """Two calls with key ranges give the same bits (the ranges are merged in a
+    fixed order, nothing is summed with atomics)."""
+    mpg.build()
+    q, k, v = inputs(384, 5000, 23)
+    scale = 2.0 / np.sqrt(128)
+    a = run(q, k, v, scale, key_splits=6)
+    b = run(q, k, v, scale, key_splits=6)
+    np.testing.assert_array_equal(a, b)
