@@ -317,6 +317,21 @@ def test_attention_workspace_holds_the_partials(L):
     assert mpg.attention_workspace_size(2048, 32768, 64, 0) == 0
 
 
+def test_attention_key_ranges_are_at_most_one_per_block(L):
+    # 1000 keys are 8 blocks of 128: asking for 8, 9 or 50 ranges gives 8, each
+    # holding partial outputs (128 floats per query) plus a maximum and a sum
+    # per query, every array padded to 256 bytes
+    def a256(x):
+        return (x + 255) // 256 * 256
+    want = a256(8 * 200 * 128 * 4) + 2 * a256(8 * 200 * 4)
+    for splits in (8, 9, 50):
+        assert mpg.attention_workspace_size(200, 1000, 128, splits) == want
+    # 1024 keys: 8 ranges of one block; 1025 keys are 9 blocks, and 8 ranges of
+    # equal length would need 2 blocks each, which leaves 5 ranges (2, 2, 2, 2, 1)
+    assert mpg.attention_workspace_size(200, 1024, 128, 8) == want
+    assert mpg.attention_workspace_size(200, 1025, 128, 8) == a256(5 * 200 * 128 * 4) + 2 * a256(5 * 200 * 4)
+
+
 def test_workspace_includes_the_conversion_pass_when_the_library_takes_it(L):
     # split modes with both operands re-read by many tiles: the library's
     # choice is the separate pass, so the query includes the hi/lo copies
