@@ -130,15 +130,18 @@ def _jump_inputs(lq, lk, seed):
     return q.astype(np.float32), k, v
 
 
+@pytest.mark.parametrize("mode", [mpg.ATTN_SPLIT_2CHAIN, mpg.ATTN_SPLIT_1CHAIN])
 @pytest.mark.parametrize("lq,lk,splits", [(256, 1000, 1), (256, 1000, 2), (160, 4100, 1)])
-def test_attention_rows_of_a_warp_rescale_apart(lq, lk, splits):
+def test_attention_rows_of_a_warp_rescale_apart(lq, lk, splits, mode):
     """Some rows of a warp move their reference maximum on a block and the
-    others do not (the fold then runs for the whole warp)."""
+    others do not (the fold then runs for the whole warp).  The one-chain
+    form has no accuracy target of its own: a sanity bar of four times the
+    two-chain one checks its folds and rescaling."""
     mpg.build()
     q, k, v = _jump_inputs(lq, lk, lq + lk)
-    O = run(q, k, v, 0.5, key_splits=splits)
+    O = run(q, k, v, 0.5, mode=mode, key_splits=splits)
     ref, den = oracle.attention(q, k, v, 0.5)
-    assert _err(O, ref, den) <= TOL_2CHAIN
+    assert _err(O, ref, den) <= (TOL_2CHAIN if mode == mpg.ATTN_SPLIT_2CHAIN else 4 * TOL_2CHAIN)
 
 
 @pytest.mark.parametrize("lq,lk,splits", [(1, 1, 0), (1, 129, 0), (129, 1, 1), (1, 3000, 0)])
