@@ -198,3 +198,19 @@ def test_attention_is_reproducible():
     a = run(q, k, v, scale, key_splits=6)
     b = run(q, k, v, scale, key_splits=6)
     np.testing.assert_array_equal(a, b)
+
+
+def test_attention_longest_context_sampled_rows(capsys):
+    """The Volta page's longest context, 131,072 keys, for 512 queries (the
+    library's key ranges: many blocks per range and a long merge); 40 rows
+    checked against the oracle."""
+    mpg.build()
+    q, k, v = inputs(512, 131072, 131)
+    scale = 2.0 / np.sqrt(128)
+    O = run(q, k, v, scale)
+    rows = np.concatenate([np.arange(0, 512, 16), [1, 127, 128, 255, 256, 383, 384, 511]])
+    ref, den = oracle.attention(q[rows], k, v, scale)
+    err = _err(O[rows], ref, den)
+    with capsys.disabled():
+        print(f"\n[attention 512 x 131072: {err:.3e}]")
+    assert err <= TOL_2CHAIN
