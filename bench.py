@@ -655,33 +655,37 @@ def ours(args):
             torch.cuda.empty_cache()
         # fused prompt attention, 2048 queries x 32768 keys, d = 128: one kernel
         # (plus the merge of key ranges) for softmax(scale Q K^T) V, against the
-        # two products S = Q K^T and O = P V above (which leave the softmax out)
-        q_a, k_a, v_a, scale_a = synthetic.attention_fused_inputs()
-        Qd = torch.from_numpy(q_a).to(device)
-        Kd = torch.from_numpy(k_a).to(device)
-        Vd = torch.from_numpy(v_a).to(device)
-        Od = torch.empty((2048, 128), dtype=torch.float32, device=device)
-        aws_b = mpg.attention_workspace_size(2048, 32768, 128, 0)
-        aws = torch.empty(max(aws_b, 16), dtype=torch.uint8, device=device)
-        useful = 4.0 * 2048 * 32768 * 128
+        # two products S = Q K^T and O = P V above (which leave the softmax out);
+        # and the Volta page's longest context, 131072 keys, two chains
         unfused = [modes.get(x, {}).get("ms") for x in ("attention_qkt_split3_prepass", "attention_pv_split3")]
-        for label, amode in (("attention_fused_2chain", mpg.ATTN_SPLIT_2CHAIN),
-                             ("attention_fused_1chain", mpg.ATTN_SPLIT_1CHAIN)):
-            fn = (lambda am=amode: mpg.attention_raw(2048, 32768, 128, Qd.data_ptr(), 128, Kd.data_ptr(), 128,
-                                                     Vd.data_ptr(), 128, Od.data_ptr(), 128, scale_a, am, 0,
-                                                     aws.data_ptr(), aws_b, sh))
-            ms = time_steps(torch, fn, 100, 5, stream) / 100
-            tf = useful / (ms * 1e-3) / 1e12
-            entry = {"ms": round(ms, 5), "tflops": round(tf, 2), "tensor_issued_tflops": round(2 * tf, 2),
-                     "frac_of_tensor_peak": round(2 * tf / peak_bf16, 4), "shape": [2048, 32768, 128],
-                     "bound": "tensor + softmax (CUDA cores); 18.9 MB of operands"}
-            if all(unfused):
-                entry["x_unfused_gemm_pair"] = round(sum(unfused) / ms, 2)
-            modes[label] = entry
-            fn()
-            torch.cuda.synchronize()
-            mode_outputs[label] = ("attention", (Od.cpu().numpy(), (q_a, k_a, v_a, scale_a)))
-        del Qd, Kd, Vd, Od, aws
+        for lk_a, rows_a in ((32768, (("attention_fused_2chain", mpg.ATTN_SPLIT_2CHAIN),
+                                      ("attention_fused_1chain", mpg.ATTN_SPLIT_1CHAIN))),
+                             (131072, (("attention_fused_2chain_131072", mpg.ATTN_SPLIT_2CHAIN),))):
+            q_a, k_a, v_a, scale_a = synthetic.attention_fused_inputs(lk=lk_a)
+            Qd = torch.from_numpy(q_a).to(device)
+            Kd = torch.from_numpy(k_a).to(device)
+            Vd = torch.from_numpy(v_a).to(device)
+            Od = torch.empty((2048, 128), dtype=torch.float32, device=device)
+            aws_b = mpg.attention_workspace_size(2048, lk_a, 128, 0)
+            aws = torch.empty(max(aws_b, 16), dtype=torch.uint8, device=device)
+            useful = 4.0 * 2048 * lk_a * 128
+            for label, amode in rows_a:
+                fn = (lambda am=amode, lk=lk_a: mpg.attention_raw(2048, lk, 128, Qd.data_ptr(), 128, Kd.data_ptr(),
+                                                                  128, Vd.data_ptr(), 128, Od.data_ptr(), 128,
+                                                                  scale_a, am, 0, aws.data_ptr(), aws_b, sh))
+                ms = time_steps(torch, fn, 100, 5, stream) / 100
+                tf = useful / (ms * 1e-3) / 1e12
+                entry = {"ms": round(ms, 5), "tflops": round(tf, 2), "tensor_issued_tflops": round(2 * tf, 2),
+                         "frac_of_tensor_peak": round(2 * tf / peak_bf16, 4), "shape": [2048, lk_a, 128],
+                         "bound": f"tensor + softmax (CUDA cores); {(2 * 2048 * 128 * 4 + 2 * lk_a * 128 * 2) / 1e6:.1f} MB "
+                                  "of operands (Q, O fp32; K, V fp16)"}
+                if lk_a == 32768 and all(unfused):
+                    entry["x_unfused_gemm_pair"] = round(sum(unfused) / ms, 2)
+                modes[label] = entry
+                fn()
+                torch.cuda.synchronize()
+                mode_outputs[label] = ("attention", (Od.cpu().numpy(), (q_a, k_a, v_a, scale_a)))
+            del Qd, Kd, Vd, Od, aws
         ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
         for lbl in [f"loguniform4096_{x}{y}" for x in ("split3", "split1", "split2a", "split4")
                     for y in ("", "_prepass")]:
