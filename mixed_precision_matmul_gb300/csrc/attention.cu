@@ -430,15 +430,15 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       tc_fence_after_sync();
       const uint32_t to = tmem_base + lane_off + T::kColO + 32u * part;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float a[4];
-        tmem_ld_4cols(to + 4 * c, a);
+      for (int c = 0; c < 2; ++c) {
+        float a[16];
+        tmem_ld_16cols(to + 16 * c, a);
         if constexpr (T::kL == 11) {
-          float b[4];
-          tmem_ld_4cols(to + 128 + 4 * c, b);
+          float b[16];
+          tmem_ld_16cols(to + 128 + 16 * c, b);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 4; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 d = ffma2(make_float2(b[i], b[i + 1]), make_float2(kLoScale, kLoScale),
                                    make_float2(a[i], a[i + 1]));
             a[i] = d.x;
@@ -448,17 +448,20 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
           tmem_ld_wait();
         }
         if (moved) {
-          const float4 f = reinterpret_cast<const float4*>(f_w)[c];
-          o[4 * c] = (o[4 * c] + a[0]) * f.x;
-          o[4 * c + 1] = (o[4 * c + 1] + a[1]) * f.y;
-          o[4 * c + 2] = (o[4 * c + 2] + a[2]) * f.z;
-          o[4 * c + 3] = (o[4 * c + 3] + a[3]) * f.w;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 f = reinterpret_cast<const float4*>(f_w)[(16 * c + i) / 4];
+            o[16 * c + i] = (o[16 * c + i] + a[i]) * f.x;
+            o[16 * c + i + 1] = (o[16 * c + i + 1] + a[i + 1]) * f.y;
+            o[16 * c + i + 2] = (o[16 * c + i + 2] + a[i + 2]) * f.z;
+            o[16 * c + i + 3] = (o[16 * c + i + 3] + a[i + 3]) * f.w;
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; i += 2) {
-            const float2 d = fadd2(make_float2(o[4 * c + i], o[4 * c + i + 1]), make_float2(a[i], a[i + 1]));
-            o[4 * c + i] = d.x;
-            o[4 * c + i + 1] = d.y;
+          for (int i = 0; i < 16; i += 2) {
+            const float2 d = fadd2(make_float2(o[16 * c + i], o[16 * c + i + 1]), make_float2(a[i], a[i + 1]));
+            o[16 * c + i] = d.x;
+            o[16 * c + i + 1] = d.y;
           }
         }
       }
