@@ -488,24 +488,24 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
       float x[32];
       const uint32_t ts = tmem_base + lane_off + T::kColS + 32u * part;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float a[8];
-        tmem_ld_8cols(ts + 8 * h, a);
+      for (int h = 0; h < 2; ++h) {
+        float a[16];
+        tmem_ld_16cols(ts + 16 * h, a);
         if constexpr (T::kL == 11) {
-          float b[8];
-          tmem_ld_8cols(ts + 128 + 8 * h, b);
+          float b[16];
+          tmem_ld_16cols(ts + 128 + 16 * h, b);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 d = ffma2(make_float2(b[i], b[i + 1]), make_float2(kLoScale, kLoScale),
                                    make_float2(a[i], a[i + 1]));
-            x[8 * h + i] = d.x;
-            x[8 * h + i + 1] = d.y;
+            x[16 * h + i] = d.x;
+            x[16 * h + i + 1] = d.y;
           }
         } else {
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[8 * h + i] = a[i];
+          for (int i = 0; i < 16; ++i) x[16 * h + i] = a[i];
         }
       }
       tc_fence_before_sync();
