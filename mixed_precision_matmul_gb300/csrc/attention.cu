@@ -14,8 +14,10 @@
 //     O^T = V^T [P_hi ; P_lo]^T   M 128 dims, N 256 = 128 queries x (hi, lo), K 128 keys
 // S keeps a query's scores in one TMEM lane, so the softmax's maxima and
 // sums stay inside a thread; O^T puts the hi and lo chains of one k-step in a
-// single N = 256 instruction (the tensor core's full rate), and P, written
-// row by row, is its K-major B operand.  The single-chain form accumulates
+// single N = 256 instruction (V^T is read once for both chains: 12 KB of
+// shared memory per k-step instead of 16, the operand reads being what the
+// tensor core waits on here), and P, written row by row, is its K-major B
+// operand.  The single-chain form accumulates
 // the hi and lo halves in one chain: S's lo products into the hi chain, O^T
 // as two N = 128 instructions into one accumulator.
 //
