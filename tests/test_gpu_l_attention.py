@@ -214,3 +214,16 @@ def test_attention_longest_context_sampled_rows(capsys):
     with capsys.disabled():
         print(f"\n[attention 512 x 131072: {err:.3e}]")
     assert err <= TOL_2CHAIN
+
+
+@pytest.mark.parametrize("mode", [mpg.ATTN_SPLIT_2CHAIN, mpg.ATTN_SPLIT_1CHAIN])
+def test_attention_one_range_of_many_blocks(mode):
+    """128 queries over 32768 keys in one key range: 256 blocks in one CTA
+    (every barrier's phase turns over many times, 64 folds of the O chains)."""
+    mpg.build()
+    q, k, v = inputs(128, 32768, 5)
+    scale = 2.0 / np.sqrt(128)
+    O = run(q, k, v, scale, mode=mode, key_splits=1)
+    rows = np.arange(0, 128, 8)
+    ref, den = oracle.attention(q[rows], k, v, scale)
+    assert _err(O[rows], ref, den) <= (TOL_2CHAIN if mode == mpg.ATTN_SPLIT_2CHAIN else 4 * TOL_2CHAIN)
