@@ -201,28 +201,6 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// 32 lanes x 8 consecutive 32-bit columns (same lane/column mapping).
-__device__ __forceinline__ void tmem_ld_8cols(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// 32 lanes x 4 consecutive 32-bit columns (same lane/column mapping).
-__device__ __forceinline__ void tmem_ld_4cols(uint32_t taddr, float* v) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr)
-               : "memory");
-#pragma unroll
-  for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(r[j]);
-}
-
 // Store 16 consecutive 32-bit columns of the warp's 32 lanes.
 __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const float* v) {
   asm volatile(
