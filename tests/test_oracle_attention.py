@@ -96,3 +96,29 @@ def test_split_query_is_the_hi_plus_lo_value(orc):
     q = Q.astype(np.float64)
     assert np.max(np.abs(hi + lo - q) / np.abs(q)) <= 2.0 ** -21
     assert 0 < np.max(np.abs(OR - OQ) / den) < 1e-6
+
+
+def test_zero_scale_gives_the_mean_of_v(orc):
+    # scale 0: every score is 0 whatever q and k, the weights uniform.  A
+    # scale applied to V or to the output instead of the scores fails here.
+    Q = synthetic.normal((4, 7), 206)
+    K = synthetic.normal((29, 7), 207)
+    V = synthetic.normal((29, 7), 208)
+    O, _ = orc.attention(Q, K, V, scale=0.0)
+    assert np.max(np.abs(O - V.astype(np.float64).mean(axis=0))) < 1e-15
+
+
+def test_a_common_shift_of_the_keys_leaves_o_unchanged(orc):
+    # k_j -> k_j + u adds scale * q_i . u to every score of row i: the
+    # softmax of a row does not change (binary64 inputs, so the shift is
+    # exact in the scores up to rounding).  A softmax over the query axis
+    # changes O here: the shifts differ from row to row.
+    Q = synthetic.normal((5, 8), 209).astype(np.float64)
+    K = synthetic.normal((41, 8), 210).astype(np.float64)
+    V = synthetic.normal((41, 8), 211).astype(np.float64)
+    u = 3.0 * synthetic.normal((1, 8), 212).astype(np.float64)
+    O1, _ = orc.attention(Q, K, V, scale=0.6)
+    O2, _ = orc.attention(Q, K + u, V, scale=0.6)
+    assert np.max(np.abs(O1 - O2)) < 1e-12
+    # and the per-row shifts differ (so a softmax over the wrong axis would show)
+    assert np.ptp(Q @ u.T) > 1.0
