@@ -67,20 +67,23 @@ typedef enum { MPG_F32 = 0, MPG_F16 = 1, MPG_BF16 = 2 } mpg_dtype;
  *   SPLIT_FP16_3CHAIN  fp32 inputs split on load into fp16 hi/lo halves
  *                (see mpg_options for the exact split); hi*hi, hi*lo and lo*hi
  *                accumulate in three separate fp32 accumulators that are summed
- *                in plain fp32 in the epilogue: acc = hh + 2^-11 * (hl + lh),
- *                per K chunk, the chunk totals added in fp32 (split_chunk_k).
+ *                in plain fp32 in the epilogue: acc = hh + 2^-L * (hl + lh)
+ *                (L = 11 by default, 0 with split_plain_lo), per K chunk, the
+ *                chunk totals added in fp32 (split_chunk_k).
  *   SPLIT_FP16_1CHAIN  the same three products accumulated in ONE accumulator
- *                (the shared-chain variant, kept for comparison; its lo is the
- *                plain fp16(x*2^s - hi), without the 2^11 scale).
+ *                over the whole K range (the shared-chain variant, kept for
+ *                comparison; its lo is the plain fp16(x*2^s - hi), without the
+ *                2^11 scale).
  *   FP32_FFMA    plain fp32 CUDA-core product: each output is one sequential
  *                fmaf chain over k in ascending order (the comparator).
  *   SPLIT_A_FP16_2CHAIN  the split of "qsa_prompt_attn ...", "What's going
- *                on": only A is split into fp16 hi and lo (lo scaled by 2^11),
- *                B is rounded to fp16 (RNE); A_hi*B and A_lo*B accumulate in two
- *                separate chains summed in fp32: acc = hb + 2^-11 * lb (per K
- *                chunk, as for the three-chain split).  fp32 inputs.
+ *                on": only A is split into fp16 hi and lo (lo scaled by 2^L,
+ *                L = 11 by default), B is rounded to fp16 (RNE); A_hi*B and
+ *                A_lo*B accumulate in two separate chains summed in fp32:
+ *                acc = hb + 2^-L * lb (per K chunk, as for the three-chain
+ *                split).  fp32 inputs.
  *   SPLIT_FP16_4CHAIN  the three-chain split plus the lo*lo product in a
- *                fourth chain: acc = hh + (2^-11 * (hl + lh) + 2^-22 * ll).
+ *                fourth chain: acc = hh + (2^-L * (hl + lh) + 2^-2L * ll).
  *                fp32 inputs; 128 x 64 tiles. */
 typedef enum {
   MPG_FP16_F32ACC = 0,
@@ -107,8 +110,8 @@ typedef enum {
  * means the defaults. */
 typedef struct {
   /* Split modes: A is split as x*2^split_exp_a and B as x*2^split_exp_b before
-   * hi = fp16(x*2^s), lo = fp16((x*2^s - hi) * 2^L) (L = 11 for 3CHAIN, 0 for
-   * 1CHAIN); the scale is undone exactly in the epilogue.  Use it to lift
+   * hi = fp16(x*2^s), lo = fp16((x*2^s - hi) * 2^L) (L: see split_plain_lo);
+   * the scale is undone exactly in the epilogue.  Use it to lift
    * operands whose magnitudes sit below fp16's normal range (2^-14), e.g.
    * softmax probabilities.  Default 0.  Range [-100, 100]. */
   int32_t split_exp_a;
@@ -127,7 +130,7 @@ typedef struct {
   int64_t wait_timeout_ns;
   /* The split modes except the one-chain form: the K loop accumulates in chunks of this many k
    * elements.  Each chunk starts fresh hh / hl / lh accumulators on the tensor
-   * cores; the epilogue adds the chunk's hh + 2^-11*(hl + lh) to an fp32
+   * cores; the epilogue adds the chunk's hh + 2^-L*(hl + lh) to an fp32
    * running sum with round-to-nearest.  This bounds how long the tensor
    * cores' own fp32 accumulation runs (its rounding is not round-to-nearest).
    * 0 = default: 512 for the three- and four-chain splits, one chunk for the
@@ -192,7 +195,20 @@ typedef struct {
    *       (MPG_ERR_WORKSPACE if the workspace is too small);
    *   -1 = never.  Other kernels ignore it. */
   int32_t tail_split;
-  int32_t reserved[3];
+  /* The lo half's scale 2^L in the split modes.
+   *   0 (default) = L = 11 in the forms with separate lo chains (3CHAIN,
+   *       A-only 2CHAIN, 4CHAIN): lo = fp16((x*2^s - hi) * 2^11), the lo
+   *       chains scaled back by 2^-11 in fp32 in the epilogue, which keeps
+   *       lo out of fp16's subnormals for |x*2^s| >= 2^-3; L = 0 in the
+   *       one-chain form (its single accumulator holds hi and lo products
+   *       at one scale);
+   *   1 = L = 0 in every split form: the plain lo = fp16(x*2^s - hi).  With
+   *       3CHAIN this is the three-chain split with the unscaled lo, whose
+   *       operands are bit for bit those of 1CHAIN: the two then differ in
+   *       the number of accumulator chains alone.
+   * Other values: MPG_ERR_INVALID_ARG. */
+  int32_t split_plain_lo;
+  int32_t reserved[2];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);
@@ -248,23 +264,33 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch,
  * raw allocations, and real-time or long-running services that allow no
  * allocation (and no allocation failure) after start-up.  This entry point
  * takes the same arguments as
- * mpg_gemm_ex minus the workspace; when the problem is split along K, the
- * partial sums go to a scratch array compiled into the library
- * (MPG_NOALLOC_SCRATCH_BYTES = 16 MiB of device memory, present on every GPU
- * that loads the library until the process exits).  It allocates nothing.
- *   - Problems whose split-K partial sums would exceed that size (splits x
- *     batch x m x n x 4 bytes) are rejected with MPG_ERR_WORKSPACE before
- *     anything is launched; use mpg_gemm with a workspace for those.
+ * mpg_gemm_ex minus the workspace and behaves as mpg_gemm_ex given a
+ * workspace of MPG_NOALLOC_SCRATCH_BYTES bytes: that workspace is a scratch
+ * array compiled into the library (16 MiB of device memory, present on every
+ * GPU that loads the library until the process exits).  It holds split-K
+ * partial sums, and the copies that the conversion pass or the aligned-copy
+ * path make when they fit.  It allocates nothing.
+ *   - With a split count forced by mpg_options.splitk whose partial sums
+ *     (splits x batch x m x n x 4 bytes) exceed the scratch, the call returns
+ *     MPG_ERR_WORKSPACE before anything is launched; an automatic split
+ *     count falls back to one split instead.  A conversion pass forced with
+ *     mpg_options.prepass = 1 whose copies exceed the scratch also returns
+ *     MPG_ERR_WORKSPACE.  Use mpg_gemm with a workspace for those.
  *   - The first call on a device looks up the scratch array's device address
- *     (once per device, with that device current); make that first call
- *     before any stream capture.
+ *     (once per device, with that device current) and keeps it for the life
+ *     of the process; make that first call before any stream capture.  After
+ *     cudaDeviceReset the kept address (like the library's other per-device
+ *     state) is no longer valid: do not call the library again in that
+ *     process.
  *   - Every call on a device shares the one scratch array, and each call
- *     overwrites the part it uses: calls that can overlap on the GPU
- *     (different streams without ordering) race.  Order them on one stream.
+ *     overwrites the part it uses (nothing in it needs to start at zero):
+ *     calls that can overlap on the GPU (different streams without ordering)
+ *     race.  Order them on one stream.
  *   - The split tail (mpg_options.tail_split) is never taken here: its
  *     partial sums can outgrow the scratch.
- * Results equal mpg_gemm_ex's for the same arguments and options with
- * tail_split = -1. */
+ * Results are bit for bit those of mpg_gemm_ex for the same arguments and
+ * options with tail_split = -1 and a workspace of MPG_NOALLOC_SCRATCH_BYTES
+ * bytes. */
 #define MPG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
                             const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
@@ -401,11 +427,27 @@ int64_t mpg_acc_matrix_offset(int lane, int j, int64_t tile_row, int64_t tile_co
 /* Inverse of mpg_acc_offset: offset in [0,128) -> (lane, j).  Returns 0 or -1. */
 int mpg_acc_decode(int offset, int* lane, int* j);
 
-/* Accumulator map of the tcgen05 path used by this library (M = 128,
- * cta_group::1): value `reg` returned by tcgen05.ld.32x32b to lane `lane` of
- * warp `warp`, reading columns starting at `col_base`, holds D(row, col) with
- * row = 32*(warp % 4) + lane and col = col_base + reg.  Returns 0 or -1. */
-int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int* col);
+/* Accumulator map of the tcgen05 paths of this library: cta_group::1 with
+ * M = 128 (m_shape 128) and cta_group::2 with M = 256 (m_shape 256, the CTA
+ * pair, where each CTA's TMEM holds 128 of the rows and every column).  The
+ * tcgen05 counterpart of the fragment map of "feat(cuda-device): derive the
+ * m16n8k16 accumulator fragment layout", section "API".
+ * Value `reg` returned by tcgen05.ld.32x32b to lane `lane` of warp `warp` of
+ * the CTA of rank `cta_rank` in the pair (0 for M = 128), reading columns
+ * from `col_base` on, holds D(row, col) with
+ *     row = 128*cta_rank + 32*(warp % 4) + lane,   col = col_base + reg.
+ * col_base + reg < 512 (the TMEM columns of an SM).  Returns 0, or -1 for an
+ * out-of-range argument (outputs untouched). */
+int mpg_tmem_acc_coords(int m_shape, int cta_rank, int warp, int lane, int reg, int col_base, int* row, int* col);
+
+/* Inverse of mpg_tmem_acc_coords for loads of `load_cols` columns per
+ * tcgen05.ld (a power of two, 1 .. 128; col_base a multiple of it): D(row,
+ * col), row < m_shape, col < 512, comes from register `reg` of lane `lane`
+ * of warp `warp` (the lowest index, 0 .. 3, of the warps that reach its lane
+ * quarter; warp + 4j reads the same lanes) of CTA `cta_rank`, in the load
+ * that starts at column `col_base`.  Returns 0 or -1. */
+int mpg_tmem_acc_decode(int m_shape, int row, int col, int load_cols, int* cta_rank, int* warp, int* lane, int* reg,
+                        int* col_base);
 
 /* ---- operand fragment maps of mma.sync m16n8k16 (f16 / bf16 operands) -----
  * The cuda-oxide page derives the accumulator numeral and notes that the A
@@ -455,6 +497,24 @@ mpg_status mpg_probe_mma_m16n8k16_fragments(const uint32_t* Afrag, const uint32_
  * each, not overlapping; blocks in [0, 2^40].  MPG_ERR_INVALID_ARG for bad
  * arguments, before any launch. */
 mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t blocks, int scalar, void* stream);
+
+/* One tcgen05.mma pass of the library's one-CTA path (cta_group::1, M = 128,
+ * N = n, K = 64 as four K = 16 instructions of kind::f16, fp32 accumulator in
+ * TMEM, both operands K-major in 128-byte swizzled shared memory, the
+ * operand layout and descriptors of the product kernels), followed by
+ * tcgen05.ld.32x32b.x32 of every column by the four warps of the CTA.
+ *   A: device, 128 x 64 fp16 (raw codes), row-major, ld 64.
+ *   B: device, n x 64 fp16: row j holds column j of the K x N operand (B
+ *      column-major with ld 64).
+ *   n: 64, 128 or 256.
+ *   D: device, 128 * n floats, the loads unscattered:
+ *      D[((warp*32 + lane) * (n/32) + c) * 32 + reg] is register `reg` of lane
+ *      `lane` of warp `warp` in the load of columns 32c .. 32c+31.  Placing
+ *      each value with mpg_tmem_acc_coords(128, 0, warp, lane, reg, 32c, ...)
+ *      and comparing with the host product checks the map on the hardware.
+ * Waits are bounded (1 s); MPG_ERR_INVALID_ARG for bad arguments, before any
+ * launch; a wait that expires shows in mpg_device_status. */
+mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, void* stream);
 
 /* Failure-detection self test: launches one kernel whose single wait is on an
  * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then

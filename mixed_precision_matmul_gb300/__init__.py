@@ -12,7 +12,7 @@ Entry points mirror ``include/mpgemm.h``:
   stride column-major; a leading batch dimension gives the batch stride).
 * :func:`gemm_raw`   the plain-pointer form of ``mpg_gemm_ex``.
 * :func:`acc_coords`, :func:`acc_offset`, :func:`acc_matrix_offset`,
-  :func:`acc_decode`, :func:`tmem_acc_coords`   host decode of accumulator
+  :func:`acc_decode`, :func:`tmem_acc_coords`, :func:`tmem_acc_decode`   host decode of accumulator
   fragments.
 * :func:`probe_mma_m16n8k16`, :func:`selftest_wait_timeout`,
   :func:`device_status`.
@@ -64,7 +64,8 @@ class Options(ctypes.Structure):
         ("c_dtype", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
         ("tail_split", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("split_plain_lo", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -135,8 +136,12 @@ def lib():
         L.mpg_acc_matrix_offset.restype = i64
         L.mpg_acc_decode.argtypes = [i32, pi, pi]
         L.mpg_acc_decode.restype = i32
-        L.mpg_tmem_acc_coords.argtypes = [i32, i32, i32, i32, pi, pi]
+        L.mpg_tmem_acc_coords.argtypes = [i32, i32, i32, i32, i32, i32, pi, pi]
         L.mpg_tmem_acc_coords.restype = i32
+        L.mpg_tmem_acc_decode.argtypes = [i32, i32, i32, i32, pi, pi, pi, pi, pi]
+        L.mpg_tmem_acc_decode.restype = i32
+        L.mpg_probe_tmem_acc.argtypes = [vp, vp, i32, vp, vp]
+        L.mpg_probe_tmem_acc.restype = i32
         L.mpg_probe_mma_m16n8k16.argtypes = [vp, vp, vp, vp]
         L.mpg_probe_mma_m16n8k16.restype = i32
         for nm in ("mpg_frag_a_coords", "mpg_frag_a_decode", "mpg_frag_b_coords", "mpg_frag_b_decode"):
@@ -454,11 +459,23 @@ def acc_decode(offset: int) -> tuple[int, int] | None:
     return ln.value, j.value
 
 
-def tmem_acc_coords(warp: int, lane: int, reg: int, col_base: int = 0):
+def tmem_acc_coords(warp: int, lane: int, reg: int, col_base: int = 0, m_shape: int = 128, cta_rank: int = 0):
+    """(row, col) of register `reg` of lane `lane` of warp `warp` in a
+    tcgen05.ld.32x32b from column `col_base` (mpg_tmem_acc_coords)."""
     r, c = ctypes.c_int(), ctypes.c_int()
-    if lib().mpg_tmem_acc_coords(warp, lane, reg, col_base, ctypes.byref(r), ctypes.byref(c)) != 0:
+    if lib().mpg_tmem_acc_coords(m_shape, cta_rank, warp, lane, reg, col_base, ctypes.byref(r),
+                                 ctypes.byref(c)) != 0:
         return None
     return r.value, c.value
+
+
+def tmem_acc_decode(row: int, col: int, load_cols: int = 32, m_shape: int = 128):
+    """(cta_rank, warp, lane, reg, col_base) holding D(row, col) in loads of
+    `load_cols` columns (mpg_tmem_acc_decode)."""
+    out = [ctypes.c_int() for _ in range(5)]
+    if lib().mpg_tmem_acc_decode(m_shape, row, col, load_cols, *[ctypes.byref(x) for x in out]) != 0:
+        return None
+    return tuple(x.value for x in out)
 
 
 def _pair(fn, x, y):
@@ -510,6 +527,21 @@ def probe_mma_m16n8k16_fragments(a_frag, b_frag, stream=None):
     d = torch.empty((32, 4), dtype=torch.float32, device=a.device)
     _check(lib().mpg_probe_mma_m16n8k16_fragments(a.data_ptr(), b.data_ptr(), d.data_ptr(),
                                                    _stream_handle(stream)))
+    return d
+
+
+def probe_tmem_acc(A16, Bt16, stream=None):
+    """One k-block (K = 64) of the one-CTA tcgen05 path on fp16 A (128 x 64)
+    and B given as Bt (n x 64, row j = column j of B); returns the raw
+    tcgen05.ld registers as a (4 warps, 32 lanes, n/32 loads, 32 regs) tensor."""
+    torch = _torch()
+    a = A16.to(torch.float16).contiguous()
+    bt = Bt16.to(torch.float16).contiguous()
+    n = bt.shape[0]
+    if a.shape != (128, 64) or bt.shape[1] != 64:
+        raise ValueError("A must be 128 x 64 and Bt n x 64")
+    d = torch.empty((4, 32, n // 32, 32), dtype=torch.float32, device=a.device)
+    _check(lib().mpg_probe_tmem_acc(a.data_ptr(), bt.data_ptr(), n, d.data_ptr(), _stream_handle(stream)))
     return d
 
 

@@ -36,6 +36,7 @@ SOURCES = [
     "prepass.cu",
     "tc_pair.cu",
     "attention.cu",
+    "tmem_probe.cu",
 ]
 HEADERS = ["ptx.cuh", "internal.h", "tc_gemm.cuh", "outio.cuh", "host.h", "staging.cuh"]
 

@@ -92,11 +92,36 @@ int mpg_frag_b_decode(int k, int n, int* lane, int* i) {
   return 0;
 }
 
-int mpg_tmem_acc_coords(int warp, int lane, int reg, int col_base, int* row, int* col) {
-  if (warp < 0 || lane < 0 || lane > 31 || reg < 0 || col_base < 0 || col_base + reg >= 512 || !row || !col)
+// tcgen05 accumulator: with M = 128 (cta_group::1) row i of D is TMEM lane
+// i of the CTA; with M = 256 (cta_group::2) rows 0-127 sit in the lanes of
+// CTA rank 0 and rows 128-255 in those of rank 1.  Column j of D is TMEM
+// column j (from the accumulator's base).  A warp reaches the lane quarter
+// warp % 4 only; tcgen05.ld.32x32b gives lane t of the warp the value of TMEM
+// lane 32*(warp % 4) + t, register r of column col_base + r.
+namespace {
+bool tmem_shape_ok(int m_shape) { return m_shape == 128 || m_shape == 256; }
+}  // namespace
+
+int mpg_tmem_acc_coords(int m_shape, int cta_rank, int warp, int lane, int reg, int col_base, int* row, int* col) {
+  if (!tmem_shape_ok(m_shape) || cta_rank < 0 || cta_rank >= m_shape / 128 || warp < 0 || lane < 0 || lane > 31 ||
+      reg < 0 || col_base < 0 || reg >= 512 || col_base >= 512 || col_base + reg >= 512 || !row || !col)
     return -1;
-  *row = 32 * (warp % 4) + lane;
+  *row = 128 * cta_rank + 32 * (warp % 4) + lane;
   *col = col_base + reg;
+  return 0;
+}
+
+int mpg_tmem_acc_decode(int m_shape, int row, int col, int load_cols, int* cta_rank, int* warp, int* lane, int* reg,
+                        int* col_base) {
+  if (!tmem_shape_ok(m_shape) || row < 0 || row >= m_shape || col < 0 || col >= 512 || load_cols < 1 ||
+      load_cols > 128 || (load_cols & (load_cols - 1)) != 0 || !cta_rank || !warp || !lane || !reg || !col_base)
+    return -1;
+  const int within = row % 128;   // the TMEM lane in the CTA that holds the row
+  *cta_rank = row / 128;
+  *warp = within / 32;            // the lowest warp index of that lane quarter
+  *lane = within % 32;
+  *col_base = col - col % load_cols;
+  *reg = col % load_cols;
   return 0;
 }
 

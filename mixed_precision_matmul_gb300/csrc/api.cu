@@ -255,11 +255,12 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
                                                              : plan.pre_conv;
       const int64_t sA = strideA ? strideA : L.a_outer * lda;
       const int64_t sB = strideB ? strideB : L.b_outer * ldb;
+      const float lo_mul = std::ldexp(1.0f, split_lo_exp(plan.pre_conv, o));
       e = launch_prepass(conv_a, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi, a_lo,
-                         L.a_ld, std::ldexp(1.0f, ea), dev->sm_count, st);
+                         L.a_ld, std::ldexp(1.0f, ea), lo_mul, dev->sm_count, st);
       if (e == cudaSuccess)
         e = launch_prepass(conv_b, static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi, b_lo,
-                           L.b_ld, std::ldexp(1.0f, eb), dev->sm_count, st);
+                           L.b_ld, std::ldexp(1.0f, eb), lo_mul, dev->sm_count, st);
       if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "conversion pass launch: %s", cudaGetErrorString(e));
       const mpg_dtype cdt = (plan.op == Op::kBF16) ? MPG_BF16 : MPG_F16;
       Operand Ah{a_hi, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
@@ -339,6 +340,21 @@ mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t block
   return MPG_OK;
 }
 
+mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, void* stream) {
+  t_err.clear();
+  if (!A || !B || !D) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  if (n != 64 && n != 128 && n != 256) return fail(MPG_ERR_INVALID_ARG, "n must be 64, 128 or 256");
+  if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0)
+    return fail(MPG_ERR_INVALID_ARG, "A and B must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(D) % 4 != 0) return fail(MPG_ERR_INVALID_ARG, "D not aligned to 4 bytes");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = launch_probe_tmem(A, B, n, D, dev->status, 1000000000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
 mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
   t_err.clear();
   if (timeout_ns < 1000000 || timeout_ns > 10000000000ll)
@@ -368,26 +384,29 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch, cons
   DeviceInfo* dev = nullptr;
   s = get_device(&dev);
   if (s != MPG_OK) return s;
-  // the split-K scratch this problem needs (the same choice mpg_gemm makes)
-  size_t need = 0;
-  if (k > 0 && alpha != 0.0f && mode != MPG_FP32_FFMA)
-    need = splitk_bytes(choose_splits(m, n, k, batch, dev->sm_count, o), m, n, batch);
-  if (need > MPG_NOALLOC_SCRATCH_BYTES)
-    return fail(MPG_ERR_WORKSPACE,
-                "split-K partial sums need %zu bytes, more than the %u-byte static scratch of "
-                "mpg_gemm_noalloc; call mpg_gemm with a workspace instead",
-                need, (unsigned)MPG_NOALLOC_SCRATCH_BYTES);
-  void* scratch = nullptr;
-  if (need > 0) {
-    s = noalloc_scratch(&scratch);
-    if (s != MPG_OK) return s;
+  // A forced split count whose partial sums cannot fit the scratch is
+  // refused here with a message naming the scratch; an automatic count is
+  // left to the planner, which drops to one split when the partials do not
+  // fit (as it does for a small caller workspace).
+  if (o.splitk > 0 && k > 0 && alpha != 0.0f && mode != MPG_FP32_FFMA) {
+    const size_t need = splitk_bytes(choose_splits(m, n, k, batch, dev->sm_count, o), m, n, batch);
+    if (need > MPG_NOALLOC_SCRATCH_BYTES)
+      return fail(MPG_ERR_WORKSPACE,
+                  "split-K partial sums need %zu bytes, more than the %u-byte static scratch of "
+                  "mpg_gemm_noalloc; call mpg_gemm with a workspace instead",
+                  need, (unsigned)MPG_NOALLOC_SCRATCH_BYTES);
   }
+  // The whole scratch is offered on every call, so that the planner sees
+  // the same budget whatever the split count: the same plan as mpg_gemm_ex
+  // given a workspace of MPG_NOALLOC_SCRATCH_BYTES.
+  void* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != MPG_OK) return s;
   // the split tail's partial sums would need more than the scratch holds
   // for the largest products: this entry never takes it
   o.tail_split = -1;
   return mpg_gemm_ex(m, n, k, batch, A, lda, strideA, a_dtype, a_layout, B, ldb, strideB, b_dtype, b_layout, C,
-                     ldc, strideC, alpha, beta, mode, scratch, need > 0 ? (size_t)MPG_NOALLOC_SCRATCH_BYTES : 0,
-                     stream, &o);
+                     ldc, strideC, alpha, beta, mode, scratch, (size_t)MPG_NOALLOC_SCRATCH_BYTES, stream, &o);
 }
 
 }  // extern "C"

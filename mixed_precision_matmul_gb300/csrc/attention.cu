@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) attn_kernel(const __grid_const
         const uint32_t row = (uint32_t)(8 * w0 + i);
         // q * scale * log2(e), split: the scores come out in base-2 units
         uint32_t h0, l0, h1, l1;
-        split_pair<T::kL>(xq[i].x, xq[i].y, p.scale_log2, h0, l0);
-        split_pair<T::kL>(xq[i].z, xq[i].w, p.scale_log2, h1, l1);
+        split_pair(xq[i].x, xq[i].y, p.scale_log2, T::kL == 11 ? 2048.0f : 1.0f, h0, l0);
+        split_pair(xq[i].z, xq[i].w, p.scale_log2, T::kL == 11 ? 2048.0f : 1.0f, h1, l1);
         // dims 4l..4l+3: dim half l / 16, 8-byte half (l & 1) of chunk (l / 2) % 8
         // of line `row` (hi) and `128 + row` (lo)
         const uint32_t addr = q_smem + (uint32_t)(lane >> 4) * 32768u +

@@ -107,6 +107,7 @@ bool auto_prepass_shape(int64_t m, int64_t n, int64_t k);
 bool prepass_mode(mpg_precision mode);
 bool splits_a(Conv c);
 bool splits_b(Conv c);
+int split_lo_exp(Conv c, const mpg_options& o);
 mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
                      float alpha, mpg_precision mode, const mpg_options& o, int sm_count, size_t ws_bytes,
                      Plan* plan);

@@ -62,6 +62,7 @@ struct TcParams {
   float alpha;        // already multiplied by 2^-(split_exp_a + split_exp_b)
   float beta;
   float scale_a, scale_b;  // 2^split_exp_a, 2^split_exp_b (split converter)
+  float lo_mul, lo_inv;    // split: the lo half's scale 2^L and its inverse (L = 11 or 0)
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t chunk_kb;   // k-blocks per accumulation chunk (0: the whole k range of a tile)
@@ -160,16 +161,20 @@ cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_
 // Separate conversion pass: a stored fp32 matrix (per batch `outer` lines of
 // `inner` elements, leading dimension ld_in, batch stride stride_in) into
 // packed 16-bit copies with leading dimension ld_out (batch stride
-// outer * ld_out).  conv: kRoundF16, kRoundBF16, kSplit3 (hi, lo*2^11) or
-// kSplit1 (hi, lo); `lo` is written for the split only.  x is scaled by
-// `scale` (a power of two) before the split.
+// outer * ld_out).  conv: kRoundF16, kRoundBF16, or a split (kSplit3 /
+// kSplit1: hi = fp16(x*scale), lo = fp16((x*scale - hi) * lo_mul)); `lo` is
+// written for the split only.  scale and lo_mul are powers of two.
 cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
-                           int sm_count, cudaStream_t stream);
+                           float lo_mul, int sm_count, cudaStream_t stream);
 cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream);
 cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, int scalar, int sm_count,
                                  cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+// One-CTA tcgen05 pass (M 128, N n, K 64) whose TMEM accumulator is copied
+// out unscattered, register by register (n = 64, 128 or 256).
+cudaError_t launch_probe_tmem(const void* a, const void* b, int n, float* d, uint32_t* status, uint64_t limit_ns,
+                              cudaStream_t stream);
 
 // Device status word of the current device (allocated by the runtime as a
 // module global; one per device).

@@ -172,6 +172,14 @@ bool splits_a(Conv c) {
 }
 bool splits_b(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplit4; }
 
+// Exponent L of the lo half's scale 2^L: 11 for the forms whose lo products
+// have chains of their own, unless the caller asks for the plain lo; 0 for
+// the one-chain form (and for conversions without a lo half).
+int split_lo_exp(Conv c, const mpg_options& o) {
+  if (c == Conv::kSplit3 || c == Conv::kSplitA2 || c == Conv::kSplit4) return o.split_plain_lo ? 0 : 11;
+  return 0;
+}
+
 mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Operand& A, const Operand& B,
                      float alpha, mpg_precision mode, const mpg_options& o, int sm_count, size_t ws_bytes,
                      Plan* plan) {
@@ -397,6 +405,8 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (o.cta_pair < -1 || o.cta_pair > 1) return fail(MPG_ERR_INVALID_ARG, "cta_pair must be -1, 0 or 1");
   if (o.tail_split < -1 || o.tail_split > 1) return fail(MPG_ERR_INVALID_ARG, "tail_split must be -1, 0 or 1");
   if (o.prepass < -1 || o.prepass > 1) return fail(MPG_ERR_INVALID_ARG, "prepass must be -1, 0 or 1");
+  if (o.split_plain_lo < 0 || o.split_plain_lo > 1)
+    return fail(MPG_ERR_INVALID_ARG, "split_plain_lo must be 0 or 1");
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
   if (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 4 : 2) != 0)
@@ -591,6 +601,9 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.beta = beta;
   p.scale_a = std::ldexp(1.0f, sa);
   p.scale_b = std::ldexp(1.0f, sb);
+  const int lo_exp = split_lo_exp(plan.conv, o);
+  p.lo_mul = std::ldexp(1.0f, lo_exp);
+  p.lo_inv = std::ldexp(1.0f, -lo_exp);
   p.status = dev->status;
   p.wait_limit_ns = o.wait_timeout_ns > 0 ? (uint64_t)o.wait_timeout_ns : kDefaultWaitNs;
   p.chunk_kb = 0;

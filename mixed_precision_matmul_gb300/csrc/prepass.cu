@@ -14,9 +14,9 @@ namespace mpg {
 namespace {
 
 // Convert 8 consecutive fp32 values into 8 16-bit values (hi) and, for the
-// split, 8 lo values, packed as four 32-bit words each.
+// split, 8 lo values (scaled by lo_mul), packed as four 32-bit words each.
 template <Conv CV>
-__device__ __forceinline__ void convert8(const float (&x)[8], float scale, uint4& hi, uint4& lo) {
+__device__ __forceinline__ void convert8(const float (&x)[8], float scale, float lo_mul, uint4& hi, uint4& lo) {
   uint32_t w[4], l[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -25,8 +25,7 @@ __device__ __forceinline__ void convert8(const float (&x)[8], float scale, uint4
     } else if constexpr (CV == Conv::kRoundBF16) {
       w[j] = pack_bf16x2(x[2 * j] * scale, x[2 * j + 1] * scale);
     } else {
-      constexpr int L = (CV == Conv::kSplit3) ? 11 : 0;
-      split_pair<L>(x[2 * j], x[2 * j + 1], scale, w[j], l[j]);
+      split_pair(x[2 * j], x[2 * j + 1], scale, lo_mul, w[j], l[j]);
     }
   }
   hi = make_uint4(w[0], w[1], w[2], w[3]);
@@ -40,8 +39,8 @@ __global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ 
                                                       int64_t stride_in, int64_t outer, int64_t inner,
                                                       int64_t batch, uint16_t* __restrict__ hi,
                                                       uint16_t* __restrict__ lo, int64_t ld_out, float scale,
-                                                      int vec) {
-  constexpr bool kSplit = (CV == Conv::kSplit3 || CV == Conv::kSplit1);
+                                                      float lo_mul, int vec) {
+  constexpr bool kSplit = (CV == Conv::kSplit3);
   const int64_t items_per_line = (inner + 7) / 8;
   const int64_t per_batch = outer * items_per_line;
   const int64_t total = per_batch * batch;
@@ -75,7 +74,7 @@ __global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ 
     for (int u = 0; u < 2; ++u) {
       if (!live[u]) continue;
       uint4 h, l;
-      convert8<CV>(x[u], scale, h, l);
+      convert8<CV>(x[u], scale, lo_mul, h, l);
       *reinterpret_cast<uint4*>(hi + o[u]) = h;
       if constexpr (kSplit) *reinterpret_cast<uint4*>(lo + o[u]) = l;
     }
@@ -178,7 +177,7 @@ cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64
 
 cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
                            int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
-                           int sm_count, cudaStream_t stream) {
+                           float lo_mul, int sm_count, cudaStream_t stream) {
   const int64_t total = batch * outer * ((inner + 7) / 8);
   int64_t blocks = (total + 511) / 512;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
@@ -187,19 +186,17 @@ cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t st
   switch (conv) {
     case Conv::kRoundF16:
       prepass_kernel<Conv::kRoundF16><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi,
-                                                                        lo, ld_out, scale, vec);
+                                                                        lo, ld_out, scale, 1.0f, vec);
       break;
     case Conv::kRoundBF16:
       prepass_kernel<Conv::kRoundBF16><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch,
-                                                                         hi, lo, ld_out, scale, vec);
+                                                                         hi, lo, ld_out, scale, 1.0f, vec);
       break;
     case Conv::kSplit3:
-      prepass_kernel<Conv::kSplit3><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi, lo,
-                                                                      ld_out, scale, vec);
-      break;
     case Conv::kSplit1:
-      prepass_kernel<Conv::kSplit1><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi, lo,
-                                                                      ld_out, scale, vec);
+      // one split kernel: the forms differ only in the lo half's scale
+      prepass_kernel<Conv::kSplit3><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi, lo,
+                                                                      ld_out, scale, lo_mul, vec);
       break;
     default:
       return cudaErrorInvalidValue;

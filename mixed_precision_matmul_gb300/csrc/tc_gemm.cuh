@@ -219,17 +219,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Split of two fp32 values: hi = fp16(x*s), lo = fp16((x*s - hi) * 2^L).
-// x*s and the residual are exact in fp32 (power-of-two scale; the residual of
-// an 11-bit rounding of a 24-bit significand has at most 13 bits).
-template <int L>
-__device__ __forceinline__ void split_pair(float x0, float x1, float s, uint32_t& hi, uint32_t& lo) {
+// Split of two fp32 values: hi = fp16(x*s), lo = fp16((x*s - hi) * lo_mul),
+// lo_mul = 2^L (1 or 2^11).  x*s and the residual are exact in fp32
+// (power-of-two scale; the residual of an 11-bit rounding of a 24-bit
+// significand has at most 13 bits), and so is the product with lo_mul.
+__device__ __forceinline__ void split_pair(float x0, float x1, float s, float lo_mul, uint32_t& hi, uint32_t& lo) {
   const float y0 = x0 * s, y1 = x1 * s;
   __half2 h = __floats2half2_rn(y0, y1);
   const float2 hb = __half22float2(h);
   const float r0 = y0 - hb.x, r1 = y1 - hb.y;
-  constexpr float kL = (L == 11) ? 2048.0f : 1.0f;
-  __half2 l = __floats2half2_rn(r0 * kL, r1 * kL);
+  __half2 l = __floats2half2_rn(r0 * lo_mul, r1 * lo_mul);
   hi = *reinterpret_cast<uint32_t*>(&h);
   lo = *reinterpret_cast<uint32_t*>(&l);
 }
@@ -253,7 +252,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // tf32 operands w[0..3] are the fp32 bits.
 template <class T>
 __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned short (&h)[4], float scale,
-                                           uint32_t (&w)[4], bool isA) {
+                                           float lo_mul, uint32_t (&w)[4], bool isA) {
   if constexpr (T::kOpBytes == 4) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(x[e]);
@@ -272,17 +271,16 @@ __device__ __forceinline__ void pack_chunk(const float (&x)[4], const unsigned s
   } else if constexpr (T::kConv == Conv::kSplitA2) {
     // A is split (lo scaled by 2^11), B rounded to fp16
     if (isA) {
-      split_pair<11>(x[0], x[1], scale, w[0], w[2]);
-      split_pair<11>(x[2], x[3], scale, w[1], w[3]);
+      split_pair(x[0], x[1], scale, lo_mul, w[0], w[2]);
+      split_pair(x[2], x[3], scale, lo_mul, w[1], w[3]);
     } else {
       w[0] = pack_f16x2(x[0] * scale, x[1] * scale);
       w[1] = pack_f16x2(x[2] * scale, x[3] * scale);
       w[2] = w[3] = 0;
     }
   } else {
-    constexpr int L = (T::kConv == Conv::kSplit1) ? 0 : 11;
-    split_pair<L>(x[0], x[1], scale, w[0], w[2]);
-    split_pair<L>(x[2], x[3], scale, w[1], w[3]);
+    split_pair(x[0], x[1], scale, lo_mul, w[0], w[2]);
+    split_pair(x[2], x[3], scale, lo_mul, w[1], w[3]);
   }
 }
 
@@ -571,16 +569,18 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 tc_fence_before_sync();
                 mbar_arrive(&acc_empty[ab]);
               }
+              // 2^-L undoes the lo half's scale (exact: a power of two)
+              const float lo_inv = p.lo_inv;
   #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                // three chains: hh + 2^-11 (hl + lh); two chains (A-only split): hb + 2^-11 lb
+                // three chains: hh + 2^-L (hl + lh); two chains (A-only split): hb + 2^-L lb
                 float x;
-                if constexpr (T::kConv == Conv::kSplit4)   // ... + 2^-22 ll
-                  x = x0[j] + (0x1p-11f * (x1[j] + x2[j]) + 0x1p-22f * x3[j]);
+                if constexpr (T::kConv == Conv::kSplit4)   // ... + 2^-2L ll
+                  x = x0[j] + (lo_inv * (x1[j] + x2[j]) + (lo_inv * lo_inv) * x3[j]);
                 else if constexpr (T::kConv == Conv::kSplit3)
-                  x = x0[j] + 0x1p-11f * (x1[j] + x2[j]);
+                  x = x0[j] + lo_inv * (x1[j] + x2[j]);
                 else
-                  x = x0[j] + 0x1p-11f * x1[j];
+                  x = x0[j] + lo_inv * x1[j];
                 v[h * 16 + j] = have_run ? r[j] + x : x;
               }
             }
@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 h[e] = cur.h[i][e];
               }
             }
-            pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, w[i], isA);
+            pack_chunk<T>(x, h, isA ? p.scale_a : p.scale_b, p.lo_mul, w[i], isA);
           }
           if constexpr (T::kSrc == Src::kGeneric) cur = nxt;
           if constexpr (T::kStaged) {

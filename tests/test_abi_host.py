@@ -76,6 +76,15 @@ def test_option_ranges_rejected(L):
     assert _call(opts=mpg.options(c_dtype=3)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(tail_split=2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(tail_split=-2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(split_plain_lo=2)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(split_plain_lo=-1)) == mpg.ERR_INVALID_ARG
+
+
+def test_probe_tmem_arguments_rejected_before_launch(L):
+    assert L.mpg_probe_tmem_acc(None, None, 64, None, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_tmem_acc(16, 16, 96, 16, None) == mpg.ERR_INVALID_ARG     # n not 64 / 128 / 256
+    assert L.mpg_probe_tmem_acc(8, 16, 64, 16, None) == mpg.ERR_INVALID_ARG      # A not 16-byte aligned
+    assert L.mpg_probe_tmem_acc(16, 16, 64, 2, None) == mpg.ERR_INVALID_ARG      # D not 4-byte aligned
 
 
 def test_staging_probe_arguments_rejected_before_launch(L):
@@ -247,6 +256,47 @@ def test_tmem_accumulator_map(L):
     assert rows == set(range(128))
     assert mpg.tmem_acc_coords(0, 32, 0) is None
     assert mpg.tmem_acc_coords(0, 0, 0, 512) is None
+
+
+@pytest.mark.parametrize("m_shape", [128, 256])
+def test_tmem_accumulator_map_round_trips_over_every_point(L, m_shape):
+    """Every (cta, warp, lane, register, load) of an m_shape x 256 accumulator
+    read in 32-column loads lands on a distinct point, the points cover the
+    whole accumulator (no gap, no overlap for warps 0-3; warps 4-7 repeat
+    them), and the decode is the inverse, for every load width."""
+    ncol = 256
+    hits = {}
+    for cta in range(m_shape // 128):
+        for warp in range(8):
+            for lane in range(32):
+                for col in range(ncol):
+                    cb, reg = col - col % 32, col % 32
+                    r, c = mpg.tmem_acc_coords(warp, lane, reg, cb, m_shape=m_shape, cta_rank=cta)
+                    hits.setdefault((r, c), []).append((cta, warp, lane, reg, cb))
+    assert set(hits) == {(r, c) for r in range(m_shape) for c in range(ncol)}
+    assert all(len(v) == 2 for v in hits.values())
+    for (r, c), owners in hits.items():
+        cta, warp, lane, reg, cb = owners[0]
+        assert warp < 4 and owners[1][1] == warp + 4      # the same lanes, one warpgroup apart
+        assert mpg.tmem_acc_decode(r, c, 32, m_shape=m_shape) == (cta, warp, lane, reg, cb)
+    for w in (1, 2, 4, 8, 16, 64, 128):
+        for r, c in ((0, 0), (m_shape - 1, 511), (77, 300), (m_shape // 2 + 5, 129)):
+            cta, warp, lane, reg, cb = mpg.tmem_acc_decode(r, c, w, m_shape=m_shape)
+            assert cb % w == 0 and reg < w
+            assert mpg.tmem_acc_coords(warp, lane, reg, cb, m_shape=m_shape, cta_rank=cta) == (r, c)
+
+
+def test_tmem_accumulator_map_rejects_bad_arguments(L):
+    assert mpg.tmem_acc_coords(0, 0, 0, 0, m_shape=64) is None          # only M = 128 and M = 256
+    assert mpg.tmem_acc_coords(0, 0, 0, 0, m_shape=128, cta_rank=1) is None
+    assert mpg.tmem_acc_coords(0, 0, 0, 0, m_shape=256, cta_rank=2) is None
+    assert mpg.tmem_acc_coords(-1, 0, 0, 0) is None
+    assert mpg.tmem_acc_coords(0, 0, 511, 1) is None                     # past the 512 TMEM columns
+    assert mpg.tmem_acc_decode(128, 0) is None                           # row beyond M
+    assert mpg.tmem_acc_decode(0, 512) is None
+    assert mpg.tmem_acc_decode(0, 0, 3) is None                          # load width not a power of two
+    assert mpg.tmem_acc_decode(0, 0, 256) is None
+    assert mpg.tmem_acc_decode(255, 0, m_shape=256) == (1, 3, 31, 0, 0)
 
 
 # ---------------------------------------------------------------- operand fragments

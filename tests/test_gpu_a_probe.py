@@ -95,3 +95,34 @@ def test_operand_fragment_maps_on_hardware(orc):
     A2 = torch.from_numpy(_pack_pairs(af.reshape(32, 4, 2))[:, [0, 2, 1, 3]].copy().view(np.int32)).cuda()
     d2 = mpg.probe_mma_m16n8k16_fragments(A2, B).cpu().numpy()
     assert not np.array_equal(d2, d)
+
+
+@pytest.mark.parametrize("n", [64, 128, 256])
+def test_tmem_accumulator_map_on_hardware(orc, n):
+    """One k-block (K = 64, four tcgen05.mma kind::f16) of the one-CTA path;
+    the raw tcgen05.ld registers placed on the host with the exported
+    mpg_tmem_acc_coords must equal the host product at every one of the
+    128 x n points (integer inputs: every product and sum is exact).  A row
+    map shifted by a lane or a quarter, or a transposed column order inside
+    a load, would not have matched."""
+    import torch
+    mpg.build()
+    g = np.random.Generator(np.random.PCG64(7100 + n))
+    a = g.integers(-3, 4, size=(128, 64)).astype(np.float32)
+    bt = g.integers(-3, 4, size=(n, 64)).astype(np.float32)     # row j = column j of B
+    d = mpg.probe_tmem_acc(torch.from_numpy(a).cuda(), torch.from_numpy(bt).cuda()).cpu().numpy()
+    assert mpg.device_status() == mpg.OK
+    ref, _ = orc.gemm(a.astype(np.float16), np.ascontiguousarray(bt.T).astype(np.float16))
+    placed = np.full((128, n), np.nan)
+    for warp in range(4):
+        for lane in range(32):
+            for c in range(n // 32):
+                for reg in range(32):
+                    r, col = mpg.tmem_acc_coords(warp, lane, reg, 32 * c)
+                    assert np.isnan(placed[r, col])             # no point placed twice
+                    placed[r, col] = d[warp, lane, c, reg]
+    assert int(np.count_nonzero(placed != ref)) == 0
+    # wrong maps: lanes shifted by one, quarters swapped, columns reversed in a load
+    assert np.count_nonzero(np.roll(placed, 1, axis=0) != ref) > 0
+    assert np.count_nonzero(placed.reshape(4, 32, n)[[1, 0, 3, 2]].reshape(128, n) != ref) > 0
+    assert np.count_nonzero(placed.reshape(128, n // 32, 32)[:, :, ::-1].reshape(128, n) != ref) > 0

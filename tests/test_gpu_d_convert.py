@@ -213,3 +213,40 @@ def test_fp16_modes_on_fp32_take_the_pass_with_the_exact_workspace(mode, q):
     ref0 = ref - 0.5 * c.c0[0][rows, cols].astype(np.float64)   # the wrapper call used beta = 0
     den0 = den - 0.5 * np.abs(c.c0[0][rows, cols].astype(np.float64))
     assert oracle.max_rel_err(C.cpu().numpy()[rows, cols], ref0, den0) <= TOL["q16"]
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES[:5])
+@pytest.mark.parametrize("prepass", [-1, 1])
+def test_split3_plain_lo_parity(m, n, k, al, bl, pad, tile_n, prepass):
+    """The three-chain split with the plain lo = fp16(x - hi): its quantised
+    problem is the one-chain form's (hi, plain lo, three products)."""
+    mpg.build()
+    opts = mpg.options(split_plain_lo=1, prepass=prepass, tile_n=tile_n)
+    c = Case(m, n, k, mpg.SPLIT_FP16_3CHAIN, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=-1.0, opts=opts)
+    c.run()
+    C = c.result()
+    ref, den = c.reference(oracle.Q_SPLIT1)[0]
+    assert oracle.max_rel_err(C[0], ref, den) <= TOL["q16"]
+
+
+def test_chain_count_alone_on_identical_operands():
+    """Three chains against one on bit-identical operands (plain lo, one K
+    chunk, same operand scale): the only difference is whether the lo
+    products have accumulators of their own ("qsa_prompt_attn ...", "The
+    fix").  On log-uniform magnitudes the separate chains are closer to the
+    quantised problem and to the fp32-input problem."""
+    mpg.build()
+    m = n = 384
+    k = 4096
+    errs = {}
+    for name, mode, extra in (("3chain", mpg.SPLIT_FP16_3CHAIN, dict(split_plain_lo=1, split_chunk_k=-1)),
+                              ("1chain", mpg.SPLIT_FP16_1CHAIN, {})):
+        c = Case(m, n, k, mode, dist="loguniform", seed=5, opts=mpg.options(prepass=-1, **extra))
+        c.run()
+        C = c.result()[0]
+        refQ, denQ = c.reference(oracle.Q_SPLIT1)[0]
+        refR, denR = c.reference(oracle.Q_NONE)[0]
+        errs[name] = (oracle.max_rel_err(C, refQ, denQ), oracle.max_rel_err(C, refR, denR))
+    assert errs["3chain"][0] <= TOL["q16"], errs
+    assert errs["3chain"][0] < errs["1chain"][0], errs
+    assert errs["3chain"][1] < errs["1chain"][1], errs
