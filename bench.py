@@ -148,6 +148,8 @@ def mode_workspace(mpg, w):
     """Workspace of a per-mode row: the sizes-only query, or the exact one
     (which includes aligned copies of operands TMA cannot describe)."""
     code = mpg.MODE_NAMES[w.mode_name]
+    if w.host.get("no_ws"):
+        return 0
     if w.host.get("exact_ws"):
         return mpg.workspace_size_ex(w.m, w.n, w.k, w.batch, w.A.data_ptr(), w.lda, w.sa, w.dt_code, w.a_layout,
                                      w.B.data_ptr(), w.ldb, w.sb, w.dt_code, w.b_layout, code, w.opts)
@@ -253,7 +255,7 @@ def mode_cases(torch, mpg, synthetic, device):
     yield "square8192_tf32", lambda: f32_square(8192, "normal", "tf32", "col")
     # tf32 with a row-major B: transposed copy of B, then the direct path
     yield "square8192_tf32_rowB", lambda: f32_square(8192, "normal", "tf32", "row", exact_ws=True)
-    yield "square8192_fp16_onload", lambda: f32_square(8192, "normal", "fp16")
+    yield "square8192_fp16_onload", lambda: f32_square(8192, "normal", "fp16", opts=mpg.options(prepass=-1))
     yield "square8192_fp16_prepass", lambda: f32_square(8192, "normal", "fp16", opts=mpg.options(prepass=1))
     # C4: 4096^3 log-uniform: split3 vs split1 vs tf32 vs FFMA (B column-major
     # so that tf32 takes its direct path; every mode sees the same layout)
@@ -283,14 +285,21 @@ def mode_cases(torch, mpg, synthetic, device):
     # C2: batched 2048 x (64x4096 * 4096x64), padded leading dims
     for mn in ("tf32", "fp16"):
         yield f"batched2048_{mn}", lambda mn=mn: make_batched(torch, mpg, synthetic, device, mn)
-    # C3 tail: unpadded 8191 x 8177 x 8183 bf16, generic loads vs aligned copies
-    yield "tail8191_bf16_generic", lambda: make_tail(torch, mpg, synthetic, device, False)
-    yield "tail8191_bf16_copies", lambda: make_tail(torch, mpg, synthetic, device, True)
+    # C3 tail: unpadded 8191 x 8177 x 8183 bf16: generic loads (no workspace),
+    # and aligned copies in the workspace of the sizes-only query (the
+    # plain mpg_gemm + mpg_gemm_workspace_size calls) or of the exact query
+    yield "tail8191_bf16_generic", lambda: make_tail(torch, mpg, synthetic, device, "none")
+    yield "tail8191_bf16_sizes_query", lambda: make_tail(torch, mpg, synthetic, device, "sizes")
+    yield "tail8191_bf16_copies", lambda: make_tail(torch, mpg, synthetic, device, "exact")
     # C5: attention pair in split3 (conversion in the load stage, and by the separate pass)
     yield "attention_qkt_split3", lambda: make_attention(torch, mpg, synthetic, device, "qkt")
     yield "attention_pv_split3", lambda: make_attention(torch, mpg, synthetic, device, "pv")
     yield "attention_qkt_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "qkt", 1)
     yield "attention_pv_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "pv", 1)
+    # S with the two-accumulator split (hh; hl + lh), pass and on load
+    yield "attention_qkt_split3_shared_prepass", lambda: make_attention(torch, mpg, synthetic, device, "qkt", 1,
+                                                                        shared=1)
+    yield "attention_qkt_split3_shared", lambda: make_attention(torch, mpg, synthetic, device, "qkt", -1, shared=1)
 
 
 def make_batched(torch, mpg, synthetic, device, mode_name):
@@ -309,10 +318,10 @@ def make_batched(torch, mpg, synthetic, device, mode_name):
                     {"a": a, "bt": bt}, algo_bytes=algo)
 
 
-def make_tail(torch, mpg, synthetic, device, copies):
+def make_tail(torch, mpg, synthetic, device, ws):
     """8191 x 8177 x 8183 bf16 with unpadded leading dimensions (no TMA
-    descriptor exists): the generic-load path, or aligned copies in the
-    workspace the exact query asks for."""
+    descriptor exists): the generic-load path without a workspace, or aligned
+    copies in the workspace a query asks for ("sizes" / "exact")."""
     m, n, k = 8191, 8177, 8183
     a = synthetic.normal((m, k), synthetic.SEED_A)
     b = synthetic.normal((k, n), synthetic.SEED_B)
@@ -322,10 +331,11 @@ def make_tail(torch, mpg, synthetic, device, copies):
     B = bf16_tensor_from_codes(torch, b16, device)
     algo = 2 * m * k + 2 * k * n + 4 * m * n
     return Workload("tail8191", m, n, k, 1, "bf16", A, B, None, k, n, n, 0, 0, 0, mpg.ROW_MAJOR, mpg.ROW_MAJOR,
-                    mpg.BF16, 1.0, 0.0, {"a16": a16, "b16": b16, "exact_ws": copies}, algo_bytes=algo)
+                    mpg.BF16, 1.0, 0.0, {"a16": a16, "b16": b16, "exact_ws": ws == "exact", "no_ws": ws == "none"},
+                    algo_bytes=algo)
 
 
-def make_attention(torch, mpg, synthetic, device, which, prepass=-1):
+def make_attention(torch, mpg, synthetic, device, which, prepass=-1, shared=0):
     q, kk, p, v = synthetic.attention_inputs()
     if which == "qkt":
         # S = Q K^T: A = Q (2048x128 row-major), B = K^T, i.e. K stored row-major = B column-major
@@ -334,7 +344,8 @@ def make_attention(torch, mpg, synthetic, device, which, prepass=-1):
         algo = 4 * (2048 * 128 + 32768 * 128 + 2048 * 32768)
         return Workload("attention_qkt", 2048, 32768, 128, 1, "split3", A, B, None, 128, 128, 32768,
                         0, 0, 0, mpg.ROW_MAJOR, mpg.COL_MAJOR, mpg.F32, 1.0, 0.0,
-                        {"a": q, "b": kk.T}, opts=mpg.options(prepass=prepass), algo_bytes=algo)
+                        {"a": q, "b": kk.T}, opts=mpg.options(prepass=prepass, split_lo_shared=shared),
+                        algo_bytes=algo)
     A = torch.from_numpy(p).to(device)
     B = torch.from_numpy(v).to(device)
     algo = 4 * (2048 * 32768 + 32768 * 128 + 2048 * 128)
@@ -818,11 +829,12 @@ def build_targets(modes, result, peaks):
                             "err": g(f"batched2048_{m}", "max_rel_err_vs_fp64")} for m in ("tf32", "fp16")}
     t["attn_pair"] = {lbl: {"gbs_frac": g(f"attention_{lbl}", "frac_of_hbm_peak"),
                             "err": g(f"attention_{lbl}", "max_rel_err_vs_fp64")}
-                      for lbl in ("qkt_split3_prepass", "pv_split3")}
+                      for lbl in ("qkt_split3_prepass", "qkt_split3_shared_prepass", "qkt_split3_shared",
+                                  "pv_split3")}
     t["fused_attn"] = {"tf": g("attention_fused_2chain", "tflops"),
                        "issued_frac": g("attention_fused_2chain", "frac_of_tensor_peak"),
                        "err": g("attention_fused_2chain", "max_rel_err_vs_fp64")}
-    t["tail8191"] = {k: g(f"tail8191_bf16_{k}", "frac_of_tensor_peak") for k in ("generic", "copies")}
+    t["tail8191"] = {k: g(f"tail8191_bf16_{k}", "frac_of_tensor_peak") for k in ("generic", "sizes_query", "copies")}
     return t
 
 

@@ -208,7 +208,19 @@ typedef struct {
    *       the number of accumulator chains alone.
    * Other values: MPG_ERR_INVALID_ARG. */
   int32_t split_plain_lo;
-  int32_t reserved[2];
+  /* SPLIT_FP16_3CHAIN only: 1 = the hi*lo and lo*hi products share one
+   * accumulator, so the product keeps two (hh, and hl + lh), summed in fp32
+   * in the epilogue as acc = hh + 2^-L * (hl + lh).  The two lo products
+   * have the same magnitude (about 2^-11 of hh), so sharing their
+   * accumulator keeps them apart from hh as the separate chains do.  Two
+   * such accumulators fit in TMEM at once, so the epilogue of one tile
+   * overlaps the products of the next: the form for short K, e.g. attention
+   * scores (k = 128).  Taken when the whole K range is one accumulation
+   * chunk (k <= split_chunk_k, 512 by default, or split_chunk_k < 0); longer
+   * products keep the three chains.  0 (default) = three chains.  Other
+   * values: MPG_ERR_INVALID_ARG. */
+  int32_t split_lo_shared;
+  int32_t reserved[1];
 } mpg_options;
 
 void mpg_options_init(mpg_options* opt);
@@ -237,8 +249,10 @@ void mpg_options_init(mpg_options* opt);
  *                entry are ignored.  Calls that share a workspace must be
  *                ordered on one stream.
  * Pointers need only element alignment; 16-byte aligned pointers and leading
- * dimensions whose byte size is a multiple of 16 take the TMA load path, any
- * other alignment takes the generic-load path (same results, lower speed).
+ * dimensions whose byte size is a multiple of 16 take the TMA load path; for
+ * any other alignment the call copies the operands to aligned lines in the
+ * workspace when it has room (mpg_gemm_workspace_size reserves it for large
+ * products), else takes the generic-load path (same results, lower speed).
  * The memory C_b occupies must not overlap A or B. */
 mpg_status mpg_gemm(int64_t m, int64_t n, int64_t k, int64_t batch,
                     const void* A, int64_t lda, int64_t strideA, mpg_dtype a_dtype, mpg_layout a_layout,
@@ -300,7 +314,16 @@ mpg_status mpg_gemm_noalloc(int64_t m, int64_t n, int64_t k, int64_t batch,
                             const mpg_options* opt);
 
 /* Bytes of workspace mpg_gemm / mpg_gemm_ex need for this problem (0 if none).
- * Depends only on the sizes, the mode, the options and the current device.
+ * Depends only on the sizes, the mode, the options and the current device,
+ * so it covers every layout and alignment of the operands: for fp16 / bf16 /
+ * tf32 products with m >= 256, n >= 256 and m*n*k >= 2^32 it includes room
+ * for copies of both operands with 16-byte aligned lines (2 bytes per
+ * element, 4 for tf32, at the larger of the two line paddings), which the
+ * call uses for operands TMA cannot take as given (unaligned base, leading
+ * dimension or batch stride; tf32 in the wrong majorness), multiplying the
+ * copies on its TMA path, and, for fp32 operands in the fp16 / bf16 modes,
+ * for the conversion pass.  mpg_gemm_workspace_size_ex gives the exact need
+ * of one call (0 for aligned operands of those modes, the split tail aside).
  * For the fp16 / bf16 / tf32 modes it includes the split tail's partial sums
  * (mpg_options.tail_split) when the library may take it (1 to 6 full rounds
  * of 256 x 256 tiles on SMs / 2 clusters, k >= 8192, tf32 k >= 4096): up to

@@ -65,7 +65,8 @@ class Options(ctypes.Structure):
         ("cta_pair", ctypes.c_int32),
         ("tail_split", ctypes.c_int32),
         ("split_plain_lo", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("split_lo_shared", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 

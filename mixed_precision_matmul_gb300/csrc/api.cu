@@ -62,8 +62,12 @@ int mpg_version(void) { return 100; }
 const char* mpg_last_error_string(void) { return t_err.c_str(); }
 
 namespace {
-// Workspace of everything but the split tail, from the sizes alone.
-size_t regions_bytes(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, const mpg_options* opt) {
+// Workspace of everything but the split tail, from the sizes alone.  With
+// copy_room, large 16-bit and tf32 products also get room for aligned
+// copies of both operands (the sizes-only query cannot see whether the
+// operands need them).
+size_t regions_bytes(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode, const mpg_options* opt,
+                     bool copy_room) {
   mpg_options o;
   resolve_options(opt, &o);
   if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || mode == MPG_FP32_FFMA) return 0;
@@ -72,6 +76,23 @@ size_t regions_bytes(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precisi
   if (get_device(&dev) == MPG_OK) sm = dev->sm_count;
   t_err.clear();
   const size_t partials = splitk_bytes(choose_splits(m, n, k, batch, sm, o), m, n, batch);
+  if (copy_room && !o.force_generic_load && o.prepass >= 0 && (mode == MPG_FP16_F32ACC || mode == MPG_BF16_F32ACC ||
+                                                  mode == MPG_TF32) &&
+      auto_prepass_shape(m, n, k)) {
+    // Large 16-bit and tf32 products: room for copies of both operands with
+    // 16-byte aligned lines, in whichever majorness the direct path needs,
+    // so that operands TMA cannot describe as given (unaligned base,
+    // leading dimension or batch stride; tf32 in the wrong majorness) are
+    // copied and multiplied on the TMA path rather than loaded element by
+    // element.  The same room holds the conversion pass's 16-bit copies of
+    // fp32 operands in the fp16 / bf16 modes.  2 bytes per element (4 for
+    // tf32) at the worse of the two line paddings.
+    const size_t es = (mode == MPG_TF32) ? 4 : 2;
+    auto pad8 = [](int64_t x) { return (x + 7) / 8 * 8; };
+    const size_t a = align256((size_t)batch * (size_t)std::max(m * pad8(k), k * pad8(m)) * es);
+    const size_t b = align256((size_t)batch * (size_t)std::max(k * pad8(n), n * pad8(k)) * es);
+    return align256(partials) + a + b;
+  }
   if ((o.prepass == 1 && prepass_mode(mode)) ||
       (o.prepass == 0 && split_mode(mode) && auto_prepass_shape(m, n, k))) {
     // layouts are not known here: take the larger of the two line paddings
@@ -102,7 +123,7 @@ size_t tail_region(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision
 
 size_t mpg_gemm_workspace_size(int64_t m, int64_t n, int64_t k, int64_t batch, mpg_precision mode,
                                const mpg_options* opt) {
-  const size_t r = regions_bytes(m, n, k, batch, mode, opt);
+  const size_t r = regions_bytes(m, n, k, batch, mode, opt, true);
   const size_t t = tail_region(m, n, k, batch, mode, opt);
   return t ? align256(r) + t : r;
 }
@@ -113,7 +134,7 @@ size_t mpg_gemm_workspace_size_ex(int64_t m, int64_t n, int64_t k, int64_t batch
                                   mpg_precision mode, const mpg_options* opt) {
   mpg_options o;
   resolve_options(opt, &o);
-  const size_t base = regions_bytes(m, n, k, batch, mode, opt);
+  const size_t base = regions_bytes(m, n, k, batch, mode, opt, false);
   const size_t tail = tail_region(m, n, k, batch, mode, opt);
   auto with_tail = [&](size_t r) { return tail ? align256(r) + tail : r; };
   if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || o.force_generic_load) return with_tail(base);
@@ -248,11 +269,13 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       const int ea = sa_ ? o.split_exp_a : 0, eb = sa_ ? o.split_exp_b : 0;
       // the two-chain split splits A only; its B is rounded to fp16
       // the four-chain split uses the three-chain split's halves
-      const Conv conv_a = (plan.pre_conv == Conv::kSplitA2 || plan.pre_conv == Conv::kSplit4) ? Conv::kSplit3
-                                                                                              : plan.pre_conv;
-      const Conv conv_b = (plan.pre_conv == Conv::kSplitA2)  ? Conv::kRoundF16
-                          : (plan.pre_conv == Conv::kSplit4) ? Conv::kSplit3
-                                                             : plan.pre_conv;
+      // the two-accumulator split uses the three-chain split's halves too
+      const bool three_halves = plan.pre_conv == Conv::kSplitA2 || plan.pre_conv == Conv::kSplit4 ||
+                                plan.pre_conv == Conv::kSplit3M;
+      const Conv conv_a = three_halves ? Conv::kSplit3 : plan.pre_conv;
+      const Conv conv_b = (plan.pre_conv == Conv::kSplitA2) ? Conv::kRoundF16
+                          : three_halves                    ? Conv::kSplit3
+                                                            : plan.pre_conv;
       const int64_t sA = strideA ? strideA : L.a_outer * lda;
       const int64_t sB = strideB ? strideB : L.b_outer * ldb;
       const float lo_mul = std::ldexp(1.0f, split_lo_exp(plan.pre_conv, o));

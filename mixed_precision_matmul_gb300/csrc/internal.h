@@ -24,6 +24,7 @@ enum class Conv : int {
   kSplit1 = 4,    // fp32 -> hi, lo; one shared accumulator chain
   kSplitA2 = 5,   // A: fp32 -> hi, lo*2^11; B: fp32 -> fp16; two chains (A_hi B, A_lo B)
   kSplit4 = 6,    // fp32 -> hi, lo*2^11; four chains (hh, hl, lh, ll)
+  kSplit3M = 7,   // fp32 -> hi, lo*2^L; two accumulators, hh and hl + lh (one K chunk)
 };
 
 // Bits of the device status word.
@@ -43,6 +44,8 @@ struct TcParams {
   CUtensorMap map_b;
   CUtensorMap map_a_lo;  // direct split path: the lo halves of pre-split operands
   CUtensorMap map_b_lo;
+  CUtensorMap map_out;  // fp32 destination of TMA stores: C, or the split-K partials {n, m, splits*batch}
+  int32_t tma_store;    // 1: the epilogue stores its 32 x 32 blocks by TMA (fp32, beta == 0, aligned)
   const void* a;      // generic path addressing (element units of the source type)
   const void* b;
   int64_t lda, ldb, stride_a, stride_b;

@@ -168,15 +168,19 @@ bool prepass_mode(mpg_precision mode) {
 
 // Which operands carry hi and lo copies under a conversion.
 bool splits_a(Conv c) {
-  return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplitA2 || c == Conv::kSplit4;
+  return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplitA2 || c == Conv::kSplit4 ||
+         c == Conv::kSplit3M;
 }
-bool splits_b(Conv c) { return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplit4; }
+bool splits_b(Conv c) {
+  return c == Conv::kSplit3 || c == Conv::kSplit1 || c == Conv::kSplit4 || c == Conv::kSplit3M;
+}
 
 // Exponent L of the lo half's scale 2^L: 11 for the forms whose lo products
 // have chains of their own, unless the caller asks for the plain lo; 0 for
 // the one-chain form (and for conversions without a lo half).
 int split_lo_exp(Conv c, const mpg_options& o) {
-  if (c == Conv::kSplit3 || c == Conv::kSplitA2 || c == Conv::kSplit4) return o.split_plain_lo ? 0 : 11;
+  if (c == Conv::kSplit3 || c == Conv::kSplitA2 || c == Conv::kSplit4 || c == Conv::kSplit3M)
+    return o.split_plain_lo ? 0 : 11;
   return 0;
 }
 
@@ -223,7 +227,12 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       break;
     case MPG_SPLIT_FP16_3CHAIN:
       p.op = Op::kF16;
-      p.conv = Conv::kSplit3;
+      // hi*lo and lo*hi in one shared accumulator when asked for and the
+      // whole K range is one accumulation chunk
+      p.conv = (o.split_lo_shared && (o.split_chunk_k < 0 ||
+                                      k <= (o.split_chunk_k > 0 ? (int64_t)o.split_chunk_k : kDefaultSplitChunkK)))
+                   ? Conv::kSplit3M
+                   : Conv::kSplit3;
       p.st = SrcT::kF32;
       break;
     case MPG_SPLIT_FP16_1CHAIN:
@@ -304,7 +313,8 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
     bn = 64;   // four chains of 64 columns plus the running sum fill TMEM
   } else if (p.src == Src::kGeneric) {
     bn = pick_bn(m, n, batch, splits, sm_count, 128);
-  } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2 || p.conv == Conv::kSplit1) {
+  } else if (p.conv == Conv::kSplit3 || p.conv == Conv::kSplitA2 || p.conv == Conv::kSplit1 ||
+             p.conv == Conv::kSplit3M) {
     // 128-wide tiles read A once per 128 columns; for the three-chain and
     // A-only splits they hold one TMEM accumulator, 64-wide tiles two
     bn = pick_bn(m, n, batch, splits, sm_count, 128);
@@ -407,6 +417,8 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   if (o.prepass < -1 || o.prepass > 1) return fail(MPG_ERR_INVALID_ARG, "prepass must be -1, 0 or 1");
   if (o.split_plain_lo < 0 || o.split_plain_lo > 1)
     return fail(MPG_ERR_INVALID_ARG, "split_plain_lo must be 0 or 1");
+  if (o.split_lo_shared < 0 || o.split_lo_shared > 1)
+    return fail(MPG_ERR_INVALID_ARG, "split_lo_shared must be 0 or 1");
   if (m == 0 || n == 0 || batch == 0) return MPG_OK;
   if (!C) return fail(MPG_ERR_INVALID_ARG, "C is NULL");
   if (reinterpret_cast<uintptr_t>(C) % (o.c_dtype == MPG_F32 ? 4 : 2) != 0)
@@ -595,6 +607,27 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   p.b_vec_ok = vec_ok(B, b_stride);
   p.partial = splits_eff > 1 ? static_cast<float*>(workspace) : nullptr;
   p.p_vec_ok = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(workspace) % 16 == 0);
+  // TMA stores of the one-CTA epilogue: fp32 results without a C to read
+  // (beta == 0) on 16-byte aligned lines, or the split-K partial sums.
+  // Only when a row of the result is a whole number of 16-byte chunks
+  // (n % 4 == 0): measured on a GB300, a store box that ends inside a
+  // 16-byte chunk of a row wrote the rest of that chunk (C's padding).
+  p.tma_store = 0;
+  if (!plan.pair && n % 4 == 0) {
+    mpg_status ms = MPG_OK;
+    if (splits_eff > 1 && p.p_vec_ok) {
+      const Operand P{workspace, n, m * n, MPG_F32, MPG_ROW_MAJOR};
+      ms = encode_map(&p.map_out, P, n, m, (int64_t)splits_eff * batch, 32, 32);
+      p.tma_store = 1;
+    } else if (splits_eff == 1 && beta == 0.0f && o.c_dtype == MPG_F32 && p.c_vec_ok) {
+      const Operand Cop{C, ldc, p.stride_c, MPG_F32, MPG_ROW_MAJOR};
+      if (tma_ok(Cop, batch)) {
+        ms = encode_map(&p.map_out, Cop, n, m, batch, 32, 32);
+        p.tma_store = 1;
+      }
+    }
+    if (ms != MPG_OK) return ms;
+  }
   const bool split = splits_a(plan.conv);
   const int sa = split ? o.split_exp_a : 0, sb = split ? o.split_exp_b : 0;
   p.alpha = (float)std::ldexp((double)alpha, -(sa + sb));

@@ -16,6 +16,8 @@ bool tc_lookup_direct(Conv conv, Op op, int bn, TcKernel* out) {
   MPG_DIRECT_SPLIT(Conv::kSplitA2, 128)
   MPG_DIRECT_SPLIT(Conv::kSplitA2, 64)
   MPG_DIRECT_SPLIT(Conv::kSplit4, 64)
+  MPG_DIRECT_SPLIT(Conv::kSplit3M, 128)
+  MPG_DIRECT_SPLIT(Conv::kSplit3M, 64)
 #undef MPG_DIRECT_SPLIT
   if (conv != Conv::kNone) return false;
 #define MPG_DIRECT(OPV, STV, BNV)                                                  \

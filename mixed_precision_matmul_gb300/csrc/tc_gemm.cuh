@@ -50,9 +50,10 @@ struct TcTraits {
   static constexpr int kKSteps = kRowBytes / 32;   // MMAs of 32 bytes of K each
   static constexpr int kInstrK = 32 / kOpBytes;    // 16 (f16/bf16) or 8 (tf32)
   // operands that carry a hi and a lo copy in the stages
-  static constexpr bool kSplitA =
-      (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplitA2 || CV == Conv::kSplit4);
-  static constexpr bool kSplitB = (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplit4);
+  static constexpr bool kSplitA = (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplitA2 ||
+                                    CV == Conv::kSplit4 || CV == Conv::kSplit3M);
+  static constexpr bool kSplitB =
+      (CV == Conv::kSplit3 || CV == Conv::kSplit1 || CV == Conv::kSplit4 || CV == Conv::kSplit3M);
   static constexpr int kCopiesA = kSplitA ? 2 : 1;
   static constexpr int kCopiesB = kSplitB ? 2 : 1;
   static constexpr int kATile = BM * kRowBytes;
@@ -78,10 +79,13 @@ struct TcTraits {
   // chains, and the epilogue folds hh + 2^-11 (hl + lh) of every chunk into
   // an fp32 running sum (round to nearest) kept in kRunCols extra columns.
   static constexpr bool kPromote = (CV == Conv::kSplit3 || CV == Conv::kSplitA2 || CV == Conv::kSplit4);
-  static constexpr int kChainCols = (CV == Conv::kSplit4)   ? 4 * BN
-                                    : (CV == Conv::kSplit3)  ? 3 * BN
-                                    : (CV == Conv::kSplitA2) ? 2 * BN
-                                                             : BN;
+  // The two-accumulator split (hh; hl + lh) covers one K chunk and needs no
+  // running sum, so two of its accumulators fit in TMEM: the epilogue of one
+  // tile overlaps the MMAs of the next.
+  static constexpr int kChainCols = (CV == Conv::kSplit4)                            ? 4 * BN
+                                    : (CV == Conv::kSplit3)                           ? 3 * BN
+                                    : (CV == Conv::kSplitA2 || CV == Conv::kSplit3M) ? 2 * BN
+                                                                                      : BN;
   static constexpr int kRunCols = kPromote ? BN : 0;
   static constexpr int kAccStride = kPromote ? kChainCols
                                     : kChainCols <= 32 ? 32 : kChainCols <= 64 ? 64 : kChainCols <= 128 ? 128
@@ -97,6 +101,9 @@ struct TcTraits {
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kOpStage + kStgStage) + kEpiBytes +
                                     kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // each epilogue warp's staging buffer starts on a 1024-byte boundary (the
+  // 128-byte swizzle of its TMA stores repeats every 1024 bytes)
+  static_assert((kStages * (kOpStage + kStgStage)) % 1024 == 0, "staging alignment");
   static_assert(BN % BK == 0 && BM % BK == 0, "regions of MN-major tiles");
   static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : (O == Op::kBF16) ? 1u : 2u;
 };
@@ -436,9 +443,11 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       uint32_t it = 0, g = 0;   // k-block iteration; accumulation chunk
       bool ok = true;
       const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM, T::BN);
-      const uint32_t idesc_2n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BM,
-                                           (T::kConv == Conv::kSplit3 || T::kConv == Conv::kSplit4) ? 2 * T::BN
-                                                                                                    : T::BN);
+      const uint32_t idesc_2n =
+          make_idesc(T::kAbFormat, a_mn, b_mn, T::BM,
+                     (T::kConv == Conv::kSplit3 || T::kConv == Conv::kSplit4 || T::kConv == Conv::kSplit3M)
+                         ? 2 * T::BN
+                         : T::BN);
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(p, t);
         const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
@@ -470,6 +479,11 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
                 mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
                 // lh = A_lo * B_hi
                 mma_f16(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, acc);
+              } else if constexpr (T::kConv == Conv::kSplit3M) {
+                // [hh | hl] = A_hi * [B_hi | B_lo];  then lh adds into hl's columns
+                // (issued after the instruction that starts them, so always accumulating)
+                mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
+                mma_f16(d0 + T::BN, operand_desc<T>(a_lo, a_mn, ks), db_hi, idesc_n, 1u);
               } else if constexpr (T::kConv == Conv::kSplit4) {
                 // [hh | hl] = A_hi * [B_hi | B_lo];  [lh | ll] = A_lo * [B_hi | B_lo]
                 mma_f16(d0, da_hi, db_hi, idesc_2n, acc);
@@ -510,6 +524,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
     const uint32_t stg_addr = smem_addr(stg);
     uint32_t g = 0;   // accumulation chunk, in the MMA warp's order
     bool ok = true;
+    bool stores_pending = false;   // a TMA store may still be reading this warp's staging buffer
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const TileCoord tc = decode_tile(p, t);
       const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
@@ -590,6 +605,23 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
               // the next fold reads these columns back
               if (cc == cc0 + kCcPer - 1) tmem_st_wait();
             }
+          } else if constexpr (T::kConv == Conv::kSplit3M) {
+            // hh + 2^-L (hl + lh), the lo products' sum from their shared accumulator
+            const float lo_inv = p.lo_inv;
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float x0[16], x1[16];
+              const uint32_t col = cc * 32 + h * 16;
+              tmem_ld_16cols(tacc + col, x0);
+              tmem_ld_16cols(tacc + T::BN + col, x1);
+              tmem_ld_wait();
+              if (h == 1 && cc == cc0 + kCcPer - 1) {
+                tc_fence_before_sync();
+                mbar_arrive(&acc_empty[ab]);
+              }
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) v[h * 16 + j] = x0[j] + lo_inv * x1[j];
+            }
           } else {
             tmem_ld_32cols(tacc + cc * 32, v);
             tmem_ld_wait();
@@ -602,6 +634,27 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           if (!last) continue;   // chunk folded into the running sum; nothing to store yet
           const int col_base = tc.nb * T::BN + cc * 32;
           if (row_base >= p.m || col_base >= p.n) continue;
+          if (p.tma_store) {
+            // The staging image is the 128-byte swizzle of a 32 x 32 fp32 box:
+            // one TMA store writes the block (rows past m and columns past n
+            // are not written).  alpha * acc, as the register path stores it.
+            if (stores_pending) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= alpha;
+            stage_write_row(stg_addr, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int z = p.splits > 1 ? tc.s * p.batch + tc.b : tc.b;
+              tma_store_3d(&p.map_out, stg_addr, col_base, row_base, z);
+              bulk_commit();
+            }
+            stores_pending = true;
+            continue;
+          }
           // transpose through a per-warp swizzled 32x32 staging tile so that
           // global stores are row-contiguous
           stage_write_row(stg_addr, lane, v);
@@ -648,6 +701,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
         }
       }
     }
+    // this warp's TMA stores complete before the CTA may exit
+    if (stores_pending && lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ converters
     if constexpr (T::kHasConv) {

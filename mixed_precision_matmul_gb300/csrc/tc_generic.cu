@@ -27,6 +27,8 @@ bool tc_lookup_generic(Conv conv, Op op, SrcT st, int bn, TcKernel* out) {
   MPG_GENERIC(Conv::kSplit3, Op::kF16, SrcT::kF32, 64)
   MPG_GENERIC(Conv::kSplit1, Op::kF16, SrcT::kF32, 64)
   MPG_GENERIC(Conv::kSplitA2, Op::kF16, SrcT::kF32, 64)
+  MPG_GENERIC(Conv::kSplit3M, Op::kF16, SrcT::kF32, 128)
+  MPG_GENERIC(Conv::kSplit3M, Op::kF16, SrcT::kF32, 64)
 #undef MPG_GENERIC
   return false;
 }

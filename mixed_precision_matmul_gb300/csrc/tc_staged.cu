@@ -20,6 +20,8 @@ bool tc_lookup_staged(Conv conv, int bn, TcKernel* out) {
   MPG_STAGED(Conv::kSplit4, Op::kF16, 64)
   MPG_STAGED(Conv::kSplit1, Op::kF16, 128)
   MPG_STAGED(Conv::kSplit1, Op::kF16, 64)
+  MPG_STAGED(Conv::kSplit3M, Op::kF16, 128)
+  MPG_STAGED(Conv::kSplit3M, Op::kF16, 64)
 #undef MPG_STAGED
   return false;
 }

@@ -78,6 +78,7 @@ def test_option_ranges_rejected(L):
     assert _call(opts=mpg.options(tail_split=-2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(split_plain_lo=2)) == mpg.ERR_INVALID_ARG
     assert _call(opts=mpg.options(split_plain_lo=-1)) == mpg.ERR_INVALID_ARG
+    assert _call(opts=mpg.options(split_lo_shared=2)) == mpg.ERR_INVALID_ARG
 
 
 def test_probe_tmem_arguments_rejected_before_launch(L):
@@ -134,38 +135,74 @@ def _tail_bytes(tiles):
 SMS = 152   # the queries' SM count without a device
 
 
-def test_workspace_size_is_zero_for_large_problems(L):
-    # nothing but the split tail's partial sums, which tail_split = -1 drops
-    never = mpg.options(tail_split=-1)
-    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC, never) == 0
-    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.TF32) == 0
+def _pad8(x):
+    return (x + 7) // 8 * 8
+
+
+def _copy_room(m, n, k, es, batch=1):
+    # aligned copies of A and B at the larger of the two line paddings
+    return (_align256(batch * max(m * _pad8(k), k * _pad8(m)) * es) +
+            _align256(batch * max(k * _pad8(n), n * _pad8(k)) * es))
+
+
+def test_workspace_size_of_small_and_ffma_problems_is_zero(L):
     assert mpg.workspace_size(0, 8, 8, 1, mpg.TF32) == 0
     assert mpg.workspace_size(64, 64, 64, 1, mpg.FP32_FFMA) == 0
+    assert mpg.workspace_size(256, 256, 256, 1, mpg.BF16_F32ACC) == 0     # below 2^32 multiply-adds
+    assert mpg.workspace_size(128, 16384, 4096, 1, mpg.TF32) == 0         # m < 256 (and no split-K)
+
+
+def test_sizes_only_query_reserves_aligned_copies_for_large_products(L):
+    # the sizes-only query cannot see leading dimensions: large 16-bit and
+    # tf32 products get room for aligned copies of both operands, which the
+    # exact query leaves out for aligned operands
+    never = mpg.options(tail_split=-1)
+    n = 8192
+    assert mpg.workspace_size(n, n, n, 1, mpg.BF16_F32ACC, never) == _copy_room(n, n, n, 2)
+    assert mpg.workspace_size(n, n, n, 1, mpg.TF32) == _copy_room(n, n, n, 4)
+    m, n2, k = 8191, 8177, 8183
+    assert mpg.workspace_size(m, n2, k, 1, mpg.BF16_F32ACC, never) == _copy_room(m, n2, k, 2)
+    assert mpg.workspace_size(m, n2, k, 1, mpg.BF16_F32ACC, mpg.options(tail_split=-1, prepass=-1)) == 0
+    assert mpg.workspace_size(m, n2, k, 1, mpg.BF16_F32ACC, mpg.options(tail_split=-1,
+                                                                        force_generic_load=1)) == 0
+    aligned = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.BF16, mpg.ROW_MAJOR, 256, n, 0, mpg.BF16,
+                                    mpg.ROW_MAJOR, mpg.BF16_F32ACC, never)
+    assert aligned == 0
 
 
 def test_workspace_holds_the_split_tail(L):
     # fp16 / bf16 products with 1 to 6 full rounds of 256 x 256 tiles on
-    # SMs / 2 clusters and k >= 8192: up to SMs / 4 tiles cut in two
+    # SMs / 2 clusters and k >= 8192: up to SMs / 4 tiles cut in two, after
+    # the aligned-copy room of the sizes-only query
     q = _tail_bytes(SMS // 4)
-    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC) == q      # 100 tiles
-    assert mpg.workspace_size(4096, 4096, 8192, 1, mpg.FP16_F32ACC) == q      # 256 tiles
-    assert mpg.workspace_size(4096, 4096, 8191, 1, mpg.FP16_F32ACC) == q      # 128 k-blocks
-    assert mpg.workspace_size(4096, 4096, 8128, 1, mpg.FP16_F32ACC) == 0      # 127 k-blocks
-    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC) == 0      # 13 rounds
-    assert mpg.workspace_size(4096, 4096, 4096, 1, mpg.TF32) == q             # tf32: 128 k-blocks of 32
-    assert mpg.workspace_size(4096, 4096, 4064, 1, mpg.TF32) == 0
-    assert mpg.workspace_size(2048, 2048, 8192, 1, mpg.BF16_F32ACC) == 0      # 64 tiles: no full round
+
+    def ws(m, n, k, mode, **kw):
+        return mpg.workspace_size(m, n, k, 1, mode, mpg.options(**kw) if kw else None)
+
+    def room(m, n, k, mode):
+        return _copy_room(m, n, k, 4 if mode == mpg.TF32 else 2)
+
+    for m, n, k, mode, tail in ((2560, 2560, 8192, mpg.BF16_F32ACC, True),   # 100 tiles
+                                (4096, 4096, 8192, mpg.FP16_F32ACC, True),   # 256 tiles
+                                (4096, 4096, 8191, mpg.FP16_F32ACC, True),   # 128 k-blocks
+                                (4096, 4096, 8128, mpg.FP16_F32ACC, False),  # 127 k-blocks
+                                (8192, 8192, 8192, mpg.BF16_F32ACC, False),  # 13 rounds
+                                (4096, 4096, 4096, mpg.TF32, True),          # tf32: 128 k-blocks of 32
+                                (4096, 4096, 4064, mpg.TF32, False),
+                                (2048, 2048, 8192, mpg.BF16_F32ACC, False)): # 64 tiles: no full round
+        r = room(m, n, k, mode)
+        assert ws(m, n, k, mode) == (_align256(r) + q if tail else r), (m, n, k, mode)
+        assert ws(m, n, k, mode, tail_split=-1) == r
     # forced: up to SMs / 2 tiles, at any size
-    assert mpg.workspace_size(8192, 8192, 8192, 1, mpg.BF16_F32ACC,
-                              mpg.options(tail_split=1)) == _tail_bytes(SMS // 2)
-    assert mpg.workspace_size(512, 512, 256, 1, mpg.BF16_F32ACC, mpg.options(tail_split=1)) > 0
-    # never; single-CTA tiles only (cta_pair = -1); a mode that never takes pairs
-    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC, mpg.options(tail_split=-1)) == 0
-    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.BF16_F32ACC, mpg.options(cta_pair=-1)) == 0
-    assert mpg.workspace_size(2560, 2560, 8192, 1, mpg.SPLIT_FP16_1CHAIN, mpg.options(prepass=-1)) == 0
+    assert ws(8192, 8192, 8192, mpg.BF16_F32ACC, tail_split=1) == \
+        _align256(room(8192, 8192, 8192, mpg.BF16_F32ACC)) + _tail_bytes(SMS // 2)
+    assert ws(512, 512, 256, mpg.BF16_F32ACC, tail_split=1) > 0
+    # single-CTA tiles only (cta_pair = -1); a mode that never takes pairs
+    assert ws(2560, 2560, 8192, mpg.BF16_F32ACC, cta_pair=-1) == room(2560, 2560, 8192, mpg.BF16_F32ACC)
+    assert ws(2560, 2560, 8192, mpg.SPLIT_FP16_1CHAIN, prepass=-1) == 0
     # the tail follows the other regions: the conversion pass's copies first
-    with_pass = mpg.workspace_size(2560, 2560, 8192, 1, mpg.FP16_F32ACC, mpg.options(prepass=1))
-    pass_only = mpg.workspace_size(2560, 2560, 8192, 1, mpg.FP16_F32ACC, mpg.options(prepass=1, tail_split=-1))
+    with_pass = ws(2560, 2560, 8192, mpg.FP16_F32ACC, prepass=1)
+    pass_only = ws(2560, 2560, 8192, mpg.FP16_F32ACC, prepass=1, tail_split=-1)
     assert pass_only >= 2 * 2 * 2560 * 8192
     assert with_pass == _align256(pass_only) + q
 
@@ -392,8 +429,8 @@ def test_workspace_includes_the_conversion_pass_when_the_library_takes_it(L):
     assert ws >= 2 * 4 * n * n
     assert mpg.workspace_size(n, n, n, 1, mpg.SPLIT_FP16_3CHAIN, mpg.options(prepass=-1)) == 0
     assert mpg.workspace_size(256, 256, 256, 1, mpg.SPLIT_FP16_3CHAIN) == 0
-    never = mpg.options(tail_split=-1)
-    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, never) == 0   # fp16 mode: opt-in only
+    never = mpg.options(tail_split=-1, prepass=-1)
+    assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, never) == 0   # fp16 mode, pass refused
     assert mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, mpg.options(prepass=1)) >= 2 * 2 * n * n
     assert _call(opts=mpg.options(prepass=2)) == mpg.ERR_INVALID_ARG
 
@@ -404,7 +441,7 @@ def test_exact_query_includes_the_pass_for_fp16_modes_on_fp32_operands(L):
     plain = mpg.workspace_size(n, n, n, 1, mpg.FP16_F32ACC, nt)
     exact = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F32, mpg.ROW_MAJOR, 256, n, 0, mpg.F32,
                                   mpg.ROW_MAJOR, mpg.FP16_F32ACC, nt)
-    assert plain == 0 and exact >= 2 * 2 * n * n            # fp16 copies of A and B
+    assert exact >= 2 * 2 * n * n and plain >= exact        # fp16 copies of A and B
     exact16 = mpg.workspace_size_ex(n, n, n, 1, 256, n, 0, mpg.F16, mpg.ROW_MAJOR, 256, n, 0, mpg.F16,
                                     mpg.ROW_MAJOR, mpg.FP16_F32ACC, nt)
     assert exact16 == 0                                      # fp16 operands: nothing to convert

@@ -250,3 +250,43 @@ def test_chain_count_alone_on_identical_operands():
     assert errs["3chain"][0] <= TOL["q16"], errs
     assert errs["3chain"][0] < errs["1chain"][0], errs
     assert errs["3chain"][1] < errs["1chain"][1], errs
+
+
+@pytest.mark.parametrize("m,n,k,al,bl,pad,tile_n", SHAPES[:6])
+@pytest.mark.parametrize("prepass", [-1, 1])
+def test_split3_shared_lo_accumulator_parity(m, n, k, al, bl, pad, tile_n, prepass):
+    """Two accumulators (hh, and hl + lh together): the same quantised
+    problem as the three chains, within the same bars."""
+    mpg.build()
+    opts = mpg.options(split_lo_shared=1, prepass=prepass, tile_n=tile_n)
+    c = Case(m, n, k, mpg.SPLIT_FP16_3CHAIN, a_layout=al, b_layout=bl, pad=pad, alpha=1.0, beta=-1.0, opts=opts)
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
+
+
+def test_split3_shared_lo_many_tiles_both_buffers():
+    """1024 x 4096 x 128 on 128 x 128 tiles: 256 tiles over the persistent
+    CTAs, every CTA cycling through both accumulator buffers."""
+    mpg.build()
+    c = Case(1024, 4096, 128, mpg.SPLIT_FP16_3CHAIN, b_layout=Cm, dist="normal", seed=3,
+             opts=mpg.options(split_lo_shared=1, prepass=-1))
+    c.run()
+    C = c.result()
+    rows, cols = sample_points(1024, 4096, 3000, 33)
+    ref, den = c.reference_points(oracle.Q_NONE, 0, rows, cols)
+    assert oracle.max_rel_err(C[0][rows, cols], ref, den) <= TOL["split"]
+    refq, denq = c.reference_points(oracle.Q_SPLIT3, 0, rows, cols)
+    assert oracle.max_rel_err(C[0][rows, cols], refq, denq) <= TOL["q16"]
+
+
+def test_split3_shared_lo_falls_back_beyond_one_chunk():
+    """k above the accumulation chunk: the option leaves the three chains,
+    so the result is the default's bit for bit."""
+    mpg.build()
+    outs = []
+    for shared in (0, 1):
+        c = Case(200, 136, 1200, mpg.SPLIT_FP16_3CHAIN, seed=4, opts=mpg.options(split_lo_shared=shared))
+        c.run()
+        outs.append(c.result())
+    assert np.array_equal(outs[0], outs[1])

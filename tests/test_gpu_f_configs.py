@@ -83,25 +83,29 @@ def test_large_bf16_8192_beta(cta_pair, capsys):
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
 
 
-@pytest.mark.parametrize("exact_ws", [False, True])
-def test_large_bf16_tail_unpadded(exact_ws, capsys):
+@pytest.mark.parametrize("ws", ["none", "sizes", "exact"])
+def test_large_bf16_tail_unpadded(ws, capsys):
     """8191 x 8177 x 8183 with unpadded leading dimensions: row pitches of
     16366 / 16354 bytes are not multiples of 16, so no TMA descriptor exists:
     without a workspace the generic-load path runs; with the workspace the
-    exact query asks for, the operands are copied to aligned lines and
-    multiplied on the TMA path."""
+    sizes-only query or the exact query asks for, the operands are copied to
+    aligned lines and multiplied on the TMA path."""
+    import torch
     mpg.build()
     m, n, k = 8191, 8177, 8183
     c = Case(m, n, k, mpg.BF16_F32ACC, in_dtype="bf16", dist="normal", alpha=1.0, beta=0.5,
              c0=synthetic.normal((m, n), synthetic.SEED_C0))
     assert c.lda == k and c.ldb == n and c.ldc == n
-    c.run(exact_ws=exact_ws)
+    if ws == "none":
+        c.run(workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))
+    else:
+        c.run(exact_ws=(ws == "exact"))
     C = c.result()
     rows, cols = sample_points(m, n, 3000, 82)
     ref, den = c.reference_points(oracle.Q_NONE, 0, rows, cols)
     err = oracle.max_rel_err(C[0][rows, cols], ref, den)
     err_rows = row_errors(c, C, np.array([0, 8064, 8190]), oracle.Q_NONE)
-    show(capsys, f"bf16 tail (aligned copies {exact_ws}): sampled {err:.3e}, rows {err_rows:.3e}")
+    show(capsys, f"bf16 tail (workspace {ws}): sampled {err:.3e}, rows {err_rows:.3e}")
     assert err <= TOL["q16"] and err_rows <= TOL["q16"]
 
 
@@ -153,6 +157,14 @@ def test_attention_pair_split3(capsys):
               c0=np.zeros((2048, 32768), np.float32), opts=mpg.options(prepass=-1))
     cl.run()
     e_sl = row_errors(cl, cl.result(), rows, oracle.Q_NONE)
+    # the two-accumulator form (hh; hl + lh), on the pass's copies and on load
+    e_sh = []
+    for pre in (0, -1):
+        ch = Case(2048, 32768, 128, mpg.SPLIT_FP16_3CHAIN, a=q, b=np.ascontiguousarray(kk.T), b_layout=Cm,
+                  c0=np.zeros((2048, 32768), np.float32), opts=mpg.options(prepass=pre, split_lo_shared=1))
+        ch.run()
+        e_sh.append(row_errors(ch, ch.result(), rows, oracle.Q_NONE))
+        del ch
     # O = P V; P holds probabilities (<= 1): operand scale 2^14 lifts it out
     # of fp16's subnormal range
     co = Case(2048, 128, 32768, mpg.SPLIT_FP16_3CHAIN, a=p, b=v, c0=np.zeros((2048, 128), np.float32),
@@ -164,6 +176,7 @@ def test_attention_pair_split3(capsys):
     cu = Case(2048, 128, 32768, mpg.SPLIT_FP16_3CHAIN, a=p, b=v, c0=np.zeros((2048, 128), np.float32))
     cu.run()
     e_u = row_errors(cu, cu.result(), np.arange(0, 2048, 64), oracle.Q_NONE)
-    show(capsys, f"attention split3: S {e_s:.3e}, O {e_o:.3e} (O without operand scale {e_u:.3e})")
-    assert e_s <= TOL["split"] and e_sl <= TOL["split"]
+    show(capsys, f"attention split3: S {e_s:.3e} (two accumulators {e_sh[0]:.3e} / on load {e_sh[1]:.3e}), "
+                 f"O {e_o:.3e} (O without operand scale {e_u:.3e})")
+    assert e_s <= TOL["split"] and e_sl <= TOL["split"] and max(e_sh) <= TOL["split"]
     assert e_o <= TOL["split"]
