@@ -291,9 +291,10 @@ def mode_cases(torch, mpg, synthetic, device):
     yield "tail8191_bf16_generic", lambda: make_tail(torch, mpg, synthetic, device, "none")
     yield "tail8191_bf16_sizes_query", lambda: make_tail(torch, mpg, synthetic, device, "sizes")
     yield "tail8191_bf16_copies", lambda: make_tail(torch, mpg, synthetic, device, "exact")
-    # C5: attention pair in split3 (conversion in the load stage, and by the separate pass)
-    yield "attention_qkt_split3", lambda: make_attention(torch, mpg, synthetic, device, "qkt")
-    yield "attention_pv_split3", lambda: make_attention(torch, mpg, synthetic, device, "pv")
+    # C5: attention pair in split3: the library's choice (S: the conversion
+    # pass; P.V, skinny: on load), S on load, and P.V with the pass
+    yield "attention_qkt_split3_onload", lambda: make_attention(torch, mpg, synthetic, device, "qkt", -1)
+    yield "attention_pv_split3", lambda: make_attention(torch, mpg, synthetic, device, "pv", 0)
     yield "attention_qkt_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "qkt", 1)
     yield "attention_pv_split3_prepass", lambda: make_attention(torch, mpg, synthetic, device, "pv", 1)
     # S with the two-accumulator split (hh; hl + lh), pass and on load
@@ -335,7 +336,7 @@ def make_tail(torch, mpg, synthetic, device, ws):
                     algo_bytes=algo)
 
 
-def make_attention(torch, mpg, synthetic, device, which, prepass=-1, shared=0):
+def make_attention(torch, mpg, synthetic, device, which, prepass=0, shared=0):
     q, kk, p, v = synthetic.attention_inputs()
     if which == "qkt":
         # S = Q K^T: A = Q (2048x128 row-major), B = K^T, i.e. K stored row-major = B column-major
@@ -905,7 +906,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--mode", default=None,
-                    help="time only this row of the per-mode table (e.g. attention_qkt_split3)")
+                    help="time only this row of the per-mode table (e.g. attention_pv_split3)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -279,11 +279,15 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       const int64_t sA = strideA ? strideA : L.a_outer * lda;
       const int64_t sB = strideB ? strideB : L.b_outer * ldb;
       const float lo_mul = std::ldexp(1.0f, split_lo_exp(plan.pre_conv, o));
-      e = launch_prepass(conv_a, static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi, a_lo,
-                         L.a_ld, std::ldexp(1.0f, ea), lo_mul, dev->sm_count, st);
-      if (e == cudaSuccess)
-        e = launch_prepass(conv_b, static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi, b_lo,
-                           L.b_ld, std::ldexp(1.0f, eb), lo_mul, dev->sm_count, st);
+      auto kind = [](Conv c) {
+        return c == Conv::kRoundF16 ? kPassF16 : c == Conv::kRoundBF16 ? kPassBF16 : kPassSplit;
+      };
+      // both operands in one launch
+      const PassJob ja{static_cast<const float*>(A), lda, sA, L.a_outer, L.a_inner, batch, a_hi, a_lo, L.a_ld,
+                       std::ldexp(1.0f, ea), lo_mul, kind(conv_a), 0};
+      const PassJob jb{static_cast<const float*>(B), ldb, sB, L.b_outer, L.b_inner, batch, b_hi, b_lo, L.b_ld,
+                       std::ldexp(1.0f, eb), lo_mul, kind(conv_b), 0};
+      e = launch_prepass(ja, &jb, dev->sm_count, st);
       if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "conversion pass launch: %s", cudaGetErrorString(e));
       const mpg_dtype cdt = (plan.op == Op::kBF16) ? MPG_BF16 : MPG_F16;
       Operand Ah{a_hi, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};

@@ -164,12 +164,22 @@ cudaError_t launch_probe_mma(const void* a, const void* b, float* d, cudaStream_
 // Separate conversion pass: a stored fp32 matrix (per batch `outer` lines of
 // `inner` elements, leading dimension ld_in, batch stride stride_in) into
 // packed 16-bit copies with leading dimension ld_out (batch stride
-// outer * ld_out).  conv: kRoundF16, kRoundBF16, or a split (kSplit3 /
-// kSplit1: hi = fp16(x*scale), lo = fp16((x*scale - hi) * lo_mul)); `lo` is
-// written for the split only.  scale and lo_mul are powers of two.
-cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
-                           int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
-                           float lo_mul, int sm_count, cudaStream_t stream);
+// outer * ld_out).  kind: fp16 or bf16 rounding of x*scale, or the split
+// hi = fp16(x*scale), lo = fp16((x*scale - hi) * lo_mul) (lo written for
+// the split only).  scale and lo_mul are powers of two.  One launch converts
+// one or two operands.
+enum : int { kPassF16 = 0, kPassBF16 = 1, kPassSplit = 2 };
+struct PassJob {
+  const float* in;
+  int64_t ld_in, stride_in, outer, inner, batch;
+  uint16_t* hi;
+  uint16_t* lo;
+  int64_t ld_out;
+  float scale, lo_mul;
+  int kind;
+  int vec;   // set by the launcher
+};
+cudaError_t launch_prepass(const PassJob& a, const PassJob* b, int sm_count, cudaStream_t stream);
 cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d, cudaStream_t stream);
 cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, int scalar, int sm_count,
                                  cudaStream_t stream);

@@ -15,14 +15,14 @@ namespace {
 
 // Convert 8 consecutive fp32 values into 8 16-bit values (hi) and, for the
 // split, 8 lo values (scaled by lo_mul), packed as four 32-bit words each.
-template <Conv CV>
-__device__ __forceinline__ void convert8(const float (&x)[8], float scale, float lo_mul, uint4& hi, uint4& lo) {
+__device__ __forceinline__ void convert8(const float (&x)[8], int kind, float scale, float lo_mul, uint4& hi,
+                                         uint4& lo) {
   uint32_t w[4], l[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    if constexpr (CV == Conv::kRoundF16) {
+    if (kind == kPassF16) {
       w[j] = pack_f16x2(x[2 * j] * scale, x[2 * j + 1] * scale);   // scale: 1, or 2^s for a split's B
-    } else if constexpr (CV == Conv::kRoundBF16) {
+    } else if (kind == kPassBF16) {
       w[j] = pack_bf16x2(x[2 * j] * scale, x[2 * j + 1] * scale);
     } else {
       split_pair(x[2 * j], x[2 * j + 1], scale, lo_mul, w[j], l[j]);
@@ -32,51 +32,54 @@ __device__ __forceinline__ void convert8(const float (&x)[8], float scale, float
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// One work item = 8 consecutive elements of one line; each thread handles two
+struct PassJobs {
+  PassJob job[2];
+  int64_t items0, total;   // work items of job 0, of both
+};
+
+// One work item = 8 consecutive elements of one line of one operand; the
+// items of both operands form one index range.  Each thread handles two
 // items per loop trip, loading both before converting either.
-template <Conv CV>
-__global__ void __launch_bounds__(256) prepass_kernel(const float* __restrict__ in, int64_t ld_in,
-                                                      int64_t stride_in, int64_t outer, int64_t inner,
-                                                      int64_t batch, uint16_t* __restrict__ hi,
-                                                      uint16_t* __restrict__ lo, int64_t ld_out, float scale,
-                                                      float lo_mul, int vec) {
-  constexpr bool kSplit = (CV == Conv::kSplit3);
-  const int64_t items_per_line = (inner + 7) / 8;
-  const int64_t per_batch = outer * items_per_line;
-  const int64_t total = per_batch * batch;
+__global__ void __launch_bounds__(256) prepass_kernel(const __grid_constant__ PassJobs J) {
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total; i0 += 2 * step) {
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < J.total; i0 += 2 * step) {
     float x[2][8];
     int64_t o[2];
+    int jb[2];
     bool live[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int64_t i = i0 + u * step;
-      live[u] = i < total;
-      const int64_t ii = live[u] ? i : 0;
+      live[u] = i < J.total;
+      jb[u] = (live[u] && i >= J.items0) ? 1 : 0;
+      const PassJob& P = J.job[jb[u]];
+      const int64_t ii = live[u] ? (jb[u] ? i - J.items0 : i) : 0;
+      const int64_t items_per_line = (P.inner + 7) / 8;
+      const int64_t per_batch = P.outer * items_per_line;
       const int64_t b = ii / per_batch;
       const int64_t r = ii - b * per_batch;
       const int64_t line = r / items_per_line;
       const int64_t c = (r - line * items_per_line) * 8;
-      const float* src = in + b * stride_in + line * ld_in + c;
-      o[u] = b * outer * ld_out + line * ld_out + c;   // ld_out % 8 == 0: 16-byte aligned
-      if (vec && c + 7 < inner) {
+      const float* src = P.in + b * P.stride_in + line * P.ld_in + c;
+      o[u] = b * P.outer * P.ld_out + line * P.ld_out + c;   // ld_out % 8 == 0: 16-byte aligned
+      if (live[u] && P.vec && c + 7 < P.inner) {
         const float4 v0 = __ldg(reinterpret_cast<const float4*>(src));
         const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
         x[u][0] = v0.x; x[u][1] = v0.y; x[u][2] = v0.z; x[u][3] = v0.w;
         x[u][4] = v1.x; x[u][5] = v1.y; x[u][6] = v1.z; x[u][7] = v1.w;
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[u][e] = (live[u] && c + e < inner) ? __ldg(src + e) : 0.0f;
+        for (int e = 0; e < 8; ++e) x[u][e] = (live[u] && c + e < P.inner) ? __ldg(src + e) : 0.0f;
       }
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       if (!live[u]) continue;
+      const PassJob& P = J.job[jb[u]];
       uint4 h, l;
-      convert8<CV>(x[u], scale, lo_mul, h, l);
-      *reinterpret_cast<uint4*>(hi + o[u]) = h;
-      if constexpr (kSplit) *reinterpret_cast<uint4*>(lo + o[u]) = l;
+      convert8(x[u], P.kind, P.scale, P.lo_mul, h, l);
+      *reinterpret_cast<uint4*>(P.hi + o[u]) = h;
+      if (P.kind == kPassSplit) *reinterpret_cast<uint4*>(P.lo + o[u]) = l;
     }
   }
 }
@@ -175,32 +178,22 @@ cudaError_t launch_copy_pad(const void* in, int elem_bytes, int64_t ld_in, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_prepass(Conv conv, const float* in, int64_t ld_in, int64_t stride_in, int64_t outer,
-                           int64_t inner, int64_t batch, uint16_t* hi, uint16_t* lo, int64_t ld_out, float scale,
-                           float lo_mul, int sm_count, cudaStream_t stream) {
-  const int64_t total = batch * outer * ((inner + 7) / 8);
-  int64_t blocks = (total + 511) / 512;
+cudaError_t launch_prepass(const PassJob& a, const PassJob* b, int sm_count, cudaStream_t stream) {
+  PassJobs J;
+  J.job[0] = a;
+  J.job[1] = b ? *b : a;
+  for (int i = 0; i < (b ? 2 : 1); ++i) {
+    PassJob& P = J.job[i];
+    if (P.kind != kPassF16 && P.kind != kPassBF16 && P.kind != kPassSplit) return cudaErrorInvalidValue;
+    P.vec = reinterpret_cast<uintptr_t>(P.in) % 16 == 0 && P.ld_in % 4 == 0 && (P.batch == 1 || P.stride_in % 4 == 0);
+  }
+  auto items = [](const PassJob& P) { return P.batch * P.outer * ((P.inner + 7) / 8); };
+  J.items0 = items(J.job[0]);
+  J.total = J.items0 + (b ? items(J.job[1]) : 0);
+  int64_t blocks = (J.total + 511) / 512;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
   if (blocks < 1) blocks = 1;
-  const int vec = reinterpret_cast<uintptr_t>(in) % 16 == 0 && ld_in % 4 == 0 && (batch == 1 || stride_in % 4 == 0);
-  switch (conv) {
-    case Conv::kRoundF16:
-      prepass_kernel<Conv::kRoundF16><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi,
-                                                                        lo, ld_out, scale, 1.0f, vec);
-      break;
-    case Conv::kRoundBF16:
-      prepass_kernel<Conv::kRoundBF16><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch,
-                                                                         hi, lo, ld_out, scale, 1.0f, vec);
-      break;
-    case Conv::kSplit3:
-    case Conv::kSplit1:
-      // one split kernel: the forms differ only in the lo half's scale
-      prepass_kernel<Conv::kSplit3><<<(int)blocks, 256, 0, stream>>>(in, ld_in, stride_in, outer, inner, batch, hi, lo,
-                                                                      ld_out, scale, lo_mul, vec);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
+  prepass_kernel<<<(int)blocks, 256, 0, stream>>>(J);
   return cudaGetLastError();
 }
 
