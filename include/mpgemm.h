@@ -173,7 +173,10 @@ typedef struct {
    * and the 256 x 256 tiles give every pair of SMs at least one tile (many
    * small batched products keep the finer one-CTA tiles), 1 = always where
    * it applies,
-   * -1 = never (one CTA per 128-row tile).  Other configurations ignore it. */
+   * -1 = never (one CTA per 128-row tile).  The three-chain split on the
+   * conversion pass's copies takes pairs (256 x 128 tiles, the same bits as
+   * single CTAs) only with 1: on a GB300 it measured slower than single
+   * CTAs.  Other configurations ignore it. */
   int32_t cta_pair;
   /* Split tail for the CTA-pair kernel.  A persistent grid of P clusters
    * takes tiles in rounds of P; when the last round holds R < P tiles, the

@@ -133,9 +133,11 @@ struct AttnParams {
 cudaError_t launch_attention(const AttnParams& p, bool two_chain, cudaStream_t stream);
 int attention_smem_bytes();
 
-// The 16-bit direct product on a CTA pair (cta_group::2, 256 x 256 tiles per
-// cluster of two CTAs); false for operand types it does not cover.
-bool tc_lookup_pair(Op op, TcKernel* out);
+// The 16-bit and tf32 direct product on a CTA pair (cta_group::2, 256 x 256
+// tiles per cluster of two CTAs), and the three-chain split on the
+// conversion pass's fp16 copies (256 x 128 tiles); false for combinations it
+// does not cover.
+bool tc_lookup_pair(Op op, Conv conv, TcKernel* out);
 
 // Plain fp32 FFMA comparator.
 struct FfmaParams {

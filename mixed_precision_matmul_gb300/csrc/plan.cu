@@ -337,12 +337,20 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
   // would take 128 x 256 tiles too: narrower products, e.g. many small
   // batched ones, keep the finer tiles instead of multiplying padding), or
   // forced with cta_pair = 1.
-  const bool pair_ok = p.src == Src::kTmaDirect && p.conv == Conv::kNone && (o.tile_n == 0 || o.tile_n == 256);
-  const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + 255) / 256);
-  if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && o.tile_n == 0 && m > 128 && n > 128 &&
+  // The three-chain split on the conversion pass's copies also runs on
+  // pairs, with 256 x 128 tiles, when asked for (cta_pair = 1).  Measured on
+  // a GB300 at 4096^3 it is slower than single CTAs (360 against 412
+  // TFLOP/s with 512-k chunks, 428 against 444 with one chunk), so the
+  // library's own choice keeps single CTAs for the split.
+  const bool split_pair = p.prepass && p.conv == Conv::kSplit3;
+  const int pair_bn = split_pair ? 128 : 256;
+  const bool pair_ok = p.src == Src::kTmaDirect && (p.conv == Conv::kNone || split_pair) &&
+                       (o.tile_n == 0 || o.tile_n == pair_bn);
+  const int64_t pair_tiles = batch * ((m + 255) / 256) * ((n + pair_bn - 1) / pair_bn);
+  if (pair_ok && (o.cta_pair == 1 || (o.cta_pair == 0 && !split_pair && o.tile_n == 0 && m > 128 && n > 128 &&
                                       pair_tiles * 2 >= sm_count))) {
     p.pair = true;
-    p.bn = 256;
+    p.bn = pair_bn;
   }
 
   if (p.prepass) {
@@ -432,14 +440,17 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
   return MPG_OK;
 }
 
-// Clusters of two CTAs of the pair kernel that fit on the device at once,
-// asked once per device (both pair kernels have the same launch shape).
+// Clusters of two CTAs of a pair kernel that fit on the device at once,
+// asked once per device and launch shape (the plain pair kernels share one;
+// the split's has less shared memory).
 mpg_status pair_clusters(DeviceInfo* dev, const TcKernel& kern, int* out) {
   static std::mutex mu;
-  static int cached[kMaxDevices];
+  static int cached[kMaxDevices][2];
   const int devid = (int)(dev - g_devices);
+  const int shape = kern.bn == 128 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached[devid] <= 0) {
+  int& slot = cached[devid][shape];
+  if (slot <= 0) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(2);
@@ -459,9 +470,9 @@ mpg_status pair_clusters(DeviceInfo* dev, const TcKernel& kern, int* out) {
       return fail(MPG_ERR_UNSUPPORTED, "no resident cluster of two CTAs for the pair kernel: %s",
                   e != cudaSuccess ? cudaGetErrorString(e) : "occupancy 0");
     }
-    cached[devid] = n;
+    slot = n;
   }
-  *out = cached[devid];
+  *out = slot;
   return MPG_OK;
 }
 
@@ -470,7 +481,7 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
                      float beta, const mpg_options& o, void* workspace, cudaStream_t stream,
                      const Operand* A_lo, const Operand* B_lo) {
   TcKernel kern;
-  const bool found = plan.pair ? mpg::tc_lookup_pair(plan.op, &kern)
+  const bool found = plan.pair ? mpg::tc_lookup_pair(plan.op, plan.conv, &kern)
                                : mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern);
   if (!found) return fail(MPG_ERR_UNSUPPORTED, "no kernel for this configuration");
   if (kern.smem_bytes > dev->max_smem_optin)
@@ -567,7 +578,8 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
   }
   // split tail: the last round's R tiles become 2R halves of their k range
   int64_t tail_tiles = 0;
-  if (plan.pair && splits_eff == 1 && o.tail_split >= 0 && p.num_k_blk >= 2 && tiles > 0) {
+  if (plan.pair && plan.conv == Conv::kNone && splits_eff == 1 && o.tail_split >= 0 && p.num_k_blk >= 2 &&
+      tiles > 0) {
     const int64_t P = clusters;
     const int64_t full = tiles / P, rem = tiles % P;
     if (o.tail_split == 1) {

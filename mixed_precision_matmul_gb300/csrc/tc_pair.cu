@@ -32,13 +32,21 @@
 namespace mpg {
 namespace {
 
-template <Op O>
+template <Op O, Conv CV = Conv::kNone>
 struct PairTraits {
   static constexpr Op kOp = O;
+  // The three-chain split on the conversion pass's copies: the pair's tile
+  // is 256 x 128.  One N = 256 instruction makes hh and hl at once: its B
+  // operand [B_hi | B_lo] is split between the CTAs as the instruction
+  // splits N, so CTA 0 holds B_hi (all 128 columns) and CTA 1 holds B_lo.
+  // lh (N = 128) reads B_hi halved between the CTAs: each CTA also holds 64
+  // of B_hi's columns.  Per SM and stage: A_hi, A_lo (128 rows each), one
+  // whole B half and a quarter.
+  static constexpr bool kSplit = (CV == Conv::kSplit3);
   static constexpr int BM = 128;    // rows of A held by one CTA
   static constexpr int BMP = 256;   // rows of the pair's tile
-  static constexpr int BN = 256;    // columns of the pair's tile (the instruction's N)
-  static constexpr int BNH = 128;   // columns of B held by one CTA
+  static constexpr int BN = kSplit ? 128 : 256;    // columns of the pair's tile
+  static constexpr int BNH = 128;   // B rows of one CTA's (first) B tile
   static constexpr int kOpBytes = (O == Op::kTF32) ? 4 : 2;
   static constexpr int BK = 128 / kOpBytes;   // one 128-byte line of k per stage (64, tf32 32)
   static constexpr int kRowBytes = 128;
@@ -47,18 +55,23 @@ struct PairTraits {
   static constexpr int kKSteps = BK / kInstrK;
   static constexpr int kATile = BM * kRowBytes;
   static constexpr int kBTile = BNH * kRowBytes;
-  static constexpr int kOpStage = kATile + kBTile;   // 32 KB of this CTA's halves
-  static constexpr int kStages = 6;
+  static constexpr int kBHalfTile = (BN / 2) * kRowBytes;   // split: this CTA's half of B_hi for lh
+  // plain: A half, B half (32 KB); split: A_hi, A_lo, B_hi or B_lo, B_hi half (56 KB)
+  static constexpr int kOpStage = kSplit ? 2 * kATile + kBTile + kBHalfTile : kATile + kBTile;
+  static constexpr int kStages = kSplit ? 3 : 6;
   static constexpr int kEpiWarps = 8;
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
-  static constexpr int kAccStride = BN;
-  static constexpr int kAccBufs = 2;
+  // split: hh | hl (256 columns), lh (128), the running sum of the K chunks (128)
+  static constexpr int kAccStride = kSplit ? 3 * BN : BN;
+  static constexpr int kAccBufs = kSplit ? 1 : 2;
+  static constexpr int kRunBase = kSplit ? 3 * BN : 0;
   static constexpr int kTmemCols = 512;
   static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr int kSmemBytes = 1024 + kStages * kOpStage + kEpiBytes + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kAccBufs * kAccStride <= kTmemCols, "TMEM budget");
+  static_assert(kAccBufs * kAccStride + (kSplit ? BN : 0) <= kTmemCols, "TMEM budget");
+  static_assert(!kSplit || O == Op::kF16, "the split's halves are fp16");
   static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : (O == Op::kBF16) ? 1u : 2u;
 };
 
@@ -241,8 +254,27 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
               for (int g = 0; g < rows / T::BK; ++g) tma_load_3d_pair(d + g * kRegion, map, bar, row0 + g * T::BK, k0, tc.b);
             }
           };
-          load_half(&p.map_a, dst, p.a_mn_major != 0, tc.mb * T::BMP + (int)rank * T::BM, T::BM);
-          load_half(&p.map_b, dst + T::kATile, p.b_mn_major != 0, tc.nb * T::BN + (int)rank * T::BNH, T::BNH);
+          if constexpr (T::kSplit) {
+            // A_hi, A_lo (this CTA's rows); B_hi (rank 0) or B_lo (rank 1), all
+            // of the tile's columns, in the 64-row boxes of the maps; this
+            // CTA's half of B_hi's columns
+            const int arow = tc.mb * T::BMP + (int)rank * T::BM;
+            load_half(&p.map_a, dst, p.a_mn_major != 0, arow, T::BM);
+            load_half(&p.map_a_lo, dst + T::kATile, p.a_mn_major != 0, arow, T::BM);
+            const CUtensorMap* bx = rank == 0 ? &p.map_b : &p.map_b_lo;
+            uint8_t* bdst = dst + 2 * T::kATile;
+            if (p.b_mn_major) {
+              load_half(bx, bdst, true, tc.nb * T::BN, T::BN);
+            } else {
+              for (int h = 0; h < 2; ++h)
+                load_half(bx, bdst + h * T::kBHalfTile, false, tc.nb * T::BN + h * (T::BN / 2), T::BN / 2);
+            }
+            load_half(&p.map_b, bdst + T::kBTile, p.b_mn_major != 0, tc.nb * T::BN + (int)rank * (T::BN / 2),
+                      T::BN / 2);
+          } else {
+            load_half(&p.map_a, dst, p.a_mn_major != 0, tc.mb * T::BMP + (int)rank * T::BM, T::BM);
+            load_half(&p.map_b, dst + T::kATile, p.b_mn_major != 0, tc.nb * T::BN + (int)rank * T::BNH, T::BNH);
+          }
         }
       }
       // A stage is released (op_empty) only after both halves landed and the
@@ -254,7 +286,52 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
-    if (lane == 0 && rank == 0) {
+    if constexpr (T::kSplit) {
+      if (lane == 0 && rank == 0) {
+        // The split: per k-step [hh | hl] += A_hi [B_hi | B_lo] (N = 256) and
+        // lh += A_lo B_hi (N = 128), in K chunks of chunk_kb k-blocks, each
+        // chunk on fresh chains that the epilogue folds into its running sum.
+        const bool a_mn = p.a_mn_major != 0;
+        const bool b_mn = p.b_mn_major != 0;
+        const uint32_t idesc_2n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BMP, 2 * T::BN);
+        const uint32_t idesc_n = make_idesc(T::kAbFormat, a_mn, b_mn, T::BMP, T::BN);
+        uint32_t it = 0, g = 0;
+        bool ok = true;
+        for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl) {
+          const TileCoord tc = decode_item(p, t);
+          const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
+          for (int c0 = tc.kb0; c0 < tc.kb1 && ok; c0 += ck, ++g) {
+            const int c1 = min(tc.kb1, c0 + ck);
+            if (!mbar_wait(&acc_empty[0], (g & 1u) ^ 1u, ctl)) { ok = false; break; }
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            tc_fence_after_sync();
+            const uint32_t d0 = tmem_base;
+            for (int kb = c0; kb < c1; ++kb, ++it) {
+              const uint32_t st = it % T::kStages;
+              const uint32_t ph = (it / T::kStages) & 1u;
+              if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
+              tc_fence_after_sync();
+              const uint32_t a_hi = op_smem + st * T::kOpStage;
+              const uint32_t a_lo = a_hi + T::kATile;
+              const uint32_t bx = a_hi + 2 * T::kATile;
+              const uint32_t bh = bx + T::kBTile;
+#pragma unroll
+              for (int ks = 0; ks < T::kKSteps; ++ks) {
+                const uint32_t acc = (kb > c0 || ks > 0) ? 1u : 0u;
+                mma_pair<T::kOp>(d0, operand_desc<T>(a_hi, a_mn, ks), operand_desc<T>(bx, b_mn, ks), idesc_2n, acc);
+                mma_pair<T::kOp>(d0 + 2 * T::BN, operand_desc<T>(a_lo, a_mn, ks), operand_desc<T>(bh, b_mn, ks),
+                                 idesc_n, acc);
+              }
+              mma_commit_multicast(&op_empty[st], 0x3);
+            }
+            if (!ok) break;
+            mma_commit_multicast(&acc_full[0], 0x3);
+          }
+        }
+        mma_commit_multicast(done_bar, 0x1);
+        drain_wait(done_bar, 0, p.wait_limit_ns);
+      }
+    } else if (lane == 0 && rank == 0) {
       const bool a_mn = p.a_mn_major != 0;
       const bool b_mn = p.b_mn_major != 0;
       const uint32_t idesc = make_idesc(T::kAbFormat, a_mn, b_mn, T::BMP, T::BN);
@@ -287,6 +364,131 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
       // every MMA of the pair completes before either CTA releases TMEM
       mma_commit_multicast(done_bar, 0x1);
       drain_wait(done_bar, 0, p.wait_limit_ns);
+    }
+  } else if constexpr (T::kSplit) {
+    // ------------------------------------------------------------ epilogue of the split
+    // Each K chunk: hh + 2^-L (hl + lh) added to the running sum (TMEM
+    // columns of its own, round to nearest in fp32); after the last chunk,
+    // alpha * sum + beta * C in C's type.
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    float* stg = epi_base + (warp - 2) * 1024;
+    const uint32_t stg_addr = smem_addr(stg);
+    constexpr int kColGroups = T::kEpiWarps / 4;
+    constexpr int kCcPer = T::BN / 32 / kColGroups;
+    const int cc0 = ((warp - 2) / 4) * kCcPer;
+    const uint32_t acc_empty0 = cluster_smem_addr(smem_addr(acc_empty), 0);
+    const uint32_t tacc = tmem_base + lane_off;
+    const uint32_t trun = tmem_base + lane_off + T::kRunBase;
+    const float lo_inv = p.lo_inv;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int t = (int)cid; t < p.num_tiles && ok; t += (int)ncl) {
+      const TileCoord tc = decode_item(p, t);
+      const int ck = p.chunk_kb > 0 ? p.chunk_kb : (tc.kb1 - tc.kb0);
+      const int nchunks = (tc.kb1 - tc.kb0 + ck - 1) / ck;
+      void* out;
+      int64_t ldo;
+      float alpha, beta;
+      bool vec_ok;
+      int out_dt;
+      if (p.splits > 1) {
+        out = p.partial + ((int64_t)tc.s * p.batch + tc.b) * (int64_t)p.m * p.n;
+        ldo = p.n;
+        alpha = 1.0f;
+        beta = 0.0f;
+        vec_ok = p.p_vec_ok != 0;
+        out_dt = kOutF32;
+      } else {
+        out = static_cast<uint8_t*>(p.c) + (int64_t)tc.b * p.stride_c * (p.c_dtype == kOutF32 ? 4 : 2);
+        ldo = p.ldc;
+        alpha = p.alpha;
+        beta = p.beta;
+        vec_ok = p.c_vec_ok != 0;
+        out_dt = p.c_dtype;
+      }
+      const int row_base = tc.mb * T::BMP + (int)rank * T::BM + 32 * q;
+#pragma unroll 1
+      for (int ci = 0; ci < nchunks; ++ci, ++g) {
+        if (!warp_wait(&acc_full[0], g & 1u, ctl)) { ok = false; break; }
+        tc_fence_after_sync();
+        const bool last = (ci == nchunks - 1);
+#pragma unroll 1
+        for (int cc = cc0; cc < cc0 + kCcPer; ++cc) {
+          float v[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x0[16], x1[16], x2[16], r[16];
+            const uint32_t col = cc * 32 + h * 16;
+            tmem_ld_16cols(tacc + col, x0);
+            tmem_ld_16cols(tacc + T::BN + col, x1);
+            tmem_ld_16cols(tacc + 2 * T::BN + col, x2);
+            if (ci > 0) tmem_ld_16cols(trun + col, r);
+            tmem_ld_wait();
+            if (h == 1 && cc == cc0 + kCcPer - 1) {
+              // this warp's share of the chains is in registers: hand the
+              // accumulator back to rank 0 (the running sum has columns of its own)
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acc_empty0);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float x = x0[j] + lo_inv * (x1[j] + x2[j]);
+              v[h * 16 + j] = ci > 0 ? r[j] + x : x;
+            }
+          }
+          if (!last) {
+            tmem_st_16cols(trun + cc * 32, v);
+            tmem_st_16cols(trun + cc * 32 + 16, v + 16);
+            if (cc == cc0 + kCcPer - 1) tmem_st_wait();
+            continue;
+          }
+          const int col_base = tc.nb * T::BN + cc * 32;
+          if (row_base >= p.m || col_base >= p.n) continue;
+          stage_write_row(stg_addr, lane, v);
+          __syncwarp();
+          if (vec_ok && col_base + 32 <= p.n) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = i * 4 + (lane >> 3);
+              const int ch = lane & 7;
+              const float4 x = stage_read_chunk(stg_addr, lane, i);
+              const int grow = row_base + r;
+              if (grow < p.m) {
+                const int64_t idx = (int64_t)grow * ldo + col_base + ch * 4;
+                float4 o;
+                if (beta != 0.0f) {
+                  const float4 c0 = out_load4(out, idx, out_dt);
+                  o.x = fmaf(beta, c0.x, alpha * x.x);
+                  o.y = fmaf(beta, c0.y, alpha * x.y);
+                  o.z = fmaf(beta, c0.z, alpha * x.z);
+                  o.w = fmaf(beta, c0.w, alpha * x.w);
+                } else {
+                  o.x = alpha * x.x;
+                  o.y = alpha * x.y;
+                  o.z = alpha * x.z;
+                  o.w = alpha * x.w;
+                }
+                out_store4(out, idx, o, out_dt);
+              }
+            }
+          } else {
+            const int gcol = col_base + lane;
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+              const float x = stage_read_elem(stg_addr, lane, r);
+              const int grow = row_base + r;
+              if (grow < p.m && gcol < p.n) {
+                const int64_t idx = (int64_t)grow * ldo + gcol;
+                out_store(out, idx, (beta != 0.0f) ? fmaf(beta, out_load(out, idx, out_dt), alpha * x) : alpha * x,
+                          out_dt);
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -462,7 +664,13 @@ void pair_fill(TcKernel* out) {
 
 }  // namespace
 
-bool tc_lookup_pair(Op op, TcKernel* out) {
+bool tc_lookup_pair(Op op, Conv conv, TcKernel* out) {
+  if (conv == Conv::kSplit3) {
+    if (op != Op::kF16) return false;
+    pair_fill<PairTraits<Op::kF16, Conv::kSplit3>>(out);
+    return true;
+  }
+  if (conv != Conv::kNone) return false;
   switch (op) {
     case Op::kF16: pair_fill<PairTraits<Op::kF16>>(out); return true;
     case Op::kBF16: pair_fill<PairTraits<Op::kBF16>>(out); return true;

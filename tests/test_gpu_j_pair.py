@@ -235,3 +235,44 @@ def test_pair_beta_zero_does_not_read_c(mode, dt, tail):
         assert eR <= TOL["tf32"], eR
     else:
         assert eQ <= TOL["q16"], eQ
+
+
+# ---------------------------------------------------------------- the split on pairs
+@pytest.mark.parametrize("al,bl", [(R, R), (R, Cm), (Cm, R), (Cm, Cm)])
+@pytest.mark.parametrize("m,n,k,batch,kw", [
+    (512, 384, 1024, 1, {}),
+    (300, 200, 700, 1, {}),                        # tails in both CTAs' rows and in the columns
+    (260, 130, 1536, 2, dict(split_chunk_k=256)),  # batches, more K chunks
+    (512, 256, 640, 1, dict(split_chunk_k=-1)),    # one chunk
+    (384, 256, 512, 1, dict(split_plain_lo=1)),
+])
+def test_split3_pair_equals_single_cta(al, bl, m, n, k, batch, kw):
+    """The three-chain split on the conversion pass's copies, on CTA pairs
+    (256 x 128 tiles) and on single CTAs: the same products accumulated in
+    the same K order and the same chunk folds, so the same bits; and within
+    the split's bars against the oracle."""
+    mpg.build()
+    outs = []
+    for cp in (1, -1):
+        c = Case(m, n, k, mpg.SPLIT_FP16_3CHAIN, batch=batch, a_layout=al, b_layout=bl, pad=(4, 8, 4),
+                 alpha=1.0, beta=-0.5, dist="loguniform", seed=21, opts=mpg.options(prepass=1, cta_pair=cp, **kw))
+        c.run()
+        outs.append(c.result())
+    assert np.array_equal(outs[0], outs[1])
+    c.opts = mpg.options(prepass=1, cta_pair=1, **kw)
+    q = oracle.Q_SPLIT1 if kw.get("split_plain_lo") else oracle.Q_SPLIT3
+    for bi in range(batch):
+        ref, den = c.reference(q, [bi])[0]
+        assert oracle.max_rel_err(outs[0][bi], ref, den) <= TOL["q16"]
+        refr, denr = c.reference(oracle.Q_NONE, [bi])[0]
+        assert oracle.max_rel_err(outs[0][bi], refr, denr) <= TOL["split"]
+
+
+def test_split3_pair_split_k_and_scales():
+    """Split-K partial sums from the pair kernel, with operand exponents."""
+    mpg.build()
+    c = Case(256, 256, 8192, mpg.SPLIT_FP16_3CHAIN, alpha=2.0, dist="normal", seed=22,
+             opts=mpg.options(prepass=1, cta_pair=1, splitk=3, split_exp_a=3, split_exp_b=-2))
+    c.run()
+    eR, eQ = c.errors()
+    assert eQ <= TOL["q16"] and eR <= TOL["split"], (eR, eQ)
