@@ -130,6 +130,9 @@ __device__ __forceinline__ TileCoord decode_tile(const TcParams& p, int t) {
   const int within = r - g * group_size;
   c.mb = first_m + within % gm;
   c.nb = within / gm;
+  // serpentine: odd groups walk the columns backwards, starting on the B
+  // panels the previous group read last (still in L2)
+  if (g & 1) c.nb = p.num_n_blk - 1 - c.nb;
   c.kb0 = c.s * p.kb_per_split;
   c.kb1 = min(p.num_k_blk, c.kb0 + p.kb_per_split);
   c.tail = -1;
