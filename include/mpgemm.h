@@ -542,6 +542,22 @@ mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t block
  * launch; a wait that expires shows in mpg_device_status. */
 mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, void* stream);
 
+/* The same check for the CTA-pair path (cta_group::2, M = 256): a cluster of
+ * two CTAs runs one k-block (K = 64) with the pair kernels' operand layout;
+ * the CTA of rank r holds rows 128r .. 128r+127 of A and columns
+ * (n/2) r .. (n/2) r + n/2 - 1 of B, and each CTA's TMEM receives its 128
+ * rows of D and every column.
+ *   A: device, 256 x 64 fp16, row-major, ld 64.
+ *   B: device, n x 64 fp16 (row j = column j of B), n = 64, 128 or 256.
+ *   D: device, 256 * n floats:
+ *      D[(((4 r + warp)*32 + lane) * (n/32) + c) * 32 + reg] is register `reg`
+ *      of lane `lane` of warp `warp` of the CTA of rank r in the load of
+ *      columns 32c .. 32c+31; placed with mpg_tmem_acc_coords(256, r, warp,
+ *      lane, reg, 32c, ...).
+ * Waits are bounded (1 s); MPG_ERR_INVALID_ARG for bad arguments, before any
+ * launch. */
+mpg_status mpg_probe_tmem_acc_pair(const void* A, const void* B, int n, float* D, void* stream);
+
 /* Failure-detection self test: launches one kernel whose single wait is on an
  * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then
  * synchronises.  Returns MPG_ERR_TIMEOUT when the kernel gave up the wait and

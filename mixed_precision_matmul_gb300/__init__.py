@@ -143,6 +143,8 @@ def lib():
         L.mpg_tmem_acc_decode.restype = i32
         L.mpg_probe_tmem_acc.argtypes = [vp, vp, i32, vp, vp]
         L.mpg_probe_tmem_acc.restype = i32
+        L.mpg_probe_tmem_acc_pair.argtypes = [vp, vp, i32, vp, vp]
+        L.mpg_probe_tmem_acc_pair.restype = i32
         L.mpg_probe_mma_m16n8k16.argtypes = [vp, vp, vp, vp]
         L.mpg_probe_mma_m16n8k16.restype = i32
         for nm in ("mpg_frag_a_coords", "mpg_frag_a_decode", "mpg_frag_b_coords", "mpg_frag_b_decode"):
@@ -543,6 +545,22 @@ def probe_tmem_acc(A16, Bt16, stream=None):
         raise ValueError("A must be 128 x 64 and Bt n x 64")
     d = torch.empty((4, 32, n // 32, 32), dtype=torch.float32, device=a.device)
     _check(lib().mpg_probe_tmem_acc(a.data_ptr(), bt.data_ptr(), n, d.data_ptr(), _stream_handle(stream)))
+    return d
+
+
+def probe_tmem_acc_pair(A16, Bt16, stream=None):
+    """One k-block (K = 64) of the CTA-pair tcgen05 path (M = 256) on fp16 A
+    (256 x 64) and Bt (n x 64, row j = column j of B); returns the raw
+    tcgen05.ld registers as a (2 CTAs, 4 warps, 32 lanes, n/32 loads, 32 regs)
+    tensor."""
+    torch = _torch()
+    a = A16.to(torch.float16).contiguous()
+    bt = Bt16.to(torch.float16).contiguous()
+    n = bt.shape[0]
+    if a.shape != (256, 64) or bt.shape[1] != 64:
+        raise ValueError("A must be 256 x 64 and Bt n x 64")
+    d = torch.empty((2, 4, 32, n // 32, 32), dtype=torch.float32, device=a.device)
+    _check(lib().mpg_probe_tmem_acc_pair(a.data_ptr(), bt.data_ptr(), n, d.data_ptr(), _stream_handle(stream)))
     return d
 
 

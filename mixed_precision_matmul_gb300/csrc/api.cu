@@ -382,6 +382,22 @@ mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, voi
   return MPG_OK;
 }
 
+mpg_status mpg_probe_tmem_acc_pair(const void* A, const void* B, int n, float* D, void* stream) {
+  t_err.clear();
+  if (!A || !B || !D) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  if (n != 64 && n != 128 && n != 256) return fail(MPG_ERR_INVALID_ARG, "n must be 64, 128 or 256");
+  if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0)
+    return fail(MPG_ERR_INVALID_ARG, "A and B must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(D) % 4 != 0) return fail(MPG_ERR_INVALID_ARG, "D not aligned to 4 bytes");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e =
+      launch_probe_tmem_pair(A, B, n, D, dev->status, 1000000000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
 mpg_status mpg_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
   t_err.clear();
   if (timeout_ns < 1000000 || timeout_ns > 10000000000ll)

@@ -190,6 +190,11 @@ cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream
 // out unscattered, register by register (n = 64, 128 or 256).
 cudaError_t launch_probe_tmem(const void* a, const void* b, int n, float* d, uint32_t* status, uint64_t limit_ns,
                               cudaStream_t stream);
+// The same on a cluster of two CTAs (cta_group::2, M = 256): A 256 x 64,
+// the CTA of rank r holding rows 128r .. 128r+127; B n x 64 split between
+// the CTAs by columns.
+cudaError_t launch_probe_tmem_pair(const void* a, const void* b, int n, float* d, uint32_t* status,
+                                   uint64_t limit_ns, cudaStream_t stream);
 
 // Device status word of the current device (allocated by the runtime as a
 // module global; one per device).

@@ -27,6 +27,8 @@
 // Every wait is bounded.  A timeout raises the abort flag of both CTAs, so
 // the pair stops together; every role then drains what it has in flight and
 // the pair meets at a final cluster barrier before TMEM is released.
+#include <cstring>
+
 #include "tc_gemm.cuh"
 
 namespace mpg {
@@ -662,7 +664,122 @@ void pair_fill(TcKernel* out) {
   out->bn = T::BN;
 }
 
+// Hardware check of the M = 256 (cta_group::2) accumulator map: a cluster of
+// two CTAs runs one k-block (K = 64, four K = 16 instructions of kind::f16)
+// with the pair kernels' operand layout and descriptors -- CTA r holds rows
+// 128r .. 128r+127 of A and columns (n/2) r .. (n/2) r + n/2 - 1 of B -- and
+// every warp of both CTAs copies out its raw tcgen05.ld.32x32b.x32
+// registers, unscattered.
+constexpr int kPairProbeK = 64;
+constexpr int kPairProbeSmem = 1024 + 128 * 128 + 128 * 128 + 64;
+
+__global__ void __launch_bounds__(128, 1) probe_tmem_pair_kernel(const uint16_t* __restrict__ A,
+                                                                  const uint16_t* __restrict__ B, int n,
+                                                                  float* __restrict__ D, uint32_t* status,
+                                                                  uint64_t limit_ns) {
+  using T = PairTraits<Op::kF16>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_tile = smem;                 // 128 lines of 128 bytes (this CTA's rows of A)
+  uint8_t* b_tile = smem + 128 * 128;     // n / 2 lines of 128 bytes (this CTA's columns of B)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_tile + 128 * 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int nh = n / 2;
+
+  const uint32_t a_addr = smem_addr(a_tile), b_addr = smem_addr(b_tile);
+  for (int i = threadIdx.x; i < (128 + nh) * 8; i += blockDim.x) {
+    const bool isA = i < 128 * 8;
+    const int w = isA ? i : i - 128 * 8;
+    const int line = w >> 3, ch = w & 7;
+    const uint16_t* src = isA ? A + (size_t)(128 * rank + line) * kPairProbeK : B + (size_t)(nh * rank + line) * kPairProbeK;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + ch * 8);
+    st_shared_v4((isA ? a_addr : b_addr) + swz_chunk_offset<128>(line, ch), v.x, v.y, v.z, v.w);
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  const uint32_t ncols = n <= 64 ? 64 : n <= 128 ? 128 : 256;
+  if (warp == 0) {
+    tmem_alloc_pair(tmem_slot, ncols);
+    tmem_relinquish_pair();
+    tc_fence_before_sync();
+  }
+  // both CTAs' operands, barriers and TMEM are in place before rank 0 issues
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  WaitCtl ctl;
+  ctl.abort = abort_flag;
+  ctl.peer_abort = cluster_generic_ptr(const_cast<int*>(abort_flag), rank ^ 1u);
+  ctl.status = status;
+  ctl.limit_ns = limit_ns;
+
+  if (rank == 0 && threadIdx.x == 0) {
+    const uint32_t idesc = make_idesc(0u /* f16 */, false, false, 256, (uint32_t)n);
+#pragma unroll
+    for (int ks = 0; ks < T::kKSteps; ++ks)
+      mma_pair<Op::kF16>(tmem_base, operand_desc<T>(a_addr, false, ks), operand_desc<T>(b_addr, false, ks), idesc,
+                         ks > 0 ? 1u : 0u);
+    mma_commit_multicast(bar, 0x3);
+  }
+  __syncwarp();
+  const bool ok = warp_wait(bar, 0, ctl);
+  tc_fence_after_sync();
+  if (ok) {
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    for (int c = 0; c < n / 32; ++c) {
+      float v[32];
+      tmem_ld_32cols(tmem_base + lane_off + c * 32, v);
+      tmem_ld_wait();
+      float* out = D + ((size_t)((rank * 4 + warp) * 32 + lane) * (n / 32) + c) * 32;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) out[r] = v[r];
+    }
+  } else if (rank == 0) {
+    drain_wait(bar, 0, limit_ns);   // the pair's MMAs may still run: let them finish
+  }
+  tc_fence_before_sync();
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, ncols);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_probe_tmem_pair(const void* a, const void* b, int n, float* d, uint32_t* status,
+                                   uint64_t limit_ns, cudaStream_t stream) {
+  if (n != 64 && n != 128 && n != 256) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(probe_tmem_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairProbeSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kPairProbeSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint16_t* pa = static_cast<const uint16_t*>(a);
+  const uint16_t* pb = static_cast<const uint16_t*>(b);
+  e = cudaLaunchKernelEx(&cfg, probe_tmem_pair_kernel, pa, pb, n, d, status, limit_ns);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 bool tc_lookup_pair(Op op, Conv conv, TcKernel* out) {
   if (conv == Conv::kSplit3) {

@@ -86,6 +86,9 @@ def test_probe_tmem_arguments_rejected_before_launch(L):
     assert L.mpg_probe_tmem_acc(16, 16, 96, 16, None) == mpg.ERR_INVALID_ARG     # n not 64 / 128 / 256
     assert L.mpg_probe_tmem_acc(8, 16, 64, 16, None) == mpg.ERR_INVALID_ARG      # A not 16-byte aligned
     assert L.mpg_probe_tmem_acc(16, 16, 64, 2, None) == mpg.ERR_INVALID_ARG      # D not 4-byte aligned
+    assert L.mpg_probe_tmem_acc_pair(None, None, 64, None, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_tmem_acc_pair(16, 16, 32, 16, None) == mpg.ERR_INVALID_ARG     # n not 64 / 128 / 256
+    assert L.mpg_probe_tmem_acc_pair(16, 24, 64, 16, None) == mpg.ERR_INVALID_ARG     # B not 16-byte aligned
 
 
 def test_staging_probe_arguments_rejected_before_launch(L):

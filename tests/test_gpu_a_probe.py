@@ -126,3 +126,30 @@ def test_tmem_accumulator_map_on_hardware(orc, n):
     assert np.count_nonzero(np.roll(placed, 1, axis=0) != ref) > 0
     assert np.count_nonzero(placed.reshape(4, 32, n)[[1, 0, 3, 2]].reshape(128, n) != ref) > 0
     assert np.count_nonzero(placed.reshape(128, n // 32, 32)[:, :, ::-1].reshape(128, n) != ref) > 0
+
+
+@pytest.mark.parametrize("n", [64, 128, 256])
+def test_tmem_accumulator_map_on_hardware_cta_pair(orc, n):
+    """The M = 256 map on a CTA pair (cta_group::2): the raw registers of both
+    CTAs placed with mpg_tmem_acc_coords(256, rank, ...) equal the host
+    product at every one of the 256 x n points; swapping the CTAs' halves
+    would not."""
+    import torch
+    mpg.build()
+    g = np.random.Generator(np.random.PCG64(7200 + n))
+    a = g.integers(-3, 4, size=(256, 64)).astype(np.float32)
+    bt = g.integers(-3, 4, size=(n, 64)).astype(np.float32)
+    d = mpg.probe_tmem_acc_pair(torch.from_numpy(a).cuda(), torch.from_numpy(bt).cuda()).cpu().numpy()
+    assert mpg.device_status() == mpg.OK
+    ref, _ = orc.gemm(a.astype(np.float16), np.ascontiguousarray(bt.T).astype(np.float16))
+    placed = np.full((256, n), np.nan)
+    for rank in range(2):
+        for warp in range(4):
+            for lane in range(32):
+                for c in range(n // 32):
+                    for reg in range(32):
+                        r, col = mpg.tmem_acc_coords(warp, lane, reg, 32 * c, m_shape=256, cta_rank=rank)
+                        assert np.isnan(placed[r, col])
+                        placed[r, col] = d[rank, warp, lane, c, reg]
+    assert int(np.count_nonzero(placed != ref)) == 0
+    assert np.count_nonzero(np.concatenate([placed[128:], placed[:128]]) != ref) > 0
