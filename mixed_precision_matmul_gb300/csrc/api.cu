@@ -253,7 +253,8 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
           Bc = Operand{ws + L.off_b, L.b_ld, L.b_outer * L.b_ld, b_dtype, L.b_layout};
         }
         if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "aligned copy launch: %s", cudaGetErrorString(e));
-        return launch_tc(plan, dev, m, n, k, batch, Ac, Bc, C, ldc, strideC, alpha, beta, o, workspace, st);
+        return launch_tc(plan, dev, m, n, k, batch, Ac, Bc, C, ldc, strideC, alpha, beta, o, workspace, st, nullptr,
+                         nullptr, true);
       }
       if (!plan.prepass)
         return launch_tc(plan, dev, m, n, k, batch, Aop, Bop, C, ldc, strideC, alpha, beta, o, workspace, st);
@@ -295,7 +296,7 @@ mpg_status mpg_gemm_ex(int64_t m, int64_t n, int64_t k, int64_t batch, const voi
       Operand Al{a_lo, L.a_ld, L.a_outer * L.a_ld, cdt, a_layout};
       Operand Bl{b_lo, L.b_ld, L.b_outer * L.b_ld, cdt, b_layout};
       return launch_tc(plan, dev, m, n, k, batch, Ah, Bh, C, ldc, strideC, alpha, beta, o, workspace, st,
-                       sa_ ? &Al : nullptr, sb_ ? &Bl : nullptr);
+                       sa_ ? &Al : nullptr, sb_ ? &Bl : nullptr, true);
     }
   }
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));

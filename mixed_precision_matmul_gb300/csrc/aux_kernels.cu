@@ -3,6 +3,7 @@
 // accumulator-layout probe, the epilogue-staging probe and the bounded-wait
 // self test.
 #include <algorithm>
+#include <cstring>
 
 #include "internal.h"
 #include "outio.cuh"
@@ -41,6 +42,7 @@ __global__ void scale_c_kernel(void* c, int c_dtype, int64_t ldc, int64_t stride
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int32_t splits, void* c, int c_dtype,
                                      int64_t ldc, int64_t stride_c, int32_t m, int32_t n, int32_t batch,
                                      float alpha, float beta) {
+  griddep_wait();   // launched as a programmatic dependent of the product that writes the partials
   const int64_t per = (int64_t)m * n;
   const int64_t total = per * batch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -141,8 +143,21 @@ cudaError_t launch_scale_c(void* c, int c_dtype, int64_t ldc, int64_t stride_c, 
 cudaError_t launch_splitk_reduce(const float* partial, int32_t splits, void* c, int c_dtype, int64_t ldc,
                                  int64_t stride_c, int32_t m, int32_t n, int32_t batch, float alpha, float beta,
                                  cudaStream_t stream) {
-  splitk_reduce_kernel<<<grid_for((int64_t)m * n * batch), 256, 0, stream>>>(partial, splits, c, c_dtype, ldc,
-                                                                                  stride_c, m, n, batch, alpha, beta);
+  // a programmatic dependent of the product: it may be scheduled as the
+  // product's CTAs finish and waits (griddep_wait) for all of their partials
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)grid_for((int64_t)m * n * batch));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, splits, c, c_dtype, ldc, stride_c, m, n,
+                                     batch, alpha, beta);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -117,6 +117,6 @@ mpg_status validate(int64_t m, int64_t n, int64_t k, int64_t batch, const Operan
 mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, int64_t k, int64_t batch,
                      const Operand& A, const Operand& B, float* C, int64_t ldc, int64_t strideC, float alpha,
                      float beta, const mpg_options& o, void* workspace, cudaStream_t stream,
-                     const Operand* A_lo = nullptr, const Operand* B_lo = nullptr);
+                     const Operand* A_lo = nullptr, const Operand* B_lo = nullptr, bool dependent = false);
 
 }  // namespace mpg

@@ -479,7 +479,7 @@ mpg_status pair_clusters(DeviceInfo* dev, const TcKernel& kern, int* out) {
 mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, int64_t k, int64_t batch,
                      const Operand& A, const Operand& B, float* C, int64_t ldc, int64_t strideC, float alpha,
                      float beta, const mpg_options& o, void* workspace, cudaStream_t stream,
-                     const Operand* A_lo, const Operand* B_lo) {
+                     const Operand* A_lo, const Operand* B_lo, bool dependent) {
   TcKernel kern;
   const bool found = plan.pair ? mpg::tc_lookup_pair(plan.op, plan.conv, &kern)
                                : mpg::tc_kernel_lookup(plan.src, plan.conv, plan.op, plan.st, plan.bn, &kern);
@@ -666,25 +666,37 @@ mpg_status launch_tc(const Plan& plan, DeviceInfo* dev, int64_t m, int64_t n, in
 
   void* args[] = {&p};
   cudaError_t e;
-  if (plan.pair) {
-    // clusters of two CTAs; as many clusters as can be resident at once
+  {
+    // persistent grid: clusters of two CTAs for the pair kernels (as many
+    // clusters as can be resident at once), one CTA per SM otherwise.  A
+    // product whose operands the previous kernel of this call wrote (the
+    // conversion pass, aligned copies) is that kernel's programmatic
+    // dependent: its set-up overlaps the other's end (the kernel waits with
+    // griddepcontrol.wait before reading anything).
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(p.num_tiles, clusters)));
+    cfg.gridDim = plan.pair ? dim3((unsigned)(2 * std::min<int64_t>(p.num_tiles, clusters)))
+                            : dim3((unsigned)std::min<int64_t>(tiles, dev->sm_count));
     cfg.blockDim = dim3((unsigned)kern.block);
     cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (plan.pair) {
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = 2;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    if (dependent) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na].val.programmaticStreamSerializationAllowed = 1;
+      ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelExC(&cfg, kern.fn, args);
-  } else {
-    const int grid = (int)std::min<int64_t>(tiles, dev->sm_count);
-    e = cudaLaunchKernel(kern.fn, dim3(grid), dim3(kern.block), args, kern.smem_bytes, stream);
   }
   if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   if (splits_eff > 1) {

@@ -41,6 +41,7 @@ struct PassJobs {
 // items of both operands form one index range.  Each thread handles two
 // items per loop trip, loading both before converting either.
 __global__ void __launch_bounds__(256) prepass_kernel(const __grid_constant__ PassJobs J) {
+  griddep_launch_dependents();   // the product may set itself up meanwhile
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < J.total; i0 += 2 * step) {
     float x[2][8];
@@ -93,6 +94,7 @@ template <int ES>
 __global__ void __launch_bounds__(256) copy_pad_kernel(const uint8_t* __restrict__ in, int64_t ld_in,
                                                        int64_t stride_in, int64_t outer, int64_t inner, int64_t batch,
                                                        uint8_t* __restrict__ out, int64_t ld_out) {
+  griddep_launch_dependents();   // the product may set itself up meanwhile
   using E = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
   const E* src = reinterpret_cast<const E*>(in);
   E* dst = reinterpret_cast<E*>(out);
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __rest
                                                           int64_t stride_in, int64_t outer, int64_t inner,
                                                           uint32_t* __restrict__ out, int64_t ld_out) {
   __shared__ uint32_t tile[32][33];
+  griddep_launch_dependents();   // the product may set itself up meanwhile
   const int64_t b = blockIdx.z;
   const int64_t o0 = (int64_t)blockIdx.y * 32, i0 = (int64_t)blockIdx.x * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads

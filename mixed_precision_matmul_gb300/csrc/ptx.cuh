@@ -88,6 +88,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched as a programmatic
+// dependent of the one before it on the stream may start while that one is
+// still running; griddep_wait blocks until it has completed and its memory
+// is visible (it returns at once for an ordinary launch), and
+// griddep_launch_dependents lets this grid's own dependents be scheduled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // proxy fences
 // ---------------------------------------------------------------------------
 // Make generic-proxy writes to shared memory visible to the async proxy

@@ -375,6 +375,11 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the end of the kernel that wrote this
+  // product's operands (the conversion pass or aligned copies); nothing of
+  // theirs is read before this point
+  griddep_wait();
+  griddep_launch_dependents();
 
   WaitCtl ctl;
   ctl.abort = abort_flag;

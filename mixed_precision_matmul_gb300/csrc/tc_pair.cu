@@ -221,6 +221,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_pair_kernel(const __grid_co
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up may overlap the end of the kernel that wrote the operands
+  griddep_wait();
+  griddep_launch_dependents();
 
   WaitCtl ctl;
   ctl.abort = abort_flag;
