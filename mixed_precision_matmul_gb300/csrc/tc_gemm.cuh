@@ -65,9 +65,22 @@ struct TcTraits {
   static constexpr int kStgBTile = kStaged ? BN * 128 : 0;
   static constexpr int kStgStage = kStgATile + kStgBTile;
   static constexpr int kBudget = 196 * 1024;
-  static constexpr int kStagesRaw = kBudget / (kOpStage + kStgStage);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static_assert(kStages >= 2, "pipeline needs two stages");
+  // Ring depths.  Without staging one ring of operand stages carries the
+  // loads in flight.  On the staged path the fp32 staging ring (TMA from L2
+  // or HBM) carries them and the ring of converted operand stages the
+  // hand-off from the converter warps to the MMAs: equal depths where the
+  // budget gives both three or more stages (measured best for the splits),
+  // else two operand stages and the rest to staging (fp32 -> fp16 / bf16 on
+  // 256-wide tiles: 2 + 3 stages instead of 2 + 2, 443 -> 529 TFLOP/s at
+  // 8192^3; two operand stages with the splits' larger ones measured slower).
+  static constexpr int kEqualRaw = kBudget / (kOpStage + kStgStage);
+  static constexpr int kEqual = kEqualRaw > 8 ? 8 : kEqualRaw;
+  static constexpr int kOpRaw = !kStaged ? kBudget / kOpStage : (kEqual >= 3 ? kEqual : 2);
+  static constexpr int kStagesOp = kOpRaw > 8 ? 8 : kOpRaw;
+  static constexpr int kStgRaw =
+      !kStaged ? 0 : (kEqual >= 3 ? kEqual : (kBudget - kStagesOp * kOpStage) / kStgStage);
+  static constexpr int kStagesStg = kStgRaw > 8 ? 8 : kStgRaw;
+  static_assert(kStagesOp >= 2 && (!kStaged || kStagesStg >= 2), "pipeline needs two stages");
   static constexpr int kConvWarps = kHasConv ? 8 : 0;
   static constexpr int kConvThreads = kConvWarps * 32;
   static constexpr int kEpiWarps = kHasConv ? 4 : 8;
@@ -97,13 +110,13 @@ struct TcTraits {
                                    : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
-  static constexpr int kNumBars = 4 * kStages + 2 * kAccBufs + 1;
-  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kOpStage + kStgStage) + kEpiBytes +
+  static constexpr int kNumBars = 2 * kStagesOp + 2 * kStagesStg + 2 * kAccBufs + 1;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStagesOp * kOpStage + kStagesStg * kStgStage + kEpiBytes +
                                     kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // each epilogue warp's staging buffer starts on a 1024-byte boundary (the
   // 128-byte swizzle of its TMA stores repeats every 1024 bytes)
-  static_assert((kStages * (kOpStage + kStgStage)) % 1024 == 0, "staging alignment");
+  static_assert((kStagesOp * kOpStage) % 1024 == 0 && (kStagesStg * kStgStage) % 1024 == 0, "staging alignment");
   static_assert(BN % BK == 0 && BM % BK == 0, "regions of MN-major tiles");
   static constexpr uint32_t kAbFormat = (O == Op::kF16) ? 0u : (O == Op::kBF16) ? 1u : 2u;
 };
@@ -332,14 +345,14 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
   // 1024-byte aligned base (swizzle atoms repeat every 1024 bytes)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* op_base = smem;
-  uint8_t* stg_base = op_base + T::kStages * T::kOpStage;
-  float* epi_base = reinterpret_cast<float*>(stg_base + T::kStages * T::kStgStage);
+  uint8_t* stg_base = op_base + T::kStagesOp * T::kOpStage;
+  float* epi_base = reinterpret_cast<float*>(stg_base + T::kStagesStg * T::kStgStage);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_base) + T::kEpiBytes);
   uint64_t* op_full = bars;                       // operand stage ready for the MMA
-  uint64_t* op_empty = bars + T::kStages;         // operand stage consumed by the MMA
-  uint64_t* stg_full = bars + 2 * T::kStages;     // staging filled by TMA
-  uint64_t* stg_empty = bars + 3 * T::kStages;    // staging read by the converters
-  uint64_t* acc_full = bars + 4 * T::kStages;     // accumulator complete
+  uint64_t* op_empty = bars + T::kStagesOp;       // operand stage consumed by the MMA
+  uint64_t* stg_full = bars + 2 * T::kStagesOp;   // staging filled by TMA
+  uint64_t* stg_empty = stg_full + T::kStagesStg; // staging read by the converters
+  uint64_t* acc_full = stg_empty + T::kStagesStg; // accumulator complete
   uint64_t* acc_empty = acc_full + T::kAccBufs;   // accumulator drained by the epilogue
   uint64_t* done_bar = acc_empty + T::kAccBufs;   // all MMAs of this CTA finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -349,15 +362,17 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < T::kStages; ++i) {
+    for (int i = 0; i < T::kStagesOp; ++i) {
       if constexpr (T::kHasConv) {
         mbar_init(&op_full[i], T::kConvThreads);
       } else {
         mbar_init(&op_full[i], 1);
       }
       mbar_init(&op_empty[i], 1);
+    }
+    for (int i = 0; i < T::kStagesStg; ++i) {
       mbar_init(&stg_full[i], 1);
-      mbar_init(&stg_empty[i], T::kConvThreads > 0 ? T::kConvThreads : 1);
+      mbar_init(&stg_empty[i], T::kConvThreads);
     }
     for (int i = 0; i < T::kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -403,13 +418,14 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
         constexpr int kABytes = T::BM * kLineBytes;
         constexpr int kStageBytes = T::kStaged ? T::kStgStage : T::kOpStage;
         constexpr int kRegion = T::BK * kLineBytes;  // bytes of one MN-major region
+        constexpr uint32_t kRing = T::kStaged ? T::kStagesStg : T::kStagesOp;   // the ring it fills
         uint32_t it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
           const TileCoord tc = decode_tile(p, t);
           for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
-            const uint32_t st = it % T::kStages;
-            const uint32_t ph = (it / T::kStages) & 1u;
+            const uint32_t st = it % kRing;
+            const uint32_t ph = (it / kRing) & 1u;
             if (!mbar_wait(&emptyb[st], ph ^ 1u, ctl)) { ok = false; break; }
             uint8_t* dst = (T::kStaged ? stg_base + st * T::kStgStage : op_base + st * T::kOpStage);
             mbar_arrive_expect_tx(&fullb[st], kStageBytes);
@@ -436,9 +452,9 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           }
         }
         // let copies already issued land before the CTA may exit
-        const uint32_t n_drain = it < (uint32_t)T::kStages ? it : (uint32_t)T::kStages;
+        const uint32_t n_drain = it < kRing ? it : kRing;
         for (uint32_t i = it - n_drain; i < it; ++i)
-          drain_wait(&fullb[i % T::kStages], (i / T::kStages) & 1u, p.wait_limit_ns);
+          drain_wait(&fullb[i % kRing], (i / kRing) & 1u, p.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -467,8 +483,8 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           tc_fence_after_sync();
           const uint32_t d0 = tmem_base + ab * T::kAccStride;
           for (int kb = c0; kb < c1; ++kb, ++it) {
-            const uint32_t st = it % T::kStages;
-            const uint32_t ph = (it / T::kStages) & 1u;
+            const uint32_t st = it % T::kStagesOp;
+            const uint32_t ph = (it / T::kStagesOp) & 1u;
             if (!mbar_wait(&op_full[st], ph, ctl)) { ok = false; break; }
             tc_fence_after_sync();
             const uint32_t a_hi = op_smem + st * T::kOpStage;
@@ -801,8 +817,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(p, t);
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++it) {
-          const uint32_t st = it % T::kStages;
-          const uint32_t ph = (it / T::kStages) & 1u;
+          // the staging ring (read) and the operand ring (written) turn at
+          // their own depths
+          const uint32_t ss = T::kStaged ? it % T::kStagesStg : 0u;
+          const uint32_t sph = T::kStaged ? (it / T::kStagesStg) & 1u : 0u;
+          const uint32_t st = it % T::kStagesOp;
+          const uint32_t ph = (it / T::kStagesOp) & 1u;
           if constexpr (T::kSrc == Src::kGeneric) {
             if (kb + 1 < tc.kb1) {
               gather(tc, kb + 1, nxt);
@@ -815,7 +835,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             }
           }
           if constexpr (T::kStaged) {
-            if (!warp_wait(&stg_full[st], ph, ctl)) { ok = false; break; }
+            if (!warp_wait(&stg_full[ss], sph, ctl)) { ok = false; break; }
           }
           uint32_t w[kPerThread][4];
           // ---- convert (staging written by TMA, 128B-swizzled fp32; or the
@@ -829,7 +849,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             float x[4];
             unsigned short h[4];
             if constexpr (T::kStaged) {
-              const uint32_t base = stg_smem + st * T::kStgStage + (isA ? 0u : (uint32_t)T::kStgATile);
+              const uint32_t base = stg_smem + ss * T::kStgStage + (isA ? 0u : (uint32_t)T::kStgATile);
               const float4 v = ld_shared_f4(base + swz_chunk_offset<128>(lg, ch));
               x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
               h[0] = h[1] = h[2] = h[3] = 0;
@@ -848,7 +868,7 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
             // so the reads are complete; order them before the TMA's
             // (async-proxy) refill of this buffer, then hand it back.
             fence_proxy_async_smem();
-            mbar_arrive(&stg_empty[st]);
+            mbar_arrive(&stg_empty[ss]);
           }
           if (!warp_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
           // ---- scatter into the swizzled operand tiles
