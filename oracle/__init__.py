@@ -80,6 +80,8 @@ def _load():
                                         vp, i32, i64, i32, i32, i32,
                                         vp, i64, dbl, dbl, i64, vp, vp, vp, vp, i32]
         lib.orc_gemm_points.restype = i32
+        lib.orc_gemm_fma_chain_f32.argtypes = [i64, i64, i64, vp, vp, vp, i64, ctypes.c_float, ctypes.c_float, vp]
+        lib.orc_gemm_fma_chain_f32.restype = i32
         lib.orc_acc_coords.argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.orc_acc_coords.restype = i32
         for nm in ("orc_frag_a_coords", "orc_frag_b_coords"):
@@ -272,6 +274,30 @@ def gemm_points(A, B, k: int, rows, cols, C0=None, alpha: float = 1.0, beta: flo
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return ref, den
+
+
+def gemm_fma_chain_f32(A, B, C0=None, alpha: float = 1.0, beta: float = 0.0) -> np.ndarray:
+    """The plain fp32 comparator's result, exactly: per element one fmaf
+    chain over k ascending from +0, then alpha*acc (beta == 0, C0 unread)
+    or fmaf(beta, C0, alpha*acc), all in fp32.  A (m x k), B (k x n), C0
+    (m x n) are logical row-major values, cast to float32."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    m, k = A.shape
+    n = B.shape[1]
+    if B.shape[0] != k:
+        raise ValueError("inner dimensions differ")
+    out = np.empty((m, n), dtype=np.float32)
+    c_ptr, ldc0 = None, 0
+    if C0 is not None:
+        C0 = np.ascontiguousarray(C0, dtype=np.float32)
+        c_ptr, ldc0 = C0.ctypes.data, n
+    rc = lib.orc_gemm_fma_chain_f32(m, n, k, A.ctypes.data, B.ctypes.data, c_ptr, ldc0,
+                                    float(np.float32(alpha)), float(np.float32(beta)), out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
 
 
 def max_rel_err(C: np.ndarray, ref: np.ndarray, den: np.ndarray) -> float:

@@ -363,6 +363,32 @@ int orc_gemm_points(int64_t k,
 }
 
 /* ------------------------------------------------------------------------- */
+/* The plain fp32 comparator's own result                                      */
+/* ------------------------------------------------------------------------- */
+
+/* "tile_matmul(): use the cuBLASDx register-accumulator API ...", spike
+ * results, second bullet: fp32 has no matrix instruction, so the fp32 product
+ * is a chain of scalar fused multiply-adds.  Reading (listed in the design
+ * notes): each output element is ONE chain in fp32, k ascending from an
+ * accumulator of +0, each step one correctly rounded fmaf, then
+ * out = alpha*acc rounded to fp32 when beta == 0 (C0 is not read), else
+ * fmaf(beta, C0, alpha*acc).  A and B are row-major fp32 (m x k, k x n),
+ * C0 row-major with ldc0 (may be NULL when beta == 0), out row-major m x n. */
+int orc_gemm_fma_chain_f32(int64_t m, int64_t n, int64_t k, const float* A, const float* B,
+                           const float* C0, int64_t ldc0, float alpha, float beta, float* out) {
+  if (m < 0 || n < 0 || k < 0) return -1;
+  if (beta != 0.0f && !C0) return -1;
+  for (int64_t i = 0; i < m; ++i)
+    for (int64_t j = 0; j < n; ++j) {
+      float acc = 0.0f;
+      for (int64_t kk = 0; kk < k; ++kk) acc = fmaf(A[i * k + kk], B[kk * n + j], acc);
+      const float t = alpha * acc;
+      out[i * n + j] = (beta != 0.0f) ? fmaf(beta, C0[i * ldc0 + j], t) : t;
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* The m16n8k16 f32 accumulator fragment, from the PTX row/col formulas        */
 /* ------------------------------------------------------------------------- */
 

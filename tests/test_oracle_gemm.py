@@ -183,3 +183,66 @@ def test_four_chain_split_keeps_lo_lo(orc):
     rows, cols = np.array([0, 3, 7]), np.array([9, 0, 4])
     p4, _ = orc.gemm_points(A, B, 27, rows, cols, a_q=orc.Q_SPLIT4, b_q=orc.Q_SPLIT4)
     assert np.array_equal(p4, rR[rows, cols])
+
+
+# ---- the fp32 comparator's exact result (one fmaf chain per element)
+
+def test_fma_chain_is_fused_and_ascending(orc):
+    """k = 2: -1 * 1, then (1 + 2^-12)^2 - 1 in ONE rounding gives
+    2^-11 + 2^-24 exactly; a separate multiply would round the square to
+    1 + 2^-11 first (a tie to even) and give 2^-11, and the descending
+    order (square first) gives 2^-11 too."""
+    x = 1.0 + 2.0 ** -12
+    out = orc.gemm_fma_chain_f32(np.array([[-1.0, x]]), np.array([[1.0], [x]]))
+    assert out[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+
+
+def test_fma_chain_order_decides_cancellation(orc):
+    """1 + 2^24 - 2^24 in k order: 1 + 2^24 rounds to 2^24 (a tie to even),
+    so the chain ends at 0 although the exact sum is 1."""
+    out = orc.gemm_fma_chain_f32(np.array([[1.0, 2.0 ** 24, -(2.0 ** 24)]]), np.ones((3, 1)))
+    assert out[0, 0] == 0.0
+    out = orc.gemm_fma_chain_f32(np.array([[-(2.0 ** 24), 2.0 ** 24, 1.0]]), np.ones((3, 1)))
+    assert out[0, 0] == 1.0
+
+
+def test_fma_chain_small_integers_exact(orc):
+    g = np.random.Generator(np.random.PCG64(31))
+    A = g.integers(-8, 9, size=(9, 40))
+    B = g.integers(-8, 9, size=(40, 7))
+    out = orc.gemm_fma_chain_f32(A, B)
+    assert np.array_equal(out.astype(np.int64), A @ B)
+
+
+def test_fma_chain_epilogue_roundings(orc):
+    """alpha * acc is rounded to fp32 on its own, then beta * C0 is added in
+    one fmaf: acc = 3, alpha = 1 + 2^-23 gives t = 3 + 2^-21 (1.5 ulp, a tie
+    to even), and fmaf(1, -3, t) = 2^-21.  Fusing alpha instead would give
+    3 * 2^-23.  With beta = 0 C0 is not read (NaN stays out)."""
+    one = np.ones((1, 1))
+    out = orc.gemm_fma_chain_f32(np.array([[3.0]]), one, np.array([[-3.0]]), alpha=1.0 + 2.0 ** -23, beta=1.0)
+    assert out[0, 0] == np.float32(2.0 ** -21)
+    x = 1.0 + 2.0 ** -12
+    out = orc.gemm_fma_chain_f32(np.array([[-1.0]]), one, np.array([[x]]), alpha=1.0, beta=x)
+    assert out[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+    out = orc.gemm_fma_chain_f32(np.array([[2.0]]), one, np.array([[np.nan]]), alpha=0.5, beta=0.0)
+    assert out[0, 0] == 1.0
+    assert orc.gemm_fma_chain_f32(np.zeros((2, 0)), np.zeros((0, 3)), np.full((2, 3), 4.0), 1.0, 0.5).tolist() == \
+        [[2.0] * 3] * 2
+
+
+def test_fma_chain_within_the_recursive_summation_bound(orc):
+    """|chain - exact| <= gamma_k * sum |a||b| with gamma_k = k u / (1 - k u),
+    u = 2^-24 (the error bound of recursive summation with fused steps),
+    the exact value from the fp64 reference on the same fp32 inputs."""
+    g = np.random.Generator(np.random.PCG64(32))
+    m, n, k = 20, 17, 300
+    A = g.standard_normal((m, k)).astype(np.float32)
+    B = g.standard_normal((k, n)).astype(np.float32)
+    out = orc.gemm_fma_chain_f32(A, B)
+    ref, den = orc.gemm(A, B)
+    u = 2.0 ** -24
+    gamma = k * u / (1 - k * u)
+    err = np.abs(out.astype(np.float64) - ref)
+    assert np.all(err <= gamma * den)
+    assert np.max(err / den) > 0          # and it is not the fp64 value
