@@ -10,7 +10,10 @@
 // k-major so both operands are read as float4 broadcasts), 8 x 8 outputs per
 // thread in registers.  Interior tiles of aligned operands load float4
 // vectors; edge tiles and unaligned operands load element by element with
-// bounds checks.  Any layout, leading dimension and tail.
+// bounds checks.  Any layout, leading dimension and tail.  The 64 chains of
+// a thread advance two at a time with the packed fp32 FMA (__ffma2_rn: two
+// independent correctly rounded fmaf in one instruction), which halves the
+// issue slots the multiply-adds take and leaves each chain's steps unchanged.
 #include "internal.h"
 #include "outio.cuh"
 
@@ -123,11 +126,13 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
     const float* a = p.a + (int64_t)bz * p.stride_a;
     const float* b = p.b + (int64_t)bz * p.stride_b;
     void* c = static_cast<uint8_t*>(p.c) + (int64_t)bz * p.stride_c * (p.c_dtype == kOutF32 ? 4 : 2);
-    float acc[8][8];
+    // acc[i][j] holds columns 2j and 2j+1 of row i: one packed fp32 FMA
+    // (two independent correctly rounded fmaf) per pair
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
     Loader<A_COL, B_COL> ld;
     const int num_kt = (p.k + kBK - 1) / kBK;
@@ -144,11 +149,14 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
         const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4]);
         const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][64 + tx * 4]);
         const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const float2 bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                              make_float2(b1.z, b1.w)};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
+          const float2 ai = make_float2(av[i], av[i]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+          for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, bv[j], acc[i][j]);
+        }
       }
       if (kt + 1 < num_kt) ld.store(As[cur ^ 1], Bs[cur ^ 1]);
       __syncthreads();
@@ -162,9 +170,8 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
         const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
         if (gn >= p.n) continue;
         const int64_t idx = (int64_t)gm * p.ldc + gn;
-        out_store(c, idx,
-                  (p.beta != 0.0f) ? fmaf(p.beta, out_load(c, idx, p.c_dtype), p.alpha * acc[i][j]) : p.alpha * acc[i][j],
-                  p.c_dtype);
+        const float t = p.alpha * ((j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x);
+        out_store(c, idx, (p.beta != 0.0f) ? fmaf(p.beta, out_load(c, idx, p.c_dtype), t) : t, p.c_dtype);
       }
     }
     __syncthreads();
