@@ -891,7 +891,7 @@ def reference(args):
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
-NCU_TRAFFIC = {"gemm_bf16_8192": 1544310272}   # tc_pair_kernel (serpentine tile order), one --set full capture
+NCU_TRAFFIC = {"gemm_bf16_8192": 1560924928}   # tc_pair_kernel (serpentine tile order), dram__bytes_read + _write of one launch
 
 
 def main():
