@@ -87,3 +87,22 @@ def test_torch_api_output_type_follows_c():
     mpg.gemm(A, B, C32, mode="fp16", opts=mpg.options(c_dtype=mpg.F16))
     torch.cuda.synchronize()
     assert oracle.max_rel_err(C32.cpu().numpy(), ref, den) <= TOL["q16"]
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("name,mode,dt,m,n,k,beta,kw", [
+    ("pair_tail", mpg.BF16_F32ACC, "bf16", 520, 516, 320, 0.5, dict(cta_pair=1, tail_split=1)),
+    ("pair_beta0", mpg.BF16_F32ACC, "bf16", 300, 260, 190, 0.0, dict(cta_pair=1)),
+    ("pass_split3", mpg.SPLIT_FP16_3CHAIN, "f32", 300, 200, 300, 0.5, dict(prepass=1)),
+    ("pass_split3_shared", mpg.SPLIT_FP16_3CHAIN, "f32", 300, 200, 300, 0.0, dict(prepass=1, split_lo_shared=1)),
+    ("onload_fp16_beta0", mpg.FP16_F32ACC, "f32", 257, 132, 100, 0.0, dict(prepass=-1)),
+    ("generic_split4", mpg.SPLIT_FP16_4CHAIN, "f32", 140, 70, 96, 0.5, dict(force_generic_load=1)),
+])
+def test_sixteen_bit_output_on_other_paths(out, name, mode, dt, m, n, k, beta, kw):
+    """16-bit C from the CTA pairs (with the split tail's fixup, and with
+    beta = 0), the conversion pass's copies (three chains and the shared lo
+    accumulator), the load-stage converter and generic loads."""
+    mpg.build()
+    got, ref, den = _run(mode, dt, out, m, n, k, beta=beta, opts=mpg.options(**kw))
+    tol = TOL["split"] if mode in (mpg.SPLIT_FP16_3CHAIN, mpg.SPLIT_FP16_4CHAIN) else TOL["q16"]
+    assert np.all(np.abs(got - ref) <= _ulp(ref, out) + tol * den), name
