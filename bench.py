@@ -710,6 +710,20 @@ def ours(args):
                 torch.cuda.synchronize()
                 mode_outputs[label] = ("attention", (Od.cpu().numpy(), (q_a, k_a, v_a, scale_a)))
             del Qd, Kd, Vd, Od, aws
+        # the fp32 multiply-add pipe's sustained rate on this GPU, measured live
+        # by the register-only probe (the ceiling of the FFMA comparator)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        pout = torch.empty(8 * sms, dtype=torch.float32, device=device)
+        pipe = {}
+        for packed in (False, True):
+            ms = time_steps(torch, lambda pk=packed: mpg.probe_fma_rate(8 * sms, 4096, pk, out=pout, stream=sh),
+                            5, 2, stream) / 5
+            pipe["packed" if packed else "scalar"] = round(2.0 * 32 * 4096 * 256 * 8 * sms / (ms * 1e-3) / 1e12, 1)
+        torch.cuda.synchronize()
+        pipe_ok = bool(torch.all(pout == 496 + 32 * 4096).item())
+        modes["fma_pipe_probe"] = {"tflops": max(pipe.values()), **pipe, "checked": pipe_ok,
+                                   "bound": "alu: fp32 multiply-add pipe, registers only"}
+        del pout
         ffma = modes.get("loguniform4096_ffma", {}).get("tflops")
         for lbl in [f"loguniform4096_{x}{y}" for x in ("split3", "split1", "split2a", "split4")
                     for y in ("", "_prepass")]:
@@ -803,14 +817,17 @@ def build_targets(modes, result, peaks):
 
     ffma_tf = g("loguniform4096_ffma", "tflops")
     ffma_pk = ffma_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+    ffma_meas = g("fma_pipe_probe", "tflops")
     t = {
         "peaks": {"bf16": bf16, "tf32": round(0.5 * bf16, 1), "hbm_gbs": hbm,
-                  "fp32_ffma": round(ffma_pk, 1), "src": "measured bf16/HBM; tf32 = bf16/2; "
-                                                          "ffma = 152 SMs x 128 x 2 x 2070 MHz"},
+                  "fp32_ffma": round(ffma_pk, 1), "fp32_fma_measured": ffma_meas,
+                  "src": "measured bf16/HBM; tf32 = bf16/2; ffma = 152 SMs x 128 x 2 x 2070 MHz; "
+                         "fp32_fma_measured = register-only multiply-add probe, live"},
         "bf16_8192": {"tf": result["value"], "frac": result["roofline"]["frac"], "bar": 0.7},
         "tf32_8192": {"tf": g("square8192_tf32", "tflops"), "frac": g("square8192_tf32", "frac_of_tensor_peak"),
                       "err": g("square8192_tf32", "max_rel_err_vs_fp64"), "bar": 0.6, "err_bar": 2e-3},
         "ffma_4096": {"tf": ffma_tf, "frac": round(ffma_tf / ffma_pk, 3) if ffma_tf else None,
+                      "frac_measured": round(ffma_tf / ffma_meas, 3) if ffma_tf and ffma_meas else None,
                       "err": g("loguniform4096_ffma", "max_rel_err_vs_fp64")},
     }
     for lbl, key in (("loguniform4096_split3", "split3_load"), ("loguniform4096_split3_prepass", "split3_pass"),

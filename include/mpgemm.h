@@ -558,6 +558,20 @@ mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, voi
  * launch. */
 mpg_status mpg_probe_tmem_acc_pair(const void* A, const void* B, int n, float* D, void* stream);
 
+/* Throughput probe of the fp32 multiply-add pipe that bounds MPG_FP32_FFMA
+ * (the plain fp32 comparator of "tile_matmul(): use the cuBLASDx
+ * register-accumulator API ...", spike results, second bullet: fp32 stays
+ * FFMA-bound).  Launches `blocks` blocks of 256 threads; every thread runs
+ * `iters` rounds of 32 independent fp32 multiply-adds held in registers, as
+ * scalar fmaf (packed = 0) or as 16 packed pairs (packed = 1), with no memory
+ * traffic inside the loop: 2 * 32 * iters * 256 * blocks flops.  Time it with
+ * events on `stream` to measure the pipe's sustained rate on this GPU.
+ *   out: device, `blocks` floats; out[b] = 496 + 32 * iters on return (the
+ *        chains' exact end values, so the work cannot be skipped).
+ *   blocks in [1, 65535], iters in [1, 2^19], packed 0 or 1.
+ * MPG_ERR_INVALID_ARG for bad arguments, before any launch. */
+mpg_status mpg_probe_fma_rate(float* out, int64_t blocks, int iters, int packed, void* stream);
+
 /* Failure-detection self test: launches one kernel whose single wait is on an
  * mbarrier nothing ever arrives at, bounded by timeout_ns (1 ms .. 10 s), then
  * synchronises.  Returns MPG_ERR_TIMEOUT when the kernel gave up the wait and

@@ -145,6 +145,8 @@ def lib():
         L.mpg_probe_tmem_acc.restype = i32
         L.mpg_probe_tmem_acc_pair.argtypes = [vp, vp, i32, vp, vp]
         L.mpg_probe_tmem_acc_pair.restype = i32
+        L.mpg_probe_fma_rate.argtypes = [vp, ctypes.c_int64, i32, i32, vp]
+        L.mpg_probe_fma_rate.restype = i32
         L.mpg_probe_mma_m16n8k16.argtypes = [vp, vp, vp, vp]
         L.mpg_probe_mma_m16n8k16.restype = i32
         for nm in ("mpg_frag_a_coords", "mpg_frag_a_decode", "mpg_frag_b_coords", "mpg_frag_b_decode"):
@@ -546,6 +548,19 @@ def probe_tmem_acc(A16, Bt16, stream=None):
     d = torch.empty((4, 32, n // 32, 32), dtype=torch.float32, device=a.device)
     _check(lib().mpg_probe_tmem_acc(a.data_ptr(), bt.data_ptr(), n, d.data_ptr(), _stream_handle(stream)))
     return d
+
+
+def probe_fma_rate(blocks, iters, packed=True, out=None, stream=None):
+    """mpg_probe_fma_rate: `blocks` blocks of 256 threads, each thread
+    32 x iters independent fp32 multiply-adds in registers (packed pairs or
+    scalar fmaf); returns the (blocks,) output, every entry 496 + 32 * iters.
+    Time it with events on `stream`: 2 * 32 * iters * 256 * blocks flops."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(blocks, dtype=torch.float32, device="cuda")
+    _check(lib().mpg_probe_fma_rate(out.data_ptr(), int(blocks), int(iters), 1 if packed else 0,
+                                    _stream_handle(stream)))
+    return out
 
 
 def probe_tmem_acc_pair(A16, Bt16, stream=None):

@@ -368,6 +368,21 @@ mpg_status mpg_probe_epilogue_staging(const float* in, float* out, int64_t block
   return MPG_OK;
 }
 
+mpg_status mpg_probe_fma_rate(float* out, int64_t blocks, int iters, int packed, void* stream) {
+  t_err.clear();
+  if (!out) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(out) % 4 != 0) return fail(MPG_ERR_INVALID_ARG, "out not aligned to 4 bytes");
+  if (blocks < 1 || blocks > 65535) return fail(MPG_ERR_INVALID_ARG, "blocks outside [1, 65535]");
+  if (iters < 1 || iters > (1 << 19)) return fail(MPG_ERR_INVALID_ARG, "iters outside [1, 2^19]");
+  if (packed != 0 && packed != 1) return fail(MPG_ERR_INVALID_ARG, "packed must be 0 or 1");
+  DeviceInfo* dev = nullptr;
+  mpg_status s = get_device(&dev);
+  if (s != MPG_OK) return s;
+  cudaError_t e = launch_probe_fma(out, blocks, iters, packed, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MPG_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MPG_OK;
+}
+
 mpg_status mpg_probe_tmem_acc(const void* A, const void* B, int n, float* D, void* stream) {
   t_err.clear();
   if (!A || !B || !D) return fail(MPG_ERR_INVALID_ARG, "NULL pointer");

@@ -220,6 +220,45 @@ cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, in
   return cudaGetLastError();
 }
 
+// Throughput probe of the fp32 multiply-add pipe, the bound of the FFMA
+// comparator: every thread runs `iters` rounds of 32 independent fmaf chains
+// (acc = fmaf(1, acc, 1), from acc = 0 .. 31), as scalar fmaf or as 16
+// packed pairs (__ffma2_rn), with no memory traffic inside the loop.  The
+// chains end at i + iters exactly, so thread 0 of each block writes
+// 496 + 32 * iters, which checks that the work was done.
+__global__ void __launch_bounds__(256) probe_fma_kernel(float* __restrict__ out, int iters, int packed, float a,
+                                                         float b) {
+  float s = 0.0f;
+  if (packed) {
+    float2 acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = make_float2((float)(2 * i), (float)(2 * i + 1));
+    const float2 av = make_float2(a, a), bv = make_float2(b, b);
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = __ffma2_rn(av, acc[i], bv);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s += acc[i].x + acc[i].y;
+  } else {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = (float)i;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = fmaf(a, acc[i], b);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s += acc[i];
+  }
+  if (threadIdx.x == 0) out[blockIdx.x] = s;
+}
+
+cudaError_t launch_probe_fma(float* out, int64_t blocks, int iters, int packed, cudaStream_t stream) {
+  probe_fma_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out, iters, packed, 1.0f, 1.0f);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();

@@ -186,6 +186,9 @@ cudaError_t launch_probe_mma_frag(const uint32_t* a, const uint32_t* b, float* d
 cudaError_t launch_probe_staging(const float* in, float* out, int64_t blocks, int scalar, int sm_count,
                                  cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+// fp32 multiply-add throughput: `blocks` blocks of 256 threads, each thread
+// 32 x iters independent fmaf (scalar or packed pairs).
+cudaError_t launch_probe_fma(float* out, int64_t blocks, int iters, int packed, cudaStream_t stream);
 // One-CTA tcgen05 pass (M 128, N n, K 64) whose TMEM accumulator is copied
 // out unscattered, register by register (n = 64, 128 or 256).
 cudaError_t launch_probe_tmem(const void* a, const void* b, int n, float* d, uint32_t* status, uint64_t limit_ns,

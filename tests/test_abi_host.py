@@ -91,6 +91,16 @@ def test_probe_tmem_arguments_rejected_before_launch(L):
     assert L.mpg_probe_tmem_acc_pair(16, 24, 64, 16, None) == mpg.ERR_INVALID_ARG     # B not 16-byte aligned
 
 
+def test_fma_probe_arguments_rejected_before_launch(L):
+    assert L.mpg_probe_fma_rate(None, 1, 1, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_fma_rate(2, 1, 1, 0, None) == mpg.ERR_INVALID_ARG          # out not 4-byte aligned
+    assert L.mpg_probe_fma_rate(16, 0, 1, 0, None) == mpg.ERR_INVALID_ARG         # no blocks
+    assert L.mpg_probe_fma_rate(16, 65536, 1, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_fma_rate(16, 1, 0, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_fma_rate(16, 1, (1 << 19) + 1, 0, None) == mpg.ERR_INVALID_ARG
+    assert L.mpg_probe_fma_rate(16, 1, 1, 2, None) == mpg.ERR_INVALID_ARG          # packed not 0 / 1
+
+
 def test_staging_probe_arguments_rejected_before_launch(L):
     assert L.mpg_probe_epilogue_staging(None, None, -1, 0, None) == mpg.ERR_INVALID_ARG
     assert L.mpg_probe_epilogue_staging(None, None, 1, 0, None) == mpg.ERR_INVALID_ARG

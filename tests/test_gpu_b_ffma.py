@@ -44,3 +44,27 @@ def test_ffma_bit_exact_fma_chain(m, n, k, batch, al, bl, pad, beta):
         ref = oracle.gemm_fma_chain_f32(c.a[bi], c.b[bi], c.c0[bi], 0.75, beta)
         assert np.array_equal(got[bi].view(np.uint32), ref.view(np.uint32)), \
             (bi, int(np.sum(got[bi].view(np.uint32) != ref.view(np.uint32))))
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_fma_rate_probe_does_its_work(packed):
+    """The fp32 multiply-add throughput probe: every block's chains end at
+    their exact values, and the measured rate is a plausible fraction of the
+    pipe's nominal rate (SMs x 128 lanes x 2 flop x the maximum SM clock)."""
+    import torch
+    mpg.build()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    blocks, iters = 4 * sms, 2048
+    out = mpg.probe_fma_rate(blocks, iters, packed)
+    torch.cuda.synchronize()
+    assert mpg.device_status() == mpg.OK
+    assert torch.all(out == 496 + 32 * iters)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        mpg.probe_fma_rate(blocks, iters, packed, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    tflops = 2.0 * 32 * iters * 256 * blocks * 5 / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    nominal = sms * 128 * 2 * 2.07e9 / 1e12
+    assert 0.3 * nominal < tflops < 1.05 * nominal, (tflops, nominal)
