@@ -301,6 +301,9 @@ def mode_cases(torch, mpg, synthetic, device):
     yield "attention_qkt_split3_shared_prepass", lambda: make_attention(torch, mpg, synthetic, device, "qkt", 1,
                                                                         shared=1)
     yield "attention_qkt_split3_shared", lambda: make_attention(torch, mpg, synthetic, device, "qkt", -1, shared=1)
+    # the P.V shape's own ceiling: the same P and V in tf32 on the direct TMA
+    # path (no conversion stage at all), for the split's fraction of it
+    yield "attention_pv_tf32_ceiling", lambda: make_attention(torch, mpg, synthetic, device, "pv_tf32")
 
 
 def make_batched(torch, mpg, synthetic, device, mode_name):
@@ -348,8 +351,14 @@ def make_attention(torch, mpg, synthetic, device, which, prepass=0, shared=0):
                         {"a": q, "b": kk.T}, opts=mpg.options(prepass=prepass, split_lo_shared=shared),
                         algo_bytes=algo)
     A = torch.from_numpy(p).to(device)
-    B = torch.from_numpy(v).to(device)
     algo = 4 * (2048 * 32768 + 32768 * 128 + 2048 * 128)
+    if which == "pv_tf32":
+        # tf32's direct path takes B column-major: V stored transposed
+        B = torch.from_numpy(np.ascontiguousarray(v.T)).to(device)
+        return Workload("attention_pv", 2048, 128, 32768, 1, "tf32", A, B, None, 32768, 32768, 128,
+                        0, 0, 0, mpg.ROW_MAJOR, mpg.COL_MAJOR, mpg.F32, 1.0, 0.0,
+                        {"a": p, "b": v}, opts=mpg.options(), algo_bytes=algo)
+    B = torch.from_numpy(v).to(device)
     # P holds probabilities (<= 1): lift it into fp16's normal range by 2^14
     opts = mpg.options(split_exp_a=14, prepass=prepass)
     return Workload("attention_pv", 2048, 128, 32768, 1, "split3", A, B, None, 32768, 128, 128,
@@ -849,6 +858,10 @@ def build_targets(modes, result, peaks):
                             "err": g(f"attention_{lbl}", "max_rel_err_vs_fp64")}
                       for lbl in ("qkt_split3_prepass", "qkt_split3_shared_prepass", "qkt_split3_shared",
                                   "pv_split3")}
+    ceil = g("attention_pv_tf32_ceiling", "frac_of_hbm_peak")
+    t["attn_pair"]["pv_split3"]["tf32_ceiling_frac"] = ceil
+    pv = t["attn_pair"]["pv_split3"]["gbs_frac"]
+    t["attn_pair"]["pv_split3"]["of_ceiling"] = round(pv / ceil, 3) if pv and ceil else None
     t["fused_attn"] = {"tf": g("attention_fused_2chain", "tflops"),
                        "issued_frac": g("attention_fused_2chain", "frac_of_tensor_peak"),
                        "err": g("attention_fused_2chain", "max_rel_err_vs_fp64")}
