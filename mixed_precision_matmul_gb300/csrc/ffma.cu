@@ -181,17 +181,30 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_gemm_kernel(const FfmaParams
 }  // namespace
 
 cudaError_t launch_ffma(const FfmaParams& p, cudaStream_t stream) {
-  dim3 grid((p.n + kBN - 1) / kBN, (p.m + kBM - 1) / kBM, p.batch < 65535 ? p.batch : 65535);
   // float4 loads need 16-byte aligned bases, leading dimensions and batch strides
   auto aligned = [&](const float* x, int64_t ld, int64_t stride) {
     return reinterpret_cast<uintptr_t>(x) % 16 == 0 && ld % 4 == 0 && (p.batch == 1 || stride % 4 == 0);
   };
-  const int av = aligned(p.a, p.lda, p.stride_a), bv = aligned(p.b, p.ldb, p.stride_b);
-  if (p.a_col_major && p.b_col_major) ffma_gemm_kernel<true, true><<<grid, kThreads, 0, stream>>>(p, av, bv);
-  else if (p.a_col_major) ffma_gemm_kernel<true, false><<<grid, kThreads, 0, stream>>>(p, av, bv);
-  else if (p.b_col_major) ffma_gemm_kernel<false, true><<<grid, kThreads, 0, stream>>>(p, av, bv);
-  else ffma_gemm_kernel<false, false><<<grid, kThreads, 0, stream>>>(p, av, bv);
-  return cudaGetLastError();
+  // Rows in slices of at most 65535 tile rows (the grid's y limit): each
+  // slice is the same product on A's and C's rows from its first row on.
+  constexpr int64_t kSliceRows = (int64_t)65535 * kBM;
+  const int64_t c_es = (p.c_dtype == kOutF32) ? 4 : 2;
+  for (int64_t r0 = 0; r0 < p.m; r0 += kSliceRows) {
+    FfmaParams q = p;
+    q.m = (int32_t)(p.m - r0 < kSliceRows ? p.m - r0 : kSliceRows);
+    q.a = p.a + (p.a_col_major ? r0 : r0 * p.lda);
+    q.c = static_cast<uint8_t*>(p.c) + r0 * p.ldc * c_es;
+    dim3 grid((unsigned)(((int64_t)q.n + kBN - 1) / kBN), (unsigned)((q.m + kBM - 1) / kBM),
+              q.batch < 65535 ? q.batch : 65535);
+    const int av = aligned(q.a, q.lda, q.stride_a), bv = aligned(q.b, q.ldb, q.stride_b);
+    if (q.a_col_major && q.b_col_major) ffma_gemm_kernel<true, true><<<grid, kThreads, 0, stream>>>(q, av, bv);
+    else if (q.a_col_major) ffma_gemm_kernel<true, false><<<grid, kThreads, 0, stream>>>(q, av, bv);
+    else if (q.b_col_major) ffma_gemm_kernel<false, true><<<grid, kThreads, 0, stream>>>(q, av, bv);
+    else ffma_gemm_kernel<false, false><<<grid, kThreads, 0, stream>>>(q, av, bv);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace mpg

@@ -102,3 +102,33 @@ def test_batch_strides_not_packed(mode):
         assert np.all(np.isnan(gap)), "gap between batches written"
         ref, den = oracle.gemm(base.a[b], base.b[b], base.c0[b], 1.0, 0.5, q, q)
         assert oracle.max_rel_err(got[:, :n], ref, den) <= tol
+
+
+def test_taller_than_one_grid_of_tile_rows():
+    """m above 65535 tile rows of 128 (the grid's y limit): the FFMA
+    comparator launches its tile rows in slices, the tensor-core paths take
+    their tiles persistently.  Rows at the start, at the slice boundaries
+    and at the end are checked (FFMA bit for bit against the fmaf chain)."""
+    import numpy as np
+    import torch
+    import oracle
+    import synthetic
+    mpg.build()
+    m, n, k = 65535 * 128 + 300, 6, 5
+    a = synthetic.normal((m, k), 7001)
+    b = synthetic.normal((k, n), 7002)
+    A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    rows = np.array([0, 1, 127, 65535 * 128 - 1, 65535 * 128, 65535 * 128 + 1, m - 2, m - 1])
+    for mode in (mpg.FP32_FFMA, mpg.TF32):
+        C = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+        mpg.gemm(A, B, C, alpha=1.5, beta=0.0, mode=mode)
+        torch.cuda.synchronize()
+        assert mpg.device_status() == mpg.OK
+        got = C[torch.from_numpy(rows).cuda()].cpu().numpy()
+        if mode == mpg.FP32_FFMA:
+            ref = oracle.gemm_fma_chain_f32(a[rows], b, None, 1.5, 0.0)
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+        else:
+            ref, den = oracle.gemm(a[rows], b, None, 1.5, 0.0)
+            assert oracle.max_rel_err(got, ref, den) <= 2e-3
+        del C
