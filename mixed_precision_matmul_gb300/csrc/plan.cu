@@ -298,7 +298,13 @@ mpg_status make_plan(int64_t m, int64_t n, int64_t k, int64_t batch, const Opera
       const bool cb = !tma_ok(B, batch) || B.layout != b_out;
       const CopyLayout L =
           copy_layout(m, n, k, batch, A, B, ca, cb, splitk_bytes(splits, m, n, batch), a_out, b_out);
-      if (L.end <= ws_bytes) {
+      // a transposing copy runs on a grid of 32 x 32 blocks: batches and
+      // blocks along the copy's lines within the grid's y and z limits
+      auto transpose_fits = [&](bool copy, mpg_layout in, mpg_layout out, int64_t ld) {
+        return !copy || in == out || (batch <= 65535 && (ld + 31) / 32 <= 65535);
+      };
+      if (L.end <= ws_bytes && transpose_fits(ca, A.layout, a_out, L.a_ld) &&
+          transpose_fits(cb, B.layout, b_out, L.b_ld)) {
         p.src = Src::kTmaDirect;
         p.copy_a = ca;
         p.copy_b = cb;

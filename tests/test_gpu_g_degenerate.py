@@ -132,3 +132,32 @@ def test_taller_than_one_grid_of_tile_rows():
             ref, den = oracle.gemm(a[rows], b, None, 1.5, 0.0)
             assert oracle.max_rel_err(got, ref, den) <= 2e-3
         del C
+
+
+def test_tf32_column_major_a_too_long_for_the_transposing_copy():
+    """tf32 wants A row-major: a column-major A is normally copied transposed
+    into the workspace, on a grid of 32 x 32 blocks.  With k above 65535 x 32
+    that grid cannot cover A's rows, and the product runs on generic loads
+    instead of failing."""
+    import numpy as np
+    import torch
+    import oracle
+    mpg.build()
+    m, n, k = 64, 8, 65535 * 32 + 100
+    g = np.random.Generator(np.random.PCG64(7003))
+    at = g.standard_normal((k, m), dtype=np.float32)        # column-major A: k lines of m
+    b = g.standard_normal((k, n), dtype=np.float32)
+    At, B = torch.from_numpy(at).cuda(), torch.from_numpy(b).cuda()
+    C = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    ws_bytes = mpg.workspace_size_ex(m, n, k, 1, At.data_ptr(), m, 0, mpg.F32, mpg.COL_MAJOR, B.data_ptr(), n, 0,
+                                     mpg.F32, mpg.ROW_MAJOR, mpg.TF32)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    mpg.gemm_raw(m, n, k, 1, At.data_ptr(), m, 0, mpg.F32, mpg.COL_MAJOR, B.data_ptr(), n, 0, mpg.F32, mpg.ROW_MAJOR,
+                 C.data_ptr(), n, 0, 1.0, 0.0, mpg.TF32, ws.data_ptr(), ws_bytes, 0)
+    torch.cuda.synchronize()
+    assert mpg.device_status() == mpg.OK
+    rows = np.repeat(np.arange(0, m, 9), n)
+    cols = np.tile(np.arange(n), len(rows) // n)
+    ref, den = oracle.gemm_points(at, b, k, rows, cols, a_col_major=True)
+    got = C.cpu().numpy()[rows, cols]
+    assert oracle.max_rel_err(got, ref, den) <= 2e-3
