@@ -522,9 +522,13 @@ def ours(args):
 
     w = make_headline(torch, mpg, synthetic, device)
     C = w.C0.clone()
+    # the workspace a caller sizes with mpg_gemm_workspace_size (allocated
+    # once, outside the timed region)
+    hws_bytes = mpg.workspace_size(w.m, w.n, w.k, w.batch, mpg.MODE_NAMES[w.mode_name], w.opts)
+    hws = torch.empty(max(hws_bytes, 16), dtype=torch.uint8, device=device)
 
     def step():
-        run_step(mpg, w, C, stream=sh)
+        run_step(mpg, w, C, hws.data_ptr(), hws_bytes, stream=sh)
 
     # warm-up, then the timed region bracketed by barrier + synchronize
     for _ in range(args.warmup):
@@ -573,7 +577,7 @@ def ours(args):
             "l2": "inputs > L2 (768 MB per step), no flush",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "gpu_launches": args.steps,   # one tcgen05 kernel per step at this shape (no split-K)
+        "gpu_launches": args.steps,   # one tcgen05 kernel per step at this shape (no split-K, no split tail)
         "clocks": clocks,
     }
     # roofline of the dominant kernel (the only kernel of the step)
@@ -753,7 +757,7 @@ def ours(args):
         # the timed steps fed C back into itself (beta != 0); the oracle's
         # reference is one product from the original C0
         C1 = w.C0.clone()
-        run_step(mpg, w, C1, stream=sh)
+        run_step(mpg, w, C1, hws.data_ptr(), hws_bytes, stream=sh)
         torch.cuda.synchronize()
         Chost = C1.cpu().numpy()
         secs, err = cpu_baseline_leg(orc, w, Chost[rows], rows, nthreads, orc.Q_NONE)
