@@ -864,12 +864,12 @@ __global__ void __launch_bounds__(T::kThreads, 1) tc_gemm_kernel(const __grid_co
           }
           if constexpr (T::kSrc == Src::kGeneric) cur = nxt;
           if constexpr (T::kStaged) {
-            // Every staging value has been consumed by the conversion above
-            // (the instructions that use the loaded values issue before this
-            // arrive), so no read of the buffer is outstanding when the
-            // producer refills it; hand it back.  A proxy fence here (reads
-            // before an async-proxy write) measured 8 % of the fp32 -> fp16
-            // on-load product and orders nothing the reads still need.
+            // The staging reads must have completed before the producer's
+            // TMA (async proxy) refills this buffer: the conversion that
+            // consumes them is register arithmetic the compiler may place
+            // after the arrive, so nothing else orders the loads before it.
+            // The proxy fence does; then hand the buffer back.
+            fence_proxy_async_smem();
             mbar_arrive(&stg_empty[ss]);
           }
           if (!warp_wait(&op_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
