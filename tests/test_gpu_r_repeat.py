@@ -67,3 +67,30 @@ def test_repeated_runs_give_identical_bits(case):
     got = outs[0].cpu().numpy()[rows, cols]
     ref, den = oracle.gemm_points(a, b, k, rows, cols, a_q=q, b_q=q)
     assert oracle.max_rel_err(got, ref, den) <= 1e-5, name
+
+
+@pytest.mark.parametrize("amode", ["two", "one"])
+def test_fused_attention_repeated_runs_give_identical_bits(amode):
+    """The fused attention's hand-offs (S read out while the next S goes in,
+    the flag exchange, the P writes, the folds, the merge of key ranges)
+    under repetition: a dozen runs, identical bits, and the first run within
+    the bar against the oracle on sampled rows."""
+    import torch
+    mpg.build()
+    lq, lk, d = 2048, 8192 + 77, 128
+    q = synthetic.normal((lq, d), 9400)
+    kk = synthetic.normal((lk, d), 9401).astype(np.float16)
+    vv = synthetic.normal((lk, d), 9402).astype(np.float16)
+    Q = torch.from_numpy(q).cuda()
+    K, V = torch.from_numpy(kk).cuda(), torch.from_numpy(vv).cuda()
+    mode = mpg.ATTN_SPLIT_2CHAIN if amode == "two" else mpg.ATTN_SPLIT_1CHAIN
+    outs = [mpg.attention(Q, K, V, scale=0.125, mode=mode) for _ in range(12)]
+    torch.cuda.synchronize()
+    assert mpg.device_status() == mpg.OK
+    first = outs[0].view(torch.int32)
+    for i, O in enumerate(outs[1:], 1):
+        assert int((O.view(torch.int32) != first).sum().item()) == 0, (amode, i)
+    rows = np.arange(0, lq, 97)
+    ref, den = oracle.attention(q[rows], kk, vv, 0.125)
+    err = float(np.max(np.abs(outs[0].cpu().numpy()[rows] - ref) / den))
+    assert err <= 5e-6, err
